@@ -1,0 +1,327 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused low-bit dequantize-and-multiply on GB300.
+
+Default workload: one Llama-7B-shaped decoder layer at decode (M = 1 token),
+2-bit Lloyd-Max G=32 weights with 3.5% binary16 anchor columns — the seven
+projections (q, k, v, o: 4096x4096; gate, up: 11008x4096; down: 4096x11008)
+run as ONE grouped GEMV launch per step.  Eight distinct layer copies (720 MB)
+rotate, so every step streams its weights from HBM, not L2.
+
+metric: weight GB/s = algorithmic bytes (codes + scales + offsets + anchor
+weights + anchor indices + x + y) / time; `roofline.frac` against the measured
+HBM copy bandwidth; equivalent tok/s of a 32-layer stack.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl lq|reference]
+
+Under torchrun each rank runs its own replica (the layer needs no exchange);
+the slowest rank's time sets the aggregate.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "dequant-GEMV weight GB/s (% of GB300 HBM peak); dequant-GEMM TFLOP/s"
+WORKLOAD = "llama-7b decoder layer, decode M=1, 2-bit Lloyd-Max G=32 + 3.5% fp16 anchors, 7 projections per launch"
+ROTATE = 8          # distinct layer copies in HBM (8 x 90 MB > 129 MB L2)
+STACK_LAYERS = 32   # layers of the 7B stack for the tok/s equivalent
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def layer_packs(M: int, copy: int):
+    """Host-side packed 2-bit weights and x for one layer copy."""
+    from math import floor
+    out = []
+    for i, (name, N, K) in enumerate(synth.LAYER_SHAPES["7b"]):
+        A = int(floor(0.035 * K))
+        pk = synth.random_packed_2bit(N, K, A, sigma=0.02, seed=100 + copy, cfg=2, matrix_id=i)
+        outl = synth.outlier_channels(K, 0.01, seed=100 + copy, cfg=2)
+        xb = synth.activations(M, K, "f16", synth.channel_sigma(K, outl, 20.0), seed=100 + copy, cfg=2, matrix_id=i)
+        out.append((name, pk, xb))
+    return out
+
+
+def algorithmic_bytes(packs, M: int) -> int:
+    total = 0
+    for _, pk, _ in packs:
+        N, K, A = pk["N"], pk["K"], pk["A"]
+        total += N * K // 4 + 2 * 2 * N * (K // 32) + 2 * N * A + 4 * A + 2 * M * K + 4 * M * N
+    return total
+
+
+class ClockSampler:
+    """nvidia-smi SM clock and throttle-reason samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.lines: list[str] = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_baseline(packs, seconds: float = 12.0):
+    """The oracle as it stands (plain C, one thread) on a bounded sample of rows."""
+    from oracle import oracle as O
+    O.build()
+    done_bytes, t_used, rows_done = 0, 0.0, 0
+    rows_per = 4
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        for i, (_, pk, xb) in enumerate(packs):
+            n0 = (rows_done * 37 + i * 101) % (pk["N"] - rows_per)
+            s = time.perf_counter()
+            O.gemv_2bit_rows(pk, xb, "f16", n0, n0 + rows_per)
+            t_used += time.perf_counter() - s
+            K, A = pk["K"], pk["A"]
+            done_bytes += rows_per * (K // 4 + 4 * (K // 32) + 2 * A)
+        rows_done += rows_per
+    return done_bytes / t_used / 1e9, f"{rows_done} rows of each of the 7 projections (oracle fmaf dequant + fp64 dot), weight bytes only"
+
+
+def run_reference(args):
+    """The oracle on the host cores, same metric and workload, bounded sample per step."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    packs = layer_packs(1, 0)
+    from oracle import oracle as O
+    O.build()
+    per_step = max(1.0, 60.0 / max(1, args.steps + args.warmup))
+    vals = []
+    for s in range(args.warmup + args.steps):
+        gbs, sample = cpu_baseline(packs, seconds=min(per_step, 8.0))
+        if s >= args.warmup:
+            vals.append(gbs)
+    v = statistics.median(vals)
+    layer_bytes = algorithmic_bytes(packs, 1)
+    line = {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(layer_bytes / (v * 1e9) * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample": sample},
+            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_lq(args):
+    import torch
+
+    import bit_weight_quantized_dequant_gb300 as lq
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    lq.build()
+    M = 1
+    hbm, bf16, bf16_sus, peak_kind = peaks()
+
+    h = lq.Handle(local)
+    copies = []
+    host_copy0 = None
+    for c in range(ROTATE):
+        packs = layer_packs(M, c + 17 * rank)
+        if c == 0:
+            host_copy0 = packs
+        mats = []
+        for name, pk, xb in packs:
+            w = lq.QuantWeights.from_host(pk, lq.FMT_2BIT, device=f"cuda:{local}")
+            x = torch.from_numpy(xb).view(torch.float16).to(f"cuda:{local}")
+            y = torch.empty((M, pk["N"]), dtype=torch.float32, device=f"cuda:{local}")
+            mats.append((w, x, y))
+        copies.append([h.problem(w, x, y) for (w, x, y) in mats] + [mats])
+    layer_bytes = algorithmic_bytes(host_copy0, M)
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        h.gemv_grouped(copies[i % ROTATE][:-1], stream=stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    t_all0 = torch.cuda.Event(enable_timing=True)
+    t_all1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        time.sleep(0.3)
+        t_all0.record(stream)
+        for i in range(args.steps):
+            starts[i].record(stream)
+            step(i)
+            ends[i].record(stream)
+        t_all1.record(stream)
+        torch.cuda.synchronize()
+        # keep the GPU busy a little longer so the sampler sees the loaded clocks
+        extra_until = time.perf_counter() + 1.0
+        j = 0
+        while time.perf_counter() < extra_until:
+            step(j)
+            j += 1
+            if j % 64 == 0:
+                torch.cuda.synchronize()
+        torch.cuda.synchronize()
+    h.sync()
+    total_ms = t_all0.elapsed_time(t_all1)
+    launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    if dist:
+        t = torch.tensor([total_ms], device=f"cuda:{local}")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * layer_bytes / (ms_per_step * 1e-3) / 1e9
+    kern_ms = statistics.mean(launch_ms)
+    achieved = layer_bytes / (kern_ms * 1e-3) / 1e9
+
+    # end to end through the public API: x from pinned host memory in, y back to pinned host memory, every step
+    mats0 = copies[0][-1]
+    xs_host = [x.cpu().pin_memory() for (_, x, _) in mats0]
+    ys_host = [torch.empty_like(y, device="cpu").pin_memory() for (_, _, y) in mats0]
+    h2d = sum(t.numel() * t.element_size() for t in xs_host)
+    d2h = sum(t.numel() * t.element_size() for t in ys_host)
+
+    def e2e_step(i):
+        c = copies[i % ROTATE]
+        for (w, x, y), xh in zip(c[-1], xs_host):
+            x.copy_(xh, non_blocking=True)
+        h.gemv_grouped(c[:-1], stream=stream)
+        for (w, x, y), yh in zip(c[-1], ys_host):
+            yh.copy_(y, non_blocking=True)
+
+    for i in range(args.warmup):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    e2e_val = world * layer_bytes / (e2e_ms * 1e-3) / 1e9
+
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        with open(tpath) as f:
+            traffic = json.load(f).get("gemv_7b_layer_m1_bytes_per_launch")
+
+    if rank == 0:
+        cpu_v, sample = cpu_baseline(host_copy0)
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "M": M, "layer_bytes": layer_bytes, "rotated_copies": ROTATE,
+                       "l2": f"inputs larger than L2: {ROTATE} distinct layer copies ({ROTATE * layer_bytes / 1e6:.0f} MB)",
+                       "parallelism": f"replicas x{world}"},
+            "frac_of_hbm": round(value / world / hbm, 4),
+            "tok_s_32_layer_stack": round(1e3 / (ms_per_step * STACK_LAYERS), 1),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm, "unit": "GB/s",
+                         "frac": round(achieved / hbm, 4), "traffic": traffic, "peak_kind": peak_kind,
+                         "kernel": "gemv_kernel<1,2bit> (one grouped launch per layer)",
+                         "algorithmic_bytes_per_launch": layer_bytes},
+            "cpu_baseline": {"value": round(cpu_v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": args.steps,
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    h.close()
+    if dist:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="lq", choices=["lq", "reference"])
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_lq(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,228 @@
+"""ctypes binding of the liblq C ABI (include/lq.h).
+
+Tensors are PyTorch CUDA tensors; only their device pointers, the current CUDA
+stream and plain sizes cross the boundary.
+"""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+from pathlib import Path
+
+LQ_OK, LQ_ERR_INVALID_ARG, LQ_ERR_UNSUPPORTED, LQ_ERR_ALIGNMENT, LQ_ERR_WORKSPACE, LQ_ERR_CUDA, LQ_ERR_TIMEOUT = range(7)
+FMT_2BIT, FMT_NF4 = 1, 2
+F32, F16, BF16 = 0, 1, 2
+
+#: every entry point include/lq.h declares
+EXPORTED = ("lq_create", "lq_destroy", "lq_status_string", "lq_sync", "lq_dequant", "lq_gemv",
+            "lq_gemv_grouped", "lq_gemm")
+
+_LIB = None
+
+
+class LQError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = _LIB.lq_status_string(status).decode() if _LIB is not None else str(status)
+        super().__init__(f"{where}: {msg} (status {status})")
+
+
+class lq_problem(ctypes.Structure):
+    _fields_ = [
+        ("format", ctypes.c_int), ("M", ctypes.c_int), ("N", ctypes.c_int), ("K", ctypes.c_int),
+        ("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("offsets", ctypes.c_void_p),
+        ("anchor_idx", ctypes.c_void_p), ("anchor_w", ctypes.c_void_p),
+        ("A", ctypes.c_int), ("ld_anchor", ctypes.c_int),
+        ("x", ctypes.c_void_p), ("x_dtype", ctypes.c_int), ("y", ctypes.c_void_p), ("y_dtype", ctypes.c_int),
+        ("batch", ctypes.c_int),
+        ("stride_codes", ctypes.c_int64), ("stride_scales", ctypes.c_int64), ("stride_offsets", ctypes.c_int64),
+        ("stride_anchor_idx", ctypes.c_int64), ("stride_anchor_w", ctypes.c_int64),
+        ("stride_x", ctypes.c_int64), ("stride_y", ctypes.c_int64),
+    ]
+
+
+def library_path() -> Path:
+    from .build import LIB
+    return LIB
+
+
+def load_library(build_if_missing: bool = True):
+    """Load liblq.so (building it first if asked and needed); raises if it cannot be loaded."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = library_path()
+    if build_if_missing:
+        from .build import build
+        path = build()
+    if not path.exists():
+        raise RuntimeError(f"liblq.so not built at {path}; run bit_weight_quantized_dequant_gb300.build()")
+    L = ctypes.CDLL(str(path))
+    P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    L.lq_create.argtypes = [ctypes.POINTER(P), I, S]
+    L.lq_create.restype = I
+    L.lq_destroy.argtypes = [P]
+    L.lq_destroy.restype = I
+    L.lq_sync.argtypes = [P]
+    L.lq_sync.restype = I
+    L.lq_status_string.argtypes = [I]
+    L.lq_status_string.restype = ctypes.c_char_p
+    L.lq_dequant.argtypes = [P, I, P, P, P, P, P, I, I, P, I, I, I, P]
+    L.lq_dequant.restype = I
+    L.lq_gemv.argtypes = [P, I, P, P, P, P, P, I, I, P, I, P, I, I, I, I, P]
+    L.lq_gemv.restype = I
+    L.lq_gemm.argtypes = [P, I, P, P, P, P, P, I, I, P, I, P, I, I, I, I, P]
+    L.lq_gemm.restype = I
+    L.lq_gemv_grouped.argtypes = [P, ctypes.POINTER(lq_problem), I, P]
+    L.lq_gemv_grouped.restype = I
+    _LIB = L
+    return L
+
+
+def exported_symbols(path: Path | None = None) -> list[str]:
+    """Names from EXPORTED that the library resolves (no GPU needed)."""
+    L = ctypes.CDLL(str(path or library_path()))
+    return [n for n in EXPORTED if hasattr(L, n)]
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else int(t.data_ptr())
+
+
+def _dtype_code(t) -> int:
+    import torch
+    return {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}[t.dtype]
+
+
+def _stream(stream) -> int | None:
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream) or None
+
+
+@dataclass
+class QuantWeights:
+    """One quantized matrix W [N][K] in device memory (layouts as in include/lq.h)."""
+    format: int
+    N: int
+    K: int
+    codes: object                 # uint8 tensor
+    scales: object                # float16 [N][K/32] (2-bit) or float32 [N][K/64] (NF4)
+    offsets: object = None        # float16 [N][K/32] (2-bit)
+    anchor_idx: object = None     # int32 [A]
+    anchor_w: object = None       # float16 [N][ld_anchor]
+    A: int = 0
+    ld_anchor: int = 0
+
+    @staticmethod
+    def from_host(packed: dict, fmt: int, device="cuda") -> "QuantWeights":
+        """Copy a packed host dict (numpy arrays, bit patterns as uint16) to the device."""
+        import numpy as np
+        import torch
+
+        def t(a, dtype):
+            return torch.from_numpy(np.ascontiguousarray(a)).view(dtype).to(device)
+        if fmt == FMT_2BIT:
+            A = int(packed["A"])
+            return QuantWeights(FMT_2BIT, int(packed["N"]), int(packed["K"]), t(packed["codes"], torch.uint8),
+                                t(packed["scales"], torch.float16), t(packed["offsets"], torch.float16),
+                                t(packed["anchor_idx"], torch.int32) if A > 0 else None,
+                                t(packed["anchor_w"], torch.float16) if A > 0 else None, A, int(packed["ld_anchor"]))
+        return QuantWeights(FMT_NF4, int(packed["N"]), int(packed["K"]), t(packed["codes"], torch.uint8),
+                            t(packed["absmax"], torch.float32))
+
+    def args(self):
+        return (self.format, _ptr(self.codes), _ptr(self.scales), _ptr(self.offsets), _ptr(self.anchor_idx),
+                _ptr(self.anchor_w), int(self.A), int(self.ld_anchor))
+
+
+class Handle:
+    """An lq handle on one CUDA device, with its split-K workspace."""
+
+    def __init__(self, device: int = 0, workspace_bytes: int = 0):
+        self._lib = load_library()
+        h = ctypes.c_void_p()
+        st = self._lib.lq_create(ctypes.byref(h), int(device), int(workspace_bytes))
+        if st != LQ_OK:
+            raise LQError(st, "lq_create")
+        self._h = h
+        self.device = device
+
+    def close(self):
+        if getattr(self, "_h", None):
+            st = self._lib.lq_destroy(self._h)
+            self._h = None
+            if st != LQ_OK:
+                raise LQError(st, "lq_destroy")
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    @property
+    def raw(self):
+        return self._h
+
+    def sync(self):
+        st = self._lib.lq_sync(self._h)
+        if st != LQ_OK:
+            raise LQError(st, "lq_sync")
+
+    def dequant(self, w: QuantWeights, out=None, out_dtype=None, stream=None):
+        import torch
+        if out is None:
+            out = torch.empty((w.N, w.K), dtype=out_dtype or torch.float32, device=w.codes.device)
+        fmt, c, s, o, ai, aw, A, ld = w.args()
+        st = self._lib.lq_dequant(self._h, fmt, c, s, o, ai, aw, A, ld, _ptr(out), _dtype_code(out), w.N, w.K,
+                                  _stream(stream))
+        if st != LQ_OK:
+            raise LQError(st, "lq_dequant")
+        return out
+
+    def _mm(self, fn, name, w: QuantWeights, x, y=None, y_dtype=None, stream=None):
+        import torch
+        M = x.shape[0]
+        if y is None:
+            y = torch.empty((M, w.N), dtype=y_dtype or torch.float32, device=x.device)
+        fmt, c, s, o, ai, aw, A, ld = w.args()
+        st = fn(self._h, fmt, c, s, o, ai, aw, A, ld, _ptr(x), _dtype_code(x), _ptr(y), _dtype_code(y), M, w.N, w.K,
+                _stream(stream))
+        if st != LQ_OK:
+            raise LQError(st, name)
+        return y
+
+    def gemv(self, w: QuantWeights, x, y=None, y_dtype=None, stream=None):
+        """y = x * W_eff^T for 1 <= M <= 32 tokens (decode)."""
+        return self._mm(self._lib.lq_gemv, "lq_gemv", w, x, y, y_dtype, stream)
+
+    def gemm(self, w: QuantWeights, x, y=None, y_dtype=None, stream=None):
+        """y = x * W_eff^T on the tcgen05 tensor-core path (prefill)."""
+        return self._mm(self._lib.lq_gemm, "lq_gemm", w, x, y, y_dtype, stream)
+
+    @staticmethod
+    def problem(w: QuantWeights, x, y, batch: int = 1, strides: dict | None = None) -> lq_problem:
+        """Describe one (batched) product for gemv_grouped; strides are in bytes."""
+        p = lq_problem()
+        fmt, c, s, o, ai, aw, A, ld = w.args()
+        p.format, p.M, p.N, p.K = fmt, int(x.shape[-2]), w.N, w.K
+        p.codes, p.scales, p.offsets, p.anchor_idx, p.anchor_w = c, s, o, ai, aw
+        p.A, p.ld_anchor = A, ld
+        p.x, p.x_dtype, p.y, p.y_dtype = _ptr(x), _dtype_code(x), _ptr(y), _dtype_code(y)
+        p.batch = int(batch)
+        for k, v in (strides or {}).items():
+            setattr(p, "stride_" + k, int(v))
+        return p
+
+    def gemv_grouped(self, problems, stream=None):
+        arr = (lq_problem * len(problems))(*problems)
+        st = self._lib.lq_gemv_grouped(self._h, arr, len(problems), _stream(stream))
+        if st != LQ_OK:
+            raise LQError(st, "lq_gemv_grouped")

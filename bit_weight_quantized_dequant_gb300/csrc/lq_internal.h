@@ -1,0 +1,72 @@
+// Host-side internals of liblq: the handle and the launch entry points that the
+// C ABI (lq_api.cu) dispatches to after validating arguments.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/lq.h"
+
+struct lq_handle_s {
+    int device = 0;
+    int num_sms = 0;
+    int max_smem_optin = 0;
+    void* workspace = nullptr;          // device scratch: [counters | partial sums]
+    size_t workspace_bytes = 0;
+    unsigned* counters = nullptr;       // per-strip arrival counters (zero between calls)
+    size_t num_counters = 0;
+    float* partials = nullptr;          // split-K partial sums
+    size_t partial_floats = 0;
+    int* status_flag = nullptr;         // device word: nonzero after a bounded wait ran out
+};
+
+namespace lq {
+
+constexpr int kMaxGroup = 16;           // problems per grouped GEMV launch
+constexpr int kGemvStripRows = 64;      // output rows per GEMV thread block (4 warps x 16)
+constexpr int kGemvThreads = 128;
+
+// One problem of a grouped GEMV launch as the kernel sees it.
+struct GemvDesc {
+    const uint8_t* codes;
+    const void* scales;
+    const uint16_t* offsets;
+    const int32_t* anchor_idx;
+    const uint16_t* anchor_w;
+    const void* x;
+    void* y;
+    int64_t stride_codes, stride_scales, stride_offsets, stride_anchor_idx, stride_anchor_w, stride_x, stride_y;
+    int N, K, A, ld_anchor, batch;
+    int KC;            // K columns per code split (multiple of 256 unless the split is the whole row)
+    int S;             // code splits
+    int parts;         // S, plus one anchor part when S > 1 and A > 0
+    int strips;        // ceil(N / 64)
+    int64_t unit_begin;   // first global unit of this problem
+    int64_t strip_begin;  // first global strip (counters index)
+    int64_t partial_begin;  // first float of this problem's split-K partial sums
+};
+
+struct GemvParams {
+    GemvDesc d[kMaxGroup];
+    int count;
+    int M;
+    int format;
+    int x_bf16;
+    int y_dtype;
+    int kc_pad;        // smem columns reserved for one code split (multiple of 256)
+    int a_pad;         // smem columns reserved for anchors (multiple of 16)
+    float* partials;
+    unsigned* counters;
+    int64_t total_units;
+};
+
+lq_status launch_dequant(lq_handle h, int format, const uint8_t* codes, const void* scales, const uint16_t* offsets,
+                         const int32_t* anchor_idx, const uint16_t* anchor_w, int A, int ld_anchor, void* w_out,
+                         int out_dtype, int N, int K, cudaStream_t stream);
+
+lq_status launch_gemv(lq_handle h, const lq_problem* problems, int count, cudaStream_t stream);
+
+lq_status launch_gemm(lq_handle h, const lq_problem& p, cudaStream_t stream);
+
+}  // namespace lq

@@ -1,0 +1,193 @@
+/*
+ * lq.h — C ABI of liblq.so: fused dequantize-and-multiply for linear layers whose
+ * weights are stored low-bit, on one GB300 (sm_103a).
+ *
+ * y[m][n] = sum_k x[m][k] * W_eff[n][k]      (x: M x K tokens, W: N x K, out x in)
+ *
+ * Weight formats
+ * --------------
+ * LQ_FMT_2BIT_LM_G32 — the otf-llm 4.0.1 README, "Theoretical & Mathematical
+ *   Foundations": 2-bit codes q index the Lloyd-Max codebook
+ *   C = {-1.52, -0.45, +0.45, +1.52} (section 2), a group of G = 32 consecutive
+ *   input columns of one output row shares a binary16 scale S_g and offset Z_g
+ *   fitted by least squares (section 3), and a sorted set of input columns
+ *   ("outlier anchors", section 4) is kept exactly in binary16:
+ *       W_eff[n][k] = fmaf(S_g, C[q], Z_g)          (fp32, one rounding)
+ *       W_eff[n][anchor_idx[a]] = anchor_w[n][a]    (replaces the 2-bit value)
+ *   Storage (all row-major, device memory):
+ *       codes      uint8   [N][K/4]   column 4j+i of a row in bits 2i..2i+1 of byte j
+ *       scales     binary16[N][K/32]  S_g
+ *       offsets    binary16[N][K/32]  Z_g
+ *       anchor_idx int32   [A]        strictly increasing columns in [0, K)
+ *       anchor_w   binary16[N][ld_anchor], ld_anchor >= A, ld_anchor % 8 == 0
+ *   Anchor columns store code 0 in `codes`; their code is never used.
+ *
+ * LQ_FMT_NF4_B64 — the AirQuant README, "Fundamentacao Teorica" item 2 (NF4,
+ *   block-wise, the QLoRA NormalFloat data type): blocks of 64 consecutive input
+ *   columns share an fp32 absmax, codes index the 16 NF4 levels T:
+ *       W_eff[n][k] = T[q] * absmax_b                 (fp32, one rounding)
+ *   Storage: codes uint8 [N][K/2] (column 2j in the low nibble of byte j, 2j+1 in
+ *   the high nibble), scales = absmax float32 [N][K/64]; offsets, anchor_idx and
+ *   anchor_w are NULL and A = 0.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Ownership: the caller owns every buffer passed in.  The library owns the
+ *   handle and the device workspace that lq_create allocates; no other call
+ *   allocates memory.
+ * - Asynchrony: compute calls enqueue work on `stream` (a cudaStream_t, NULL for
+ *   the legacy default stream) and return without waiting.  A returned LQ_OK
+ *   means the arguments were valid and the launch was accepted.
+ * - Errors: arguments are validated on the host before anything is launched; an
+ *   invalid call returns an error status and enqueues nothing.  No call traps
+ *   on the device.  Device-side waits are bounded; a wait that runs out records
+ *   a flag that lq_sync() reports as LQ_ERR_TIMEOUT.
+ * - Alignment: every device pointer must be 16-byte aligned.
+ * - Workspace: calls that split K across thread blocks keep partial sums and
+ *   arrival counters in the handle's workspace.  One handle serves one stream
+ *   at a time; calls on one handle that overlap on the GPU race.
+ * - Device: a handle belongs to the device given to lq_create; calls switch to
+ *   that device for the launch and switch back.
+ * - Arithmetic: dequantized weights follow the definitions above exactly
+ *   (lq_dequant is bit-exact).  lq_gemv multiplies binary16-rounded weights by
+ *   binary16 x on tensor cores with fp32 accumulation (|error| <= 1e-3 *
+ *   sum_k |W_eff||x|); bf16 x is converted to binary16 (exact for |x| < 65504).
+ *   lq_gemm multiplies in the dtype of x (bf16 or binary16) with fp32
+ *   accumulation (|error| <= 4e-3 * sum_k |W_eff||x| for bf16).
+ */
+#ifndef LQ_H_
+#define LQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(_WIN32)
+#define LQ_API __declspec(dllexport)
+#else
+#define LQ_API __attribute__((visibility("default")))
+#endif
+
+typedef enum lq_status {
+    LQ_OK = 0,
+    LQ_ERR_INVALID_ARG = 1,   /* null pointer, bad size, bad enum, unsorted anchors ... */
+    LQ_ERR_UNSUPPORTED = 2,   /* valid but not handled by this entry point (e.g. M out of range) */
+    LQ_ERR_ALIGNMENT = 3,     /* a pointer or leading dimension breaks the 16-byte rule */
+    LQ_ERR_WORKSPACE = 4,     /* the handle's workspace is too small for this call */
+    LQ_ERR_CUDA = 5,          /* a CUDA runtime call or launch failed */
+    LQ_ERR_TIMEOUT = 6        /* a bounded device-side wait ran out (reported by lq_sync) */
+} lq_status;
+
+typedef enum lq_format {
+    LQ_FMT_2BIT_LM_G32 = 1,
+    LQ_FMT_NF4_B64 = 2
+} lq_format;
+
+typedef enum lq_dtype {
+    LQ_F32 = 0,
+    LQ_F16 = 1,
+    LQ_BF16 = 2
+} lq_dtype;
+
+typedef struct lq_handle_s* lq_handle;
+
+/*
+ * One problem of a grouped call: `batch` independent products of the same
+ * shape.  Member b of the batch reads and writes at the base pointers plus
+ * b * stride_* BYTES.  Pointers, strides and layouts as described above; x is
+ * [M][K] and y is [M][N], both row-major.
+ */
+typedef struct lq_problem {
+    int format;                /* lq_format */
+    int M, N, K;
+    const uint8_t* codes;
+    const void* scales;        /* binary16 S_g (2-bit) or fp32 absmax (NF4) */
+    const uint16_t* offsets;   /* binary16 Z_g (2-bit) or NULL */
+    const int32_t* anchor_idx; /* 2-bit only, may be NULL when A == 0 */
+    const uint16_t* anchor_w;  /* 2-bit only, may be NULL when A == 0 */
+    int A;
+    int ld_anchor;
+    const void* x;
+    int x_dtype;               /* LQ_F16 or LQ_BF16 */
+    void* y;
+    int y_dtype;               /* LQ_F32, LQ_F16 or LQ_BF16 */
+    int batch;                 /* >= 1 */
+    int64_t stride_codes, stride_scales, stride_offsets, stride_anchor_idx, stride_anchor_w;
+    int64_t stride_x, stride_y;
+} lq_problem;
+
+/*
+ * lq_create — make a handle for CUDA device `device`.
+ *   workspace_bytes: device scratch for split-K partial sums and counters;
+ *   0 selects the default (256 MiB).  Allocated and zeroed here, once.
+ *   Returns LQ_ERR_INVALID_ARG for a null `out` or a bad device, LQ_ERR_CUDA when
+ *   the allocation fails.  On failure *out is set to NULL.
+ */
+LQ_API lq_status lq_create(lq_handle* out, int device, size_t workspace_bytes);
+
+/* lq_destroy — synchronize the handle's device and free the handle and its workspace. NULL is a no-op. */
+LQ_API lq_status lq_destroy(lq_handle h);
+
+/* lq_status_string — static English text for a status code; never NULL. */
+LQ_API const char* lq_status_string(int status);
+
+/*
+ * lq_sync — wait for the device and report errors raised on it: LQ_ERR_CUDA for
+ * an asynchronous CUDA error, LQ_ERR_TIMEOUT when a bounded device wait ran out
+ * since the last lq_sync (the flag is cleared).
+ */
+LQ_API lq_status lq_sync(lq_handle h);
+
+/*
+ * lq_dequant — W_eff as dense [N][K] in out_dtype (LQ_F32, LQ_F16 or LQ_BF16).
+ * fp32 output is bit-exact to the definitions above; binary16/bf16 outputs are
+ * the round-to-nearest-even conversion of that fp32 value.
+ * Format rules: K % 32 == 0 (2-bit) or K % 64 == 0 (NF4); N >= 1; anchors as above.
+ */
+LQ_API lq_status lq_dequant(lq_handle h, int format,
+                            const uint8_t* codes, const void* scales, const uint16_t* offsets,
+                            const int32_t* anchor_idx, const uint16_t* anchor_w, int A, int ld_anchor,
+                            void* w_out, int out_dtype, int N, int K, void* stream);
+
+/*
+ * lq_gemv — decode-sized product y = x * W_eff^T for 1 <= M <= 32 tokens, with
+ * split-K over thread blocks and the anchor columns folded into the same fp32
+ * accumulator.  x: [M][K] binary16 or bf16; y: [M][N] in y_dtype.
+ * LQ_ERR_UNSUPPORTED for M outside 1..32.
+ */
+LQ_API lq_status lq_gemv(lq_handle h, int format,
+                         const uint8_t* codes, const void* scales, const uint16_t* offsets,
+                         const int32_t* anchor_idx, const uint16_t* anchor_w, int A, int ld_anchor,
+                         const void* x, int x_dtype, void* y, int y_dtype,
+                         int M, int N, int K, void* stream);
+
+/*
+ * lq_gemv_grouped — several lq_gemv problems (e.g. the seven projections of one
+ * decoder layer, or many small matrices as a batch) in ONE launch.  `problems`
+ * is a host array of `count` entries, read before the call returns.  All
+ * problems must share format, M, x_dtype and y_dtype.
+ */
+LQ_API lq_status lq_gemv_grouped(lq_handle h, const lq_problem* problems, int count, void* stream);
+
+/*
+ * lq_gemm — prefill-sized product for M >= 1 (tuned for M >= 256) on the
+ * tcgen05 tensor cores: x tiles arrive by TMA, weight tiles are dequantized by
+ * the CTA into tensor memory, the fp32 accumulator lives in tensor memory, and
+ * the anchor columns are appended as extra K-blocks of the same accumulator.
+ * x: [M][K] bf16 or binary16 (the multiply runs in that dtype); y: [M][N] in
+ * y_dtype.  2-bit: K % 64 == 0; NF4: K % 64 == 0.
+ */
+LQ_API lq_status lq_gemm(lq_handle h, int format,
+                         const uint8_t* codes, const void* scales, const uint16_t* offsets,
+                         const int32_t* anchor_idx, const uint16_t* anchor_w, int A, int ld_anchor,
+                         const void* x, int x_dtype, void* y, int y_dtype,
+                         int M, int N, int K, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LQ_H_ */

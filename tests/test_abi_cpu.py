@@ -1,0 +1,109 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds for sm_103a,
+loads, exports every entry point include/lq.h declares, and its validation
+rejects bad arguments before touching a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import bit_weight_quantized_dequant_gb300 as lq
+from bit_weight_quantized_dequant_gb300 import _lq
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = lq.build()
+    return _lq.load_library(build_if_missing=False), path
+
+
+def declared_symbols():
+    src = open(os.path.join(ROOT, "include", "lq.h")).read()
+    return sorted(set(re.findall(r"LQ_API\s+[\w\s\*]+?\b(lq_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_binding_list():
+    assert declared_symbols() == sorted(_lq.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    _, path = lib
+    assert sorted(_lq.exported_symbols(path)) == declared_symbols()
+
+
+def test_status_strings(lib):
+    L, _ = lib
+    for s in range(7):
+        assert L.lq_status_string(s)
+    assert L.lq_status_string(99) == b"unknown status"
+
+
+def _fake_handle():
+    # Only used with arguments that fail validation, which happens before the handle is read.
+    return ctypes.c_void_p(0x1000)
+
+
+def test_validation_rejects_before_launch(lib):
+    L, _ = lib
+    h = _fake_handle()
+    A16 = 0x10000          # 16-byte aligned fake device addresses (never dereferenced)
+    # null handle
+    assert L.lq_dequant(None, 1, A16, A16, A16, None, None, 0, 0, A16, 0, 4, 64, None) == _lq.LQ_ERR_INVALID_ARG
+    # bad format
+    assert L.lq_dequant(h, 7, A16, A16, A16, None, None, 0, 0, A16, 0, 4, 64, None) == _lq.LQ_ERR_INVALID_ARG
+    # K not a multiple of the group
+    assert L.lq_dequant(h, 1, A16, A16, A16, None, None, 0, 0, A16, 0, 4, 48, None) == _lq.LQ_ERR_INVALID_ARG
+    # NF4 needs K % 64
+    assert L.lq_dequant(h, 2, A16, A16, None, None, None, 0, 0, A16, 0, 4, 96, None) == _lq.LQ_ERR_INVALID_ARG
+    # misaligned codes pointer
+    assert L.lq_dequant(h, 1, A16 + 4, A16, A16, None, None, 0, 0, A16, 0, 4, 64, None) == _lq.LQ_ERR_ALIGNMENT
+    # anchors given but no pointers
+    assert L.lq_dequant(h, 1, A16, A16, A16, None, None, 3, 8, A16, 0, 4, 64, None) == _lq.LQ_ERR_INVALID_ARG
+    # ld_anchor not a multiple of 8
+    assert L.lq_dequant(h, 1, A16, A16, A16, A16, A16, 3, 4 + 1, A16, 0, 4, 64, None) == _lq.LQ_ERR_ALIGNMENT
+    # ld_anchor < A
+    assert L.lq_dequant(h, 1, A16, A16, A16, A16, A16, 9, 8, A16, 0, 4, 64, None) == _lq.LQ_ERR_INVALID_ARG
+    # anchors with NF4
+    assert L.lq_dequant(h, 2, A16, A16, None, A16, A16, 1, 8, A16, 0, 4, 64, None) == _lq.LQ_ERR_INVALID_ARG
+    # bad output dtype
+    assert L.lq_dequant(h, 1, A16, A16, A16, None, None, 0, 0, A16, 9, 4, 64, None) == _lq.LQ_ERR_INVALID_ARG
+    # gemv: M out of range, bad x dtype, misaligned y
+    assert L.lq_gemv(h, 1, A16, A16, A16, None, None, 0, 0, A16, 1, A16, 0, 33, 4, 64, None) == _lq.LQ_ERR_UNSUPPORTED
+    assert L.lq_gemv(h, 1, A16, A16, A16, None, None, 0, 0, A16, 1, A16, 0, 0, 4, 64, None) == _lq.LQ_ERR_UNSUPPORTED
+    assert L.lq_gemv(h, 1, A16, A16, A16, None, None, 0, 0, A16, 0, A16, 0, 1, 4, 64, None) == _lq.LQ_ERR_INVALID_ARG
+    assert L.lq_gemv(h, 1, A16, A16, A16, None, None, 0, 0, A16, 1, A16 + 2, 0, 1, 4, 64, None) == _lq.LQ_ERR_ALIGNMENT
+    # gemm: K % 64
+    assert L.lq_gemm(h, 1, A16, A16, A16, None, None, 0, 0, A16, 2, A16, 0, 256, 4, 96, None) == _lq.LQ_ERR_UNSUPPORTED
+
+
+def test_grouped_validation(lib):
+    L, _ = lib
+    h = _fake_handle()
+    A16 = 0x10000
+    p = _lq.lq_problem()
+    p.format, p.M, p.N, p.K = 1, 1, 64, 256
+    p.codes = p.scales = p.offsets = p.x = p.y = A16
+    p.x_dtype, p.y_dtype, p.batch = 1, 0, 1
+    q = _lq.lq_problem.from_buffer_copy(p)
+    q.M = 2                                         # mixed M in one launch
+    arr = (_lq.lq_problem * 2)(p, q)
+    assert L.lq_gemv_grouped(h, arr, 2, None) == _lq.LQ_ERR_UNSUPPORTED
+    assert L.lq_gemv_grouped(h, arr, 0, None) == _lq.LQ_ERR_INVALID_ARG
+    big = (_lq.lq_problem * 17)(*([p] * 17))
+    assert L.lq_gemv_grouped(h, big, 17, None) == _lq.LQ_ERR_UNSUPPORTED
+    r = _lq.lq_problem.from_buffer_copy(p)
+    r.batch, r.stride_codes = 2, 8                  # stride not a multiple of 16 bytes
+    assert L.lq_gemv_grouped(h, (_lq.lq_problem * 1)(r), 1, None) == _lq.LQ_ERR_ALIGNMENT
+
+
+def test_create_without_device_reports_error(lib):
+    """No GPU in this container: lq_create must fail cleanly, not crash."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    L, _ = lib
+    h = ctypes.c_void_p()
+    st = L.lq_create(ctypes.byref(h), 0, 0)
+    assert st in (_lq.LQ_ERR_CUDA, _lq.LQ_ERR_INVALID_ARG) and not h.value
