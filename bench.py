@@ -228,7 +228,7 @@ def run_lq(args):
         t_all1.record(stream)
         torch.cuda.synchronize()
         # keep the GPU busy a little longer so the sampler sees the loaded clocks
-        extra_until = time.perf_counter() + 1.0
+        extra_until = time.perf_counter() + 0.3
         j = 0
         while time.perf_counter() < extra_until:
             step(j)
