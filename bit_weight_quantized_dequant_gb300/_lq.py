@@ -15,7 +15,7 @@ F32, F16, BF16 = 0, 1, 2
 
 #: every entry point include/lq.h declares
 EXPORTED = ("lq_create", "lq_destroy", "lq_status_string", "lq_sync", "lq_dequant", "lq_gemv",
-            "lq_gemv_grouped", "lq_gemm")
+            "lq_gemv_grouped", "lq_gemm", "lq_gemv_noalloc")
 
 _LIB = None
 
@@ -73,6 +73,8 @@ def load_library(build_if_missing: bool = True):
     L.lq_gemv.restype = I
     L.lq_gemm.argtypes = [P, I, P, P, P, P, P, I, I, P, I, P, I, I, I, I, P]
     L.lq_gemm.restype = I
+    L.lq_gemv_noalloc.argtypes = [I, P, P, P, P, P, I, I, P, I, P, I, I, I, I, P]
+    L.lq_gemv_noalloc.restype = I
     L.lq_gemv_grouped.argtypes = [P, ctypes.POINTER(lq_problem), I, P]
     L.lq_gemv_grouped.restype = I
     _LIB = L

@@ -5,6 +5,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <mutex>
 #include <vector>
 
 #include "lq_internal.h"
@@ -272,6 +273,79 @@ LQ_API lq_status lq_gemm(lq_handle h, int format, const uint8_t* codes, const vo
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if ((s = check_anchor_order(anchor_idx, A, K, st)) != LQ_OK) return s;
     return lq::launch_gemm(h, p, st);
+}
+
+// ---- the allocation-free GEMV entry point ---------------------------------------
+//
+// Scratch for split-K partial sums and arrival counters lives in this file-scope
+// device array instead of a handle's cudaMalloc'd workspace.  Every GPU that loads
+// the library holds it until the process exits.  In host code the array's name is
+// only a host-side stand-in, so its device address is looked up once per device
+// (cudaGetSymbolAddress, with that device current) and passed to the kernel.
+
+namespace {
+
+constexpr size_t kStaticCounters = 16384;           // 64 KiB of arrival counters
+constexpr size_t kStaticPartialFloats = 2u << 20;   // 8 MiB of split-K partial sums
+constexpr size_t kStaticScratchBytes = kStaticCounters * sizeof(unsigned) + kStaticPartialFloats * sizeof(float);
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+struct StaticScratchSlot {
+    bool ready = false;
+    void* base = nullptr;
+    int num_sms = 0;
+    int max_smem_optin = 0;
+};
+
+std::mutex g_static_mutex;
+StaticScratchSlot g_static_slots[kMaxDevices];
+
+// Device address of the scratch array on the current device (set up on first use).
+lq_status static_scratch(StaticScratchSlot& out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return LQ_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return LQ_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_static_mutex);
+    StaticScratchSlot& slot = g_static_slots[dev];
+    if (!slot.ready) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || ptr == nullptr) return LQ_ERR_CUDA;
+        if (cudaDeviceGetAttribute(&slot.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&slot.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+            return LQ_ERR_CUDA;
+        slot.base = ptr;
+        slot.ready = true;
+    }
+    out = slot;
+    return LQ_OK;
+}
+
+}  // namespace
+
+LQ_API lq_status lq_gemv_noalloc(int format, const uint8_t* codes, const void* scales, const uint16_t* offsets,
+                                 const int32_t* anchor_idx, const uint16_t* anchor_w, int A, int ld_anchor,
+                                 const void* x, int x_dtype, void* y, int y_dtype, int M, int N, int K,
+                                 void* stream) {
+    lq_problem p = make_problem(format, codes, scales, offsets, anchor_idx, anchor_w, A, ld_anchor, x, x_dtype, y,
+                                y_dtype, M, N, K);
+    lq_status s = check_problem(p);
+    if (s != LQ_OK) return s;
+    if (M < 1 || M > 32) return LQ_ERR_UNSUPPORTED;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if ((s = check_anchor_order(anchor_idx, A, K, st)) != LQ_OK) return s;
+    StaticScratchSlot slot;
+    if ((s = static_scratch(slot)) != LQ_OK) return s;
+    lq::GemvWorkspace ws;
+    ws.num_sms = slot.num_sms;
+    ws.max_smem_optin = slot.max_smem_optin;
+    ws.counters = static_cast<unsigned*>(slot.base);
+    ws.num_counters = kStaticCounters;
+    ws.partials = reinterpret_cast<float*>(static_cast<char*>(slot.base) + kStaticCounters * sizeof(unsigned));
+    ws.partial_floats = kStaticPartialFloats;
+    ws.clear_counters = true;
+    return lq::launch_gemv_ws(ws, &p, 1, st);
 }
 
 }  // extern "C"

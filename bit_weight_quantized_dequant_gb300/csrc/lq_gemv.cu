@@ -477,6 +477,18 @@ int round_up(int a, int b) { return (a + b - 1) / b * b; }
 }  // namespace
 
 lq_status launch_gemv(lq_handle h, const lq_problem* probs, int count, cudaStream_t stream) {
+    GemvWorkspace ws;
+    ws.num_sms = h->num_sms;
+    ws.max_smem_optin = h->max_smem_optin;
+    ws.partials = h->partials;
+    ws.partial_floats = h->partial_floats;
+    ws.counters = h->counters;
+    ws.num_counters = h->num_counters;
+    ws.clear_counters = false;
+    return launch_gemv_ws(ws, probs, count, stream);
+}
+
+lq_status launch_gemv_ws(const GemvWorkspace& ws, const lq_problem* probs, int count, cudaStream_t stream) {
     GemvParams P;
     memset(&P, 0, sizeof(P));
     const int M = probs[0].M;
@@ -502,7 +514,7 @@ lq_status launch_gemv(lq_handle h, const lq_problem* probs, int count, cudaStrea
         const int64_t st = (int64_t)probs[i].batch * ((probs[i].N + kGemvStripRows - 1) / kGemvStripRows);
         units += st * S[i];
     }
-    const int64_t want = 3LL * h->num_sms;
+    const int64_t want = 3LL * ws.num_sms;
     if (units < want) {
         for (int i = 0; i < count; ++i) {
             const int max_s = std::max(1, probs[i].K / kStep);
@@ -558,16 +570,19 @@ lq_status launch_gemv(lq_handle h, const lq_problem* probs, int count, cudaStrea
         kc_pad = std::max(kc_pad, round_up(d.KC, kStep));
         if (d.A > 0 && (d.S == 1 || d.parts > d.S)) a_pad = std::max(a_pad, round_up(d.A, 16));
     }
-    if ((size_t)strip > h->num_counters || (size_t)partial_floats > h->partial_floats) return LQ_ERR_WORKSPACE;
+    if ((size_t)strip > ws.num_counters || (size_t)partial_floats > ws.partial_floats) return LQ_ERR_WORKSPACE;
     P.kc_pad = kc_pad;
     P.a_pad = a_pad;
-    P.partials = h->partials;
-    P.counters = h->counters;
+    P.partials = ws.partials;
+    P.counters = ws.counters;
     P.total_units = unit;
     if (unit == 0) return LQ_OK;
     if (unit > 0x7fffffffLL) return LQ_ERR_UNSUPPORTED;
     const size_t smem = (size_t)M * (kc_pad + a_pad) * sizeof(uint16_t);
-    if (smem > (size_t)h->max_smem_optin) return LQ_ERR_UNSUPPORTED;
+    if (smem > (size_t)ws.max_smem_optin) return LQ_ERR_UNSUPPORTED;
+    if (ws.clear_counters && strip > 0 &&
+        cudaMemsetAsync(ws.counters, 0, sizeof(unsigned) * (size_t)strip, stream) != cudaSuccess)
+        return LQ_ERR_CUDA;
     if (P.format == LQ_FMT_2BIT_LM_G32) return run_fmt<LQ_FMT_2BIT_LM_G32>(P, smem, stream);
     return run_fmt<LQ_FMT_NF4_B64>(P, smem, stream);
 }

@@ -65,7 +65,19 @@ lq_status launch_dequant(lq_handle h, int format, const uint8_t* codes, const vo
                          const int32_t* anchor_idx, const uint16_t* anchor_w, int A, int ld_anchor, void* w_out,
                          int out_dtype, int N, int K, cudaStream_t stream);
 
+// Device scratch a GEMV launch may use for split-K partial sums and arrival counters.
+struct GemvWorkspace {
+    int num_sms;
+    int max_smem_optin;
+    float* partials;
+    size_t partial_floats;
+    unsigned* counters;
+    size_t num_counters;
+    bool clear_counters;   // zero the counters this launch uses before it runs
+};
+
 lq_status launch_gemv(lq_handle h, const lq_problem* problems, int count, cudaStream_t stream);
+lq_status launch_gemv_ws(const GemvWorkspace& ws, const lq_problem* problems, int count, cudaStream_t stream);
 
 lq_status launch_gemm(lq_handle h, const lq_problem& p, cudaStream_t stream);
 

@@ -186,6 +186,36 @@ LQ_API lq_status lq_gemm(lq_handle h, int format,
                          const void* x, int x_dtype, void* y, int y_dtype,
                          int M, int N, int K, void* stream);
 
+/*
+ * lq_gemv_noalloc — lq_gemv for callers that cannot allocate device memory.
+ * The paper has no counterpart to this entry point; it exists for deployment.
+ *
+ * Some callers may not call cudaMalloc at all: a plugin running inside a host
+ * application whose own allocator owns every byte of device memory, or a
+ * service that must not grow or fragment its memory after start-up.  Such a
+ * caller cannot create an lq handle, because lq_create allocates the handle's
+ * workspace.  This entry point takes no handle and allocates nothing (no
+ * cudaMalloc, cudaFree or allocating library call).  The caller still provides
+ * x, y and the packed weights; the split-K scratch is a fixed file-scope device
+ * array of 8.06 MiB (16384 arrival counters + 2^21 fp32 partial sums) that every
+ * GPU loading the library holds until the process exits.
+ *
+ * - Runs on the CURRENT device.  Its first call on a device looks up the
+ *   array's device address (cudaGetSymbolAddress); make that first call before
+ *   any stream capture.
+ * - Problems whose split-K scratch exceeds the array return LQ_ERR_WORKSPACE
+ *   before anything is launched (roughly M * N * (K-splits + 1) <= 2^21 fp32).
+ * - All calls share the one array: each call clears the counters it uses on
+ *   `stream` before its kernel runs, and calls that overlap on the GPU (other
+ *   streams, other threads) race and give wrong results.
+ * Arguments, layouts, results and the other errors are those of lq_gemv.
+ */
+LQ_API lq_status lq_gemv_noalloc(int format,
+                                 const uint8_t* codes, const void* scales, const uint16_t* offsets,
+                                 const int32_t* anchor_idx, const uint16_t* anchor_w, int A, int ld_anchor,
+                                 const void* x, int x_dtype, void* y, int y_dtype,
+                                 int M, int N, int K, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

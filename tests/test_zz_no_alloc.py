@@ -1,0 +1,75 @@
+"""lq_gemv_noalloc: the decode product for callers that may not allocate device memory.
+
+Such callers (a plugin inside an application that owns all device memory, or a
+service that must not allocate after start-up) cannot create a handle, because
+lq_create allocates the handle's workspace.  lq_gemv_noalloc takes no handle and
+keeps its split-K scratch in a fixed device array inside the library.  These
+tests call it through the C ABI and compare it with lq_gemv on two calls in a
+row, within the GEMV tolerance (1e-3 * sum_k |W_eff||x|).  The file name keeps it
+last in collection order, so a run that stops at the first failure has already
+run every other test.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+from oracle import oracle as O
+from tests._util import quantized_2bit, x_for
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-3
+
+
+@pytest.fixture(scope="module")
+def lqm():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import bit_weight_quantized_dequant_gb300 as lq
+    lq.build()
+    return lq
+
+
+def _noalloc(L, w, x, y, stream=None):
+    fmt, c, s, o, ai, aw, A, ld = w.args()
+    return L.lq_gemv_noalloc(fmt, c, s, o, ai, aw, A, ld, x.data_ptr(), 1, y.data_ptr(), 0, x.shape[0], w.N, w.K,
+                             stream)
+
+
+def test_noalloc_matches_gemv_on_two_calls_in_a_row(lqm):
+    torch.cuda.set_device(0)
+    L = lqm.load_library()
+    # K = 11008 splits into several K-parts plus an anchor part, so the scratch is used
+    N, K, M = 700, 11008, 4
+    p, outl = quantized_2bit(N, K, seed=77)
+    w = lqm.QuantWeights.from_host(p, lqm.FMT_2BIT)
+    xb = x_for(M, K, "f16", outl, seed=77)
+    x = torch.from_numpy(xb).view(torch.float16).cuda()
+    with lqm.Handle(0) as h:
+        y_ref = h.gemv(w, x).cpu().numpy().astype(np.float64)
+    _, E = O.matmul_ref(O.dequant_2bit(p), xb, "f16")
+    for call in range(2):
+        y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+        st = _noalloc(L, w, x, y)
+        assert st == lqm.LQ_OK, L.lq_status_string(st)
+        torch.cuda.synchronize()
+        got = y.cpu().numpy().astype(np.float64)
+        assert np.all(np.isfinite(got)), f"call {call}: unwritten outputs"
+        assert np.all(np.abs(got - y_ref) <= TOL * E + 1e-30), f"call {call}: differs from lq_gemv"
+
+
+def test_noalloc_rejects_problems_beyond_its_scratch(lqm):
+    L = lqm.load_library()
+    N = K = 8192
+    M = 32
+    codes = torch.zeros((N, K // 4), dtype=torch.uint8, device="cuda")
+    sc = torch.zeros((N, K // 32), dtype=torch.float16, device="cuda")
+    x = torch.zeros((M, K), dtype=torch.float16, device="cuda")
+    y = torch.full((M, N), 3.0, dtype=torch.float32, device="cuda")
+    st = L.lq_gemv_noalloc(1, codes.data_ptr(), sc.data_ptr(), sc.data_ptr(), None, None, 0, 0, x.data_ptr(), 1,
+                           y.data_ptr(), 0, M, N, K, None)
+    assert st == lqm.LQ_ERR_WORKSPACE
+    torch.cuda.synchronize()
+    assert torch.all(y == 3.0)
