@@ -341,7 +341,8 @@ LQ_API lq_status lq_gemv_noalloc(int format, const uint8_t* codes, const void* s
     ws.num_sms = slot.num_sms;
     ws.max_smem_optin = slot.max_smem_optin;
     ws.counters = static_cast<unsigned*>(slot.base);
-    ws.num_counters = kStaticCounters;
+    ws.num_counters = kStaticCounters - 64;              // the last words hold the timeout flag
+    ws.status = reinterpret_cast<int*>(static_cast<unsigned*>(slot.base) + kStaticCounters - 1);
     ws.partials = reinterpret_cast<float*>(static_cast<char*>(slot.base) + kStaticCounters * sizeof(unsigned));
     ws.partial_floats = kStaticPartialFloats;
     ws.clear_counters = true;

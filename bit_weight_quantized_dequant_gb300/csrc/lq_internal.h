@@ -74,10 +74,14 @@ struct GemvWorkspace {
     unsigned* counters;
     size_t num_counters;
     bool clear_counters;   // zero the counters this launch uses before it runs
+    int* status;           // device word raised when a bounded wait runs out
 };
 
 lq_status launch_gemv(lq_handle h, const lq_problem* problems, int count, cudaStream_t stream);
 lq_status launch_gemv_ws(const GemvWorkspace& ws, const lq_problem* problems, int count, cudaStream_t stream);
+bool gemv_tma_eligible(const lq_problem* problems, int count);
+lq_status launch_gemv_regs(const GemvWorkspace& ws, const lq_problem* problems, int count, cudaStream_t stream);
+lq_status launch_gemv_tma(const GemvWorkspace& ws, const lq_problem* problems, int count, cudaStream_t stream);
 
 lq_status launch_gemm(lq_handle h, const lq_problem& p, cudaStream_t stream);
 

@@ -299,3 +299,19 @@ def test_errors_on_device_launch_nothing(lqm, handle):
     torch.cuda.synchronize()
     assert torch.all(y == 7.0)               # nothing ran
     handle.sync()
+
+
+# ---------------------------------------------------------------- both decode kernels on the same shapes
+
+@pytest.mark.parametrize("kernel", ["regs", "tma"])
+@pytest.mark.parametrize("M", [1, 8, 32])
+def test_gemv_kernel_choice_same_results(lqm, handle, monkeypatch, kernel, M):
+    """The register-fed and the TMA-fed kernels both meet the bound on a K % 256 == 0 shape."""
+    monkeypatch.setenv("LQ_GEMV_KERNEL", kernel)
+    N, K = 300, 3072
+    p, outl = quantized_2bit(N, K, seed=50 + M)
+    xb = x_for(M, K, "f16", outl, seed=50 + M)
+    _gemv_check(lqm, handle, p, lqm.FMT_2BIT, xb, "f16")
+    pn = quantized_nf4(N, K, seed=60 + M)
+    xn = x_for(M, K, "bf16", None, seed=60 + M)
+    _gemv_check(lqm, handle, pn, lqm.FMT_NF4, xn, "bf16")
