@@ -39,7 +39,7 @@ namespace {
 
 constexpr int kRows = 128;               // rows per unit
 constexpr int kCWarps = 8;               // consumer warps (16 rows each)
-constexpr int kThreadsT = (kCWarps + 1) * 32;
+constexpr int kThreadsT = (kCWarps + 2) * 32;   // consumers, producer, epilogue
 constexpr int kMaxStages = 4;
 constexpr int kStageBytes = 24576;
 constexpr int kScalesOff = 16384;        // 2-bit scales tile (128 x 32 B) / NF4 absmax tile (128 x 16 B)
@@ -210,20 +210,21 @@ __device__ __forceinline__ void stage_anchor(const uint8_t* tile, const uint16_t
 template <int NT, int FMT>
 __global__ void __launch_bounds__(kThreadsT, 2) gemv_tma_kernel(const __grid_constant__ Params P) {
     extern __shared__ uint8_t smem_raw[];
+    const int NS = P.nstages, M = P.M;
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* stages = base;
-    uint16_t* xslots = reinterpret_cast<uint16_t*>(base + P.nstages * kStageBytes);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(xslots + 2 * P.x_slot_halves);
-    // bars: full[NS], empty[NS], xfull[2], xempty[2], consumer sync
+    uint16_t* xslots = reinterpret_cast<uint16_t*>(base + NS * kStageBytes);
+    float* epi = reinterpret_cast<float*>(xslots + 2 * P.x_slot_halves);          // [2][M][kRows]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(epi + 2 * M * kRows);
+    // bars: full[NS], empty[NS], xfull[2], xempty[2], efull[2], eempty[2]
     __shared__ long long s_unit[2];
+    __shared__ long long s_eunit[2];
     __shared__ int s_abort;
-    __shared__ int s_last;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int NS = P.nstages;
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + NS);
-    const uint32_t xfull0 = smem_u32(bars + 2 * NS), xempty0 = smem_u32(bars + 2 * NS + 2);
-    const uint32_t cbar = smem_u32(bars + 2 * NS + 4);
+    const uint32_t xfull0 = smem_u32(bars + 2 * NS), xempty0 = xfull0 + 16;
+    const uint32_t efull0 = xfull0 + 32, eempty0 = xfull0 + 48;
 
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) {
@@ -233,32 +234,60 @@ __global__ void __launch_bounds__(kThreadsT, 2) gemv_tma_kernel(const __grid_con
         for (int s = 0; s < 2; ++s) {
             mbar_init(xfull0 + 8 * s, 1);
             mbar_init(xempty0 + 8 * s, kCWarps);
+            mbar_init(efull0 + 8 * s, kCWarps);
+            mbar_init(eempty0 + 8 * s, 1);
         }
-        mbar_init(cbar, kCWarps);
         s_abort = 0;
         fence_mbar_init();
     }
     __syncthreads();
-    volatile int* abort = &s_abort;
-    const int M = P.M;
     constexpr int SC = FMT == LQ_FMT_2BIT_LM_G32 ? kSC2 : kSCNF4;
+    // Every thread gives up only on its own timeout: all threads of a role wait on the
+    // same barriers in the same order, so they stop at the same place.
+    int own_abort = 0;
+    volatile int* abort = &own_abort;
 
     if (warp == kCWarps) {
-        // ------------------------------------------------------------ producer
+        // ------------------------------------------------------------ producer (TMA)
         if (lane == 0) {
             for (int i = 0; i < P.count; ++i) {
                 prefetch_tensormap(&P.maps[i].codes);
+                prefetch_tensormap(&P.maps[i].scales);
                 if (FMT == LQ_FMT_2BIT_LM_G32) {
-                    prefetch_tensormap(&P.maps[i].scales);
                     prefetch_tensormap(&P.maps[i].offsets);
                     if (P.d[i].A > 0) prefetch_tensormap(&P.maps[i].anchors);
-                } else {
-                    prefetch_tensormap(&P.maps[i].scales);
                 }
             }
-            pdl_wait();  // the x pre-pass has finished writing
             int xs = 0, xph = 0, slot = 0, ph = 0;
-            bool ok = true;
+            bool ok = true, first = true;
+            // weight tiles of stage `idx` of unit U (code stages first, then anchor stages)
+            auto issue_stage = [&](const Unit& U, int idx) -> bool {
+                if (!mbar_wait_bounded(empty0 + 8 * slot, ph ^ 1, abort, P.status)) return false;
+                const uint32_t dst = smem_u32(stages + slot * kStageBytes), fb = full0 + 8 * slot;
+                const int row0 = U.strip * kRows;
+                const int nst = (U.klen + SC - 1) / SC;
+                if (idx < nst) {
+                    const int col = U.k0 + idx * SC;
+                    if (FMT == LQ_FMT_2BIT_LM_G32) {
+                        mbar_arrive_expect_tx(fb, 16384 + 4096 + 4096);
+                        tma_load_3d(dst, &P.maps[U.p].codes, col / 4, row0, (int)U.l, fb);
+                        tma_load_3d(dst + kScalesOff, &P.maps[U.p].scales, col / 32, row0, (int)U.l, fb);
+                        tma_load_3d(dst + kOffsetsOff, &P.maps[U.p].offsets, col / 32, row0, (int)U.l, fb);
+                    } else {
+                        mbar_arrive_expect_tx(fb, 16384 + 2048);
+                        tma_load_3d(dst, &P.maps[U.p].codes, col / 2, row0, (int)U.l, fb);
+                        tma_load_3d(dst + kScalesOff, &P.maps[U.p].scales, col / 64, row0, (int)U.l, fb);
+                    }
+                } else {
+                    mbar_arrive_expect_tx(fb, 16384);
+                    tma_load_3d(dst, &P.maps[U.p].anchors, U.a0 + (idx - nst) * kSCA, row0, (int)U.l, fb);
+                }
+                if (++slot == NS) {
+                    slot = 0;
+                    ph ^= 1;
+                }
+                return true;
+            };
             while (ok) {
                 const unsigned claimed = atomicAdd(P.sched, 1u);
                 const int64_t u = (int64_t)claimed < P.total_units ? (int64_t)claimed : -1;
@@ -270,6 +299,16 @@ __global__ void __launch_bounds__(kThreadsT, 2) gemv_tma_kernel(const __grid_con
                 }
                 const Unit U = decode_unit(P, u);
                 const Desc& D = P.d[U.p];
+                const int total = (U.klen + SC - 1) / SC + (U.alen + kSCA - 1) / kSCA;
+                // the first unit's weight tiles do not depend on x: start them before waiting
+                // for the x pre-pass (at most a ring's worth, the consumers need x to drain it)
+                const int pre = first ? min(total, NS) : 0;
+                for (int i = 0; i < pre && ok; ++i) ok = issue_stage(U, i);
+                if (!ok) break;
+                if (first) {
+                    pdl_wait();
+                    first = false;
+                }
                 const uint32_t code_b = (uint32_t)(M * round_up_d(U.klen, 256) * 2);
                 const uint32_t anch_b = (uint32_t)(M * round_up_d(U.alen, kSCA) * 2);
                 const uint32_t xdst = smem_u32(xslots + (size_t)xs * P.x_slot_halves);
@@ -283,38 +322,7 @@ __global__ void __launch_bounds__(kThreadsT, 2) gemv_tma_kernel(const __grid_con
                               xfull0 + 8 * xs);
                 xs ^= 1;
                 if (xs == 0) xph ^= 1;
-                const int row0 = U.strip * kRows;
-                const int nst = (U.klen + SC - 1) / SC;
-                for (int st = 0; st < nst && ok; ++st) {
-                    if (!(ok = mbar_wait_bounded(empty0 + 8 * slot, ph ^ 1, abort, P.status))) break;
-                    const uint32_t dst = smem_u32(stages + slot * kStageBytes), fb = full0 + 8 * slot;
-                    const int col = U.k0 + st * SC;
-                    if (FMT == LQ_FMT_2BIT_LM_G32) {
-                        mbar_arrive_expect_tx(fb, 16384 + 4096 + 4096);
-                        tma_load_3d(dst, &P.maps[U.p].codes, col / 4, row0, (int)U.l, fb);
-                        tma_load_3d(dst + kScalesOff, &P.maps[U.p].scales, col / 32, row0, (int)U.l, fb);
-                        tma_load_3d(dst + kOffsetsOff, &P.maps[U.p].offsets, col / 32, row0, (int)U.l, fb);
-                    } else {
-                        mbar_arrive_expect_tx(fb, 16384 + 2048);
-                        tma_load_3d(dst, &P.maps[U.p].codes, col / 2, row0, (int)U.l, fb);
-                        tma_load_3d(dst + kScalesOff, &P.maps[U.p].scales, col / 64, row0, (int)U.l, fb);
-                    }
-                    if (++slot == NS) {
-                        slot = 0;
-                        ph ^= 1;
-                    }
-                }
-                const int nas = (U.alen + kSCA - 1) / kSCA;
-                for (int st = 0; st < nas && ok; ++st) {
-                    if (!(ok = mbar_wait_bounded(empty0 + 8 * slot, ph ^ 1, abort, P.status))) break;
-                    const uint32_t dst = smem_u32(stages + slot * kStageBytes), fb = full0 + 8 * slot;
-                    mbar_arrive_expect_tx(fb, 16384);
-                    tma_load_3d(dst, &P.maps[U.p].anchors, U.a0 + st * kSCA, row0, (int)U.l, fb);
-                    if (++slot == NS) {
-                        slot = 0;
-                        ph ^= 1;
-                    }
-                }
+                for (int i = pre; i < total && ok; ++i) ok = issue_stage(U, i);
             }
             if (!ok) {
                 // unwinding after a timeout: let the copies already issued land (bounded)
@@ -335,26 +343,69 @@ __global__ void __launch_bounds__(kThreadsT, 2) gemv_tma_kernel(const __grid_con
         return;
     }
 
+    if (warp == kCWarps + 1) {
+        // ------------------------------------------------------------ epilogue warp
+        int eb = 0, eph = 0;
+        for (;;) {
+            if (!mbar_wait_bounded(efull0 + 8 * eb, eph, abort, P.status)) break;
+            const int64_t u = s_eunit[eb];
+            if (u < 0) break;
+            const Unit U = decode_unit(P, u);
+            const Desc& D = P.d[U.p];
+            const float* acc = epi + (size_t)eb * M * kRows;
+            const int N = D.N;
+            void* y = static_cast<char*>(D.y) + U.l * D.stride_y;
+            if (D.parts == 1) {
+                for (int idx = lane; idx < M * kRows; idx += 32) {
+                    const int m = idx / kRows, r = idx - m * kRows, n = U.strip * kRows + r;
+                    if (n < N) store_out(y, (size_t)m * N + n, P.y_dtype, acc[idx]);
+                }
+            } else {
+                const int64_t strip_id = D.strip_begin + U.l * D.strips + U.strip;
+                float* strip_base = P.partials + D.partial_begin + (U.l * D.strips + U.strip) * (int64_t)D.parts * M * kRows;
+                float* mine = strip_base + (int64_t)U.part * M * kRows;
+                for (int idx = lane; idx < M * kRows; idx += 32) mine[idx] = acc[idx];
+                __threadfence();
+                __syncwarp();
+                unsigned last = 0;
+                if (lane == 0) last = atomicAdd(P.counters + strip_id, 1u) == (unsigned)(D.parts - 1);
+                last = __shfl_sync(0xffffffffu, last, 0);
+                if (last) {
+                    __threadfence();
+                    for (int idx = lane; idx < M * kRows; idx += 32) {
+                        const int m = idx / kRows, r = idx - m * kRows, n = U.strip * kRows + r;
+                        if (n >= N) continue;
+                        float sum = 0.f;
+                        for (int pp = 0; pp < D.parts; ++pp) sum += __ldcg(strip_base + (int64_t)pp * M * kRows + idx);
+                        store_out(y, (size_t)m * N + n, P.y_dtype, sum);
+                    }
+                    if (lane == 0) P.counters[strip_id] = 0u;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(eempty0 + 8 * eb);
+            eb ^= 1;
+            if (eb == 0) eph ^= 1;
+        }
+        return;
+    }
+
     // ---------------------------------------------------------------- consumers
     const int g = lane >> 2, t = lane & 3;
     uint32_t TL[4], TH[4];
     if (FMT == LQ_FMT_NF4_B64) nf4_tables(TL, TH);
-    // Consumers give up only on their own timeouts, never because another thread did: all
-    // consumer warps wait on the same barriers in the same order, so they stop at the same place.
-    int own_abort = 0;
-    abort = &own_abort;
-    int xs = 0, xph = 0, slot = 0, ph = 0, cph = 0;
-    auto consumer_sync = [&]() -> bool {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(cbar);
-        const bool r = mbar_wait_bounded(cbar, cph, abort, P.status);
-        cph ^= 1;
-        return r;
-    };
+    int xs = 0, xph = 0, slot = 0, ph = 0, eb = 0, eph = 0;
     for (;;) {
         if (!mbar_wait_bounded(xfull0 + 8 * xs, xph, abort, P.status)) break;
         const int64_t u = s_unit[xs];
-        if (u < 0) break;
+        if (u < 0) {
+            // tell the epilogue warp there is no more work
+            if (!mbar_wait_bounded(eempty0 + 8 * eb, eph ^ 1, abort, P.status)) break;
+            if (tid == 0) s_eunit[eb] = -1;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(efull0 + 8 * eb);
+            break;
+        }
         const Unit U = decode_unit(P, u);
         const Desc& D = P.d[U.p];
         const uint16_t* xb = xslots + (size_t)xs * P.x_slot_halves;
@@ -397,60 +448,27 @@ __global__ void __launch_bounds__(kThreadsT, 2) gemv_tma_kernel(const __grid_con
         xs ^= 1;
         if (xs == 0) xph ^= 1;
 
-        // ---- epilogue
-        const int N = D.N;
-        void* y = static_cast<char*>(D.y) + U.l * D.stride_y;
-        const int rg = U.strip * kRows + 16 * warp + g, rg8 = rg + 8;
-        if (D.parts == 1) {
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                const int m0 = 8 * nt + 2 * t, m1 = m0 + 1;
-                if (rg < N) {
-                    if (m0 < M) store_out(y, (size_t)m0 * N + rg, P.y_dtype, acc[nt][0]);
-                    if (m1 < M) store_out(y, (size_t)m1 * N + rg, P.y_dtype, acc[nt][1]);
-                }
-                if (rg8 < N) {
-                    if (m0 < M) store_out(y, (size_t)m0 * N + rg8, P.y_dtype, acc[nt][2]);
-                    if (m1 < M) store_out(y, (size_t)m1 * N + rg8, P.y_dtype, acc[nt][3]);
-                }
-            }
-            continue;
-        }
-        const int64_t strip_id = D.strip_begin + U.l * D.strips + U.strip;
-        float* strip_base = P.partials + D.partial_begin + (U.l * D.strips + U.strip) * (int64_t)D.parts * M * kRows;
-        float* mine = strip_base + (int64_t)U.part * M * kRows;
+        // ---- hand the accumulators to the epilogue warp
+        if (!mbar_wait_bounded(eempty0 + 8 * eb, eph ^ 1, abort, P.status)) break;
+        float* out = epi + (size_t)eb * M * kRows;
         const int r = 16 * warp + g;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             const int m0 = 8 * nt + 2 * t, m1 = m0 + 1;
             if (m0 < M) {
-                mine[m0 * kRows + r] = acc[nt][0];
-                mine[m0 * kRows + r + 8] = acc[nt][2];
+                out[m0 * kRows + r] = acc[nt][0];
+                out[m0 * kRows + r + 8] = acc[nt][2];
             }
             if (m1 < M) {
-                mine[m1 * kRows + r] = acc[nt][1];
-                mine[m1 * kRows + r + 8] = acc[nt][3];
+                out[m1 * kRows + r] = acc[nt][1];
+                out[m1 * kRows + r + 8] = acc[nt][3];
             }
         }
-        __threadfence();
-        if (!consumer_sync()) break;
-        if (tid == 0) {
-            const unsigned old = atomicAdd(P.counters + strip_id, 1u);
-            s_last = (old == (unsigned)(D.parts - 1));
-        }
-        if (!consumer_sync()) break;
-        if (s_last) {
-            __threadfence();
-            for (int idx = tid; idx < M * kRows; idx += kCWarps * 32) {
-                const int m = idx / kRows, rr = idx - m * kRows;
-                const int n = U.strip * kRows + rr;
-                if (n >= N) continue;
-                float sum = 0.f;
-                for (int pp = 0; pp < D.parts; ++pp) sum += __ldcg(strip_base + ((int64_t)pp * M + m) * kRows + rr);
-                store_out(y, (size_t)m * N + n, P.y_dtype, sum);
-            }
-            if (tid == 0) P.counters[strip_id] = 0u;
-        }
+        if (tid == 0) s_eunit[eb] = u;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(efull0 + 8 * eb);
+        eb ^= 1;
+        if (eb == 0) eph ^= 1;
     }
 }
 
@@ -465,28 +483,22 @@ struct PrepDesc {
     uint16_t* xaperm;
     int64_t xperm_stride, xaperm_stride;   // halves
     int K, Kp, A, a_pad, batch;
-    int64_t work_begin;        // first flat work item of this problem
+    int64_t work_begin;        // first work item (8 halves) of this problem in pass 1
+    int64_t anchor_begin;      // first work item (one anchor of one token) in pass 2
 };
 
 struct PrepParams {
     PrepDesc d[kMaxGroup];
     int count, M, x_bf16, format;
-    int64_t total;
+    int64_t total, total_anchor;
 };
 
-__device__ __forceinline__ bool is_anchor(const int32_t* idx, int A, int k) {
-    int lo = 0, hi = A;
-    while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        const int v = __ldg(idx + mid);
-        if (v < k) lo = mid + 1;
-        else hi = mid;
-    }
-    return lo < A && __ldg(idx + lo) == k;
+__device__ __forceinline__ uint16_t to_half_bits(uint16_t raw, int x_bf16) {
+    return x_bf16 ? __half_as_ushort(__float2half_rn(bf16_bits_to_float(raw))) : raw;
 }
 
-// Output-major: each thread writes 8 consecutive binary16 of the fragment-ordered
-// copy (one 16-byte store) and gathers its 8 source columns (L1-resident x row).
+// Pass 1, output-major: each thread writes 8 consecutive binary16 of the fragment-ordered
+// copy of x (one 16-byte store), gathering its 8 source columns from the x row.
 __global__ void __launch_bounds__(256) xprep_kernel(const __grid_constant__ PrepParams P) {
     pdl_launch_dependents();
     const int M = P.M;
@@ -495,46 +507,66 @@ __global__ void __launch_bounds__(256) xprep_kernel(const __grid_constant__ Prep
         while (p + 1 < P.count && w >= P.d[p + 1].work_begin) ++p;
         const PrepDesc& D = P.d[p];
         const int64_t local = w - D.work_begin;                 // in units of 8 halves
-        const int64_t per_member = (int64_t)M * (D.Kp + D.a_pad) / 8;
+        const int64_t per_member = (int64_t)M * D.Kp / 8;
         const int64_t l = local / per_member;
-        const int64_t rem = local - l * per_member;
+        const int64_t d0 = 8 * (local - l * per_member);
         const uint16_t* x = reinterpret_cast<const uint16_t*>(reinterpret_cast<const char*>(D.x) + l * D.stride_x);
-        const int32_t* aidx = D.anchor_idx
-            ? reinterpret_cast<const int32_t*>(reinterpret_cast<const char*>(D.anchor_idx) + l * D.stride_anchor_idx)
-            : nullptr;
-        const bool code_part = rem < (int64_t)M * D.Kp / 8;
-        const int64_t d0 = 8 * (code_part ? rem : rem - (int64_t)M * D.Kp / 8);   // first half of the 8
-        const int line = (int)(d0 >> 4), pos0 = (int)(d0 & 15);               // 16-half line, position 0 or 8
+        const int line = (int)(d0 >> 4), pos0 = (int)(d0 & 15);
         const int bi = line / M, m = line - bi * M;
         uint16_t v[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             const int pos = pos0 + e, tt = pos >> 2, hh = pos & 3;
-            uint16_t raw = 0;
-            bool have = false;
-            if (code_part) {
-                int k;
-                if (P.format == LQ_FMT_2BIT_LM_G32) {
-                    k = (bi >> 4) * 256 + tt * 64 + ((bi >> 2) & 3) * 16 + hh * 4 + (bi & 3);
-                } else {
-                    k = (bi >> 2) * 64 + tt * 16 + (bi & 3) * 4 + hh;
-                }
-                if (k < D.K && !(D.A > 0 && is_anchor(aidx, D.A, k))) {
-                    raw = x[(int64_t)m * D.K + k];
-                    have = true;
-                }
-            } else {
-                const int a = 16 * bi + 2 * tt + (hh & 1) + 8 * (hh >> 1);
-                if (a < D.A) {
-                    raw = x[(int64_t)m * D.K + __ldg(aidx + a)];
-                    have = true;
-                }
-            }
-            v[e] = have ? (P.x_bf16 ? __half_as_ushort(__float2half_rn(bf16_bits_to_float(raw))) : raw) : 0;
+            const int k = P.format == LQ_FMT_2BIT_LM_G32
+                ? (bi >> 4) * 256 + tt * 64 + ((bi >> 2) & 3) * 16 + hh * 4 + (bi & 3)
+                : (bi >> 2) * 64 + tt * 16 + (bi & 3) * 4 + hh;
+            v[e] = k < D.K ? to_half_bits(x[(int64_t)m * D.K + k], P.x_bf16) : (uint16_t)0;
         }
-        uint16_t* dst = (code_part ? D.xperm + l * D.xperm_stride : D.xaperm + l * D.xaperm_stride) + d0;
+        uint16_t* dst = D.xperm + l * D.xperm_stride + d0;
         *reinterpret_cast<uint4*>(dst) = make_uint4((uint32_t)v[0] | ((uint32_t)v[1] << 16), (uint32_t)v[2] | ((uint32_t)v[3] << 16),
                                                     (uint32_t)v[4] | ((uint32_t)v[5] << 16), (uint32_t)v[6] | ((uint32_t)v[7] << 16));
+    }
+}
+
+// Pass 2 (after pass 1): zero x at the anchor columns (the anchors replace those weights)
+// and write x gathered at the anchor columns, zero-padded to a multiple of 64.
+__global__ void __launch_bounds__(256) xanchor_kernel(const __grid_constant__ PrepParams P) {
+    pdl_launch_dependents();
+    pdl_wait();  // pass 1 has finished writing
+    const int M = P.M;
+    for (int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; w < P.total_anchor; w += (int64_t)gridDim.x * blockDim.x) {
+        int p = 0;
+        while (p + 1 < P.count && w >= P.d[p + 1].anchor_begin) ++p;
+        const PrepDesc& D = P.d[p];
+        const int64_t local = w - D.anchor_begin;
+        const int64_t per_member = (int64_t)M * D.a_pad;
+        const int64_t l = local / per_member;
+        const int rem = (int)(local - l * per_member);
+        const int m = rem / D.a_pad, a = rem - m * D.a_pad;
+        uint16_t v = 0;
+        if (a < D.A) {
+            const uint16_t* x = reinterpret_cast<const uint16_t*>(reinterpret_cast<const char*>(D.x) + l * D.stride_x);
+            const int32_t* aidx =
+                reinterpret_cast<const int32_t*>(reinterpret_cast<const char*>(D.anchor_idx) + l * D.stride_anchor_idx);
+            const int k = __ldg(aidx + a);
+            v = to_half_bits(x[(int64_t)m * D.K + k], P.x_bf16);
+            int bi, tt, hh;
+            if (P.format == LQ_FMT_2BIT_LM_G32) {
+                const int r = k & 255, e = r & 15;
+                tt = r >> 6;
+                bi = (k >> 8) * 16 + ((r >> 4) & 3) * 4 + (e & 3);
+                hh = e >> 2;
+            } else {
+                const int r = k & 63, e = r & 15;
+                tt = r >> 4;
+                bi = (k >> 6) * 4 + (e >> 2);
+                hh = e & 3;
+            }
+            D.xperm[l * D.xperm_stride + ((int64_t)bi * M + m) * 16 + tt * 4 + hh] = 0;
+        }
+        const int s = a & 15;
+        const int tt = (s & 7) >> 1, hh = (s & 1) + 2 * (s >> 3);
+        D.xaperm[l * D.xaperm_stride + ((int64_t)(a >> 4) * M + m) * 16 + tt * 4 + hh] = v;
     }
 }
 
@@ -626,7 +658,7 @@ lq_status launch_gemv_tma(const GemvWorkspace& ws, const lq_problem* probs, int 
     Q.x_bf16 = probs[0].x_dtype == LQ_BF16;
 
     // columns per split: the x slot (M x KC binary16) stays <= 16 KiB
-    int kc_target = M <= 4 ? 2048 : (M <= 8 ? 1024 : 512);
+    int kc_target = M <= 4 ? 2048 : 512;
     kc_target = std::max(kc_target, SC);
 
     // first pass: splits
@@ -664,7 +696,7 @@ lq_status launch_gemv_tma(const GemvWorkspace& ws, const lq_problem* probs, int 
         }
     }
 
-    int64_t unit = 0, strip = 0, partial_floats = 0, prep = 0, xperm_halves = 0;
+    int64_t unit = 0, strip = 0, partial_floats = 0, prep = 0, prep_a = 0, xperm_halves = 0;
     int x_slot = 0;
     for (int i = 0; i < count; ++i) {
         const lq_problem& q = probs[i];
@@ -711,7 +743,9 @@ lq_status launch_gemv_tma(const GemvWorkspace& ws, const lq_problem* probs, int 
         e.xperm_stride = d.xperm_stride;
         e.xaperm_stride = d.xaperm_stride;
         e.work_begin = prep;
-        prep += (int64_t)q.batch * M * (d.Kp + d.a_pad) / 8;
+        prep += (int64_t)q.batch * M * d.Kp / 8;
+        e.anchor_begin = prep_a;
+        prep_a += (int64_t)q.batch * M * d.a_pad;
         xperm_halves += (int64_t)q.batch * M * (d.Kp + d.a_pad);
     }
     // workspace: [partials | x pre-pass output] in the float area, [sched(2) | strip counters] in the counters
@@ -736,6 +770,7 @@ lq_status launch_gemv_tma(const GemvWorkspace& ws, const lq_problem* probs, int 
     P.counters = ws.counters + 2;
     P.status = ws.status;
     Q.total = prep;
+    Q.total_anchor = prep_a;
 
     // tensor maps
     for (int i = 0; i < count; ++i) {
@@ -764,13 +799,27 @@ lq_status launch_gemv_tma(const GemvWorkspace& ws, const lq_problem* probs, int 
     if (ws.clear_counters && cudaMemsetAsync(ws.counters, 0, sizeof(unsigned) * (size_t)(strip + 2), stream) != cudaSuccess)
         return LQ_ERR_CUDA;
 
-    // pre-pass then the main kernel (programmatic dependent launch)
+    // x passes, then the main kernel, chained by programmatic dependent launch
     const int prep_grid = (int)std::min<int64_t>((Q.total + 255) / 256, (int64_t)ws.num_sms * 8);
     xprep_kernel<<<std::max(1, prep_grid), 256, 0, stream>>>(Q);
     if (cudaPeekAtLastError() != cudaSuccess) return LQ_ERR_CUDA;
+    if (Q.total_anchor > 0) {
+        cudaLaunchConfig_t cfg;
+        memset(&cfg, 0, sizeof(cfg));
+        cfg.gridDim = dim3((unsigned)std::max<int64_t>(1, std::min<int64_t>((Q.total_anchor + 255) / 256, (int64_t)ws.num_sms * 8)));
+        cfg.blockDim = dim3(256);
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, xanchor_kernel, Q) != cudaSuccess) return LQ_ERR_CUDA;
+    }
 
     auto smem_for = [&](int ns) {
-        return 1024 + (size_t)ns * kStageBytes + 2 * (size_t)P.x_slot_halves * 2 + (2 * ns + 5) * 8;
+        return 1024 + (size_t)ns * kStageBytes + 2 * (size_t)P.x_slot_halves * 2 + 2 * (size_t)M * kRows * 4 +
+               (2 * ns + 8) * 8;
     };
     // two CTAs per SM when they fit (4 stages, else 3), otherwise one CTA with 4 stages
     int per_sm = 2;
