@@ -490,14 +490,14 @@ lq_status launch_gemv(lq_handle h, const lq_problem* probs, int count, cudaStrea
     return launch_gemv_ws(ws, probs, count, stream);
 }
 
-// The TMA-fed kernel takes every problem whose K is a multiple of 256; the
-// register-fed kernel below covers the rest (any K % 32 == 0).
+// The streaming kernel takes every launch whose K are multiples of 256; the
+// split-K kernel below covers the rest (any K % 32 == 0).
 // LQ_GEMV_KERNEL=regs forces the register-fed kernel (for comparisons and tests).
 lq_status launch_gemv_ws(const GemvWorkspace& ws, const lq_problem* probs, int count, cudaStream_t stream) {
     const char* force = getenv("LQ_GEMV_KERNEL");
     const bool regs_only = force && strcmp(force, "regs") == 0;
-    if (!regs_only && gemv_tma_eligible(probs, count)) {
-        const lq_status s = launch_gemv_tma(ws, probs, count, stream);
+    if (!regs_only && gemv_stream_eligible(probs, count)) {
+        const lq_status s = launch_gemv_stream(ws, probs, count, stream);
         if (s != LQ_ERR_UNSUPPORTED) return s;
     }
     return launch_gemv_regs(ws, probs, count, stream);

@@ -1,0 +1,503 @@
+// Streaming decode GEMV (the fast path of lq_gemv / lq_gemv_grouped for K % 256 == 0).
+//
+// Decode reads every weight once per token (otf-llm 4.0.1 README, section 1, "The
+// Memory-Bound Bottleneck"), so the kernel is a bandwidth streamer with the
+// section 3/4 reconstruction done in registers:
+//
+//  * Two small pre-pass kernels write x once per call as binary16 in mma-fragment
+//    order with the anchor columns zeroed (anchors replace those weights), and x
+//    gathered at the anchor columns.  They chain to the main kernel by programmatic
+//    dependent launch; each main CTA issues its first weight loads before it waits.
+//  * One CTA = 8 warps over one tile of 16 x (8 / ks) rows and the full K: the ks
+//    warps of a row tile split K into contiguous slices, so no partial sums leave
+//    the CTA (shared-memory reduction at the end, no atomics, no workspace).
+//  * Each thread streams its two rows with 16-byte loads (64 codes per row per
+//    256-column step) and 4-byte scale/offset loads, two steps ahead of use.
+//  * x fragments come straight from the pre-permuted copy (L1-resident, one 8-byte
+//    load per mma).  Lanes whose token does not exist load harmless neighbouring
+//    values: they only feed output columns that are never stored.
+//  * Dequantization is a PRMT lookup in byte-split binary16 tables of
+//    fmaf(S, C[q], Z); the multiply-accumulate is mma.sync m16n8k16 (binary16 in,
+//    fp32 accumulate) with tokens as the n dimension.  Anchors are extra k-blocks
+//    of the same accumulator, shared round-robin by the warps of a row tile.
+//  * NF4: eight byte-split registers hold the 16 binary16 levels; each mma block
+//    stays inside one 64-column block so its fp32 absmax scales the partial sums.
+
+#include <algorithm>
+#include <cstring>
+
+#include "lq_common.cuh"
+#include "lq_dq.cuh"
+#include "lq_internal.h"
+#include "lq_tma.cuh"
+
+namespace lq {
+namespace {
+
+constexpr int kWarps = 8;
+constexpr int kThreadsS = kWarps * 32;
+constexpr int kXPad = 256;   // halves of padding after each x copy (fragment loads of absent tokens)
+
+// ---- pre-pass: x -> binary16, anchors zeroed, fragment order ------------------------
+
+struct PrepDesc {
+    const uint16_t* x;
+    int64_t stride_x;          // bytes
+    const int32_t* anchor_idx;
+    int64_t stride_anchor_idx; // bytes
+    uint16_t* xperm;
+    uint16_t* xaperm;
+    int64_t xperm_stride, xaperm_stride;   // halves
+    int K, Kp, A, a_pad, batch;
+    int64_t work_begin;        // first work item (8 halves) of this problem in pass 1
+    int64_t anchor_begin;      // first work item (one anchor of one token) in pass 2
+};
+
+struct PrepParams {
+    PrepDesc d[kMaxGroup];
+    int count, M, x_bf16, format;
+    int64_t total, total_anchor;
+};
+
+__device__ __forceinline__ uint16_t to_half_bits(uint16_t raw, int x_bf16) {
+    return x_bf16 ? __half_as_ushort(__float2half_rn(bf16_bits_to_float(raw))) : raw;
+}
+
+// Pass 1, output-major: each thread writes 8 consecutive binary16 of the fragment-ordered
+// copy of x (one 16-byte store), gathering its 8 source columns from the x row.
+__global__ void __launch_bounds__(256) xprep_kernel(const __grid_constant__ PrepParams P) {
+    pdl_launch_dependents();
+    const int M = P.M;
+    for (int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; w < P.total; w += (int64_t)gridDim.x * blockDim.x) {
+        int p = 0;
+        while (p + 1 < P.count && w >= P.d[p + 1].work_begin) ++p;
+        const PrepDesc& D = P.d[p];
+        const int64_t local = w - D.work_begin;                 // in units of 8 halves
+        const int64_t per_member = (int64_t)M * D.Kp / 8;
+        const int64_t l = local / per_member;
+        const int64_t d0 = 8 * (local - l * per_member);
+        const uint16_t* x = reinterpret_cast<const uint16_t*>(reinterpret_cast<const char*>(D.x) + l * D.stride_x);
+        const int line = (int)(d0 >> 4), pos0 = (int)(d0 & 15);
+        const int bi = line / M, m = line - bi * M;
+        uint16_t v[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int pos = pos0 + e, tt = pos >> 2, hh = pos & 3;
+            const int k = P.format == LQ_FMT_2BIT_LM_G32
+                ? (bi >> 4) * 256 + tt * 64 + ((bi >> 2) & 3) * 16 + hh * 4 + (bi & 3)
+                : (bi >> 2) * 64 + tt * 16 + (bi & 3) * 4 + hh;
+            v[e] = k < D.K ? to_half_bits(x[(int64_t)m * D.K + k], P.x_bf16) : (uint16_t)0;
+        }
+        uint16_t* dst = D.xperm + l * D.xperm_stride + d0;
+        *reinterpret_cast<uint4*>(dst) = make_uint4((uint32_t)v[0] | ((uint32_t)v[1] << 16), (uint32_t)v[2] | ((uint32_t)v[3] << 16),
+                                                    (uint32_t)v[4] | ((uint32_t)v[5] << 16), (uint32_t)v[6] | ((uint32_t)v[7] << 16));
+    }
+}
+
+// Pass 2 (after pass 1): zero x at the anchor columns (the anchors replace those weights)
+// and write x gathered at the anchor columns, zero-padded to a multiple of 64.
+__global__ void __launch_bounds__(256) xanchor_kernel(const __grid_constant__ PrepParams P) {
+    pdl_launch_dependents();
+    pdl_wait();  // pass 1 has finished writing
+    const int M = P.M;
+    for (int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; w < P.total_anchor; w += (int64_t)gridDim.x * blockDim.x) {
+        int p = 0;
+        while (p + 1 < P.count && w >= P.d[p + 1].anchor_begin) ++p;
+        const PrepDesc& D = P.d[p];
+        const int64_t local = w - D.anchor_begin;
+        const int64_t per_member = (int64_t)M * D.a_pad;
+        const int64_t l = local / per_member;
+        const int rem = (int)(local - l * per_member);
+        const int m = rem / D.a_pad, a = rem - m * D.a_pad;
+        uint16_t v = 0;
+        if (a < D.A) {
+            const uint16_t* x = reinterpret_cast<const uint16_t*>(reinterpret_cast<const char*>(D.x) + l * D.stride_x);
+            const int32_t* aidx =
+                reinterpret_cast<const int32_t*>(reinterpret_cast<const char*>(D.anchor_idx) + l * D.stride_anchor_idx);
+            const int k = __ldg(aidx + a);
+            v = to_half_bits(x[(int64_t)m * D.K + k], P.x_bf16);
+            int bi, tt, hh;
+            if (P.format == LQ_FMT_2BIT_LM_G32) {
+                const int r = k & 255, e = r & 15;
+                tt = r >> 6;
+                bi = (k >> 8) * 16 + ((r >> 4) & 3) * 4 + (e & 3);
+                hh = e >> 2;
+            } else {
+                const int r = k & 63, e = r & 15;
+                tt = r >> 4;
+                bi = (k >> 6) * 4 + (e >> 2);
+                hh = e & 3;
+            }
+            D.xperm[l * D.xperm_stride + ((int64_t)bi * M + m) * 16 + tt * 4 + hh] = 0;
+        }
+        const int s = a & 15;
+        const int tt = (s & 7) >> 1, hh = (s & 1) + 2 * (s >> 3);
+        D.xaperm[l * D.xaperm_stride + ((int64_t)(a >> 4) * M + m) * 16 + tt * 4 + hh] = v;
+    }
+}
+
+
+struct SDesc {
+    const uint8_t* codes;
+    const void* scales;
+    const uint16_t* offsets;
+    const uint16_t* anchor_w;
+    const uint16_t* xperm;      // [batch][K/16][M][16] (+ padding)
+    const uint16_t* xaperm;     // [batch][a_pad/16][M][16] (+ padding)
+    void* y;
+    int64_t stride_codes, stride_scales, stride_offsets, stride_anchor_w, stride_y;
+    int64_t xperm_stride, xaperm_stride;   // halves
+    int N, K, A, ld_anchor, batch, ks, tiles;   // ks: warps per row tile (K slices); tiles: CTAs per member
+    int64_t block_begin;
+};
+
+struct SParams {
+    SDesc d[kMaxGroup];
+    int count, M, y_dtype;
+};
+
+template <int NT, int MT>
+__device__ __forceinline__ void mma_xg(float (&acc)[NT][4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                       const uint2 (&b)[NT]) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) mma_f16_16816(acc[nt], a0, a1, a2, a3, b[nt].x, b[nt].y);
+}
+
+// x fragment of mma block bi for this thread (n-tile nt): 8 bytes from the permuted copy
+template <int MT>
+__device__ __forceinline__ uint2 xfrag(const uint16_t* xp, int bi, int M, int nt) {
+    const int MM = MT > 0 ? MT : M;
+    return __ldg(reinterpret_cast<const uint2*>(xp + (bi * MM + 8 * nt) * 16));
+}
+
+struct Step2 {
+    uint4 c0, c1;
+    uint32_t s0, z0, s1, z1;
+};
+
+struct StepNF4 {
+    uint2 c0[4], c1[4];
+    float a0[4], a1[4];
+};
+
+template <int FMT, int MT, int NT>
+__global__ void __launch_bounds__(kThreadsS) gemv_stream_kernel(const __grid_constant__ SParams P) {
+    __shared__ float red[kWarps][16][(NT * 8) + 1];
+    const int64_t bid = blockIdx.x;
+    int p = 0;
+    while (p + 1 < P.count && bid >= P.d[p + 1].block_begin) ++p;
+    const SDesc& D = P.d[p];
+    const int64_t local = bid - D.block_begin;
+    const int64_t l = local / D.tiles;
+    const int tile = (int)(local - l * D.tiles);
+    const int M = MT > 0 ? MT : P.M;
+    const int N = D.N, K = D.K, ks = D.ks, rtiles = kWarps / ks;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int rt = warp / ks, slice = warp - rt * ks;
+    const int rg = (tile * rtiles + rt) * 16 + g, rg8 = rg + 8;
+    const bool vg = rg < N, vg8 = rg8 < N;
+    const int64_t rgc = vg ? rg : 0, rg8c = vg8 ? rg8 : 0;
+
+    // this warp's slice of K in 256-column steps
+    const int nsteps = K / 256;
+    const int s_begin = (int)((int64_t)nsteps * slice / ks), s_end = (int)((int64_t)nsteps * (slice + 1) / ks);
+
+    float acc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+
+    const uint8_t* codes = D.codes + l * D.stride_codes;
+    const uint16_t* xp = D.xperm + l * D.xperm_stride + g * 16 + t * 4;
+
+    if (FMT == LQ_FMT_2BIT_LM_G32) {
+        const uint16_t* sc = reinterpret_cast<const uint16_t*>(static_cast<const char*>(D.scales) + l * D.stride_scales);
+        const uint16_t* of = reinterpret_cast<const uint16_t*>(reinterpret_cast<const char*>(D.offsets) + l * D.stride_offsets);
+        const uint8_t* cg = codes + rgc * (K / 4) + 16 * t;
+        const uint8_t* cg8 = codes + rg8c * (K / 4) + 16 * t;
+        const uint16_t* sg = sc + rgc * (K / 32) + 2 * t;
+        const uint16_t* sg8 = sc + rg8c * (K / 32) + 2 * t;
+        const uint16_t* zg = of + rgc * (K / 32) + 2 * t;
+        const uint16_t* zg8 = of + rg8c * (K / 32) + 2 * t;
+        auto load = [&](int s) {
+            Step2 f;
+            f.c0 = vg ? ldg128(cg + 64 * s) : make_uint4(0, 0, 0, 0);
+            f.c1 = vg8 ? ldg128(cg8 + 64 * s) : make_uint4(0, 0, 0, 0);
+            f.s0 = vg ? ldg32(sg + 8 * s) : 0u;
+            f.z0 = vg ? ldg32(zg + 8 * s) : 0u;
+            f.s1 = vg8 ? ldg32(sg8 + 8 * s) : 0u;
+            f.z1 = vg8 ? ldg32(zg8 + 8 * s) : 0u;
+            return f;
+        };
+        Step2 f0 = load(s_begin < s_end ? s_begin : 0);
+        Step2 f1 = load(s_begin + 1 < s_end ? s_begin + 1 : 0);
+        pdl_wait();   // the x passes have finished
+        for (int s = s_begin; s < s_end; ++s) {
+            const Step2 f2 = load(s + 2 < s_end ? s + 2 : s);
+            uint2 xb[16][NT];
+#pragma unroll
+            for (int b = 0; b < 16; ++b)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) xb[b][nt] = xfrag<MT>(xp, s * 16 + b, M, nt);
+            uint32_t RA[4], RB[4];
+            lut2_bits((uint16_t)f0.s0, (uint16_t)f0.z0, RA[0], RB[0]);
+            lut2_bits((uint16_t)(f0.s0 >> 16), (uint16_t)(f0.z0 >> 16), RA[1], RB[1]);
+            lut2_bits((uint16_t)f0.s1, (uint16_t)f0.z1, RA[2], RB[2]);
+            lut2_bits((uint16_t)(f0.s1 >> 16), (uint16_t)(f0.z1 >> 16), RA[3], RB[3]);
+            const uint32_t w0[4] = {f0.c0.x, f0.c0.y, f0.c0.z, f0.c0.w};
+            const uint32_t w1[4] = {f0.c1.x, f0.c1.y, f0.c1.z, f0.c1.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    uint32_t a0, a1, a2, a3;
+                    expand2_fast(w0[i], j, RA[i >> 1], RB[i >> 1], a0, a2);
+                    expand2_fast(w1[i], j, RA[2 + (i >> 1)], RB[2 + (i >> 1)], a1, a3);
+                    mma_xg<NT, MT>(acc, a0, a1, a2, a3, xb[i * 4 + j]);
+                }
+            }
+            f0 = f1;
+            f1 = f2;
+        }
+        // anchors: binary16 weights straight into the A fragment, blocks shared round-robin by the slices
+        if (D.A > 0) {
+            const uint16_t* aw = reinterpret_cast<const uint16_t*>(reinterpret_cast<const char*>(D.anchor_w) + l * D.stride_anchor_w);
+            const uint16_t* awg = aw + rgc * D.ld_anchor;
+            const uint16_t* awg8 = aw + rg8c * D.ld_anchor;
+            const uint16_t* xa = D.xaperm + l * D.xaperm_stride + g * 16 + t * 4;
+            const int A = D.A;
+            auto pair = [&](const uint16_t* row, int a, bool v) -> uint32_t {
+                if (!v || a >= A) return 0u;
+                const uint32_t w = ldg32(row + a);
+                return (a + 1 < A) ? w : (w & 0xFFFFu);
+            };
+            for (int ab = slice; ab < (A + 15) / 16; ab += ks) {
+                const int a = 16 * ab + 2 * t;
+                const uint32_t a0 = pair(awg, a, vg), a2 = pair(awg, a + 8, vg);
+                const uint32_t a1 = pair(awg8, a, vg8), a3 = pair(awg8, a + 8, vg8);
+                uint2 xb[NT];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) xb[nt] = xfrag<MT>(xa, ab, M, nt);
+                mma_xg<NT, MT>(acc, a0, a1, a2, a3, xb);
+            }
+        }
+    } else {
+        const float* am = reinterpret_cast<const float*>(static_cast<const char*>(D.scales) + l * D.stride_scales);
+        const uint8_t* cg = codes + rgc * (K / 2) + 8 * t;
+        const uint8_t* cg8 = codes + rg8c * (K / 2) + 8 * t;
+        const float* ag = am + rgc * (K / 64);
+        const float* ag8 = am + rg8c * (K / 64);
+        uint32_t TL[4], TH[4];
+        nf4_tables(TL, TH);
+        auto load = [&](int s) {
+            StepNF4 f;
+#pragma unroll
+            for (int nb = 0; nb < 4; ++nb) {
+                f.c0[nb] = vg ? ldg64(cg + 128 * s + 32 * nb) : make_uint2(0, 0);
+                f.c1[nb] = vg8 ? ldg64(cg8 + 128 * s + 32 * nb) : make_uint2(0, 0);
+                f.a0[nb] = vg ? __ldg(ag + 4 * s + nb) : 0.f;
+                f.a1[nb] = vg8 ? __ldg(ag8 + 4 * s + nb) : 0.f;
+            }
+            return f;
+        };
+        StepNF4 f0 = load(s_begin < s_end ? s_begin : 0);
+        StepNF4 f1 = load(s_begin + 1 < s_end ? s_begin + 1 : 0);
+        pdl_wait();
+        for (int s = s_begin; s < s_end; ++s) {
+            const StepNF4 f2 = load(s + 2 < s_end ? s + 2 : s);
+#pragma unroll
+            for (int nb = 0; nb < 4; ++nb) {
+                uint2 xb[4][NT];
+#pragma unroll
+                for (int b = 0; b < 4; ++b)
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) xb[b][nt] = xfrag<MT>(xp, (s * 4 + nb) * 4 + b, M, nt);
+                float part[NT][4];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) part[nt][0] = part[nt][1] = part[nt][2] = part[nt][3] = 0.f;
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    uint32_t a0, a1, a2, a3;
+                    expand_nf4_fast(b < 2 ? f0.c0[nb].x : f0.c0[nb].y, b & 1, TL, TH, a0, a2);
+                    expand_nf4_fast(b < 2 ? f0.c1[nb].x : f0.c1[nb].y, b & 1, TL, TH, a1, a3);
+                    mma_xg<NT, MT>(part, a0, a1, a2, a3, xb[b]);
+                }
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    acc[nt][0] = __fmaf_rn(f0.a0[nb], part[nt][0], acc[nt][0]);
+                    acc[nt][1] = __fmaf_rn(f0.a0[nb], part[nt][1], acc[nt][1]);
+                    acc[nt][2] = __fmaf_rn(f0.a1[nb], part[nt][2], acc[nt][2]);
+                    acc[nt][3] = __fmaf_rn(f0.a1[nb], part[nt][3], acc[nt][3]);
+                }
+            }
+            f0 = f1;
+            f1 = f2;
+        }
+    }
+
+    // ---- reduce the K slices of each row tile in shared memory, then store y
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int m0 = 8 * nt + 2 * t, m1 = m0 + 1;
+        if (m0 < M) {
+            red[warp][g][m0] = acc[nt][0];
+            red[warp][g + 8][m0] = acc[nt][2];
+        }
+        if (m1 < M) {
+            red[warp][g][m1] = acc[nt][1];
+            red[warp][g + 8][m1] = acc[nt][3];
+        }
+    }
+    __syncthreads();
+    void* y = static_cast<char*>(D.y) + l * D.stride_y;
+    for (int idx = threadIdx.x; idx < rtiles * 16 * M; idx += kThreadsS) {
+        const int rtile = idx / (16 * M), rem = idx - rtile * 16 * M;
+        const int m = rem / 16, r = rem - m * 16;
+        const int n = (tile * rtiles + rtile) * 16 + r;
+        if (n >= N) continue;
+        float sum = 0.f;
+        for (int sl = 0; sl < ks; ++sl) sum += red[rtile * ks + sl][r][m];
+        store_out(y, (size_t)m * N + n, P.y_dtype, sum);
+    }
+}
+
+template <int FMT, int MT, int NT>
+lq_status launch_s(const SParams& P, int64_t blocks, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(kThreadsS);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, gemv_stream_kernel<FMT, MT, NT>, P) != cudaSuccess) return LQ_ERR_CUDA;
+    return cudaPeekAtLastError() == cudaSuccess ? LQ_OK : LQ_ERR_CUDA;
+}
+
+template <int FMT>
+lq_status launch_s_fmt(const SParams& P, int64_t blocks, cudaStream_t stream) {
+    switch (P.M) {
+        case 1: return launch_s<FMT, 1, 1>(P, blocks, stream);
+        case 2: return launch_s<FMT, 2, 1>(P, blocks, stream);
+        case 3: return launch_s<FMT, 3, 1>(P, blocks, stream);
+        case 4: return launch_s<FMT, 4, 1>(P, blocks, stream);
+        case 5: return launch_s<FMT, 5, 1>(P, blocks, stream);
+        case 6: return launch_s<FMT, 6, 1>(P, blocks, stream);
+        case 7: return launch_s<FMT, 7, 1>(P, blocks, stream);
+        case 8: return launch_s<FMT, 8, 1>(P, blocks, stream);
+        default:
+            if (P.M <= 16) return launch_s<FMT, 0, 2>(P, blocks, stream);
+            return launch_s<FMT, 0, 4>(P, blocks, stream);
+    }
+}
+
+int round_up(int a, int b) { return (a + b - 1) / b * b; }
+
+}  // namespace
+
+bool gemv_stream_eligible(const lq_problem* probs, int count) {
+    for (int i = 0; i < count; ++i)
+        if (probs[i].K % 256 != 0) return false;
+    return true;
+}
+
+lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* probs, int count, cudaStream_t stream) {
+    SParams P;
+    PrepParams Q;
+    memset(&P, 0, sizeof(P));
+    memset(&Q, 0, sizeof(Q));
+    const int M = probs[0].M;
+    const int fmt = probs[0].format;
+    P.count = Q.count = count;
+    P.M = Q.M = M;
+    P.y_dtype = probs[0].y_dtype;
+    Q.format = fmt;
+    Q.x_bf16 = probs[0].x_dtype == LQ_BF16;
+
+    int64_t blocks = 0, prep = 0, prep_a = 0, xhalves = 0;
+    for (int i = 0; i < count; ++i) {
+        const lq_problem& q = probs[i];
+        const int A = fmt == LQ_FMT_2BIT_LM_G32 ? q.A : 0;
+        SDesc& d = P.d[i];
+        PrepDesc& e = Q.d[i];
+        d.codes = q.codes;
+        d.scales = q.scales;
+        d.offsets = q.offsets;
+        d.anchor_w = q.anchor_w;
+        d.y = q.y;
+        d.stride_codes = q.stride_codes;
+        d.stride_scales = q.stride_scales;
+        d.stride_offsets = q.stride_offsets;
+        d.stride_anchor_w = q.stride_anchor_w;
+        d.stride_y = q.stride_y;
+        d.N = q.N;
+        d.K = q.K;
+        d.A = A;
+        d.ld_anchor = q.ld_anchor;
+        d.batch = q.batch;
+        // warps per row tile: each slice gets >= 4 steps of 256 columns when K allows
+        const int steps = q.K / 256;
+        d.ks = steps >= 32 ? 8 : (steps >= 16 ? 4 : (steps >= 8 ? 2 : 1));
+        const int rows_per_cta = 16 * (kWarps / d.ks);
+        d.tiles = (q.N + rows_per_cta - 1) / rows_per_cta;
+        d.block_begin = blocks;
+        blocks += (int64_t)q.batch * d.tiles;
+        const int a_pad = A > 0 ? round_up(A, 64) : 0;
+        d.xperm_stride = (int64_t)M * q.K + kXPad;
+        d.xaperm_stride = (int64_t)M * a_pad + kXPad;
+        xhalves += (int64_t)q.batch * (d.xperm_stride + d.xaperm_stride) + 2 * 128;
+        e.x = static_cast<const uint16_t*>(q.x);
+        e.stride_x = q.stride_x;
+        e.anchor_idx = A > 0 ? q.anchor_idx : nullptr;
+        e.stride_anchor_idx = q.stride_anchor_idx;
+        e.K = q.K;
+        e.Kp = q.K;
+        e.A = A;
+        e.a_pad = a_pad;
+        e.batch = q.batch;
+        e.xperm_stride = d.xperm_stride;
+        e.xaperm_stride = d.xaperm_stride;
+        e.work_begin = prep;
+        prep += (int64_t)q.batch * M * q.K / 8;
+        e.anchor_begin = prep_a;
+        prep_a += (int64_t)q.batch * M * a_pad;
+    }
+    if (blocks > 0x7fffffffLL) return LQ_ERR_UNSUPPORTED;
+    if ((size_t)((xhalves + 1) / 2 + 64) > ws.partial_floats) return LQ_ERR_WORKSPACE;
+    uint16_t* xp = reinterpret_cast<uint16_t*>((reinterpret_cast<uintptr_t>(ws.partials) + 255) & ~uintptr_t(255));
+    for (int i = 0; i < count; ++i) {
+        P.d[i].xperm = Q.d[i].xperm = xp;
+        xp += (int64_t)probs[i].batch * P.d[i].xperm_stride;
+        xp = reinterpret_cast<uint16_t*>((reinterpret_cast<uintptr_t>(xp) + 255) & ~uintptr_t(255));
+        P.d[i].xaperm = Q.d[i].xaperm = xp;
+        xp += (int64_t)probs[i].batch * P.d[i].xaperm_stride;
+        xp = reinterpret_cast<uint16_t*>((reinterpret_cast<uintptr_t>(xp) + 255) & ~uintptr_t(255));
+    }
+    Q.total = prep;
+    Q.total_anchor = prep_a;
+    if (blocks == 0) return LQ_OK;
+
+    // x passes, then the main kernel, chained by programmatic dependent launch
+    const int prep_grid = (int)std::min<int64_t>((Q.total + 255) / 256, (int64_t)ws.num_sms * 8);
+    xprep_kernel<<<std::max(1, prep_grid), 256, 0, stream>>>(Q);
+    if (cudaPeekAtLastError() != cudaSuccess) return LQ_ERR_CUDA;
+    if (Q.total_anchor > 0) {
+        cudaLaunchConfig_t cfg;
+        memset(&cfg, 0, sizeof(cfg));
+        cfg.gridDim = dim3((unsigned)std::max<int64_t>(1, std::min<int64_t>((Q.total_anchor + 255) / 256, (int64_t)ws.num_sms * 8)));
+        cfg.blockDim = dim3(256);
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, xanchor_kernel, Q) != cudaSuccess) return LQ_ERR_CUDA;
+    }
+    if (fmt == LQ_FMT_2BIT_LM_G32) return launch_s_fmt<LQ_FMT_2BIT_LM_G32>(P, blocks, stream);
+    return launch_s_fmt<LQ_FMT_NF4_B64>(P, blocks, stream);
+}
+
+}  // namespace lq

@@ -79,9 +79,9 @@ struct GemvWorkspace {
 
 lq_status launch_gemv(lq_handle h, const lq_problem* problems, int count, cudaStream_t stream);
 lq_status launch_gemv_ws(const GemvWorkspace& ws, const lq_problem* problems, int count, cudaStream_t stream);
-bool gemv_tma_eligible(const lq_problem* problems, int count);
+bool gemv_stream_eligible(const lq_problem* problems, int count);
 lq_status launch_gemv_regs(const GemvWorkspace& ws, const lq_problem* problems, int count, cudaStream_t stream);
-lq_status launch_gemv_tma(const GemvWorkspace& ws, const lq_problem* problems, int count, cudaStream_t stream);
+lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* problems, int count, cudaStream_t stream);
 
 lq_status launch_gemm(lq_handle h, const lq_problem& p, cudaStream_t stream);
 

@@ -303,7 +303,7 @@ def test_errors_on_device_launch_nothing(lqm, handle):
 
 # ---------------------------------------------------------------- both decode kernels on the same shapes
 
-@pytest.mark.parametrize("kernel", ["regs", "tma"])
+@pytest.mark.parametrize("kernel", ["regs", "stream"])
 @pytest.mark.parametrize("M", [1, 8, 32])
 def test_gemv_kernel_choice_same_results(lqm, handle, monkeypatch, kernel, M):
     """The register-fed and the TMA-fed kernels both meet the bound on a K % 256 == 0 shape."""
