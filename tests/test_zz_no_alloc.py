@@ -62,8 +62,8 @@ def test_noalloc_matches_gemv_on_two_calls_in_a_row(lqm):
 
 def test_noalloc_rejects_problems_beyond_its_scratch(lqm):
     L = lqm.load_library()
-    N = K = 8192
-    M = 32
+    # K % 256 != 0 takes the split-K kernel, whose partial sums here (~4.5 M floats) exceed the scratch
+    N, K, M = 8192, 8224, 32
     codes = torch.zeros((N, K // 4), dtype=torch.uint8, device="cuda")
     sc = torch.zeros((N, K // 32), dtype=torch.float16, device="cuda")
     x = torch.zeros((M, K), dtype=torch.float16, device="cuda")
