@@ -24,6 +24,7 @@
 //    stays inside one 64-column block so its fp32 absmax scales the partial sums.
 
 #include <algorithm>
+#include <cstdlib>
 #include <cstring>
 
 #include "lq_common.cuh"
@@ -195,8 +196,7 @@ __global__ void __launch_bounds__(kThreadsS) gemv_stream_kernel(const __grid_con
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
     const int rt = warp / ks, slice = warp - rt * ks;
     const int rg = (tile * rtiles + rt) * 16 + g, rg8 = rg + 8;
-    const bool vg = rg < N, vg8 = rg8 < N;
-    const int64_t rgc = vg ? rg : 0, rg8c = vg8 ? rg8 : 0;
+    const int64_t rgc = rg < N ? rg : 0, rg8c = rg8 < N ? rg8 : 0;
 
     // this warp's slice of K in 256-column steps
     const int nsteps = K / 256;
@@ -206,57 +206,70 @@ __global__ void __launch_bounds__(kThreadsS) gemv_stream_kernel(const __grid_con
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
 
+    // Rows past N read row 0 (results for them are never stored), so every load is unconditional.
     const uint8_t* codes = D.codes + l * D.stride_codes;
-    const uint16_t* xp = D.xperm + l * D.xperm_stride + g * 16 + t * 4;
+    const int MM = MT > 0 ? MT : M;
+    const uint16_t* xp = D.xperm + l * D.xperm_stride + g * 16 + t * 4 + (int64_t)s_begin * 256 * MM;
+    const int steps = s_end - s_begin;
 
     if (FMT == LQ_FMT_2BIT_LM_G32) {
         const uint16_t* sc = reinterpret_cast<const uint16_t*>(static_cast<const char*>(D.scales) + l * D.stride_scales);
         const uint16_t* of = reinterpret_cast<const uint16_t*>(reinterpret_cast<const char*>(D.offsets) + l * D.stride_offsets);
-        const uint8_t* cg = codes + rgc * (K / 4) + 16 * t;
-        const uint8_t* cg8 = codes + rg8c * (K / 4) + 16 * t;
-        const uint16_t* sg = sc + rgc * (K / 32) + 2 * t;
-        const uint16_t* sg8 = sc + rg8c * (K / 32) + 2 * t;
-        const uint16_t* zg = of + rgc * (K / 32) + 2 * t;
-        const uint16_t* zg8 = of + rg8c * (K / 32) + 2 * t;
-        auto load = [&](int s) {
-            Step2 f;
-            f.c0 = vg ? ldg128(cg + 64 * s) : make_uint4(0, 0, 0, 0);
-            f.c1 = vg8 ? ldg128(cg8 + 64 * s) : make_uint4(0, 0, 0, 0);
-            f.s0 = vg ? ldg32(sg + 8 * s) : 0u;
-            f.z0 = vg ? ldg32(zg + 8 * s) : 0u;
-            f.s1 = vg8 ? ldg32(sg8 + 8 * s) : 0u;
-            f.z1 = vg8 ? ldg32(zg8 + 8 * s) : 0u;
-            return f;
+        const uint8_t* cg = codes + rgc * (K / 4) + 16 * t + 64 * s_begin;
+        const uint8_t* cg8 = codes + rg8c * (K / 4) + 16 * t + 64 * s_begin;
+        const uint16_t* sg = sc + rgc * (K / 32) + 2 * t + 8 * s_begin;
+        const uint16_t* sg8 = sc + rg8c * (K / 32) + 2 * t + 8 * s_begin;
+        const uint16_t* zg = of + rgc * (K / 32) + 2 * t + 8 * s_begin;
+        const uint16_t* zg8 = of + rg8c * (K / 32) + 2 * t + 8 * s_begin;
+        // step i of this warp's slice (i clamped into the slice: loads past the end repeat the last step)
+        auto load = [&](Step2& f, int i) {
+            i = min(i, steps - 1);
+            f.c0 = ldg128(cg + 64 * i);
+            f.c1 = ldg128(cg8 + 64 * i);
+            f.s0 = ldg32(sg + 8 * i);
+            f.z0 = ldg32(zg + 8 * i);
+            f.s1 = ldg32(sg8 + 8 * i);
+            f.z1 = ldg32(zg8 + 8 * i);
         };
-        Step2 f0 = load(s_begin < s_end ? s_begin : 0);
-        Step2 f1 = load(s_begin + 1 < s_end ? s_begin + 1 : 0);
-        pdl_wait();   // the x passes have finished
-        for (int s = s_begin; s < s_end; ++s) {
-            const Step2 f2 = load(s + 2 < s_end ? s + 2 : s);
+        auto compute = [&](const Step2& f, int i) {
+            const uint16_t* xs = xp + (int64_t)i * 256 * MM;
             uint2 xb[16][NT];
 #pragma unroll
             for (int b = 0; b < 16; ++b)
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) xb[b][nt] = xfrag<MT>(xp, s * 16 + b, M, nt);
+                for (int nt = 0; nt < NT; ++nt) xb[b][nt] = xfrag<MT>(xs, b, M, nt);
             uint32_t RA[4], RB[4];
-            lut2_bits((uint16_t)f0.s0, (uint16_t)f0.z0, RA[0], RB[0]);
-            lut2_bits((uint16_t)(f0.s0 >> 16), (uint16_t)(f0.z0 >> 16), RA[1], RB[1]);
-            lut2_bits((uint16_t)f0.s1, (uint16_t)f0.z1, RA[2], RB[2]);
-            lut2_bits((uint16_t)(f0.s1 >> 16), (uint16_t)(f0.z1 >> 16), RA[3], RB[3]);
-            const uint32_t w0[4] = {f0.c0.x, f0.c0.y, f0.c0.z, f0.c0.w};
-            const uint32_t w1[4] = {f0.c1.x, f0.c1.y, f0.c1.z, f0.c1.w};
+            lut2_bits((uint16_t)f.s0, (uint16_t)f.z0, RA[0], RB[0]);
+            lut2_bits((uint16_t)(f.s0 >> 16), (uint16_t)(f.z0 >> 16), RA[1], RB[1]);
+            lut2_bits((uint16_t)f.s1, (uint16_t)f.z1, RA[2], RB[2]);
+            lut2_bits((uint16_t)(f.s1 >> 16), (uint16_t)(f.z1 >> 16), RA[3], RB[3]);
+            const uint32_t w0[4] = {f.c0.x, f.c0.y, f.c0.z, f.c0.w};
+            const uint32_t w1[4] = {f.c1.x, f.c1.y, f.c1.z, f.c1.w};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+            for (int ii = 0; ii < 4; ++ii) {
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     uint32_t a0, a1, a2, a3;
-                    expand2_fast(w0[i], j, RA[i >> 1], RB[i >> 1], a0, a2);
-                    expand2_fast(w1[i], j, RA[2 + (i >> 1)], RB[2 + (i >> 1)], a1, a3);
-                    mma_xg<NT, MT>(acc, a0, a1, a2, a3, xb[i * 4 + j]);
+                    expand2_fast(w0[ii], j, RA[ii >> 1], RB[ii >> 1], a0, a2);
+                    expand2_fast(w1[ii], j, RA[2 + (ii >> 1)], RB[2 + (ii >> 1)], a1, a3);
+                    mma_xg<NT, MT>(acc, a0, a1, a2, a3, xb[ii * 4 + j]);
                 }
             }
-            f0 = f1;
-            f1 = f2;
+        };
+        // three register buffers, two steps in flight, unrolled so the buffers never move
+        Step2 fa, fb, fc;
+        load(fa, 0);
+        load(fb, 1);
+        pdl_wait();   // the x passes have finished
+        for (int i = 0; i < steps; i += 3) {
+            load(fc, i + 2);
+            compute(fa, i);
+            if (i + 1 >= steps) break;
+            load(fa, i + 3);
+            compute(fb, i + 1);
+            if (i + 2 >= steps) break;
+            load(fb, i + 4);
+            compute(fc, i + 2);
         }
         // anchors: binary16 weights straight into the A fragment, blocks shared round-robin by the slices
         if (D.A > 0) {
@@ -265,15 +278,15 @@ __global__ void __launch_bounds__(kThreadsS) gemv_stream_kernel(const __grid_con
             const uint16_t* awg8 = aw + rg8c * D.ld_anchor;
             const uint16_t* xa = D.xaperm + l * D.xaperm_stride + g * 16 + t * 4;
             const int A = D.A;
-            auto pair = [&](const uint16_t* row, int a, bool v) -> uint32_t {
-                if (!v || a >= A) return 0u;
+            auto pair = [&](const uint16_t* row, int a) -> uint32_t {
+                if (a >= A) return 0u;
                 const uint32_t w = ldg32(row + a);
                 return (a + 1 < A) ? w : (w & 0xFFFFu);
             };
             for (int ab = slice; ab < (A + 15) / 16; ab += ks) {
                 const int a = 16 * ab + 2 * t;
-                const uint32_t a0 = pair(awg, a, vg), a2 = pair(awg, a + 8, vg);
-                const uint32_t a1 = pair(awg8, a, vg8), a3 = pair(awg8, a + 8, vg8);
+                const uint32_t a0 = pair(awg, a), a2 = pair(awg, a + 8);
+                const uint32_t a1 = pair(awg8, a), a3 = pair(awg8, a + 8);
                 uint2 xb[NT];
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) xb[nt] = xfrag<MT>(xa, ab, M, nt);
@@ -282,55 +295,59 @@ __global__ void __launch_bounds__(kThreadsS) gemv_stream_kernel(const __grid_con
         }
     } else {
         const float* am = reinterpret_cast<const float*>(static_cast<const char*>(D.scales) + l * D.stride_scales);
-        const uint8_t* cg = codes + rgc * (K / 2) + 8 * t;
-        const uint8_t* cg8 = codes + rg8c * (K / 2) + 8 * t;
-        const float* ag = am + rgc * (K / 64);
-        const float* ag8 = am + rg8c * (K / 64);
+        const uint8_t* cg = codes + rgc * (K / 2) + 8 * t + 128 * s_begin;
+        const uint8_t* cg8 = codes + rg8c * (K / 2) + 8 * t + 128 * s_begin;
+        const float* ag = am + rgc * (K / 64) + 4 * s_begin;
+        const float* ag8 = am + rg8c * (K / 64) + 4 * s_begin;
         uint32_t TL[4], TH[4];
         nf4_tables(TL, TH);
-        auto load = [&](int s) {
-            StepNF4 f;
+        auto load = [&](StepNF4& f, int i) {
+            i = min(i, steps - 1);
 #pragma unroll
             for (int nb = 0; nb < 4; ++nb) {
-                f.c0[nb] = vg ? ldg64(cg + 128 * s + 32 * nb) : make_uint2(0, 0);
-                f.c1[nb] = vg8 ? ldg64(cg8 + 128 * s + 32 * nb) : make_uint2(0, 0);
-                f.a0[nb] = vg ? __ldg(ag + 4 * s + nb) : 0.f;
-                f.a1[nb] = vg8 ? __ldg(ag8 + 4 * s + nb) : 0.f;
+                f.c0[nb] = ldg64(cg + 128 * i + 32 * nb);
+                f.c1[nb] = ldg64(cg8 + 128 * i + 32 * nb);
+                f.a0[nb] = __ldg(ag + 4 * i + nb);
+                f.a1[nb] = __ldg(ag8 + 4 * i + nb);
             }
-            return f;
         };
-        StepNF4 f0 = load(s_begin < s_end ? s_begin : 0);
-        StepNF4 f1 = load(s_begin + 1 < s_end ? s_begin + 1 : 0);
-        pdl_wait();
-        for (int s = s_begin; s < s_end; ++s) {
-            const StepNF4 f2 = load(s + 2 < s_end ? s + 2 : s);
+        auto compute = [&](const StepNF4& f, int i) {
+            const uint16_t* xs = xp + (int64_t)i * 256 * MM;
 #pragma unroll
             for (int nb = 0; nb < 4; ++nb) {
                 uint2 xb[4][NT];
 #pragma unroll
                 for (int b = 0; b < 4; ++b)
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) xb[b][nt] = xfrag<MT>(xp, (s * 4 + nb) * 4 + b, M, nt);
+                    for (int nt = 0; nt < NT; ++nt) xb[b][nt] = xfrag<MT>(xs, nb * 4 + b, M, nt);
                 float part[NT][4];
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) part[nt][0] = part[nt][1] = part[nt][2] = part[nt][3] = 0.f;
 #pragma unroll
                 for (int b = 0; b < 4; ++b) {
                     uint32_t a0, a1, a2, a3;
-                    expand_nf4_fast(b < 2 ? f0.c0[nb].x : f0.c0[nb].y, b & 1, TL, TH, a0, a2);
-                    expand_nf4_fast(b < 2 ? f0.c1[nb].x : f0.c1[nb].y, b & 1, TL, TH, a1, a3);
+                    expand_nf4_fast(b < 2 ? f.c0[nb].x : f.c0[nb].y, b & 1, TL, TH, a0, a2);
+                    expand_nf4_fast(b < 2 ? f.c1[nb].x : f.c1[nb].y, b & 1, TL, TH, a1, a3);
                     mma_xg<NT, MT>(part, a0, a1, a2, a3, xb[b]);
                 }
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    acc[nt][0] = __fmaf_rn(f0.a0[nb], part[nt][0], acc[nt][0]);
-                    acc[nt][1] = __fmaf_rn(f0.a0[nb], part[nt][1], acc[nt][1]);
-                    acc[nt][2] = __fmaf_rn(f0.a1[nb], part[nt][2], acc[nt][2]);
-                    acc[nt][3] = __fmaf_rn(f0.a1[nb], part[nt][3], acc[nt][3]);
+                    acc[nt][0] = __fmaf_rn(f.a0[nb], part[nt][0], acc[nt][0]);
+                    acc[nt][1] = __fmaf_rn(f.a0[nb], part[nt][1], acc[nt][1]);
+                    acc[nt][2] = __fmaf_rn(f.a1[nb], part[nt][2], acc[nt][2]);
+                    acc[nt][3] = __fmaf_rn(f.a1[nb], part[nt][3], acc[nt][3]);
                 }
             }
-            f0 = f1;
-            f1 = f2;
+        };
+        StepNF4 fa, fb;
+        load(fa, 0);
+        pdl_wait();
+        for (int i = 0; i < steps; i += 2) {
+            load(fb, i + 1);
+            compute(fa, i);
+            if (i + 1 >= steps) break;
+            load(fa, i + 2);
+            compute(fb, i + 1);
         }
     }
 
@@ -417,6 +434,9 @@ lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* probs, i
     Q.x_bf16 = probs[0].x_dtype == LQ_BF16;
 
     int64_t blocks = 0, prep = 0, prep_a = 0, xhalves = 0;
+    // minimum K steps per warp (LQ_GEMV_STEPS_PER_WARP overrides, for tuning experiments)
+    int spw = 4;
+    if (const char* e = getenv("LQ_GEMV_STEPS_PER_WARP")) spw = std::max(1, atoi(e));
     for (int i = 0; i < count; ++i) {
         const lq_problem& q = probs[i];
         const int A = fmt == LQ_FMT_2BIT_LM_G32 ? q.A : 0;
@@ -437,9 +457,10 @@ lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* probs, i
         d.A = A;
         d.ld_anchor = q.ld_anchor;
         d.batch = q.batch;
-        // warps per row tile: each slice gets >= 4 steps of 256 columns when K allows
+        // warps per row tile (K slices): as many as keep >= spw steps of 256 columns per warp
         const int steps = q.K / 256;
-        d.ks = steps >= 32 ? 8 : (steps >= 16 ? 4 : (steps >= 8 ? 2 : 1));
+        d.ks = 8;
+        while (d.ks > 1 && steps < spw * d.ks) d.ks /= 2;
         const int rows_per_cta = 16 * (kWarps / d.ks);
         d.tiles = (q.N + rows_per_cta - 1) / rows_per_cta;
         d.block_begin = blocks;
