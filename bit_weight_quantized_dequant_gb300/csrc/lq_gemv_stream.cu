@@ -37,7 +37,6 @@ namespace {
 
 constexpr int kWarps = 8;
 constexpr int kThreadsS = kWarps * 32;
-constexpr int kXPad = 256;   // halves of padding after each x copy (fragment loads of absent tokens)
 
 // ---- pre-pass: x -> binary16, anchors zeroed, fragment order ------------------------
 
@@ -46,97 +45,77 @@ struct PrepDesc {
     int64_t stride_x;          // bytes
     const int32_t* anchor_idx;
     int64_t stride_anchor_idx; // bytes
-    uint16_t* xperm;
-    uint16_t* xaperm;
-    int64_t xperm_stride, xaperm_stride;   // halves
-    int K, Kp, A, a_pad, batch;
-    int64_t work_begin;        // first work item (8 halves) of this problem in pass 1
-    int64_t anchor_begin;      // first work item (one anchor of one token) in pass 2
+    uint16_t* xperm;           // [batch][K/16][M][16]
+    uint16_t* xaperm;          // [batch][a_pad/16][M][16]
+    int64_t xperm_stride, xaperm_stride;   // halves per batch member
+    int K, A, a_pad, batch;
+    int ctas;                  // CTAs per batch member
+    int64_t cta_begin;         // first CTA of this problem
 };
 
 struct PrepParams {
     PrepDesc d[kMaxGroup];
     int count, M, x_bf16, format;
-    int64_t total, total_anchor;
+    int64_t total_ctas;
 };
+
+constexpr int kPrepItems = 1024;   // 8-half output items per pre-pass CTA
 
 __device__ __forceinline__ uint16_t to_half_bits(uint16_t raw, int x_bf16) {
     return x_bf16 ? __half_as_ushort(__float2half_rn(bf16_bits_to_float(raw))) : raw;
 }
 
-// Pass 1, output-major: each thread writes 8 consecutive binary16 of the fragment-ordered
-// copy of x (one 16-byte store), gathering its 8 source columns from the x row.
+// One CTA covers kPrepItems consecutive 16-byte items of one batch member: first the
+// fragment-ordered copy of x with the anchor columns zeroed (a bitmap of the anchor
+// columns in shared memory marks them), then x gathered at the anchor columns.
 __global__ void __launch_bounds__(256) xprep_kernel(const __grid_constant__ PrepParams P) {
+    extern __shared__ uint32_t anchor_bits[];
     pdl_launch_dependents();
-    const int M = P.M;
-    for (int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; w < P.total; w += (int64_t)gridDim.x * blockDim.x) {
-        int p = 0;
-        while (p + 1 < P.count && w >= P.d[p + 1].work_begin) ++p;
-        const PrepDesc& D = P.d[p];
-        const int64_t local = w - D.work_begin;                 // in units of 8 halves
-        const int64_t per_member = (int64_t)M * D.Kp / 8;
-        const int64_t l = local / per_member;
-        const int64_t d0 = 8 * (local - l * per_member);
-        const uint16_t* x = reinterpret_cast<const uint16_t*>(reinterpret_cast<const char*>(D.x) + l * D.stride_x);
+    const int64_t cta = blockIdx.x;
+    int p = 0;
+    while (p + 1 < P.count && cta >= P.d[p + 1].cta_begin) ++p;
+    const PrepDesc& D = P.d[p];
+    const int64_t local = cta - D.cta_begin;
+    const int64_t l = local / D.ctas;
+    const int part = (int)(local - l * D.ctas);
+    const int M = P.M, K = D.K, A = D.A;
+    const uint16_t* x = reinterpret_cast<const uint16_t*>(reinterpret_cast<const char*>(D.x) + l * D.stride_x);
+    const int32_t* aidx = A > 0 ? reinterpret_cast<const int32_t*>(reinterpret_cast<const char*>(D.anchor_idx) + l * D.stride_anchor_idx)
+                                : nullptr;
+    for (int i = threadIdx.x; i < K / 32; i += blockDim.x) anchor_bits[i] = 0u;
+    __syncthreads();
+    for (int a = threadIdx.x; a < A; a += blockDim.x) {
+        const int k = __ldg(aidx + a);
+        atomicOr(&anchor_bits[k >> 5], 1u << (k & 31));
+    }
+    __syncthreads();
+    const int64_t code_items = (int64_t)M * K / 8, all_items = code_items + (int64_t)M * D.a_pad / 8;
+    const int64_t i0 = (int64_t)part * kPrepItems, i1 = min(all_items, i0 + kPrepItems);
+    for (int64_t it = i0 + threadIdx.x; it < i1; it += blockDim.x) {
+        const bool code = it < code_items;
+        const int64_t d0 = 8 * (code ? it : it - code_items);
         const int line = (int)(d0 >> 4), pos0 = (int)(d0 & 15);
         const int bi = line / M, m = line - bi * M;
         uint16_t v[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             const int pos = pos0 + e, tt = pos >> 2, hh = pos & 3;
-            const int k = P.format == LQ_FMT_2BIT_LM_G32
-                ? (bi >> 4) * 256 + tt * 64 + ((bi >> 2) & 3) * 16 + hh * 4 + (bi & 3)
-                : (bi >> 2) * 64 + tt * 16 + (bi & 3) * 4 + hh;
-            v[e] = k < D.K ? to_half_bits(x[(int64_t)m * D.K + k], P.x_bf16) : (uint16_t)0;
+            int k = -1;
+            if (code) {
+                k = P.format == LQ_FMT_2BIT_LM_G32 ? (bi >> 4) * 256 + tt * 64 + ((bi >> 2) & 3) * 16 + hh * 4 + (bi & 3)
+                                                   : (bi >> 2) * 64 + tt * 16 + (bi & 3) * 4 + hh;
+                if ((anchor_bits[k >> 5] >> (k & 31)) & 1u) k = -1;
+            } else {
+                const int a = 16 * bi + 2 * tt + (hh & 1) + 8 * (hh >> 1);
+                if (a < A) k = __ldg(aidx + a);
+            }
+            v[e] = k >= 0 ? to_half_bits(x[(int64_t)m * K + k], P.x_bf16) : (uint16_t)0;
         }
-        uint16_t* dst = D.xperm + l * D.xperm_stride + d0;
+        uint16_t* dst = (code ? D.xperm + l * D.xperm_stride : D.xaperm + l * D.xaperm_stride) + d0;
         *reinterpret_cast<uint4*>(dst) = make_uint4((uint32_t)v[0] | ((uint32_t)v[1] << 16), (uint32_t)v[2] | ((uint32_t)v[3] << 16),
                                                     (uint32_t)v[4] | ((uint32_t)v[5] << 16), (uint32_t)v[6] | ((uint32_t)v[7] << 16));
     }
 }
-
-// Pass 2 (after pass 1): zero x at the anchor columns (the anchors replace those weights)
-// and write x gathered at the anchor columns, zero-padded to a multiple of 64.
-__global__ void __launch_bounds__(256) xanchor_kernel(const __grid_constant__ PrepParams P) {
-    pdl_launch_dependents();
-    pdl_wait();  // pass 1 has finished writing
-    const int M = P.M;
-    for (int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; w < P.total_anchor; w += (int64_t)gridDim.x * blockDim.x) {
-        int p = 0;
-        while (p + 1 < P.count && w >= P.d[p + 1].anchor_begin) ++p;
-        const PrepDesc& D = P.d[p];
-        const int64_t local = w - D.anchor_begin;
-        const int64_t per_member = (int64_t)M * D.a_pad;
-        const int64_t l = local / per_member;
-        const int rem = (int)(local - l * per_member);
-        const int m = rem / D.a_pad, a = rem - m * D.a_pad;
-        uint16_t v = 0;
-        if (a < D.A) {
-            const uint16_t* x = reinterpret_cast<const uint16_t*>(reinterpret_cast<const char*>(D.x) + l * D.stride_x);
-            const int32_t* aidx =
-                reinterpret_cast<const int32_t*>(reinterpret_cast<const char*>(D.anchor_idx) + l * D.stride_anchor_idx);
-            const int k = __ldg(aidx + a);
-            v = to_half_bits(x[(int64_t)m * D.K + k], P.x_bf16);
-            int bi, tt, hh;
-            if (P.format == LQ_FMT_2BIT_LM_G32) {
-                const int r = k & 255, e = r & 15;
-                tt = r >> 6;
-                bi = (k >> 8) * 16 + ((r >> 4) & 3) * 4 + (e & 3);
-                hh = e >> 2;
-            } else {
-                const int r = k & 63, e = r & 15;
-                tt = r >> 4;
-                bi = (k >> 6) * 4 + (e >> 2);
-                hh = e & 3;
-            }
-            D.xperm[l * D.xperm_stride + ((int64_t)bi * M + m) * 16 + tt * 4 + hh] = 0;
-        }
-        const int s = a & 15;
-        const int tt = (s & 7) >> 1, hh = (s & 1) + 2 * (s >> 3);
-        D.xaperm[l * D.xaperm_stride + ((int64_t)(a >> 4) * M + m) * 16 + tt * 4 + hh] = v;
-    }
-}
-
 
 struct SDesc {
     const uint8_t* codes;
@@ -164,11 +143,14 @@ __device__ __forceinline__ void mma_xg(float (&acc)[NT][4], uint32_t a0, uint32_
     for (int nt = 0; nt < NT; ++nt) mma_f16_16816(acc[nt], a0, a1, a2, a3, b[nt].x, b[nt].y);
 }
 
-// x fragment of mma block bi for this thread (n-tile nt): 8 bytes from the permuted copy
+// x fragment of mma block bi (n-tile nt) for this thread: 8 bytes of the permuted copy.
+// `xp` already points at this thread's token and lane; for more than 8 tokens the
+// n-tile offsets come from `tok` (absent tokens read the last real token: their
+// products only reach output columns that are never stored).
 template <int MT>
-__device__ __forceinline__ uint2 xfrag(const uint16_t* xp, int bi, int M, int nt) {
+__device__ __forceinline__ uint2 xfrag(const uint16_t* xp, int bi, int M, int tok_nt) {
     const int MM = MT > 0 ? MT : M;
-    return __ldg(reinterpret_cast<const uint2*>(xp + (bi * MM + 8 * nt) * 16));
+    return __ldg(reinterpret_cast<const uint2*>(xp + bi * MM * 16 + tok_nt));
 }
 
 struct Step2 {
@@ -209,7 +191,11 @@ __global__ void __launch_bounds__(kThreadsS) gemv_stream_kernel(const __grid_con
     // Rows past N read row 0 (results for them are never stored), so every load is unconditional.
     const uint8_t* codes = D.codes + l * D.stride_codes;
     const int MM = MT > 0 ? MT : M;
-    const uint16_t* xp = D.xperm + l * D.xperm_stride + g * 16 + t * 4 + (int64_t)s_begin * 256 * MM;
+    // token of each n-tile for this lane, clamped to the last real token
+    int tok[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) tok[nt] = (min(8 * nt + g, M - 1) - min(g, M - 1)) * 16;
+    const uint16_t* xp = D.xperm + l * D.xperm_stride + min(g, M - 1) * 16 + t * 4 + (int64_t)s_begin * 256 * MM;
     const int steps = s_end - s_begin;
 
     if (FMT == LQ_FMT_2BIT_LM_G32) {
@@ -237,7 +223,7 @@ __global__ void __launch_bounds__(kThreadsS) gemv_stream_kernel(const __grid_con
 #pragma unroll
             for (int b = 0; b < 16; ++b)
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) xb[b][nt] = xfrag<MT>(xs, b, M, nt);
+                for (int nt = 0; nt < NT; ++nt) xb[b][nt] = xfrag<MT>(xs, b, M, tok[nt]);
             uint32_t RA[4], RB[4];
             lut2_bits((uint16_t)f.s0, (uint16_t)f.z0, RA[0], RB[0]);
             lut2_bits((uint16_t)(f.s0 >> 16), (uint16_t)(f.z0 >> 16), RA[1], RB[1]);
@@ -276,7 +262,7 @@ __global__ void __launch_bounds__(kThreadsS) gemv_stream_kernel(const __grid_con
             const uint16_t* aw = reinterpret_cast<const uint16_t*>(reinterpret_cast<const char*>(D.anchor_w) + l * D.stride_anchor_w);
             const uint16_t* awg = aw + rgc * D.ld_anchor;
             const uint16_t* awg8 = aw + rg8c * D.ld_anchor;
-            const uint16_t* xa = D.xaperm + l * D.xaperm_stride + g * 16 + t * 4;
+            const uint16_t* xa = D.xaperm + l * D.xaperm_stride + min(g, M - 1) * 16 + t * 4;
             const int A = D.A;
             auto pair = [&](const uint16_t* row, int a) -> uint32_t {
                 if (a >= A) return 0u;
@@ -289,7 +275,7 @@ __global__ void __launch_bounds__(kThreadsS) gemv_stream_kernel(const __grid_con
                 const uint32_t a1 = pair(awg8, a), a3 = pair(awg8, a + 8);
                 uint2 xb[NT];
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) xb[nt] = xfrag<MT>(xa, ab, M, nt);
+                for (int nt = 0; nt < NT; ++nt) xb[nt] = xfrag<MT>(xa, ab, M, tok[nt]);
                 mma_xg<NT, MT>(acc, a0, a1, a2, a3, xb);
             }
         }
@@ -319,7 +305,7 @@ __global__ void __launch_bounds__(kThreadsS) gemv_stream_kernel(const __grid_con
 #pragma unroll
                 for (int b = 0; b < 4; ++b)
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) xb[b][nt] = xfrag<MT>(xs, nb * 4 + b, M, nt);
+                    for (int nt = 0; nt < NT; ++nt) xb[b][nt] = xfrag<MT>(xs, nb * 4 + b, M, tok[nt]);
                 float part[NT][4];
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) part[nt][0] = part[nt][1] = part[nt][2] = part[nt][3] = 0.f;
@@ -433,7 +419,8 @@ lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* probs, i
     Q.format = fmt;
     Q.x_bf16 = probs[0].x_dtype == LQ_BF16;
 
-    int64_t blocks = 0, prep = 0, prep_a = 0, xhalves = 0;
+    int64_t blocks = 0, prep = 0, xhalves = 0;
+    int max_k = 0;
     // minimum K steps per warp (LQ_GEMV_STEPS_PER_WARP overrides, for tuning experiments)
     int spw = 4;
     if (const char* e = getenv("LQ_GEMV_STEPS_PER_WARP")) spw = std::max(1, atoi(e));
@@ -466,24 +453,24 @@ lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* probs, i
         d.block_begin = blocks;
         blocks += (int64_t)q.batch * d.tiles;
         const int a_pad = A > 0 ? round_up(A, 64) : 0;
-        d.xperm_stride = (int64_t)M * q.K + kXPad;
-        d.xaperm_stride = (int64_t)M * a_pad + kXPad;
+        d.xperm_stride = (int64_t)M * q.K;
+        d.xaperm_stride = (int64_t)M * a_pad;
         xhalves += (int64_t)q.batch * (d.xperm_stride + d.xaperm_stride) + 2 * 128;
         e.x = static_cast<const uint16_t*>(q.x);
         e.stride_x = q.stride_x;
         e.anchor_idx = A > 0 ? q.anchor_idx : nullptr;
         e.stride_anchor_idx = q.stride_anchor_idx;
         e.K = q.K;
-        e.Kp = q.K;
         e.A = A;
         e.a_pad = a_pad;
         e.batch = q.batch;
         e.xperm_stride = d.xperm_stride;
         e.xaperm_stride = d.xaperm_stride;
-        e.work_begin = prep;
-        prep += (int64_t)q.batch * M * q.K / 8;
-        e.anchor_begin = prep_a;
-        prep_a += (int64_t)q.batch * M * a_pad;
+        const int64_t items = ((int64_t)M * q.K + (int64_t)M * a_pad) / 8;
+        e.ctas = (int)((items + kPrepItems - 1) / kPrepItems);
+        e.cta_begin = prep;
+        prep += (int64_t)q.batch * e.ctas;
+        max_k = std::max(max_k, q.K);
     }
     if (blocks > 0x7fffffffLL) return LQ_ERR_UNSUPPORTED;
     if ((size_t)((xhalves + 1) / 2 + 64) > ws.partial_floats) return LQ_ERR_WORKSPACE;
@@ -496,27 +483,15 @@ lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* probs, i
         xp += (int64_t)probs[i].batch * P.d[i].xaperm_stride;
         xp = reinterpret_cast<uint16_t*>((reinterpret_cast<uintptr_t>(xp) + 255) & ~uintptr_t(255));
     }
-    Q.total = prep;
-    Q.total_anchor = prep_a;
+    Q.total_ctas = prep;
     if (blocks == 0) return LQ_OK;
 
-    // x passes, then the main kernel, chained by programmatic dependent launch
-    const int prep_grid = (int)std::min<int64_t>((Q.total + 255) / 256, (int64_t)ws.num_sms * 8);
-    xprep_kernel<<<std::max(1, prep_grid), 256, 0, stream>>>(Q);
+    // x pre-pass, then the main kernel, chained by programmatic dependent launch
+    if (Q.total_ctas > 0x7fffffffLL) return LQ_ERR_UNSUPPORTED;
+    const size_t prep_smem = sizeof(uint32_t) * (size_t)std::max(1, max_k / 32);
+    if (prep_smem > 48 * 1024) return LQ_ERR_UNSUPPORTED;
+    xprep_kernel<<<(unsigned)Q.total_ctas, 256, prep_smem, stream>>>(Q);
     if (cudaPeekAtLastError() != cudaSuccess) return LQ_ERR_CUDA;
-    if (Q.total_anchor > 0) {
-        cudaLaunchConfig_t cfg;
-        memset(&cfg, 0, sizeof(cfg));
-        cfg.gridDim = dim3((unsigned)std::max<int64_t>(1, std::min<int64_t>((Q.total_anchor + 255) / 256, (int64_t)ws.num_sms * 8)));
-        cfg.blockDim = dim3(256);
-        cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, xanchor_kernel, Q) != cudaSuccess) return LQ_ERR_CUDA;
-    }
     if (fmt == LQ_FMT_2BIT_LM_G32) return launch_s_fmt<LQ_FMT_2BIT_LM_G32>(P, blocks, stream);
     return launch_s_fmt<LQ_FMT_NF4_B64>(P, blocks, stream);
 }
