@@ -59,7 +59,7 @@ struct PrepParams {
     int64_t total_ctas;
 };
 
-constexpr int kPrepItems = 1024;   // 8-half output items per pre-pass CTA
+constexpr int kPrepItems = 256;    // 8-half output items per pre-pass CTA (one per thread)
 
 __device__ __forceinline__ uint16_t to_half_bits(uint16_t raw, int x_bf16) {
     return x_bf16 ? __half_as_ushort(__float2half_rn(bf16_bits_to_float(raw))) : raw;
@@ -127,13 +127,14 @@ struct SDesc {
     void* y;
     int64_t stride_codes, stride_scales, stride_offsets, stride_anchor_w, stride_y;
     int64_t xperm_stride, xaperm_stride;   // halves
-    int N, K, A, ld_anchor, batch, ks, tiles;   // ks: warps per row tile (K slices); tiles: CTAs per member
-    int64_t block_begin;
+    int N, K, A, ld_anchor, batch, ks, tiles;   // ks: warps per row tile (K slices); tiles: tiles per member
+    int64_t tile_begin;   // first global tile of this problem
 };
 
 struct SParams {
     SDesc d[kMaxGroup];
     int count, M, y_dtype;
+    int64_t total_tiles;
 };
 
 template <int NT, int MT>
@@ -153,77 +154,202 @@ __device__ __forceinline__ uint2 xfrag(const uint16_t* xp, int bi, int M, int to
     return __ldg(reinterpret_cast<const uint2*>(xp + bi * MM * 16 + tok_nt));
 }
 
+// One warp's view of a tile: rows, K slice and pointers at the first step of its slice.
+struct TileView {
+    bool valid;
+    int p, tile, rtiles, ks, rt, slice, steps;
+    int64_t l;
+};
+
+__device__ __forceinline__ TileView view_tile(const SParams& P, int64_t T, int warp) {
+    TileView v;
+    v.valid = T < P.total_tiles;
+    if (!v.valid) return v;
+    int p = 0;
+    while (p + 1 < P.count && T >= P.d[p + 1].tile_begin) ++p;
+    const SDesc& D = P.d[p];
+    const int64_t local = T - D.tile_begin;
+    v.p = p;
+    v.l = local / D.tiles;
+    v.tile = (int)(local - v.l * D.tiles);
+    v.ks = D.ks;
+    v.rtiles = kWarps / D.ks;
+    v.rt = warp / D.ks;
+    v.slice = warp - v.rt * D.ks;
+    const int nsteps = D.K / 256;
+    const int s_begin = (int)((int64_t)nsteps * v.slice / D.ks);
+    v.steps = (int)((int64_t)nsteps * (v.slice + 1) / D.ks) - s_begin;
+    v.tile = v.tile;
+    return v;
+}
+
+// Streams one thread's two rows, step after step, across the tiles of its CTA.
+template <int FMT, int MT>
+struct Loader {
+    const uint8_t *cg, *cg8;
+    const uint16_t *sg, *sg8, *zg, *zg8;   // 2-bit scales/offsets (NF4: sg/sg8 hold the absmax rows)
+    const uint16_t* xs;                    // x fragment of this lane at the current step
+    int step, steps;
+    int64_t T;
+    bool valid;
+
+    __device__ __forceinline__ void open(const SParams& P, int64_t T_, int warp, int g, int t) {
+        T = T_;
+        const TileView v = view_tile(P, T, warp);
+        valid = v.valid;
+        if (!valid) return;
+        const SDesc& D = P.d[v.p];
+        const int M = MT > 0 ? MT : P.M;
+        const int N = D.N, K = D.K;
+        const int rg = (v.tile * v.rtiles + v.rt) * 16 + g, rg8 = rg + 8;
+        const int64_t r0 = rg < N ? rg : 0, r1 = rg8 < N ? rg8 : 0;   // rows past N read row 0, never stored
+        const int s_begin = (int)((int64_t)(K / 256) * v.slice / v.ks);
+        const uint8_t* codes = D.codes + v.l * D.stride_codes;
+        const char* sc = static_cast<const char*>(D.scales) + v.l * D.stride_scales;
+        if (FMT == LQ_FMT_2BIT_LM_G32) {
+            const uint16_t* s16 = reinterpret_cast<const uint16_t*>(sc);
+            const uint16_t* o16 = reinterpret_cast<const uint16_t*>(reinterpret_cast<const char*>(D.offsets) + v.l * D.stride_offsets);
+            cg = codes + r0 * (K / 4) + 16 * t + 64 * s_begin;
+            cg8 = codes + r1 * (K / 4) + 16 * t + 64 * s_begin;
+            sg = s16 + r0 * (K / 32) + 2 * t + 8 * s_begin;
+            sg8 = s16 + r1 * (K / 32) + 2 * t + 8 * s_begin;
+            zg = o16 + r0 * (K / 32) + 2 * t + 8 * s_begin;
+            zg8 = o16 + r1 * (K / 32) + 2 * t + 8 * s_begin;
+        } else {
+            const float* am = reinterpret_cast<const float*>(sc);
+            cg = codes + r0 * (K / 2) + 8 * t + 128 * s_begin;
+            cg8 = codes + r1 * (K / 2) + 8 * t + 128 * s_begin;
+            sg = reinterpret_cast<const uint16_t*>(am + r0 * (K / 64) + 4 * s_begin);
+            sg8 = reinterpret_cast<const uint16_t*>(am + r1 * (K / 64) + 4 * s_begin);
+        }
+        const int MM = MT > 0 ? MT : M;
+        xs = D.xperm + v.l * D.xperm_stride + min(g, M - 1) * 16 + t * 4 + (int64_t)s_begin * 256 * MM;
+        step = 0;
+        steps = v.steps;
+    }
+    __device__ __forceinline__ void advance(const SParams& P, int warp, int g, int t) {
+        if (++step < steps) {
+            const int MM = MT > 0 ? MT : P.M;
+            if (FMT == LQ_FMT_2BIT_LM_G32) {
+                cg += 64; cg8 += 64; sg += 8; sg8 += 8; zg += 8; zg8 += 8;
+            } else {
+                cg += 128; cg8 += 128; sg += 8; sg8 += 8;   // 4 floats
+            }
+            xs += 256 * MM;
+        } else {
+            open(P, T + gridDim.x, warp, g, t);
+        }
+    }
+};
+
 struct Step2 {
     uint4 c0, c1;
     uint32_t s0, z0, s1, z1;
+    const uint16_t* xs;
+    int flags;   // bit 0: valid, bit 1: last step of its tile
 };
 
 struct StepNF4 {
     uint2 c0[4], c1[4];
     float a0[4], a1[4];
+    const uint16_t* xs;
+    int flags;
 };
 
 template <int FMT, int MT, int NT>
 __global__ void __launch_bounds__(kThreadsS) gemv_stream_kernel(const __grid_constant__ SParams P) {
     __shared__ float red[kWarps][16][(NT * 8) + 1];
-    const int64_t bid = blockIdx.x;
-    int p = 0;
-    while (p + 1 < P.count && bid >= P.d[p + 1].block_begin) ++p;
-    const SDesc& D = P.d[p];
-    const int64_t local = bid - D.block_begin;
-    const int64_t l = local / D.tiles;
-    const int tile = (int)(local - l * D.tiles);
     const int M = MT > 0 ? MT : P.M;
-    const int N = D.N, K = D.K, ks = D.ks, rtiles = kWarps / ks;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    const int rt = warp / ks, slice = warp - rt * ks;
-    const int rg = (tile * rtiles + rt) * 16 + g, rg8 = rg + 8;
-    const int64_t rgc = rg < N ? rg : 0, rg8c = rg8 < N ? rg8 : 0;
-
-    // this warp's slice of K in 256-column steps
-    const int nsteps = K / 256;
-    const int s_begin = (int)((int64_t)nsteps * slice / ks), s_end = (int)((int64_t)nsteps * (slice + 1) / ks);
+    int tok[NT];   // x-fragment offset of each n-tile's token (clamped to the last real token)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) tok[nt] = (min(8 * nt + g, M - 1) - min(g, M - 1)) * 16;
 
     float acc[NT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
 
-    // Rows past N read row 0 (results for them are never stored), so every load is unconditional.
-    const uint8_t* codes = D.codes + l * D.stride_codes;
-    const int MM = MT > 0 ? MT : M;
-    // token of each n-tile for this lane, clamped to the last real token
-    int tok[NT];
+    // The finished tile: anchors of this warp, then the K-slice reduction and the store of y.
+    int64_t T = blockIdx.x;
+    auto finish_tile = [&]() {
+        const TileView v = view_tile(P, T, warp);
+        const SDesc& D = P.d[v.p];
+        const int N = D.N;
+        const int rg = (v.tile * v.rtiles + v.rt) * 16 + g, rg8 = rg + 8;
+        if (FMT == LQ_FMT_2BIT_LM_G32 && D.A > 0) {
+            const int64_t r0 = rg < N ? rg : 0, r1 = rg8 < N ? rg8 : 0;
+            const uint16_t* aw = reinterpret_cast<const uint16_t*>(reinterpret_cast<const char*>(D.anchor_w) + v.l * D.stride_anchor_w);
+            const uint16_t* awg = aw + r0 * D.ld_anchor;
+            const uint16_t* awg8 = aw + r1 * D.ld_anchor;
+            const uint16_t* xa = D.xaperm + v.l * D.xaperm_stride + min(g, M - 1) * 16 + t * 4;
+            const int A = D.A;
+            const int MM = MT > 0 ? MT : M;
+            auto pair = [&](const uint16_t* row, int a) -> uint32_t {
+                if (a >= A) return 0u;
+                const uint32_t w = ldg32(row + a);
+                return (a + 1 < A) ? w : (w & 0xFFFFu);
+            };
+            for (int ab = v.slice; ab < (A + 15) / 16; ab += v.ks) {
+                const int a = 16 * ab + 2 * t;
+                const uint32_t a0 = pair(awg, a), a2 = pair(awg, a + 8);
+                const uint32_t a1 = pair(awg8, a), a3 = pair(awg8, a + 8);
+                uint2 xb[NT];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) tok[nt] = (min(8 * nt + g, M - 1) - min(g, M - 1)) * 16;
-    const uint16_t* xp = D.xperm + l * D.xperm_stride + min(g, M - 1) * 16 + t * 4 + (int64_t)s_begin * 256 * MM;
-    const int steps = s_end - s_begin;
+                for (int nt = 0; nt < NT; ++nt) xb[nt] = __ldg(reinterpret_cast<const uint2*>(xa + ab * MM * 16 + tok[nt]));
+                mma_xg<NT, MT>(acc, a0, a1, a2, a3, xb);
+            }
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int m0 = 8 * nt + 2 * t, m1 = m0 + 1;
+            if (m0 < M) {
+                red[warp][g][m0] = acc[nt][0];
+                red[warp][g + 8][m0] = acc[nt][2];
+            }
+            if (m1 < M) {
+                red[warp][g][m1] = acc[nt][1];
+                red[warp][g + 8][m1] = acc[nt][3];
+            }
+            acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+        }
+        __syncthreads();
+        void* y = static_cast<char*>(D.y) + v.l * D.stride_y;
+        const int ks = v.ks;
+        for (int idx = threadIdx.x; idx < v.rtiles * 16 * M; idx += kThreadsS) {
+            const int rtile = idx / (16 * M), rem = idx - rtile * 16 * M;
+            const int m = rem / 16, r = rem - m * 16;
+            const int n = (v.tile * v.rtiles + rtile) * 16 + r;
+            if (n >= N) continue;
+            float sum = 0.f;
+            for (int sl = 0; sl < ks; ++sl) sum += red[rtile * ks + sl][r][m];
+            store_out(y, (size_t)m * N + n, P.y_dtype, sum);
+        }
+        __syncthreads();
+        T += gridDim.x;
+    };
+
+    Loader<FMT, MT> L;
+    L.open(P, blockIdx.x, warp, g, t);
 
     if (FMT == LQ_FMT_2BIT_LM_G32) {
-        const uint16_t* sc = reinterpret_cast<const uint16_t*>(static_cast<const char*>(D.scales) + l * D.stride_scales);
-        const uint16_t* of = reinterpret_cast<const uint16_t*>(reinterpret_cast<const char*>(D.offsets) + l * D.stride_offsets);
-        const uint8_t* cg = codes + rgc * (K / 4) + 16 * t + 64 * s_begin;
-        const uint8_t* cg8 = codes + rg8c * (K / 4) + 16 * t + 64 * s_begin;
-        const uint16_t* sg = sc + rgc * (K / 32) + 2 * t + 8 * s_begin;
-        const uint16_t* sg8 = sc + rg8c * (K / 32) + 2 * t + 8 * s_begin;
-        const uint16_t* zg = of + rgc * (K / 32) + 2 * t + 8 * s_begin;
-        const uint16_t* zg8 = of + rg8c * (K / 32) + 2 * t + 8 * s_begin;
-        // step i of this warp's slice (i clamped into the slice: loads past the end repeat the last step)
-        auto load = [&](Step2& f, int i) {
-            i = min(i, steps - 1);
-            f.c0 = ldg128(cg + 64 * i);
-            f.c1 = ldg128(cg8 + 64 * i);
-            f.s0 = ldg32(sg + 8 * i);
-            f.z0 = ldg32(zg + 8 * i);
-            f.s1 = ldg32(sg8 + 8 * i);
-            f.z1 = ldg32(zg8 + 8 * i);
+        auto issue = [&](Step2& f) {
+            f.flags = L.valid ? 1 | (L.step + 1 == L.steps ? 2 : 0) : 0;
+            if (!L.valid) return;
+            f.c0 = ldg128(L.cg);
+            f.c1 = ldg128(L.cg8);
+            f.s0 = ldg32(L.sg);
+            f.z0 = ldg32(L.zg);
+            f.s1 = ldg32(L.sg8);
+            f.z1 = ldg32(L.zg8);
+            f.xs = L.xs;
+            L.advance(P, warp, g, t);
         };
-        auto compute = [&](const Step2& f, int i) {
-            const uint16_t* xs = xp + (int64_t)i * 256 * MM;
+        auto compute = [&](const Step2& f) {
             uint2 xb[16][NT];
 #pragma unroll
             for (int b = 0; b < 16; ++b)
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) xb[b][nt] = xfrag<MT>(xs, b, M, tok[nt]);
+                for (int nt = 0; nt < NT; ++nt) xb[b][nt] = xfrag<MT>(f.xs, b, M, tok[nt]);
             uint32_t RA[4], RB[4];
             lut2_bits((uint16_t)f.s0, (uint16_t)f.z0, RA[0], RB[0]);
             lut2_bits((uint16_t)(f.s0 >> 16), (uint16_t)(f.z0 >> 16), RA[1], RB[1]);
@@ -241,71 +367,51 @@ __global__ void __launch_bounds__(kThreadsS) gemv_stream_kernel(const __grid_con
                     mma_xg<NT, MT>(acc, a0, a1, a2, a3, xb[ii * 4 + j]);
                 }
             }
+            if (f.flags & 2) finish_tile();
         };
-        // three register buffers, two steps in flight, unrolled so the buffers never move
+        // three register buffers, two steps in flight across tile boundaries, unrolled so
+        // the buffers never move
         Step2 fa, fb, fc;
-        load(fa, 0);
-        load(fb, 1);
-        pdl_wait();   // the x passes have finished
-        for (int i = 0; i < steps; i += 3) {
-            load(fc, i + 2);
-            compute(fa, i);
-            if (i + 1 >= steps) break;
-            load(fa, i + 3);
-            compute(fb, i + 1);
-            if (i + 2 >= steps) break;
-            load(fb, i + 4);
-            compute(fc, i + 2);
-        }
-        // anchors: binary16 weights straight into the A fragment, blocks shared round-robin by the slices
-        if (D.A > 0) {
-            const uint16_t* aw = reinterpret_cast<const uint16_t*>(reinterpret_cast<const char*>(D.anchor_w) + l * D.stride_anchor_w);
-            const uint16_t* awg = aw + rgc * D.ld_anchor;
-            const uint16_t* awg8 = aw + rg8c * D.ld_anchor;
-            const uint16_t* xa = D.xaperm + l * D.xaperm_stride + min(g, M - 1) * 16 + t * 4;
-            const int A = D.A;
-            auto pair = [&](const uint16_t* row, int a) -> uint32_t {
-                if (a >= A) return 0u;
-                const uint32_t w = ldg32(row + a);
-                return (a + 1 < A) ? w : (w & 0xFFFFu);
-            };
-            for (int ab = slice; ab < (A + 15) / 16; ab += ks) {
-                const int a = 16 * ab + 2 * t;
-                const uint32_t a0 = pair(awg, a), a2 = pair(awg, a + 8);
-                const uint32_t a1 = pair(awg8, a), a3 = pair(awg8, a + 8);
-                uint2 xb[NT];
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) xb[nt] = xfrag<MT>(xa, ab, M, tok[nt]);
-                mma_xg<NT, MT>(acc, a0, a1, a2, a3, xb);
-            }
+        issue(fa);
+        issue(fb);
+        pdl_wait();   // the x pre-pass has finished
+        for (;;) {
+            if (!(fa.flags & 1)) break;
+            issue(fc);
+            compute(fa);
+            if (!(fb.flags & 1)) break;
+            issue(fa);
+            compute(fb);
+            if (!(fc.flags & 1)) break;
+            issue(fb);
+            compute(fc);
         }
     } else {
-        const float* am = reinterpret_cast<const float*>(static_cast<const char*>(D.scales) + l * D.stride_scales);
-        const uint8_t* cg = codes + rgc * (K / 2) + 8 * t + 128 * s_begin;
-        const uint8_t* cg8 = codes + rg8c * (K / 2) + 8 * t + 128 * s_begin;
-        const float* ag = am + rgc * (K / 64) + 4 * s_begin;
-        const float* ag8 = am + rg8c * (K / 64) + 4 * s_begin;
         uint32_t TL[4], TH[4];
         nf4_tables(TL, TH);
-        auto load = [&](StepNF4& f, int i) {
-            i = min(i, steps - 1);
+        auto issue = [&](StepNF4& f) {
+            f.flags = L.valid ? 1 | (L.step + 1 == L.steps ? 2 : 0) : 0;
+            if (!L.valid) return;
+            const float* ag = reinterpret_cast<const float*>(L.sg);
+            const float* ag8 = reinterpret_cast<const float*>(L.sg8);
 #pragma unroll
             for (int nb = 0; nb < 4; ++nb) {
-                f.c0[nb] = ldg64(cg + 128 * i + 32 * nb);
-                f.c1[nb] = ldg64(cg8 + 128 * i + 32 * nb);
-                f.a0[nb] = __ldg(ag + 4 * i + nb);
-                f.a1[nb] = __ldg(ag8 + 4 * i + nb);
+                f.c0[nb] = ldg64(L.cg + 32 * nb);
+                f.c1[nb] = ldg64(L.cg8 + 32 * nb);
+                f.a0[nb] = __ldg(ag + nb);
+                f.a1[nb] = __ldg(ag8 + nb);
             }
+            f.xs = L.xs;
+            L.advance(P, warp, g, t);
         };
-        auto compute = [&](const StepNF4& f, int i) {
-            const uint16_t* xs = xp + (int64_t)i * 256 * MM;
+        auto compute = [&](const StepNF4& f) {
 #pragma unroll
             for (int nb = 0; nb < 4; ++nb) {
                 uint2 xb[4][NT];
 #pragma unroll
                 for (int b = 0; b < 4; ++b)
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) xb[b][nt] = xfrag<MT>(xs, nb * 4 + b, M, tok[nt]);
+                    for (int nt = 0; nt < NT; ++nt) xb[b][nt] = xfrag<MT>(f.xs, nb * 4 + b, M, tok[nt]);
                 float part[NT][4];
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) part[nt][0] = part[nt][1] = part[nt][2] = part[nt][3] = 0.f;
@@ -324,50 +430,31 @@ __global__ void __launch_bounds__(kThreadsS) gemv_stream_kernel(const __grid_con
                     acc[nt][3] = __fmaf_rn(f.a1[nb], part[nt][3], acc[nt][3]);
                 }
             }
+            if (f.flags & 2) finish_tile();
         };
         StepNF4 fa, fb;
-        load(fa, 0);
+        issue(fa);
         pdl_wait();
-        for (int i = 0; i < steps; i += 2) {
-            load(fb, i + 1);
-            compute(fa, i);
-            if (i + 1 >= steps) break;
-            load(fa, i + 2);
-            compute(fb, i + 1);
+        for (;;) {
+            if (!(fa.flags & 1)) break;
+            issue(fb);
+            compute(fa);
+            if (!(fb.flags & 1)) break;
+            issue(fa);
+            compute(fb);
         }
-    }
-
-    // ---- reduce the K slices of each row tile in shared memory, then store y
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-        const int m0 = 8 * nt + 2 * t, m1 = m0 + 1;
-        if (m0 < M) {
-            red[warp][g][m0] = acc[nt][0];
-            red[warp][g + 8][m0] = acc[nt][2];
-        }
-        if (m1 < M) {
-            red[warp][g][m1] = acc[nt][1];
-            red[warp][g + 8][m1] = acc[nt][3];
-        }
-    }
-    __syncthreads();
-    void* y = static_cast<char*>(D.y) + l * D.stride_y;
-    for (int idx = threadIdx.x; idx < rtiles * 16 * M; idx += kThreadsS) {
-        const int rtile = idx / (16 * M), rem = idx - rtile * 16 * M;
-        const int m = rem / 16, r = rem - m * 16;
-        const int n = (tile * rtiles + rtile) * 16 + r;
-        if (n >= N) continue;
-        float sum = 0.f;
-        for (int sl = 0; sl < ks; ++sl) sum += red[rtile * ks + sl][r][m];
-        store_out(y, (size_t)m * N + n, P.y_dtype, sum);
     }
 }
 
 template <int FMT, int MT, int NT>
-lq_status launch_s(const SParams& P, int64_t blocks, cudaStream_t stream) {
+lq_status launch_s(const SParams& P, int64_t tiles, int num_sms, cudaStream_t stream) {
+    static int per_sm = 0;   // resident CTAs per SM for this instantiation
+    if (per_sm == 0 && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_stream_kernel<FMT, MT, NT>, kThreadsS, 0) != cudaSuccess)
+        return LQ_ERR_CUDA;
+    const int64_t grid = std::min<int64_t>(tiles, (int64_t)num_sms * std::max(1, per_sm));
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof(cfg));
-    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(kThreadsS);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -380,19 +467,19 @@ lq_status launch_s(const SParams& P, int64_t blocks, cudaStream_t stream) {
 }
 
 template <int FMT>
-lq_status launch_s_fmt(const SParams& P, int64_t blocks, cudaStream_t stream) {
+lq_status launch_s_fmt(const SParams& P, int64_t tiles, int num_sms, cudaStream_t stream) {
     switch (P.M) {
-        case 1: return launch_s<FMT, 1, 1>(P, blocks, stream);
-        case 2: return launch_s<FMT, 2, 1>(P, blocks, stream);
-        case 3: return launch_s<FMT, 3, 1>(P, blocks, stream);
-        case 4: return launch_s<FMT, 4, 1>(P, blocks, stream);
-        case 5: return launch_s<FMT, 5, 1>(P, blocks, stream);
-        case 6: return launch_s<FMT, 6, 1>(P, blocks, stream);
-        case 7: return launch_s<FMT, 7, 1>(P, blocks, stream);
-        case 8: return launch_s<FMT, 8, 1>(P, blocks, stream);
+        case 1: return launch_s<FMT, 1, 1>(P, tiles, num_sms, stream);
+        case 2: return launch_s<FMT, 2, 1>(P, tiles, num_sms, stream);
+        case 3: return launch_s<FMT, 3, 1>(P, tiles, num_sms, stream);
+        case 4: return launch_s<FMT, 4, 1>(P, tiles, num_sms, stream);
+        case 5: return launch_s<FMT, 5, 1>(P, tiles, num_sms, stream);
+        case 6: return launch_s<FMT, 6, 1>(P, tiles, num_sms, stream);
+        case 7: return launch_s<FMT, 7, 1>(P, tiles, num_sms, stream);
+        case 8: return launch_s<FMT, 8, 1>(P, tiles, num_sms, stream);
         default:
-            if (P.M <= 16) return launch_s<FMT, 0, 2>(P, blocks, stream);
-            return launch_s<FMT, 0, 4>(P, blocks, stream);
+            if (P.M <= 16) return launch_s<FMT, 0, 2>(P, tiles, num_sms, stream);
+            return launch_s<FMT, 0, 4>(P, tiles, num_sms, stream);
     }
 }
 
@@ -450,7 +537,7 @@ lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* probs, i
         while (d.ks > 1 && steps < spw * d.ks) d.ks /= 2;
         const int rows_per_cta = 16 * (kWarps / d.ks);
         d.tiles = (q.N + rows_per_cta - 1) / rows_per_cta;
-        d.block_begin = blocks;
+        d.tile_begin = blocks;
         blocks += (int64_t)q.batch * d.tiles;
         const int a_pad = A > 0 ? round_up(A, 64) : 0;
         d.xperm_stride = (int64_t)M * q.K;
@@ -492,8 +579,9 @@ lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* probs, i
     if (prep_smem > 48 * 1024) return LQ_ERR_UNSUPPORTED;
     xprep_kernel<<<(unsigned)Q.total_ctas, 256, prep_smem, stream>>>(Q);
     if (cudaPeekAtLastError() != cudaSuccess) return LQ_ERR_CUDA;
-    if (fmt == LQ_FMT_2BIT_LM_G32) return launch_s_fmt<LQ_FMT_2BIT_LM_G32>(P, blocks, stream);
-    return launch_s_fmt<LQ_FMT_NF4_B64>(P, blocks, stream);
+    P.total_tiles = blocks;
+    if (fmt == LQ_FMT_2BIT_LM_G32) return launch_s_fmt<LQ_FMT_2BIT_LM_G32>(P, blocks, ws.num_sms, stream);
+    return launch_s_fmt<LQ_FMT_NF4_B64>(P, blocks, ws.num_sms, stream);
 }
 
 }  // namespace lq
