@@ -188,7 +188,7 @@ template <int FMT, int MT>
 struct Loader {
     const uint8_t *cg, *cg8;
     const uint16_t *sg, *sg8, *zg, *zg8;   // 2-bit scales/offsets (NF4: sg/sg8 hold the absmax rows)
-    const uint16_t* xs;                    // x fragment of this lane at the current step
+    const uint16_t* xsrc;                  // this step's x slice in the permuted copy (+ 8 halves per lane)
     int step, steps;
     int64_t T;
     bool valid;
@@ -223,19 +223,18 @@ struct Loader {
             sg8 = reinterpret_cast<const uint16_t*>(am + r1 * (K / 64) + 4 * s_begin);
         }
         const int MM = MT > 0 ? MT : M;
-        xs = D.xperm + v.l * D.xperm_stride + min(g, M - 1) * 16 + t * 4 + (int64_t)s_begin * 256 * MM;
+        xsrc = D.xperm + v.l * D.xperm_stride + (int64_t)s_begin * 256 * MM + (threadIdx.x & 31) * 8;
         step = 0;
         steps = v.steps;
     }
     __device__ __forceinline__ void advance(const SParams& P, int warp, int g, int t) {
         if (++step < steps) {
-            const int MM = MT > 0 ? MT : P.M;
             if (FMT == LQ_FMT_2BIT_LM_G32) {
                 cg += 64; cg8 += 64; sg += 8; sg8 += 8; zg += 8; zg8 += 8;
             } else {
                 cg += 128; cg8 += 128; sg += 8; sg8 += 8;   // 4 floats
             }
-            xs += 256 * MM;
+            xsrc += 256 * (MT > 0 ? MT : P.M);
         } else {
             open(P, T + gridDim.x, warp, g, t);
         }
@@ -245,22 +244,30 @@ struct Loader {
 struct Step2 {
     uint4 c0, c1;
     uint32_t s0, z0, s1, z1;
-    const uint16_t* xs;
-    int flags;   // bit 0: valid, bit 1: last step of its tile
 };
 
 struct StepNF4 {
     uint2 c0[4], c1[4];
     float a0[4], a1[4];
-    const uint16_t* xs;
-    int flags;
 };
 
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem)), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
 template <int FMT, int MT, int NT>
-__global__ void __launch_bounds__(kThreadsS) gemv_stream_kernel(const __grid_constant__ SParams P) {
+__global__ void __launch_bounds__(kThreadsS, 2) gemv_stream_kernel(const __grid_constant__ SParams P) {
     __shared__ float red[kWarps][16][(NT * 8) + 1];
+    // per warp, three x slices of one 256-column step each (binary16, fragment order)
+    extern __shared__ __align__(16) uint16_t xring[];
     const int M = MT > 0 ? MT : P.M;
+    const int MM = MT > 0 ? MT : M;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    uint16_t* xw = xring + warp * 3 * 256 * MM;             // this warp's ring
+    const int xlane = min(g, M - 1) * 16 + t * 4;            // this lane's fragment inside a block
     int tok[NT];   // x-fragment offset of each n-tile's token (clamped to the last real token)
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) tok[nt] = (min(8 * nt + g, M - 1) - min(g, M - 1)) * 16;
@@ -271,8 +278,10 @@ __global__ void __launch_bounds__(kThreadsS) gemv_stream_kernel(const __grid_con
 
     // The finished tile: anchors of this warp, then the K-slice reduction and the store of y.
     int64_t T = blockIdx.x;
+    TileView CV = view_tile(P, T, warp);
+    int cstep = 0;
     auto finish_tile = [&]() {
-        const TileView v = view_tile(P, T, warp);
+        const TileView v = CV;
         const SDesc& D = P.d[v.p];
         const int N = D.N;
         const int rg = (v.tile * v.rtiles + v.rt) * 16 + g, rg8 = rg + 8;
@@ -281,9 +290,8 @@ __global__ void __launch_bounds__(kThreadsS) gemv_stream_kernel(const __grid_con
             const uint16_t* aw = reinterpret_cast<const uint16_t*>(reinterpret_cast<const char*>(D.anchor_w) + v.l * D.stride_anchor_w);
             const uint16_t* awg = aw + r0 * D.ld_anchor;
             const uint16_t* awg8 = aw + r1 * D.ld_anchor;
-            const uint16_t* xa = D.xaperm + v.l * D.xaperm_stride + min(g, M - 1) * 16 + t * 4;
+            const uint16_t* xa = D.xaperm + v.l * D.xaperm_stride + xlane;
             const int A = D.A;
-            const int MM = MT > 0 ? MT : M;
             auto pair = [&](const uint16_t* row, int a) -> uint32_t {
                 if (a >= A) return 0u;
                 const uint32_t w = ldg32(row + a);
@@ -326,14 +334,27 @@ __global__ void __launch_bounds__(kThreadsS) gemv_stream_kernel(const __grid_con
         }
         __syncthreads();
         T += gridDim.x;
+        CV = view_tile(P, T, warp);
+        cstep = 0;
+    };
+    auto step_done = [&]() {
+        if (++cstep == CV.steps) finish_tile();
     };
 
     Loader<FMT, MT> L;
     L.open(P, blockIdx.x, warp, g, t);
+    // the x slice of a step (source `src`) goes to ring slot `slot`, one commit group per step
+    auto issue_x = [&](int slot, const uint16_t* src, bool valid) {
+        if (valid) {
+            uint16_t* dst = xw + slot * 256 * MM + lane * 8;
+#pragma unroll
+            for (int c = 0; c < MM; ++c) cp_async16(dst + c * 256, src + c * 256);
+        }
+        cp_async_commit();
+    };
 
     if (FMT == LQ_FMT_2BIT_LM_G32) {
-        auto issue = [&](Step2& f) {
-            f.flags = L.valid ? 1 | (L.step + 1 == L.steps ? 2 : 0) : 0;
+        auto issue_w = [&](Step2& f) {
             if (!L.valid) return;
             f.c0 = ldg128(L.cg);
             f.c1 = ldg128(L.cg8);
@@ -341,15 +362,21 @@ __global__ void __launch_bounds__(kThreadsS) gemv_stream_kernel(const __grid_con
             f.z0 = ldg32(L.zg);
             f.s1 = ldg32(L.sg8);
             f.z1 = ldg32(L.zg8);
-            f.xs = L.xs;
             L.advance(P, warp, g, t);
         };
-        auto compute = [&](const Step2& f) {
+        auto issue = [&](Step2& f, int slot) {
+            issue_x(slot, L.xsrc, L.valid);
+            issue_w(f);
+        };
+        auto compute = [&](const Step2& f, int slot) {
+            cp_async_wait<2>();   // this step's x slice has landed (the two later ones may be in flight)
+            __syncwarp();
+            const uint16_t* xs = xw + slot * 256 * MM + xlane;
             uint2 xb[16][NT];
 #pragma unroll
             for (int b = 0; b < 16; ++b)
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) xb[b][nt] = xfrag<MT>(f.xs, b, M, tok[nt]);
+                for (int nt = 0; nt < NT; ++nt) xb[b][nt] = *reinterpret_cast<const uint2*>(xs + b * MM * 16 + tok[nt]);
             uint32_t RA[4], RB[4];
             lut2_bits((uint16_t)f.s0, (uint16_t)f.z0, RA[0], RB[0]);
             lut2_bits((uint16_t)(f.s0 >> 16), (uint16_t)(f.z0 >> 16), RA[1], RB[1]);
@@ -367,30 +394,37 @@ __global__ void __launch_bounds__(kThreadsS) gemv_stream_kernel(const __grid_con
                     mma_xg<NT, MT>(acc, a0, a1, a2, a3, xb[ii * 4 + j]);
                 }
             }
-            if (f.flags & 2) finish_tile();
+            __syncwarp();   // every lane has read this slot before it is refilled
+            step_done();
         };
-        // three register buffers, two steps in flight across tile boundaries, unrolled so
-        // the buffers never move
+        // three register buffers (and x slots), two steps in flight across tile boundaries,
+        // unrolled so the buffers never move
         Step2 fa, fb, fc;
-        issue(fa);
-        issue(fb);
-        pdl_wait();   // the x pre-pass has finished
+        // weights of the first two steps before waiting for the x pre-pass, then their x slices
+        const uint16_t* xs0 = L.xsrc;
+        const bool v0 = L.valid;
+        issue_w(fa);
+        const uint16_t* xs1 = L.xsrc;
+        const bool v1 = L.valid;
+        issue_w(fb);
+        pdl_wait();
+        issue_x(0, xs0, v0);
+        issue_x(1, xs1, v1);
         for (;;) {
-            if (!(fa.flags & 1)) break;
-            issue(fc);
-            compute(fa);
-            if (!(fb.flags & 1)) break;
-            issue(fa);
-            compute(fb);
-            if (!(fc.flags & 1)) break;
-            issue(fb);
-            compute(fc);
+            if (!CV.valid) break;
+            issue(fc, 2);
+            compute(fa, 0);
+            if (!CV.valid) break;
+            issue(fa, 0);
+            compute(fb, 1);
+            if (!CV.valid) break;
+            issue(fb, 1);
+            compute(fc, 2);
         }
     } else {
         uint32_t TL[4], TH[4];
         nf4_tables(TL, TH);
-        auto issue = [&](StepNF4& f) {
-            f.flags = L.valid ? 1 | (L.step + 1 == L.steps ? 2 : 0) : 0;
+        auto issue_w = [&](StepNF4& f) {
             if (!L.valid) return;
             const float* ag = reinterpret_cast<const float*>(L.sg);
             const float* ag8 = reinterpret_cast<const float*>(L.sg8);
@@ -401,17 +435,23 @@ __global__ void __launch_bounds__(kThreadsS) gemv_stream_kernel(const __grid_con
                 f.a0[nb] = __ldg(ag + nb);
                 f.a1[nb] = __ldg(ag8 + nb);
             }
-            f.xs = L.xs;
             L.advance(P, warp, g, t);
         };
-        auto compute = [&](const StepNF4& f) {
+        auto issue = [&](StepNF4& f, int slot) {
+            issue_x(slot, L.xsrc, L.valid);
+            issue_w(f);
+        };
+        auto compute = [&](const StepNF4& f, int slot) {
+            cp_async_wait<1>();
+            __syncwarp();
+            const uint16_t* xs = xw + slot * 256 * MM + xlane;
 #pragma unroll
             for (int nb = 0; nb < 4; ++nb) {
                 uint2 xb[4][NT];
 #pragma unroll
                 for (int b = 0; b < 4; ++b)
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) xb[b][nt] = xfrag<MT>(f.xs, nb * 4 + b, M, tok[nt]);
+                    for (int nt = 0; nt < NT; ++nt) xb[b][nt] = *reinterpret_cast<const uint2*>(xs + (nb * 4 + b) * MM * 16 + tok[nt]);
                 float part[NT][4];
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) part[nt][0] = part[nt][1] = part[nt][2] = part[nt][3] = 0.f;
@@ -430,32 +470,45 @@ __global__ void __launch_bounds__(kThreadsS) gemv_stream_kernel(const __grid_con
                     acc[nt][3] = __fmaf_rn(f.a1[nb], part[nt][3], acc[nt][3]);
                 }
             }
-            if (f.flags & 2) finish_tile();
+            __syncwarp();
+            step_done();
         };
         StepNF4 fa, fb;
-        issue(fa);
+        const uint16_t* xs0 = L.xsrc;
+        const bool v0 = L.valid;
+        issue_w(fa);
         pdl_wait();
+        issue_x(0, xs0, v0);
         for (;;) {
-            if (!(fa.flags & 1)) break;
-            issue(fb);
-            compute(fa);
-            if (!(fb.flags & 1)) break;
-            issue(fa);
-            compute(fb);
+            if (!CV.valid) break;
+            issue(fb, 1);
+            compute(fa, 0);
+            if (!CV.valid) break;
+            issue(fa, 0);
+            compute(fb, 1);
         }
     }
 }
 
 template <int FMT, int MT, int NT>
 lq_status launch_s(const SParams& P, int64_t tiles, int num_sms, cudaStream_t stream) {
-    static int per_sm = 0;   // resident CTAs per SM for this instantiation
-    if (per_sm == 0 && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_stream_kernel<FMT, MT, NT>, kThreadsS, 0) != cudaSuccess)
-        return LQ_ERR_CUDA;
+    const size_t smem = (size_t)kWarps * 3 * 256 * P.M * sizeof(uint16_t);   // x rings
+    static int per_sm = 0;   // resident CTAs per SM for this instantiation (same smem for a given M)
+    static size_t per_sm_smem = 0;
+    if (per_sm == 0 || per_sm_smem != smem) {
+        if (smem > 48 * 1024 &&
+            cudaFuncSetAttribute(gemv_stream_kernel<FMT, MT, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+            return LQ_ERR_CUDA;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_stream_kernel<FMT, MT, NT>, kThreadsS, smem) != cudaSuccess)
+            return LQ_ERR_CUDA;
+        per_sm_smem = smem;
+    }
     const int64_t grid = std::min<int64_t>(tiles, (int64_t)num_sms * std::max(1, per_sm));
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof(cfg));
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(kThreadsS);
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -477,9 +530,7 @@ lq_status launch_s_fmt(const SParams& P, int64_t tiles, int num_sms, cudaStream_
         case 6: return launch_s<FMT, 6, 1>(P, tiles, num_sms, stream);
         case 7: return launch_s<FMT, 7, 1>(P, tiles, num_sms, stream);
         case 8: return launch_s<FMT, 8, 1>(P, tiles, num_sms, stream);
-        default:
-            if (P.M <= 16) return launch_s<FMT, 0, 2>(P, tiles, num_sms, stream);
-            return launch_s<FMT, 0, 4>(P, tiles, num_sms, stream);
+        default: return LQ_ERR_UNSUPPORTED;   // more than 8 tokens: the split-K kernel
     }
 }
 
@@ -488,6 +539,7 @@ int round_up(int a, int b) { return (a + b - 1) / b * b; }
 }  // namespace
 
 bool gemv_stream_eligible(const lq_problem* probs, int count) {
+    if (probs[0].M > 8) return false;   // the x rings (3 steps x M tokens per warp) must stay small
     for (int i = 0; i < count; ++i)
         if (probs[i].K % 256 != 0) return false;
     return true;
