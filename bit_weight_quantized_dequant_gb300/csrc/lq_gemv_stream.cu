@@ -496,8 +496,8 @@ lq_status launch_s(const SParams& P, int64_t tiles, int num_sms, cudaStream_t st
     static int per_sm = 0;   // resident CTAs per SM for this instantiation (same smem for a given M)
     static size_t per_sm_smem = 0;
     if (per_sm == 0 || per_sm_smem != smem) {
-        if (smem > 48 * 1024 &&
-            cudaFuncSetAttribute(gemv_stream_kernel<FMT, MT, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        // static reduction buffer + dynamic x rings may pass the 48 KiB default: always opt in
+        if (cudaFuncSetAttribute(gemv_stream_kernel<FMT, MT, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
             return LQ_ERR_CUDA;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_stream_kernel<FMT, MT, NT>, kThreadsS, smem) != cudaSuccess)
             return LQ_ERR_CUDA;
