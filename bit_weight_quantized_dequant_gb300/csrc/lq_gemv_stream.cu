@@ -36,6 +36,9 @@ namespace lq {
 namespace {
 
 constexpr int kWarps = 8;
+#ifndef LQ_STREAM_MIN_BLOCKS
+#define LQ_STREAM_MIN_BLOCKS 3   // resident CTAs per SM the register allocation aims for
+#endif
 constexpr int kThreadsS = kWarps * 32;
 
 // ---- pre-pass: x -> binary16, anchors zeroed, fragment order ------------------------
@@ -259,7 +262,7 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 template <int FMT, int MT, int NT>
-__global__ void __launch_bounds__(kThreadsS, 2) gemv_stream_kernel(const __grid_constant__ SParams P) {
+__global__ void __launch_bounds__(kThreadsS, LQ_STREAM_MIN_BLOCKS) gemv_stream_kernel(const __grid_constant__ SParams P) {
     __shared__ float red[kWarps][16][(NT * 8) + 1];
     // per warp, three x slices of one 256-column step each (binary16, fragment order)
     extern __shared__ __align__(16) uint16_t xring[];
@@ -372,11 +375,6 @@ __global__ void __launch_bounds__(kThreadsS, 2) gemv_stream_kernel(const __grid_
             cp_async_wait<2>();   // this step's x slice has landed (the two later ones may be in flight)
             __syncwarp();
             const uint16_t* xs = xw + slot * 256 * MM + xlane;
-            uint2 xb[16][NT];
-#pragma unroll
-            for (int b = 0; b < 16; ++b)
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) xb[b][nt] = *reinterpret_cast<const uint2*>(xs + b * MM * 16 + tok[nt]);
             uint32_t RA[4], RB[4];
             lut2_bits((uint16_t)f.s0, (uint16_t)f.z0, RA[0], RB[0]);
             lut2_bits((uint16_t)(f.s0 >> 16), (uint16_t)(f.z0 >> 16), RA[1], RB[1]);
@@ -391,7 +389,11 @@ __global__ void __launch_bounds__(kThreadsS, 2) gemv_stream_kernel(const __grid_
                     uint32_t a0, a1, a2, a3;
                     expand2_fast(w0[ii], j, RA[ii >> 1], RB[ii >> 1], a0, a2);
                     expand2_fast(w1[ii], j, RA[2 + (ii >> 1)], RB[2 + (ii >> 1)], a1, a3);
-                    mma_xg<NT, MT>(acc, a0, a1, a2, a3, xb[ii * 4 + j]);
+                    uint2 xb[NT];
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+                        xb[nt] = *reinterpret_cast<const uint2*>(xs + (ii * 4 + j) * MM * 16 + tok[nt]);
+                    mma_xg<NT, MT>(acc, a0, a1, a2, a3, xb);
                 }
             }
             __syncwarp();   // every lane has read this slot before it is refilled
