@@ -37,7 +37,7 @@ namespace {
 
 constexpr int kWarps = 8;
 #ifndef LQ_STREAM_MIN_BLOCKS
-#define LQ_STREAM_MIN_BLOCKS 3   // resident CTAs per SM the register allocation aims for
+#define LQ_STREAM_MIN_BLOCKS 2   // resident CTAs per SM the register allocation aims for
 #endif
 constexpr int kThreadsS = kWarps * 32;
 
@@ -563,7 +563,7 @@ lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* probs, i
     int64_t blocks = 0, prep = 0, xhalves = 0;
     int max_k = 0;
     // minimum K steps per warp (LQ_GEMV_STEPS_PER_WARP overrides, for tuning experiments)
-    int spw = 4;
+    int spw = 8;
     if (const char* e = getenv("LQ_GEMV_STEPS_PER_WARP")) spw = std::max(1, atoi(e));
     for (int i = 0; i < count; ++i) {
         const lq_problem& q = probs[i];
