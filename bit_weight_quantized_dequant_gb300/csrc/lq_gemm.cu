@@ -38,24 +38,52 @@ namespace {
 
 constexpr int kBM = 128;                 // weight rows per tile (MMA M)
 constexpr int kBN = 256;                 // tokens per tile (MMA N)
-constexpr int kBK = 64;                  // columns per stage (one 128-byte swizzle row of 16-bit values)
-constexpr int kStagesG = 4;
+constexpr int kBK = 64;                  // columns per K-block (one 128-byte swizzle row of 16-bit values)
+constexpr int kStagesB = 4;              // x ring depth
 constexpr int kATile = kBM * kBK * 2;    // 16 KiB
 constexpr int kBTile = kBN * kBK * 2;    // 32 KiB
+constexpr int kChunk = 4;                // K-blocks of codes and scales per metadata load
 constexpr int kDqWarps = 8;
-constexpr int kGemmThreads = (2 + kDqWarps) * 32;
-constexpr int kTmemCols = 256;
+constexpr int kEpiWarps = 4;
+constexpr int kDqWarp0 = 3;              // warps: 0 x TMA, 1 MMA, 2 metadata, 3..10 dequant, 11..14 epilogue
+constexpr int kEpiWarp0 = kDqWarp0 + kDqWarps;
+constexpr int kGemmThreads = (kEpiWarp0 + kEpiWarps) * 32;
+constexpr int kTmemCols = 2 * kBN;       // two accumulators: the epilogue drains one while the MMA fills the other
+
+// Per-format layout of the shared memory.  The weight (A) ring is one stage shorter
+// for NF4, whose metadata chunks are larger.
+template <int FMT>
+struct GemmLayout {
+    static constexpr bool kNF4Fmt = FMT == LQ_FMT_NF4_B64;
+    static constexpr int kStagesA = kNF4Fmt ? 3 : 4;
+    // one metadata chunk (kChunk K-blocks of 128 rows):
+    //   2-bit: codes [128][64 B] (64-byte swizzle) | scales [128][8 x f16] | offsets [128][8 x f16] | anchor bits [8 x u32]
+    //   NF4:   codes [128][128 B] (128-byte swizzle) | absmax [128][4 x f32]
+    static constexpr int kCodesBytes = kBM * kChunk * (kNF4Fmt ? 32 : 16);
+    static constexpr int kScaleOff = kCodesBytes;
+    static constexpr int kOffsetOff = kScaleOff + kBM * 16;
+    static constexpr int kBitsOff = kOffsetOff + (kNF4Fmt ? 0 : kBM * 16);
+    static constexpr int kChunkBytes = ((kBitsOff + (kNF4Fmt ? 0 : 32)) + 1023) / 1024 * 1024;
+    static constexpr int kAOff = 0;
+    static constexpr int kBOff = kAOff + kStagesA * kATile;
+    static constexpr int kMetaOff = kBOff + kStagesB * kBTile;
+    static constexpr int kBarOff = kMetaOff + 2 * kChunkBytes;
+    static constexpr int kNumBars = 2 * kStagesA + 2 * kStagesB + 2 + 2 + 2 + 2;
+    static constexpr int kSmemBytes = 1024 + kBarOff + kNumBars * 8;
+};
 
 struct GemmParams {
     CUtensorMap xmap;          // x [M][K] 16-bit, box 64 x 256, 128-byte swizzle
     CUtensorMap xamap;         // x at the anchor columns [M][a_pad], same box
-    const uint8_t* codes;
+    CUtensorMap awmap;         // anchor weights [N][ld_anchor] binary16, box 64 x 128, 128-byte swizzle
+    CUtensorMap cmap;          // codes [N][K/4] or [N][K/2] bytes, box (chunk of K-blocks) x 128
+    CUtensorMap smap;          // scales [N][K/32] f16 or absmax [N][K/64] f32, box 16 bytes x 128
+    CUtensorMap omap;          // offsets [N][K/32] f16, box 16 bytes x 128
     const void* scales;
     const uint16_t* offsets;
-    const uint16_t* anchor_w;
-    const unsigned long long* anchor_bits;   // [K/64] anchor columns of each 64-column block
+    const uint32_t* anchor_bits;   // [K/32 + 8] anchor columns of each 32-column half block
     void* y;
-    int M, N, K, A, ld_anchor, a_pad, format, bf16, y_dtype;
+    int M, N, K, A, a_pad, bf16, y_dtype, meta_tma;
     int tiles_m, total_tiles;
     int* status;
 };
@@ -92,28 +120,60 @@ __device__ __forceinline__ void dq2_word(uint32_t w, uint32_t P01, uint32_t P23,
     c1[3] = prmt(P01, P23, sd >> 16);
 }
 
+// Position in this CTA's sequence of work items: (output tile, K-block), K-blocks innermost.
+struct Item {
+    int tile, kb;
+    __device__ __forceinline__ void next(int nkb) {
+        if (++kb == nkb) {
+            kb = 0;
+            tile += gridDim.x;
+        }
+    }
+};
+
+struct Ring {
+    int s = 0, ph = 0;
+    __device__ __forceinline__ void next(int depth) {
+        if (++s == depth) {
+            s = 0;
+            ph ^= 1;
+        }
+    }
+};
+
 template <int FMT>
 __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_constant__ GemmParams P) {
+    using L = GemmLayout<FMT>;
+    constexpr int SA = L::kStagesA;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-    uint8_t* atile = base;                                  // [kStagesG][128 rows][128 B]
-    uint8_t* btile = base + kStagesG * kATile;              // [kStagesG][256 rows][128 B]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(btile + kStagesG * kBTile);
-    // bars: a_full[S], b_full[S], empty[S], accum_full, tmem_empty
+    uint8_t* atile = base + L::kAOff;       // [SA][128 rows][128 B], 128-byte swizzle
+    uint8_t* btile = base + L::kBOff;       // [SB][256 rows][128 B], 128-byte swizzle
+    uint8_t* meta = base + L::kMetaOff;     // [2][chunk]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(base + L::kBarOff);
     __shared__ uint32_t s_tmem;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const uint32_t a_full0 = smem_u32(bars), b_full0 = smem_u32(bars + kStagesG), empty0 = smem_u32(bars + 2 * kStagesG);
-    const uint32_t accum_full = smem_u32(bars + 3 * kStagesG), tmem_empty = accum_full + 8;
+    const uint32_t a_full0 = smem_u32(bars), a_empty0 = a_full0 + 8 * SA;
+    const uint32_t b_full0 = a_empty0 + 8 * SA, b_empty0 = b_full0 + 8 * kStagesB;
+    const uint32_t m_full0 = b_empty0 + 8 * kStagesB, m_empty0 = m_full0 + 16;
+    const uint32_t acc_full0 = m_empty0 + 16, acc_empty0 = acc_full0 + 16;
 
     if (tid == 0) {
-        for (int s = 0; s < kStagesG; ++s) {
+        for (int s = 0; s < SA; ++s) {
             mbar_init(a_full0 + 8 * s, kDqWarps);
-            mbar_init(b_full0 + 8 * s, 1);
-            mbar_init(empty0 + 8 * s, 1);
+            mbar_init(a_empty0 + 8 * s, 1);
         }
-        mbar_init(accum_full, 1);
-        mbar_init(tmem_empty, kDqWarps);
+        for (int s = 0; s < kStagesB; ++s) {
+            mbar_init(b_full0 + 8 * s, 1);
+            mbar_init(b_empty0 + 8 * s, 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(m_full0 + 8 * i, 32);
+            mbar_init(m_empty0 + 8 * i, kDqWarps);
+            mbar_init(acc_full0 + 8 * i, 1);
+            mbar_init(acc_empty0 + 8 * i, kEpiWarps);
+        }
         fence_mbar_init();
     }
     if (warp == 1) tmem_alloc(smem_u32(&s_tmem), kTmemCols);
@@ -122,177 +182,241 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     tc_fence_after();
     const uint32_t tmem = s_tmem;
 
-    const int KB = P.K / kBK, AB = P.a_pad / kBK, NKB = KB + AB;
+    const int KB = P.K / kBK, NKB = KB + P.a_pad / kBK, NCH = (KB + kChunk - 1) / kChunk;
     int own_abort = 0;
     volatile int* abort = &own_abort;
 
     if (warp == 0) {
-        // ---------------------------------------------------------------- TMA: x tiles
+        // ---------------------------------------------------------------- TMA: x tiles, anchor weight tiles
         if (lane == 0) {
             prefetch_tensormap(&P.xmap);
-            if (AB) prefetch_tensormap(&P.xamap);
-            int s = 0, ph = 0;
-            for (int tile = blockIdx.x; tile < P.total_tiles; tile += gridDim.x) {
-                const int m0 = (tile % P.tiles_m) * kBN;
-                for (int kb = 0; kb < NKB; ++kb) {
-                    if (!mbar_wait_bounded(empty0 + 8 * s, ph ^ 1, abort, P.status)) goto tma_done;
-                    mbar_arrive_expect_tx(b_full0 + 8 * s, kBTile);
-                    if (kb < KB) tma_load_2d(smem_u32(btile + s * kBTile), &P.xmap, kb * kBK, m0, b_full0 + 8 * s);
-                    else tma_load_2d(smem_u32(btile + s * kBTile), &P.xamap, (kb - KB) * kBK, m0, b_full0 + 8 * s);
-                    if (++s == kStagesG) {
-                        s = 0;
-                        ph ^= 1;
-                    }
-                }
+            if (P.a_pad) {
+                prefetch_tensormap(&P.xamap);
+                prefetch_tensormap(&P.awmap);
             }
-        tma_done:;
+            Ring ra, rb;
+            for (Item it{(int)blockIdx.x, 0}; it.tile < P.total_tiles; it.next(NKB)) {
+                const int m0 = (it.tile % P.tiles_m) * kBN;
+                if (!mbar_wait_bounded(b_empty0 + 8 * rb.s, rb.ph ^ 1, abort, P.status)) break;
+                const uint32_t fb = b_full0 + 8 * rb.s;
+                if (it.kb < KB) {
+                    mbar_arrive_expect_tx(fb, kBTile);
+                    tma_load_2d(smem_u32(btile + rb.s * kBTile), &P.xmap, it.kb * kBK, m0, fb);
+                } else {
+                    // anchor K-block: x at the anchor columns, and the anchor weights into the A stage
+                    if (!mbar_wait_bounded(a_empty0 + 8 * ra.s, ra.ph ^ 1, abort, P.status)) break;
+                    const int n0 = (it.tile / P.tiles_m) * kBM;
+                    mbar_arrive_expect_tx(fb, kBTile + kATile);
+                    tma_load_2d(smem_u32(btile + rb.s * kBTile), &P.xamap, (it.kb - KB) * kBK, m0, fb);
+                    tma_load_2d(smem_u32(atile + ra.s * kATile), &P.awmap, (it.kb - KB) * kBK, n0, fb);
+                }
+                ra.next(SA);
+                rb.next(kStagesB);
+            }
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issue
         if (lane == 0) {
             const uint32_t idesc = idesc_f16(P.bf16 != 0, kBM, kBN);
-            int s = 0, ph = 0, tph = 0;
-            for (int tile = blockIdx.x; tile < P.total_tiles; tile += gridDim.x) {
-                // the epilogue has drained the accumulator of the previous tile
-                if (!mbar_wait_bounded(tmem_empty, tph ^ 1, abort, P.status)) break;
-                tph ^= 1;
+            Ring ra, rb;
+            bool ok = true;
+            for (int tile = blockIdx.x, lt = 0; ok && tile < P.total_tiles; tile += gridDim.x, ++lt) {
+                const int acc = lt & 1;
+                // the epilogue has drained this accumulator (two tiles ago)
+                if (!(ok = mbar_wait_bounded(acc_empty0 + 8 * acc, ((lt >> 1) & 1) ^ 1, abort, P.status))) break;
                 tc_fence_after();
-                bool ok = true;
+                const uint32_t d = tmem + acc * kBN;
                 for (int kb = 0; kb < NKB; ++kb) {
-                    if (!(ok = mbar_wait_bounded(a_full0 + 8 * s, ph, abort, P.status))) break;
-                    if (!(ok = mbar_wait_bounded(b_full0 + 8 * s, ph, abort, P.status))) break;
+                    if (!(ok = mbar_wait_bounded(a_full0 + 8 * ra.s, ra.ph, abort, P.status))) break;
+                    if (!(ok = mbar_wait_bounded(b_full0 + 8 * rb.s, rb.ph, abort, P.status))) break;
                     tc_fence_after();
-                    const uint32_t a_addr = smem_u32(atile + s * kATile), b_addr = smem_u32(btile + s * kBTile);
+                    const uint32_t a_addr = smem_u32(atile + ra.s * kATile), b_addr = smem_u32(btile + rb.s * kBTile);
 #pragma unroll
                     for (int k = 0; k < kBK / 16; ++k)
-                        tc_mma_f16(tmem, smem_desc_sw128(a_addr + 32 * k), smem_desc_sw128(b_addr + 32 * k), idesc,
+                        tc_mma_f16(d, smem_desc_sw128(a_addr + 32 * k), smem_desc_sw128(b_addr + 32 * k), idesc,
                                    (kb | k) != 0);
-                    tc_commit(empty0 + 8 * s);   // the stage is free once these MMAs have read it
-                    if (++s == kStagesG) {
-                        s = 0;
-                        ph ^= 1;
-                    }
+                    // both stages are free once these MMAs have read them
+                    tc_commit(a_empty0 + 8 * ra.s);
+                    tc_commit(b_empty0 + 8 * rb.s);
+                    ra.next(SA);
+                    rb.next(kStagesB);
                 }
-                if (!ok) break;
-                tc_commit(accum_full);
+                if (ok) tc_commit(acc_full0 + 8 * acc);
             }
         }
-    } else {
-        // ---------------------------------------------------------------- dequant + epilogue
-        const int d = tid - 64, r = d & (kBM - 1), h = d >> 7;   // row of the tile, half of the 64 columns
-        const int K = P.K, N = P.N;
-        const float C0 = -1.52f, C1 = -0.45f, C2 = 0.45f, C3 = 1.52f;
-        int s = 0, ph = 0, aph = 0;
+    } else if (warp == 2) {
+        // ---------------------------------------------------------------- metadata: codes, scales, anchor bits
+        if (lane == 0) {
+            prefetch_tensormap(&P.cmap);
+            if (P.meta_tma) {
+                prefetch_tensormap(&P.smap);
+                if (!L::kNF4Fmt) prefetch_tensormap(&P.omap);
+            }
+        }
+        Ring rm;
         for (int tile = blockIdx.x; tile < P.total_tiles; tile += gridDim.x) {
-            const int n0 = (tile / P.tiles_m) * kBM, m0 = (tile % P.tiles_m) * kBN;
-            const int64_t nr = min(n0 + r, N - 1);   // rows past N read the last row; never stored
-            bool ok = true;
-            for (int kb = 0; kb < NKB; ++kb) {
-                // warp-uniform: a lane that gives up takes its whole warp out
-                if (!(ok = __all_sync(0xffffffffu, mbar_wait_bounded(empty0 + 8 * s, ph ^ 1, abort, P.status))))
-                    break;
-                uint8_t* arow = atile + s * kATile + r * 128;
-                const int sw = r & 7;
-                if (kb < KB) {
-                    uint32_t c[4][4];
-                    if (FMT == LQ_FMT_2BIT_LM_G32) {
-                        const uint2 cw = ldg64(P.codes + nr * (K / 4) + kb * 16 + h * 8);
-                        const int64_t gi = nr * (K / 32) + kb * 2 + h;
-                        const float sf = half_bits_to_float(static_cast<const uint16_t*>(P.scales)[gi]);
-                        const float zf = half_bits_to_float(P.offsets[gi]);
-                        const uint32_t P01 = pack2(__fmaf_rn(sf, C0, zf), __fmaf_rn(sf, C1, zf), P.bf16);
-                        const uint32_t P23 = pack2(__fmaf_rn(sf, C2, zf), __fmaf_rn(sf, C3, zf), P.bf16);
-                        dq2_word(cw.x, P01, P23, c[0], c[1]);
-                        dq2_word(cw.y, P01, P23, c[2], c[3]);
-                    } else {
-                        const uint4 cw = ldg128(P.codes + nr * (K / 2) + kb * 32 + h * 16);
-                        const float am = static_cast<const float*>(P.scales)[nr * (K / 64) + kb];
-                        // this block's 16 values T[q] * absmax, one rounding, in byte-split registers
-                        uint32_t BL[4], BH[4];
-#pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            const uint32_t p01 = pack2(__fmul_rn(kNF4[4 * q4], am), __fmul_rn(kNF4[4 * q4 + 1], am), P.bf16);
-                            const uint32_t p23 = pack2(__fmul_rn(kNF4[4 * q4 + 2], am), __fmul_rn(kNF4[4 * q4 + 3], am), P.bf16);
-                            BL[q4] = prmt(p01, p23, 0x6420);
-                            BH[q4] = prmt(p01, p23, 0x7531);
-                        }
-                        const uint32_t ws[4] = {cw.x, cw.y, cw.z, cw.w};
-#pragma unroll
-                        for (int wi = 0; wi < 4; ++wi) {
-                            expand_nf4_fast(ws[wi], 0, BL, BH, c[wi][0], c[wi][1]);
-                            expand_nf4_fast(ws[wi], 1, BL, BH, c[wi][2], c[wi][3]);
+            const int n0 = (tile / P.tiles_m) * kBM;
+            for (int c = 0; c < NCH; ++c) {
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(m_empty0 + 8 * rm.s, rm.ph ^ 1, abort, P.status)))
+                    goto meta_done;
+                uint8_t* ch = meta + rm.s * L::kChunkBytes;
+                const uint32_t fb = m_full0 + 8 * rm.s;
+                const int kb0 = c * kChunk;
+                if (!P.meta_tma) {
+                    // scale rows are not 16-byte aligned: 4-byte loads, four rows per lane
+                    const int nk = min(kChunk, KB - kb0);
+                    for (int rr = lane; rr < kBM; rr += 32) {
+                        const int64_t nr = min(n0 + rr, P.N - 1);
+                        if (L::kNF4Fmt) {
+                            const float* src = static_cast<const float*>(P.scales) + nr * (P.K / 64) + kb0;
+                            for (int i = 0; i < nk; ++i)
+                                reinterpret_cast<float*>(ch + L::kScaleOff + rr * 16)[i] = __ldg(src + i);
+                        } else {
+                            const int64_t g = nr * (P.K / 32) + 2 * kb0;
+                            const uint32_t* ss = reinterpret_cast<const uint32_t*>(static_cast<const uint16_t*>(P.scales) + g);
+                            const uint32_t* so = reinterpret_cast<const uint32_t*>(P.offsets + g);
+                            for (int i = 0; i < nk; ++i) {
+                                reinterpret_cast<uint32_t*>(ch + L::kScaleOff + rr * 16)[i] = __ldg(ss + i);
+                                reinterpret_cast<uint32_t*>(ch + L::kOffsetOff + rr * 16)[i] = __ldg(so + i);
+                            }
                         }
                     }
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) sts128(arow + (((4 * h + q) ^ sw) << 4), c[q][0], c[q][1], c[q][2], c[q][3]);
-                    if (FMT == LQ_FMT_2BIT_LM_G32 && P.A > 0) {
-                        // anchor columns replace the 2-bit weights: zero them in the tile
-                        uint32_t bits = (uint32_t)(P.anchor_bits[kb] >> (32 * h));
-                        while (bits) {
-                            const int i = __ffs(bits) - 1;
-                            bits &= bits - 1;
-                            const int col = 32 * h + i;
-                            *reinterpret_cast<uint16_t*>(arow + (((col >> 3) ^ sw) << 4) + (col & 7) * 2) = 0;
-                        }
+                }
+                if (lane == 0) {
+                    uint32_t tx = L::kCodesBytes;
+                    if (P.meta_tma) tx += L::kNF4Fmt ? kBM * 16 : 2 * kBM * 16;
+                    if (!L::kNF4Fmt && P.A > 0) tx += 32;
+                    mbar_arrive_expect_tx(fb, tx);
+                    tma_load_2d(smem_u32(ch), &P.cmap, kb0 * (L::kNF4Fmt ? 32 : 16), n0, fb);
+                    if (P.meta_tma) {
+                        tma_load_2d(smem_u32(ch + L::kScaleOff), &P.smap, kb0 * (L::kNF4Fmt ? 1 : 2), n0, fb);
+                        if (!L::kNF4Fmt)
+                            tma_load_2d(smem_u32(ch + L::kOffsetOff), &P.omap, kb0 * 2, n0, fb);
                     }
+                    if (!L::kNF4Fmt && P.A > 0) bulk_load(smem_u32(ch + L::kBitsOff), P.anchor_bits + 2 * kb0, 32, fb);
                 } else {
-                    // anchor block: 32 binary16 anchor weights of this row, zero past A
-                    const int a0 = (kb - KB) * kBK + 32 * h;
-                    const uint16_t* src = P.anchor_w + nr * P.ld_anchor + a0;
-                    uint32_t v[16];
+                    mbar_arrive(fb);
+                }
+                rm.next(2);
+            }
+        }
+    meta_done:;
+    } else if (warp < kEpiWarp0) {
+        // ---------------------------------------------------------------- dequant into the A stages
+        const int d = tid - 32 * kDqWarp0, r = d & (kBM - 1), h = d >> 7;   // row of the tile, half of the 64 columns
+        const int sw = r & 7;
+        const float C0 = -1.52f, C1 = -0.45f, C2 = 0.45f, C3 = 1.52f;
+        Ring ra, rb, rm;
+        for (Item it{(int)blockIdx.x, 0}; it.tile < P.total_tiles; it.next(NKB)) {
+            uint8_t* arow = atile + ra.s * kATile + r * 128;
+            if (it.kb < KB) {
+                const int j = it.kb % kChunk;
+                // warp-uniform waits: a lane that gives up takes its whole warp out
+                if (j == 0 && !__all_sync(0xffffffffu, mbar_wait_bounded(m_full0 + 8 * rm.s, rm.ph, abort, P.status)))
+                    break;
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(a_empty0 + 8 * ra.s, ra.ph ^ 1, abort, P.status))) break;
+                const uint8_t* ch = meta + rm.s * L::kChunkBytes;
+                uint32_t c[4][4];
+                if (FMT == LQ_FMT_2BIT_LM_G32) {
+                    const uint2 cw = *reinterpret_cast<const uint2*>(ch + r * 64 + ((j ^ ((r >> 1) & 3)) << 4) + 8 * h);
+                    const float sf = half_bits_to_float(reinterpret_cast<const uint16_t*>(ch + L::kScaleOff + r * 16)[2 * j + h]);
+                    const float zf = half_bits_to_float(reinterpret_cast<const uint16_t*>(ch + L::kOffsetOff + r * 16)[2 * j + h]);
+                    const uint32_t P01 = pack2(__fmaf_rn(sf, C0, zf), __fmaf_rn(sf, C1, zf), P.bf16);
+                    const uint32_t P23 = pack2(__fmaf_rn(sf, C2, zf), __fmaf_rn(sf, C3, zf), P.bf16);
+                    dq2_word(cw.x, P01, P23, c[0], c[1]);
+                    dq2_word(cw.y, P01, P23, c[2], c[3]);
+                } else {
+                    const uint4 cw = *reinterpret_cast<const uint4*>(ch + r * 128 + (((2 * j + h) ^ sw) << 4));
+                    const float am = reinterpret_cast<const float*>(ch + L::kScaleOff + r * 16)[j];
+                    // this block's 16 values T[q] * absmax, one rounding, in byte-split registers
+                    uint32_t BL[4], BH[4];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const uint4 u = (a0 + 8 * q < P.A) ? *reinterpret_cast<const uint4*>(src + 8 * q) : make_uint4(0, 0, 0, 0);
-                        v[4 * q] = u.x;
-                        v[4 * q + 1] = u.y;
-                        v[4 * q + 2] = u.z;
-                        v[4 * q + 3] = u.w;
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        const uint32_t p01 = pack2(__fmul_rn(kNF4[4 * q4], am), __fmul_rn(kNF4[4 * q4 + 1], am), P.bf16);
+                        const uint32_t p23 = pack2(__fmul_rn(kNF4[4 * q4 + 2], am), __fmul_rn(kNF4[4 * q4 + 3], am), P.bf16);
+                        BL[q4] = prmt(p01, p23, 0x6420);
+                        BH[q4] = prmt(p01, p23, 0x7531);
                     }
+                    const uint32_t ws[4] = {cw.x, cw.y, cw.z, cw.w};
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int a = a0 + 2 * i;
-                        uint32_t w = a < P.A ? v[i] : 0u;
-                        if (a + 1 >= P.A) w &= 0xFFFFu;
-                        if (P.bf16) {
-                            const float lo = half_bits_to_float((uint16_t)w), hi = half_bits_to_float((uint16_t)(w >> 16));
-                            w = pack2(lo, hi, 1);
-                        }
-                        v[i] = w;
+                    for (int wi = 0; wi < 4; ++wi) {
+                        expand_nf4_fast(ws[wi], 0, BL, BH, c[wi][0], c[wi][1]);
+                        expand_nf4_fast(ws[wi], 1, BL, BH, c[wi][2], c[wi][3]);
                     }
+                }
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) sts128(arow + (((4 * h + q) ^ sw) << 4), v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                for (int q = 0; q < 4; ++q) sts128(arow + (((4 * h + q) ^ sw) << 4), c[q][0], c[q][1], c[q][2], c[q][3]);
+                if (FMT == LQ_FMT_2BIT_LM_G32 && P.A > 0) {
+                    // anchor columns replace the 2-bit weights: zero them in the tile
+                    uint32_t bits = reinterpret_cast<const uint32_t*>(ch + L::kBitsOff)[2 * j + h];
+                    while (bits) {
+                        const int i = __ffs(bits) - 1;
+                        bits &= bits - 1;
+                        const int col = 32 * h + i;
+                        *reinterpret_cast<uint16_t*>(arow + (((col >> 3) ^ sw) << 4) + (col & 7) * 2) = 0;
+                    }
                 }
                 fence_proxy_async_smem();   // generic-proxy stores -> visible to the tensor core
                 __syncwarp();
-                if (lane == 0) mbar_arrive(a_full0 + 8 * s);
-                if (++s == kStagesG) {
-                    s = 0;
-                    ph ^= 1;
+                if (lane == 0) {
+                    mbar_arrive(a_full0 + 8 * ra.s);
+                    if (j == kChunk - 1 || it.kb == KB - 1) mbar_arrive(m_empty0 + 8 * rm.s);
                 }
+                if (j == kChunk - 1 || it.kb == KB - 1) rm.next(2);
+            } else {
+                // anchor block: TMA has put 64 binary16 anchor weights per row in the stage;
+                // zero the columns past A and convert to bf16 when x is bf16
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(b_full0 + 8 * rb.s, rb.ph, abort, P.status))) break;
+                const int a0 = (it.kb - KB) * kBK + 32 * h;
+                if (P.bf16 || a0 + 32 > P.A) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        uint4* p = reinterpret_cast<uint4*>(arow + (((4 * h + q) ^ sw) << 4));
+                        const uint4 u4 = *p;
+                        uint32_t v[4] = {u4.x, u4.y, u4.z, u4.w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int a = a0 + 8 * q + 2 * i;
+                            uint32_t w = a < P.A ? v[i] : 0u;
+                            if (a + 1 >= P.A) w &= 0xFFFFu;
+                            if (P.bf16)
+                                w = pack2(half_bits_to_float((uint16_t)w), half_bits_to_float((uint16_t)(w >> 16)), 1);
+                            v[i] = w;
+                        }
+                        *p = make_uint4(v[0], v[1], v[2], v[3]);
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(a_full0 + 8 * ra.s);
             }
-            if (!ok) break;
-            // ---- epilogue: accumulator rows of this warp's lane quarter, half of the 256 columns
-            if (!__all_sync(0xffffffffu, mbar_wait_bounded(accum_full, aph, abort, P.status))) break;
-            aph ^= 1;
+            ra.next(SA);
+            rb.next(kStagesB);
+        }
+    } else {
+        // ---------------------------------------------------------------- epilogue: TMEM -> y
+        const int quarter = warp & 3;   // the TMEM lane quarter this warp may read
+        for (int tile = blockIdx.x, lt = 0; tile < P.total_tiles; tile += gridDim.x, ++lt) {
+            const int acc = lt & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(acc_full0 + 8 * acc, (lt >> 1) & 1, abort, P.status))) break;
             tc_fence_after();
-            const int quarter = warp & 3, colhalf = (warp - 2) >> 2;
+            const int n0 = (tile / P.tiles_m) * kBM, m0 = (tile % P.tiles_m) * kBN;
             const int n = n0 + 32 * quarter + lane;
 #pragma unroll 1
-            for (int cc = 0; cc < 4; ++cc) {
-                const int col = 128 * colhalf + 32 * cc;
+            for (int cc = 0; cc < kBN / 32; ++cc) {
                 uint32_t v[32];
-                tmem_ld32(tmem + ((uint32_t)(32 * quarter) << 16) + col, v);
-                if (n < N) {
+                tmem_ld32(tmem + ((uint32_t)(32 * quarter) << 16) + acc * kBN + 32 * cc, v);
+                if (n < P.N) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
-                        const int m = m0 + col + j;
-                        if (m < P.M) store_out(P.y, (size_t)m * N + n, P.y_dtype, __uint_as_float(v[j]));
+                        const int m = m0 + 32 * cc + j;
+                        if (m < P.M) store_out(P.y, (size_t)m * P.N + n, P.y_dtype, __uint_as_float(v[j]));
                     }
                 }
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(tmem_empty);
+            if (lane == 0) mbar_arrive(acc_empty0 + 8 * acc);
         }
     }
     tc_fence_before();
@@ -332,17 +456,30 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn_g() {
     return fn;
 }
 
-// 2-D map over a row-major [rows][cols] 16-bit matrix, box 64 columns x 256 rows, 128-byte swizzle.
-bool map_x(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows) {
+// 2-D tiled map over a row-major [rows][cols] matrix with a row pitch of `ld` elements.
+bool map_2d(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* base, uint64_t cols, uint64_t rows,
+            uint64_t ld, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swz) {
     auto fn = encode_fn_g();
     if (!fn) return false;
     cuuint64_t dims[2] = {cols, rows};
-    cuuint64_t strides[1] = {cols * 2};
-    cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)kBN};
+    cuuint64_t strides[1] = {ld * (uint64_t)esize};
+    cuuint32_t box[2] = {box_cols, box_rows};
     cuuint32_t estr[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool map_16bit(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t ld, uint32_t box_rows) {
+    return map_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, base, cols, rows, ld, kBK, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+template <int FMT>
+lq_status launch_fmt(const GemmParams& P, int grid, cudaStream_t stream) {
+    constexpr int smem = GemmLayout<FMT>::kSmemBytes;
+    if (cudaFuncSetAttribute(gemm_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        return LQ_ERR_CUDA;
+    gemm_kernel<FMT><<<grid, kGemmThreads, smem, stream>>>(P);
+    return cudaPeekAtLastError() == cudaSuccess ? LQ_OK : LQ_ERR_CUDA;
 }
 
 }  // namespace
@@ -352,38 +489,57 @@ lq_status launch_gemm(lq_handle h, const lq_problem& p, cudaStream_t stream) {
     memset(&P, 0, sizeof(P));
     const int A = p.format == LQ_FMT_2BIT_LM_G32 ? p.A : 0;
     const int a_pad = A > 0 ? (A + kBK - 1) / kBK * kBK : 0;
-    P.codes = p.codes;
     P.scales = p.scales;
     P.offsets = p.offsets;
-    P.anchor_w = p.anchor_w;
     P.y = p.y;
     P.M = p.M;
     P.N = p.N;
     P.K = p.K;
     P.A = A;
-    P.ld_anchor = p.ld_anchor;
     P.a_pad = a_pad;
-    P.format = p.format;
     P.bf16 = p.x_dtype == LQ_BF16;
     P.y_dtype = p.y_dtype;
+    P.meta_tma = p.K % 256 == 0;   // scale rows 16-byte aligned: TMA boxes; else 4-byte loads
     P.tiles_m = (p.M + kBN - 1) / kBN;
     const int64_t tiles = (int64_t)P.tiles_m * ((p.N + kBM - 1) / kBM);
     if (tiles > 0x7fffffffLL) return LQ_ERR_UNSUPPORTED;
     P.total_tiles = (int)tiles;
     P.status = h->status_flag;
 
-    // workspace: anchor bitmap [K/64] | x at the anchor columns [M][a_pad]
+    // workspace: anchor bitmap [K/64 + 4] (a chunk past the last K-block is read whole) | x at the anchor columns [M][a_pad]
     char* ws = reinterpret_cast<char*>(h->partials);
-    const size_t bits_bytes = ((size_t)(p.K / 64) * 8 + 255) & ~size_t(255);
+    const size_t bits_bytes = ((size_t)(p.K / 64 + kChunk) * 8 + 255) & ~size_t(255);
     const size_t xa_bytes = (size_t)p.M * a_pad * 2;
     if (bits_bytes + xa_bytes + 256 > h->partial_floats * sizeof(float)) return LQ_ERR_WORKSPACE;
     unsigned long long* bits = reinterpret_cast<unsigned long long*>(ws);
     uint16_t* xa = reinterpret_cast<uint16_t*>(ws + bits_bytes);
-    P.anchor_bits = bits;
-    if (!map_x(&P.xmap, p.x, (uint64_t)p.K, (uint64_t)p.M)) return LQ_ERR_CUDA;
+    P.anchor_bits = reinterpret_cast<const uint32_t*>(bits);
+    if (!map_16bit(&P.xmap, p.x, (uint64_t)p.K, (uint64_t)p.M, (uint64_t)p.K, kBN)) return LQ_ERR_CUDA;
+    const bool nf4 = p.format == LQ_FMT_NF4_B64;
+    {
+        const uint64_t cbytes = (uint64_t)p.K / (nf4 ? 2 : 4);
+        if (!map_2d(&P.cmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.codes, cbytes, (uint64_t)p.N, cbytes,
+                    kChunk * (nf4 ? 32 : 16), kBM, nf4 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B))
+            return LQ_ERR_CUDA;
+    }
+    if (P.meta_tma) {
+        if (nf4) {
+            if (!map_2d(&P.smap, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, p.scales, (uint64_t)p.K / 64, (uint64_t)p.N,
+                        (uint64_t)p.K / 64, 4, kBM, CU_TENSOR_MAP_SWIZZLE_NONE))
+                return LQ_ERR_CUDA;
+        } else {
+            if (!map_2d(&P.smap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, p.scales, (uint64_t)p.K / 32, (uint64_t)p.N,
+                        (uint64_t)p.K / 32, 8, kBM, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+                !map_2d(&P.omap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, p.offsets, (uint64_t)p.K / 32, (uint64_t)p.N,
+                        (uint64_t)p.K / 32, 8, kBM, CU_TENSOR_MAP_SWIZZLE_NONE))
+                return LQ_ERR_CUDA;
+        }
+    }
     if (A > 0) {
-        if (!map_x(&P.xamap, xa, (uint64_t)a_pad, (uint64_t)p.M)) return LQ_ERR_CUDA;
-        if (cudaMemsetAsync(bits, 0, (size_t)(p.K / 64) * 8, stream) != cudaSuccess) return LQ_ERR_CUDA;
+        if (!map_16bit(&P.xamap, xa, (uint64_t)a_pad, (uint64_t)p.M, (uint64_t)a_pad, kBN)) return LQ_ERR_CUDA;
+        if (!map_16bit(&P.awmap, p.anchor_w, (uint64_t)p.ld_anchor, (uint64_t)p.N, (uint64_t)p.ld_anchor, kBM))
+            return LQ_ERR_CUDA;
+        if (cudaMemsetAsync(bits, 0, bits_bytes, stream) != cudaSuccess) return LQ_ERR_CUDA;
         const int64_t work = std::max<int64_t>((int64_t)p.M * a_pad, A);
         const int grid = (int)std::min<int64_t>((work + 255) / 256, (int64_t)h->num_sms * 8);
         gemm_prep_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(p.x), p.M, p.K, p.anchor_idx, A, a_pad,
@@ -391,19 +547,10 @@ lq_status launch_gemm(lq_handle h, const lq_problem& p, cudaStream_t stream) {
         if (cudaPeekAtLastError() != cudaSuccess) return LQ_ERR_CUDA;
     }
 
-    const size_t smem = 1024 + (size_t)kStagesG * (kATile + kBTile) + (3 * kStagesG + 2) * 8;
-    if (smem > (size_t)h->max_smem_optin) return LQ_ERR_UNSUPPORTED;
+    const int smem = nf4 ? GemmLayout<LQ_FMT_NF4_B64>::kSmemBytes : GemmLayout<LQ_FMT_2BIT_LM_G32>::kSmemBytes;
+    if (smem > h->max_smem_optin) return LQ_ERR_UNSUPPORTED;
     const int grid = (int)std::min<int64_t>(tiles, h->num_sms);
-    if (p.format == LQ_FMT_2BIT_LM_G32) {
-        if (cudaFuncSetAttribute(gemm_kernel<LQ_FMT_2BIT_LM_G32>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-            return LQ_ERR_CUDA;
-        gemm_kernel<LQ_FMT_2BIT_LM_G32><<<grid, kGemmThreads, smem, stream>>>(P);
-    } else {
-        if (cudaFuncSetAttribute(gemm_kernel<LQ_FMT_NF4_B64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-            return LQ_ERR_CUDA;
-        gemm_kernel<LQ_FMT_NF4_B64><<<grid, kGemmThreads, smem, stream>>>(P);
-    }
-    return cudaPeekAtLastError() == cudaSuccess ? LQ_OK : LQ_ERR_CUDA;
+    return nf4 ? launch_fmt<LQ_FMT_NF4_B64>(P, grid, stream) : launch_fmt<LQ_FMT_2BIT_LM_G32>(P, grid, stream);
 }
 
 }  // namespace lq
