@@ -57,13 +57,17 @@ struct GemmLayout {
     static constexpr bool kNF4Fmt = FMT == LQ_FMT_NF4_B64;
     static constexpr int kStagesA = kNF4Fmt ? 3 : 4;
     // one metadata chunk (kChunk K-blocks of 128 rows):
-    //   2-bit: codes [128][64 B] (64-byte swizzle) | scales [128][8 x f16] | offsets [128][8 x f16] | anchor bits [8 x u32]
+    //   2-bit: codes [128][64 B] (64-byte swizzle) | scales [128][8 x f16] | offsets [128][8 x f16] |
+    //          anchor bits [4][u64] | keep masks [4][32 x u32] (word w clears the halves of anchor columns 2w, 2w+1)
     //   NF4:   codes [128][128 B] (128-byte swizzle) | absmax [128][4 x f32]
     static constexpr int kCodesBytes = kBM * kChunk * (kNF4Fmt ? 32 : 16);
     static constexpr int kScaleOff = kCodesBytes;
     static constexpr int kOffsetOff = kScaleOff + kBM * 16;
     static constexpr int kBitsOff = kOffsetOff + (kNF4Fmt ? 0 : kBM * 16);
-    static constexpr int kChunkBytes = ((kBitsOff + (kNF4Fmt ? 0 : 32)) + 1023) / 1024 * 1024;
+    static constexpr int kMaskOff = kBitsOff + 32;
+    // a 2-bit slot also carries one anchor weight tile [128][64 x f16] (128-byte swizzle)
+    static constexpr int kMetaBytes = ((kNF4Fmt ? kBitsOff : kMaskOff + kChunk * 128) + 1023) / 1024 * 1024;
+    static constexpr int kChunkBytes = kNF4Fmt ? kMetaBytes : (kMetaBytes > kATile ? kMetaBytes : kATile);
     static constexpr int kAOff = 0;
     static constexpr int kBOff = kAOff + kStagesA * kATile;
     static constexpr int kMetaOff = kBOff + kStagesB * kBTile;
@@ -161,7 +165,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
 
     if (tid == 0) {
         for (int s = 0; s < SA; ++s) {
-            mbar_init(a_full0 + 8 * s, kDqWarps);
+            mbar_init(a_full0 + 8 * s, kDqWarps / 2);   // the group of four warps that owns the K-block
             mbar_init(a_empty0 + 8 * s, 1);
         }
         for (int s = 0; s < kStagesB; ++s) {
@@ -190,11 +194,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         // ---------------------------------------------------------------- TMA: x tiles, anchor weight tiles
         if (lane == 0) {
             prefetch_tensormap(&P.xmap);
-            if (P.a_pad) {
-                prefetch_tensormap(&P.xamap);
-                prefetch_tensormap(&P.awmap);
-            }
-            Ring ra, rb;
+            if (P.a_pad) prefetch_tensormap(&P.xamap);
+            Ring rb;
             for (Item it{(int)blockIdx.x, 0}; it.tile < P.total_tiles; it.next(NKB)) {
                 const int m0 = (it.tile % P.tiles_m) * kBN;
                 if (!mbar_wait_bounded(b_empty0 + 8 * rb.s, rb.ph ^ 1, abort, P.status)) break;
@@ -203,14 +204,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                     mbar_arrive_expect_tx(fb, kBTile);
                     tma_load_2d(smem_u32(btile + rb.s * kBTile), &P.xmap, it.kb * kBK, m0, fb);
                 } else {
-                    // anchor K-block: x at the anchor columns, and the anchor weights into the A stage
-                    if (!mbar_wait_bounded(a_empty0 + 8 * ra.s, ra.ph ^ 1, abort, P.status)) break;
-                    const int n0 = (it.tile / P.tiles_m) * kBM;
-                    mbar_arrive_expect_tx(fb, kBTile + kATile);
+                    // anchor K-block: x gathered at the anchor columns
+                    mbar_arrive_expect_tx(fb, kBTile);
                     tma_load_2d(smem_u32(btile + rb.s * kBTile), &P.xamap, (it.kb - KB) * kBK, m0, fb);
-                    tma_load_2d(smem_u32(atile + ra.s * kATile), &P.awmap, (it.kb - KB) * kBK, n0, fb);
                 }
-                ra.next(SA);
                 rb.next(kStagesB);
             }
         }
@@ -252,6 +249,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                 prefetch_tensormap(&P.smap);
                 if (!L::kNF4Fmt) prefetch_tensormap(&P.omap);
             }
+            if (P.a_pad) prefetch_tensormap(&P.awmap);
         }
         Ring rm;
         for (int tile = blockIdx.x; tile < P.total_tiles; tile += gridDim.x) {
@@ -262,6 +260,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                 uint8_t* ch = meta + rm.s * L::kChunkBytes;
                 const uint32_t fb = m_full0 + 8 * rm.s;
                 const int kb0 = c * kChunk;
+                if (!L::kNF4Fmt && P.A > 0) {
+                    // anchor columns of the chunk's K-blocks and the per-word keep masks
+                    const uint4 b01 = *reinterpret_cast<const uint4*>(P.anchor_bits + 2 * kb0);
+                    const uint4 b23 = *reinterpret_cast<const uint4*>(P.anchor_bits + 2 * kb0 + 4);
+                    const uint32_t bw[8] = {b01.x, b01.y, b01.z, b01.w, b23.x, b23.y, b23.z, b23.w};
+                    if (lane == 0) {
+                        reinterpret_cast<uint4*>(ch + L::kBitsOff)[0] = b01;
+                        reinterpret_cast<uint4*>(ch + L::kBitsOff)[1] = b23;
+                    }
+#pragma unroll
+                    for (int j = 0; j < kChunk; ++j) {
+                        const uint32_t half = ((lane >> 4) ? bw[2 * j + 1] : bw[2 * j]) >> (2 * (lane & 15));
+                        const uint32_t keep = ((half & 1u) ? 0xFFFF0000u : 0xFFFFFFFFu) & ((half & 2u) ? 0x0000FFFFu : 0xFFFFFFFFu);
+                        reinterpret_cast<uint32_t*>(ch + L::kMaskOff + j * 128)[lane] = keep;
+                    }
+                }
                 if (!P.meta_tma) {
                     // scale rows are not 16-byte aligned: 4-byte loads, four rows per lane
                     const int nk = min(kChunk, KB - kb0);
@@ -285,7 +299,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                 if (lane == 0) {
                     uint32_t tx = L::kCodesBytes;
                     if (P.meta_tma) tx += L::kNF4Fmt ? kBM * 16 : 2 * kBM * 16;
-                    if (!L::kNF4Fmt && P.A > 0) tx += 32;
                     mbar_arrive_expect_tx(fb, tx);
                     tma_load_2d(smem_u32(ch), &P.cmap, kb0 * (L::kNF4Fmt ? 32 : 16), n0, fb);
                     if (P.meta_tma) {
@@ -293,7 +306,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                         if (!L::kNF4Fmt)
                             tma_load_2d(smem_u32(ch + L::kOffsetOff), &P.omap, kb0 * 2, n0, fb);
                     }
-                    if (!L::kNF4Fmt && P.A > 0) bulk_load(smem_u32(ch + L::kBitsOff), P.anchor_bits + 2 * kb0, 32, fb);
+                } else {
+                    mbar_arrive(fb);
+                }
+                rm.next(2);
+            }
+            // anchor weight tiles of this tile, one per slot
+            for (int a = 0; a < P.a_pad / kBK; ++a) {
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(m_empty0 + 8 * rm.s, rm.ph ^ 1, abort, P.status)))
+                    goto meta_done;
+                const uint32_t fb = m_full0 + 8 * rm.s;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(fb, kATile);
+                    tma_load_2d(smem_u32(meta + rm.s * L::kChunkBytes), &P.awmap, a * kBK, n0, fb);
                 } else {
                     mbar_arrive(fb);
                 }
@@ -303,95 +328,129 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     meta_done:;
     } else if (warp < kEpiWarp0) {
         // ---------------------------------------------------------------- dequant into the A stages
-        const int d = tid - 32 * kDqWarp0, r = d & (kBM - 1), h = d >> 7;   // row of the tile, half of the 64 columns
+        // Two groups of four warps take alternate K-blocks (by K-block parity), so two
+        // K-blocks are in flight; each thread turns one row's 64 columns into 16-bit values.
+        const int g = (warp - kDqWarp0) >> 2, r = 32 * ((warp - kDqWarp0) & 3) + lane;
         const int sw = r & 7;
         const float C0 = -1.52f, C1 = -0.45f, C2 = 0.45f, C3 = 1.52f;
-        Ring ra, rb, rm;
+        Ring ra, rm;
         for (Item it{(int)blockIdx.x, 0}; it.tile < P.total_tiles; it.next(NKB)) {
+            const bool mine = (it.kb & 1) == g;
             uint8_t* arow = atile + ra.s * kATile + r * 128;
             if (it.kb < KB) {
                 const int j = it.kb % kChunk;
-                // warp-uniform waits: a lane that gives up takes its whole warp out
+                // every warp waits for each metadata chunk and releases it at its end, so a
+                // release never runs ahead of the load it frees (count: all dequant warps)
                 if (j == 0 && !__all_sync(0xffffffffu, mbar_wait_bounded(m_full0 + 8 * rm.s, rm.ph, abort, P.status)))
                     break;
-                if (!__all_sync(0xffffffffu, mbar_wait_bounded(a_empty0 + 8 * ra.s, ra.ph ^ 1, abort, P.status))) break;
-                const uint8_t* ch = meta + rm.s * L::kChunkBytes;
-                uint32_t c[4][4];
-                if (FMT == LQ_FMT_2BIT_LM_G32) {
-                    const uint2 cw = *reinterpret_cast<const uint2*>(ch + r * 64 + ((j ^ ((r >> 1) & 3)) << 4) + 8 * h);
-                    const float sf = half_bits_to_float(reinterpret_cast<const uint16_t*>(ch + L::kScaleOff + r * 16)[2 * j + h]);
-                    const float zf = half_bits_to_float(reinterpret_cast<const uint16_t*>(ch + L::kOffsetOff + r * 16)[2 * j + h]);
-                    const uint32_t P01 = pack2(__fmaf_rn(sf, C0, zf), __fmaf_rn(sf, C1, zf), P.bf16);
-                    const uint32_t P23 = pack2(__fmaf_rn(sf, C2, zf), __fmaf_rn(sf, C3, zf), P.bf16);
-                    dq2_word(cw.x, P01, P23, c[0], c[1]);
-                    dq2_word(cw.y, P01, P23, c[2], c[3]);
-                } else {
-                    const uint4 cw = *reinterpret_cast<const uint4*>(ch + r * 128 + (((2 * j + h) ^ sw) << 4));
-                    const float am = reinterpret_cast<const float*>(ch + L::kScaleOff + r * 16)[j];
-                    // this block's 16 values T[q] * absmax, one rounding, in byte-split registers
-                    uint32_t BL[4], BH[4];
+                if (mine) {
+                    if (!__all_sync(0xffffffffu, mbar_wait_bounded(a_empty0 + 8 * ra.s, ra.ph ^ 1, abort, P.status)))
+                        break;
+                    const uint8_t* ch = meta + rm.s * L::kChunkBytes;
+                    uint32_t c[32];   // c[4q + k]: columns 8q + 2k, 8q + 2k + 1
+                    if (FMT == LQ_FMT_2BIT_LM_G32) {
+                        const uint4 cw = *reinterpret_cast<const uint4*>(ch + r * 64 + ((j ^ ((r >> 1) & 3)) << 4));
+                        const uint32_t s2 = *reinterpret_cast<const uint32_t*>(ch + L::kScaleOff + r * 16 + 4 * j);
+                        const uint32_t z2 = *reinterpret_cast<const uint32_t*>(ch + L::kOffsetOff + r * 16 + 4 * j);
+                        const float s0 = half_bits_to_float((uint16_t)s2), z0 = half_bits_to_float((uint16_t)z2);
+                        const float s1 = half_bits_to_float((uint16_t)(s2 >> 16)), z1 = half_bits_to_float((uint16_t)(z2 >> 16));
+                        const uint32_t A01 = pack2(__fmaf_rn(s0, C0, z0), __fmaf_rn(s0, C1, z0), P.bf16);
+                        const uint32_t A23 = pack2(__fmaf_rn(s0, C2, z0), __fmaf_rn(s0, C3, z0), P.bf16);
+                        const uint32_t B01 = pack2(__fmaf_rn(s1, C0, z1), __fmaf_rn(s1, C1, z1), P.bf16);
+                        const uint32_t B23 = pack2(__fmaf_rn(s1, C2, z1), __fmaf_rn(s1, C3, z1), P.bf16);
+                        dq2_word(cw.x, A01, A23, *reinterpret_cast<uint32_t(*)[4]>(c + 0), *reinterpret_cast<uint32_t(*)[4]>(c + 4));
+                        dq2_word(cw.y, A01, A23, *reinterpret_cast<uint32_t(*)[4]>(c + 8), *reinterpret_cast<uint32_t(*)[4]>(c + 12));
+                        dq2_word(cw.z, B01, B23, *reinterpret_cast<uint32_t(*)[4]>(c + 16), *reinterpret_cast<uint32_t(*)[4]>(c + 20));
+                        dq2_word(cw.w, B01, B23, *reinterpret_cast<uint32_t(*)[4]>(c + 24), *reinterpret_cast<uint32_t(*)[4]>(c + 28));
+                        if (P.A > 0) {
+                            // anchor columns replace the 2-bit weights: clear them with the chunk's keep
+                            // masks, only in the 16-column words that hold one (the bitmap is warp-uniform)
+                            const uint2 bw = *reinterpret_cast<const uint2*>(ch + L::kBitsOff + 8 * j);
+                            const uint32_t* km = reinterpret_cast<const uint32_t*>(ch + L::kMaskOff + j * 128);
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        const uint32_t p01 = pack2(__fmul_rn(kNF4[4 * q4], am), __fmul_rn(kNF4[4 * q4 + 1], am), P.bf16);
-                        const uint32_t p23 = pack2(__fmul_rn(kNF4[4 * q4 + 2], am), __fmul_rn(kNF4[4 * q4 + 3], am), P.bf16);
-                        BL[q4] = prmt(p01, p23, 0x6420);
-                        BH[q4] = prmt(p01, p23, 0x7531);
-                    }
-                    const uint32_t ws[4] = {cw.x, cw.y, cw.z, cw.w};
-#pragma unroll
-                    for (int wi = 0; wi < 4; ++wi) {
-                        expand_nf4_fast(ws[wi], 0, BL, BH, c[wi][0], c[wi][1]);
-                        expand_nf4_fast(ws[wi], 1, BL, BH, c[wi][2], c[wi][3]);
-                    }
-                }
-#pragma unroll
-                for (int q = 0; q < 4; ++q) sts128(arow + (((4 * h + q) ^ sw) << 4), c[q][0], c[q][1], c[q][2], c[q][3]);
-                if (FMT == LQ_FMT_2BIT_LM_G32 && P.A > 0) {
-                    // anchor columns replace the 2-bit weights: zero them in the tile
-                    uint32_t bits = reinterpret_cast<const uint32_t*>(ch + L::kBitsOff)[2 * j + h];
-                    while (bits) {
-                        const int i = __ffs(bits) - 1;
-                        bits &= bits - 1;
-                        const int col = 32 * h + i;
-                        *reinterpret_cast<uint16_t*>(arow + (((col >> 3) ^ sw) << 4) + (col & 7) * 2) = 0;
-                    }
-                }
-                fence_proxy_async_smem();   // generic-proxy stores -> visible to the tensor core
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(a_full0 + 8 * ra.s);
-                    if (j == kChunk - 1 || it.kb == KB - 1) mbar_arrive(m_empty0 + 8 * rm.s);
-                }
-                if (j == kChunk - 1 || it.kb == KB - 1) rm.next(2);
-            } else {
-                // anchor block: TMA has put 64 binary16 anchor weights per row in the stage;
-                // zero the columns past A and convert to bf16 when x is bf16
-                if (!__all_sync(0xffffffffu, mbar_wait_bounded(b_full0 + 8 * rb.s, rb.ph, abort, P.status))) break;
-                const int a0 = (it.kb - KB) * kBK + 32 * h;
-                if (P.bf16 || a0 + 32 > P.A) {
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        uint4* p = reinterpret_cast<uint4*>(arow + (((4 * h + q) ^ sw) << 4));
-                        const uint4 u4 = *p;
-                        uint32_t v[4] = {u4.x, u4.y, u4.z, u4.w};
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const int a = a0 + 8 * q + 2 * i;
-                            uint32_t w = a < P.A ? v[i] : 0u;
-                            if (a + 1 >= P.A) w &= 0xFFFFu;
-                            if (P.bf16)
-                                w = pack2(half_bits_to_float((uint16_t)w), half_bits_to_float((uint16_t)(w >> 16)), 1);
-                            v[i] = w;
+                            for (int wi = 0; wi < 4; ++wi) {
+                                if (((wi < 2 ? bw.x : bw.y) >> (16 * (wi & 1))) & 0xFFFFu) {
+                                    const uint4 m0 = *reinterpret_cast<const uint4*>(km + 8 * wi);
+                                    const uint4 m1 = *reinterpret_cast<const uint4*>(km + 8 * wi + 4);
+                                    c[8 * wi + 0] &= m0.x;
+                                    c[8 * wi + 1] &= m0.y;
+                                    c[8 * wi + 2] &= m0.z;
+                                    c[8 * wi + 3] &= m0.w;
+                                    c[8 * wi + 4] &= m1.x;
+                                    c[8 * wi + 5] &= m1.y;
+                                    c[8 * wi + 6] &= m1.z;
+                                    c[8 * wi + 7] &= m1.w;
+                                }
+                            }
                         }
-                        *p = make_uint4(v[0], v[1], v[2], v[3]);
+                    } else {
+                        const uint8_t* crow = ch + r * 128;
+                        const uint4 cw0 = *reinterpret_cast<const uint4*>(crow + (((2 * j) ^ sw) << 4));
+                        const uint4 cw1 = *reinterpret_cast<const uint4*>(crow + (((2 * j + 1) ^ sw) << 4));
+                        const float am = reinterpret_cast<const float*>(ch + L::kScaleOff + r * 16)[j];
+                        // this block's 16 values T[q] * absmax, one rounding, in byte-split registers
+                        uint32_t BL[4], BH[4];
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            const uint32_t p01 = pack2(__fmul_rn(kNF4[4 * q4], am), __fmul_rn(kNF4[4 * q4 + 1], am), P.bf16);
+                            const uint32_t p23 = pack2(__fmul_rn(kNF4[4 * q4 + 2], am), __fmul_rn(kNF4[4 * q4 + 3], am), P.bf16);
+                            BL[q4] = prmt(p01, p23, 0x6420);
+                            BH[q4] = prmt(p01, p23, 0x7531);
+                        }
+                        const uint32_t ws[8] = {cw0.x, cw0.y, cw0.z, cw0.w, cw1.x, cw1.y, cw1.z, cw1.w};
+#pragma unroll
+                        for (int wi = 0; wi < 8; ++wi) {
+                            expand_nf4_fast(ws[wi], 0, BL, BH, c[4 * wi + 0], c[4 * wi + 1]);
+                            expand_nf4_fast(ws[wi], 1, BL, BH, c[4 * wi + 2], c[4 * wi + 3]);
+                        }
                     }
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) sts128(arow + ((q ^ sw) << 4), c[4 * q], c[4 * q + 1], c[4 * q + 2], c[4 * q + 3]);
+                    fence_proxy_async_smem();   // generic-proxy stores -> visible to the tensor core
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(a_full0 + 8 * ra.s);
                 }
-                fence_proxy_async_smem();
+                if (j == kChunk - 1 || it.kb == KB - 1) {
+                    if (lane == 0) mbar_arrive(m_empty0 + 8 * rm.s);
+                    rm.next(2);
+                }
+            } else {
+                // anchor block: the metadata slot holds 64 binary16 anchor weights per row; the
+                // owning group copies them into the stage, zero past A, in bf16 when x is bf16
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(m_full0 + 8 * rm.s, rm.ph, abort, P.status))) break;
+                if (mine) {
+                    if (!__all_sync(0xffffffffu, mbar_wait_bounded(a_empty0 + 8 * ra.s, ra.ph ^ 1, abort, P.status)))
+                        break;
+                    const uint8_t* srow = meta + rm.s * L::kChunkBytes + r * 128;
+                    const int a0 = (it.kb - KB) * kBK;
+                    const bool fix = P.bf16 || a0 + kBK > P.A;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const int off = (q ^ sw) << 4;
+                        const uint4 u4 = *reinterpret_cast<const uint4*>(srow + off);
+                        uint32_t v[4] = {u4.x, u4.y, u4.z, u4.w};
+                        if (fix) {
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const int a = a0 + 8 * q + 2 * i;
+                                uint32_t w = a < P.A ? v[i] : 0u;
+                                if (a + 1 >= P.A) w &= 0xFFFFu;
+                                if (P.bf16)
+                                    w = pack2(half_bits_to_float((uint16_t)w), half_bits_to_float((uint16_t)(w >> 16)), 1);
+                                v[i] = w;
+                            }
+                        }
+                        sts128(arow + off, v[0], v[1], v[2], v[3]);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(a_full0 + 8 * ra.s);
+                }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(a_full0 + 8 * ra.s);
+                if (lane == 0) mbar_arrive(m_empty0 + 8 * rm.s);
+                rm.next(2);
             }
             ra.next(SA);
-            rb.next(kStagesB);
         }
     } else {
         // ---------------------------------------------------------------- epilogue: TMEM -> y
@@ -407,10 +466,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                 uint32_t v[32];
                 tmem_ld32(tmem + ((uint32_t)(32 * quarter) << 16) + acc * kBN + 32 * cc, v);
                 if (n < P.N) {
+                    const int mb = m0 + 32 * cc, mcount = min(32, P.M - mb);
+                    const size_t o = (size_t)mb * P.N + n;
+                    if (P.y_dtype == LQ_BF16) {
+                        __nv_bfloat16* yp = static_cast<__nv_bfloat16*>(P.y) + o;
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int m = m0 + 32 * cc + j;
-                        if (m < P.M) store_out(P.y, (size_t)m * P.N + n, P.y_dtype, __uint_as_float(v[j]));
+                        for (int j = 0; j < 32; ++j)
+                            if (j < mcount) yp[(size_t)j * P.N] = __float2bfloat16_rn(__uint_as_float(v[j]));
+                    } else if (P.y_dtype == LQ_F16) {
+                        __half* yp = static_cast<__half*>(P.y) + o;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (j < mcount) yp[(size_t)j * P.N] = __float2half_rn(__uint_as_float(v[j]));
+                    } else {
+                        float* yp = static_cast<float*>(P.y) + o;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (j < mcount) yp[(size_t)j * P.N] = __uint_as_float(v[j]);
                     }
                 }
             }
