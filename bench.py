@@ -11,6 +11,12 @@ metric: weight GB/s = algorithmic bytes (codes + scales + offsets + anchor
 weights + anchor indices + x + y) / time; `roofline.frac` against the measured
 HBM copy bandwidth; equivalent tok/s of a 32-layer stack.
 
+Second figure (`gemm`): prefill of a 14B-shaped layer (q/k/v/o 5120x5120,
+gate/up 13824x5120, down 5120x13824) at M = 2048 bf16 tokens, one lq_gemm
+call per projection, for 2-bit G=32 + anchors and for NF4 block 64; TFLOP/s =
+2*M*N*K summed over the layer / step time, against the measured dense bf16
+peak.
+
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl lq|reference]
 
 Under torchrun each rank runs its own replica (the layer needs no exchange);
@@ -171,6 +177,65 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+GEMM_M = 2048
+GEMM_WORKLOAD = "14b decoder layer prefill, M=2048 bf16 tokens, 7 projections, one lq_gemm call each"
+
+
+def gemm_layer(lq, torch, h, fmt: str, device: str, steps: int, warmup: int):
+    """Time the 14B-layer prefill: returns (TFLOP/s, ms per layer, mean ms of the largest projection's launch)."""
+    from math import floor
+    mats, flops = [], 0
+    for i, (name, N, K) in enumerate(synth.LAYER_SHAPES["14b"]):
+        if fmt == "2bit":
+            pk = synth.random_packed_2bit(N, K, int(floor(0.035 * K)), sigma=0.02, seed=500, cfg=5, matrix_id=i)
+            w = lq.QuantWeights.from_host(pk, lq.FMT_2BIT, device=device)
+        else:
+            pk = synth.random_packed_nf4(N, K, sigma=0.02, seed=500, cfg=5, matrix_id=i)
+            w = lq.QuantWeights.from_host(pk, lq.FMT_NF4, device=device)
+        outl = synth.outlier_channels(K, 0.01, seed=500, cfg=5)
+        xb = synth.activations(GEMM_M, K, "bf16", synth.channel_sigma(K, outl, 20.0), seed=500, cfg=5, matrix_id=i)
+        x = torch.from_numpy(xb).view(torch.bfloat16).to(device)
+        y = torch.empty((GEMM_M, N), dtype=torch.bfloat16, device=device)
+        mats.append((name, w, x, y))
+        flops += 2 * GEMM_M * N * K
+    stream = torch.cuda.current_stream()
+
+    def step():
+        for _, w, x, y in mats:
+            h.gemm(w, x, y, stream=stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        time.sleep(0.2)
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    # the largest projection alone, for the kernel roofline
+    name, w, x, y = max(mats, key=lambda m: m[1].N * m[1].K)
+    a0 = torch.cuda.Event(enable_timing=True)
+    a1 = torch.cuda.Event(enable_timing=True)
+    reps = 10
+    a0.record(stream)
+    for _ in range(reps):
+        h.gemm(w, x, y, stream=stream)
+    a1.record(stream)
+    torch.cuda.synchronize()
+    one_ms = a0.elapsed_time(a1) / reps
+    one_flops = 2 * GEMM_M * w.N * w.K
+    launches = sum(3 if fmt == "2bit" else 1 for _ in mats)   # 2-bit: bitmap memset + anchor gather + GEMM
+    return {"fmt": fmt, "value": round(flops / (ms * 1e-3) / 1e12, 1), "unit": "TFLOP/s", "ms_per_layer": round(ms, 4),
+            "largest": {"name": name, "N": w.N, "K": w.K, "ms": round(one_ms, 4),
+                        "tflops": round(one_flops / (one_ms * 1e-3) / 1e12, 1)},
+            "launches_per_layer": launches, "clocks": clk.summary()}
+
+
 def run_lq(args):
     import torch
 
@@ -276,6 +341,19 @@ def run_lq(args):
     e2e_ms = e0.elapsed_time(e1) / args.steps
     e2e_val = world * layer_bytes / (e2e_ms * 1e-3) / 1e9
 
+    gemm = None
+    if not args.no_gemm:
+        dev = f"cuda:{local}"
+        g2 = gemm_layer(lq, torch, h, "2bit", dev, args.gemm_steps, 3)
+        g4 = gemm_layer(lq, torch, h, "nf4", dev, args.gemm_steps, 3)
+        gemm = {"workload": GEMM_WORKLOAD, "metric": "dequant-GEMM TFLOP/s", "dtype": "bf16 x bf16 -> f32 accumulate",
+                "2bit": g2, "nf4": g4,
+                "roofline": {"bound": "tensor", "achieved": g2["largest"]["tflops"], "peak": bf16, "unit": "TFLOP/s",
+                             "frac": round(g2["largest"]["tflops"] / bf16, 4), "peak_kind": peak_kind + " bf16 burst",
+                             "kernel": "gemm_kernel<2bit> on the largest projection, timed alone",
+                             "traffic": None},
+                "frac_of_bf16_peak": {"2bit": round(g2["value"] / bf16, 4), "nf4": round(g4["value"] / bf16, 4)}}
+
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tpath):
@@ -299,8 +377,9 @@ def run_lq(args):
                          "algorithmic_bytes_per_launch": layer_bytes},
             "cpu_baseline": {"value": round(cpu_v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": args.steps,
+            "gpu_launches": 2 * args.steps,   # x pre-pass + streaming GEMV per grouped call
             "clocks": clk.summary(),
+            "gemm": gemm,
         }
         print(json.dumps(line), flush=True)
     h.close()
@@ -314,6 +393,8 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="lq", choices=["lq", "reference"])
+    ap.add_argument("--gemm-steps", type=int, default=20)
+    ap.add_argument("--no-gemm", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
