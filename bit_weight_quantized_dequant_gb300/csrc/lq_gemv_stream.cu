@@ -8,11 +8,13 @@
 //    order with the anchor columns zeroed (anchors replace those weights), and x
 //    gathered at the anchor columns.  They chain to the main kernel by programmatic
 //    dependent launch; each main CTA issues its first weight loads before it waits.
-//  * One CTA = 8 warps over one tile of 16 x (8 / ks) rows and the full K: the ks
-//    warps of a row tile split K into contiguous slices, so no partial sums leave
-//    the CTA (shared-memory reduction at the end, no atomics, no workspace).
+//  * Work is cut into units of 16 rows x 256 columns (anchor columns: 16 x 64), and
+//    every warp of the launch takes an equal contiguous run of the units of all
+//    problems, so no warp waits on another and no tile tail is left.  Row-block sums
+//    leave a warp through a slot of its own; the last warp of a block adds the slots
+//    in a fixed order (an arrival count tells it), so results are reproducible.
 //  * Each thread streams its two rows with 16-byte loads (64 codes per row per
-//    256-column step) and 4-byte scale/offset loads, two steps ahead of use.
+//    unit) and 4-byte scale/offset loads, one unit ahead of use.
 //  * x fragments come straight from the pre-permuted copy (L1-resident, one 8-byte
 //    load per mma).  Lanes whose token does not exist load harmless neighbouring
 //    values: they only feed output columns that are never stored.
@@ -36,12 +38,18 @@ namespace lq {
 namespace {
 
 constexpr int kWarps = 8;
+constexpr int kAnchorCols = 48;   // anchor columns per anchor unit
 #ifndef LQ_STREAM_MIN_BLOCKS
 #define LQ_STREAM_MIN_BLOCKS 2   // resident CTAs per SM the register allocation aims for
 #endif
 constexpr int kThreadsS = kWarps * 32;
 
 // ---- pre-pass: x -> binary16, anchors zeroed, fragment order ------------------------
+//
+// One warp writes one job: a 256-column step of the fragment-ordered copy of x with
+// the anchor columns zeroed (fragment order permutes columns inside a step only), or a
+// slice of 256 anchor slots of x gathered at the anchor columns.  Every lane writes
+// 16-byte items; no job depends on another.
 
 struct PrepDesc {
     const uint16_t* x;
@@ -52,93 +60,206 @@ struct PrepDesc {
     uint16_t* xaperm;          // [batch][a_pad/16][M][16]
     int64_t xperm_stride, xaperm_stride;   // halves per batch member
     int K, A, a_pad, batch;
-    int ctas;                  // CTAs per batch member
-    int64_t cta_begin;         // first CTA of this problem
+    int jobs;                  // jobs per batch member: K/256 steps, then ceil(a_pad/256) anchor slices
+    int64_t job_begin;         // first job of this problem
+};
+
+// A region the pre-pass clears: `batch` runs of `words` 4-byte words, `stride` words apart.
+struct ZeroTask {
+    uint32_t* p;
+    int64_t words, stride;
+    int batch;
 };
 
 struct PrepParams {
     PrepDesc d[kMaxGroup];
-    int count, M, x_bf16, format;
-    int64_t total_ctas;
+    ZeroTask z[2 * kMaxGroup];
+    int count, M, x_bf16, format, zero_tasks;
+    int64_t total_jobs;
 };
 
-constexpr int kPrepItems = 256;    // 8-half output items per pre-pass CTA (one per thread)
+constexpr int kPrepWarps = 2;   // jobs per pre-pass CTA
 
 __device__ __forceinline__ uint16_t to_half_bits(uint16_t raw, int x_bf16) {
     return x_bf16 ? __half_as_ushort(__float2half_rn(bf16_bits_to_float(raw))) : raw;
 }
 
-// One CTA covers kPrepItems consecutive 16-byte items of one batch member: first the
-// fragment-ordered copy of x with the anchor columns zeroed (a bitmap of the anchor
-// columns in shared memory marks them), then x gathered at the anchor columns.
-__global__ void __launch_bounds__(256) xprep_kernel(const __grid_constant__ PrepParams P) {
-    extern __shared__ uint32_t anchor_bits[];
+__global__ void __launch_bounds__(32 * kPrepWarps) xprep_kernel(const __grid_constant__ PrepParams P) {
+    __shared__ uint32_t step_bits[kPrepWarps][8];
     pdl_launch_dependents();
-    const int64_t cta = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // the arrival counts and sums the main kernel adds into
+    for (int zt = 0; zt < P.zero_tasks; ++zt) {
+        const ZeroTask& Z = P.z[zt];
+        const int64_t total = Z.words * Z.batch;
+        for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+            const int64_t b = i / Z.words;
+            Z.p[b * Z.stride + (i - b * Z.words)] = 0u;
+        }
+    }
+    const int64_t job = (int64_t)blockIdx.x * kPrepWarps + warp;
+    if (job >= P.total_jobs) return;
     int p = 0;
-    while (p + 1 < P.count && cta >= P.d[p + 1].cta_begin) ++p;
+    while (p + 1 < P.count && job >= P.d[p + 1].job_begin) ++p;
     const PrepDesc& D = P.d[p];
-    const int64_t local = cta - D.cta_begin;
-    const int64_t l = local / D.ctas;
-    const int part = (int)(local - l * D.ctas);
+    const int64_t local = job - D.job_begin;
+    const int64_t l = local / D.jobs;
+    const int jb = (int)(local - l * D.jobs);
     const int M = P.M, K = D.K, A = D.A;
     const uint16_t* x = reinterpret_cast<const uint16_t*>(reinterpret_cast<const char*>(D.x) + l * D.stride_x);
     const int32_t* aidx = A > 0 ? reinterpret_cast<const int32_t*>(reinterpret_cast<const char*>(D.anchor_idx) + l * D.stride_anchor_idx)
                                 : nullptr;
-    for (int i = threadIdx.x; i < K / 32; i += blockDim.x) anchor_bits[i] = 0u;
-    __syncthreads();
-    for (int a = threadIdx.x; a < A; a += blockDim.x) {
-        const int k = __ldg(aidx + a);
-        atomicOr(&anchor_bits[k >> 5], 1u << (k & 31));
-    }
-    __syncthreads();
-    const int64_t code_items = (int64_t)M * K / 8, all_items = code_items + (int64_t)M * D.a_pad / 8;
-    const int64_t i0 = (int64_t)part * kPrepItems, i1 = min(all_items, i0 + kPrepItems);
-    for (int64_t it = i0 + threadIdx.x; it < i1; it += blockDim.x) {
-        const bool code = it < code_items;
-        const int64_t d0 = 8 * (code ? it : it - code_items);
-        const int line = (int)(d0 >> 4), pos0 = (int)(d0 & 15);
-        const int bi = line / M, m = line - bi * M;
-        uint16_t v[8];
+    const int steps = K / 256;
+    if (jb < steps) {
+        // anchor columns of this step, as 8 words of bits
+        const int k0 = jb * 256;
+        if (lane < 8) step_bits[warp][lane] = 0u;
+        __syncwarp();
+        for (int a0 = 0; a0 < A; a0 += 8 * 32) {
+            int kk[8];   // all loads of a round issue before any of them is used
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const int pos = pos0 + e, tt = pos >> 2, hh = pos & 3;
-            int k = -1;
-            if (code) {
-                k = P.format == LQ_FMT_2BIT_LM_G32 ? (bi >> 4) * 256 + tt * 64 + ((bi >> 2) & 3) * 16 + hh * 4 + (bi & 3)
-                                                   : (bi >> 2) * 64 + tt * 16 + (bi & 3) * 4 + hh;
-                if ((anchor_bits[k >> 5] >> (k & 31)) & 1u) k = -1;
-            } else {
-                const int a = 16 * bi + 2 * tt + (hh & 1) + 8 * (hh >> 1);
-                if (a < A) k = __ldg(aidx + a);
+            for (int j = 0; j < 8; ++j) {
+                const int a = a0 + 32 * j + lane;
+                kk[j] = a < A ? __ldg(aidx + a) - k0 : -1;
             }
-            v[e] = k >= 0 ? to_half_bits(x[(int64_t)m * K + k], P.x_bf16) : (uint16_t)0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (kk[j] >= 0 && kk[j] < 256) atomicOr(&step_bits[warp][kk[j] >> 5], 1u << (kk[j] & 31));
         }
-        uint16_t* dst = (code ? D.xperm + l * D.xperm_stride : D.xaperm + l * D.xaperm_stride) + d0;
-        *reinterpret_cast<uint4*>(dst) = make_uint4((uint32_t)v[0] | ((uint32_t)v[1] << 16), (uint32_t)v[2] | ((uint32_t)v[3] << 16),
-                                                    (uint32_t)v[4] | ((uint32_t)v[5] << 16), (uint32_t)v[6] | ((uint32_t)v[7] << 16));
+        __syncwarp();
+        uint16_t* dst = D.xperm + l * D.xperm_stride + (int64_t)k0 * M;
+        for (int it = lane; it < 32 * M; it += 32) {
+            const int d0 = 8 * it, line = d0 >> 4, pos0 = d0 & 15;
+            const int bl = line / M, m = line - bl * M;   // mma block inside the step, token
+            uint16_t v[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int pos = pos0 + e, tt = pos >> 2, hh = pos & 3;
+                const int kl = P.format == LQ_FMT_2BIT_LM_G32 ? tt * 64 + ((bl >> 2) & 3) * 16 + hh * 4 + (bl & 3)
+                                                               : (bl >> 2) * 64 + tt * 16 + (bl & 3) * 4 + hh;
+                const bool anchor = (step_bits[warp][kl >> 5] >> (kl & 31)) & 1u;
+                v[e] = anchor ? (uint16_t)0 : to_half_bits(x[(int64_t)m * K + k0 + kl], P.x_bf16);
+            }
+            *reinterpret_cast<uint4*>(dst + d0) = make_uint4((uint32_t)v[0] | ((uint32_t)v[1] << 16), (uint32_t)v[2] | ((uint32_t)v[3] << 16),
+                                                            (uint32_t)v[4] | ((uint32_t)v[5] << 16), (uint32_t)v[6] | ((uint32_t)v[7] << 16));
+        }
+    } else {
+        // x gathered at anchor slots [256 * j, 256 * j + 256) (zero past A)
+        const int a_base = (jb - steps) * 256, n_slots = min(256, D.a_pad - a_base);
+        uint16_t* dst = D.xaperm + l * D.xaperm_stride + (int64_t)a_base * M;
+        for (int it = lane; it < n_slots * M / 8; it += 32) {
+            const int d0 = 8 * it, line = d0 >> 4, pos0 = d0 & 15;
+            const int bl = line / M, m = line - bl * M;
+            uint16_t v[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int pos = pos0 + e, tt = pos >> 2, hh = pos & 3;
+                const int a = a_base + 16 * bl + 2 * tt + (hh & 1) + 8 * (hh >> 1);
+                v[e] = a < A ? to_half_bits(x[(int64_t)m * K + __ldg(aidx + a)], P.x_bf16) : (uint16_t)0;
+            }
+            *reinterpret_cast<uint4*>(dst + d0) = make_uint4((uint32_t)v[0] | ((uint32_t)v[1] << 16), (uint32_t)v[2] | ((uint32_t)v[3] << 16),
+                                                            (uint32_t)v[4] | ((uint32_t)v[5] << 16), (uint32_t)v[6] | ((uint32_t)v[7] << 16));
+        }
     }
 }
 
-struct SDesc {
+// ---- main kernel ---------------------------------------------------------------
+//
+// Work unit: 16 output rows x 256 code columns of one batch member (code unit), or
+// 16 rows x 48 anchor columns (anchor unit: three mma blocks, the register size of a
+// code unit's loads).  A problem's units are ordered member,
+// 16-row block, then K (code units, then anchor units).  All units of the launch
+// form one sequence, and warp w of W takes the contiguous range [U*w/W, U*(w+1)/W):
+// every warp does the same work to within one unit, whatever the shapes.  A warp
+// keeps the sums of the row block it is in and writes them to its own slot when it
+// leaves the block; an arrival count per row block tells the warp that completes the
+// block to add the slots in warp order and write y (the result does not depend on
+// timing).
+
+struct FDesc {
     const uint8_t* codes;
     const void* scales;
     const uint16_t* offsets;
     const uint16_t* anchor_w;
-    const uint16_t* xperm;      // [batch][K/16][M][16] (+ padding)
-    const uint16_t* xaperm;     // [batch][a_pad/16][M][16] (+ padding)
+    const uint16_t* xperm;      // [batch][K/16][M][16]
+    const uint16_t* xaperm;     // [batch][a_pad/16][M][16]
+    float* part;                // partial sums [batch][rblocks][cmax][M][16], one slot per contributing warp
+    unsigned* cnt;              // arrival counts [batch][rblocks]
     void* y;
-    int64_t stride_codes, stride_scales, stride_offsets, stride_anchor_w, stride_y;
-    int64_t xperm_stride, xaperm_stride;   // halves
-    int N, K, A, ld_anchor, batch, ks, tiles;   // ks: warps per row tile (K slices); tiles: tiles per member
-    int64_t tile_begin;   // first global tile of this problem
+    int64_t stride_codes, stride_scales, stride_offsets, stride_anchor_w, stride_y;   // bytes per member
+    int64_t xperm_stride, xaperm_stride;                                               // halves per member
+    int N, K, A, ld_anchor, batch;
+    int steps, su, rblocks;     // code units per row block; units per row block (code + anchor)
+    int cmax;                   // most warps that can share one row block
+    int64_t unit_begin;         // first unit of this problem in the launch
 };
 
-struct SParams {
-    SDesc d[kMaxGroup];
+struct FParams {
+    FDesc d[kMaxGroup];
     int count, M, y_dtype;
-    int64_t total_tiles;
+    int64_t total_units, total_warps;
 };
+
+
+// Position of a unit: problem, member, 16-row block, unit inside the row block, with
+// the problem's units per row block cached.
+struct Pos {
+    int p, rb, s, steps, su;
+    int64_t l;
+};
+
+// (rare paths are kept out of line: the unrolled unit loop must stay small)
+__device__ __noinline__ Pos locate(const FParams& P, int64_t u) {
+    Pos q;
+    q.p = 0;
+    while (q.p + 1 < P.count && u >= P.d[q.p + 1].unit_begin) ++q.p;
+    const FDesc& D = P.d[q.p];
+    int64_t loc = u - D.unit_begin;
+    const int64_t per_member = (int64_t)D.rblocks * D.su;
+    q.l = loc / per_member;
+    loc -= q.l * per_member;
+    q.rb = (int)(loc / D.su);
+    q.s = (int)(loc - (int64_t)q.rb * D.su);
+    q.steps = D.steps;
+    q.su = D.su;
+    return q;
+}
+
+__device__ __forceinline__ void next_block(const FParams& P, Pos& q) {
+    const FDesc& D = P.d[q.p];
+    if (++q.rb == D.rblocks) {
+        q.rb = 0;
+        if (++q.l == D.batch) {
+            q.l = 0;
+            if (++q.p < P.count) {
+                q.steps = P.d[q.p].steps;
+                q.su = P.d[q.p].su;
+            }
+        }
+    }
+}
+
+// Next unit; returns true when the row block changes.
+__device__ __forceinline__ bool next_pos(const FParams& P, Pos& q) {
+    if (++q.s < q.su) return false;
+    q.s = 0;
+    next_block(P, q);
+    return true;
+}
+
+// The warp whose range [U*w/W, U*(w+1)/W) holds unit u.
+__device__ __noinline__ int64_t owner_warp(int64_t u, int64_t W, int64_t U) { return ((u + 1) * W - 1) / U; }
+
+// The last warp of a row block adds the slots of its nc contributors in order and writes y.
+__device__ __noinline__ void finish_block(const float* slots, int nc, int M, void* y, int N, int row0, int y_dtype,
+                                          int lane) {
+    for (int i = lane; i < 16 * M; i += 32) {
+        const int m = i >> 4, row = row0 + (i & 15);
+        float sum = 0.f;
+        for (int c = 0; c < nc; ++c) sum += __ldcg(slots + c * M * 16 + i);
+        if (row < N) store_out(y, (size_t)m * N + row, y_dtype, sum);
+    }
+}
 
 template <int NT, int MT>
 __device__ __forceinline__ void mma_xg(float (&acc)[NT][4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -146,103 +267,6 @@ __device__ __forceinline__ void mma_xg(float (&acc)[NT][4], uint32_t a0, uint32_
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) mma_f16_16816(acc[nt], a0, a1, a2, a3, b[nt].x, b[nt].y);
 }
-
-// x fragment of mma block bi (n-tile nt) for this thread: 8 bytes of the permuted copy.
-// `xp` already points at this thread's token and lane; for more than 8 tokens the
-// n-tile offsets come from `tok` (absent tokens read the last real token: their
-// products only reach output columns that are never stored).
-template <int MT>
-__device__ __forceinline__ uint2 xfrag(const uint16_t* xp, int bi, int M, int tok_nt) {
-    const int MM = MT > 0 ? MT : M;
-    return __ldg(reinterpret_cast<const uint2*>(xp + bi * MM * 16 + tok_nt));
-}
-
-// One warp's view of a tile: rows, K slice and pointers at the first step of its slice.
-struct TileView {
-    bool valid;
-    int p, tile, rtiles, ks, rt, slice, steps;
-    int64_t l;
-};
-
-__device__ __forceinline__ TileView view_tile(const SParams& P, int64_t T, int warp) {
-    TileView v;
-    v.valid = T < P.total_tiles;
-    if (!v.valid) return v;
-    int p = 0;
-    while (p + 1 < P.count && T >= P.d[p + 1].tile_begin) ++p;
-    const SDesc& D = P.d[p];
-    const int64_t local = T - D.tile_begin;
-    v.p = p;
-    v.l = local / D.tiles;
-    v.tile = (int)(local - v.l * D.tiles);
-    v.ks = D.ks;
-    v.rtiles = kWarps / D.ks;
-    v.rt = warp / D.ks;
-    v.slice = warp - v.rt * D.ks;
-    const int nsteps = D.K / 256;
-    const int s_begin = (int)((int64_t)nsteps * v.slice / D.ks);
-    v.steps = (int)((int64_t)nsteps * (v.slice + 1) / D.ks) - s_begin;
-    v.tile = v.tile;
-    return v;
-}
-
-// Streams one thread's two rows, step after step, across the tiles of its CTA.
-template <int FMT, int MT>
-struct Loader {
-    const uint8_t *cg, *cg8;
-    const uint16_t *sg, *sg8, *zg, *zg8;   // 2-bit scales/offsets (NF4: sg/sg8 hold the absmax rows)
-    const uint16_t* xsrc;                  // this step's x slice in the permuted copy (+ 8 halves per lane)
-    int step, steps;
-    int64_t T;
-    bool valid;
-
-    __device__ __forceinline__ void open(const SParams& P, int64_t T_, int warp, int g, int t) {
-        T = T_;
-        const TileView v = view_tile(P, T, warp);
-        valid = v.valid;
-        if (!valid) return;
-        const SDesc& D = P.d[v.p];
-        const int M = MT > 0 ? MT : P.M;
-        const int N = D.N, K = D.K;
-        const int rg = (v.tile * v.rtiles + v.rt) * 16 + g, rg8 = rg + 8;
-        const int64_t r0 = rg < N ? rg : 0, r1 = rg8 < N ? rg8 : 0;   // rows past N read row 0, never stored
-        const int s_begin = (int)((int64_t)(K / 256) * v.slice / v.ks);
-        const uint8_t* codes = D.codes + v.l * D.stride_codes;
-        const char* sc = static_cast<const char*>(D.scales) + v.l * D.stride_scales;
-        if (FMT == LQ_FMT_2BIT_LM_G32) {
-            const uint16_t* s16 = reinterpret_cast<const uint16_t*>(sc);
-            const uint16_t* o16 = reinterpret_cast<const uint16_t*>(reinterpret_cast<const char*>(D.offsets) + v.l * D.stride_offsets);
-            cg = codes + r0 * (K / 4) + 16 * t + 64 * s_begin;
-            cg8 = codes + r1 * (K / 4) + 16 * t + 64 * s_begin;
-            sg = s16 + r0 * (K / 32) + 2 * t + 8 * s_begin;
-            sg8 = s16 + r1 * (K / 32) + 2 * t + 8 * s_begin;
-            zg = o16 + r0 * (K / 32) + 2 * t + 8 * s_begin;
-            zg8 = o16 + r1 * (K / 32) + 2 * t + 8 * s_begin;
-        } else {
-            const float* am = reinterpret_cast<const float*>(sc);
-            cg = codes + r0 * (K / 2) + 8 * t + 128 * s_begin;
-            cg8 = codes + r1 * (K / 2) + 8 * t + 128 * s_begin;
-            sg = reinterpret_cast<const uint16_t*>(am + r0 * (K / 64) + 4 * s_begin);
-            sg8 = reinterpret_cast<const uint16_t*>(am + r1 * (K / 64) + 4 * s_begin);
-        }
-        const int MM = MT > 0 ? MT : M;
-        xsrc = D.xperm + v.l * D.xperm_stride + (int64_t)s_begin * 256 * MM + (threadIdx.x & 31) * 8;
-        step = 0;
-        steps = v.steps;
-    }
-    __device__ __forceinline__ void advance(const SParams& P, int warp, int g, int t) {
-        if (++step < steps) {
-            if (FMT == LQ_FMT_2BIT_LM_G32) {
-                cg += 64; cg8 += 64; sg += 8; sg8 += 8; zg += 8; zg8 += 8;
-            } else {
-                cg += 128; cg8 += 128; sg += 8; sg8 += 8;   // 4 floats
-            }
-            xsrc += 256 * (MT > 0 ? MT : P.M);
-        } else {
-            open(P, T + gridDim.x, warp, g, t);
-        }
-    }
-};
 
 struct Step2 {
     uint4 c0, c1;
@@ -254,22 +278,19 @@ struct StepNF4 {
     float a0[4], a1[4];
 };
 
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem)), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
+// A warp walks its range as segments: the units of its range inside one row block.
+// Inside a segment the code units run in a tight loop (one unit of loads in flight,
+// pointers only move), then the anchor units; the row block's sums leave through
+// flush() at the segment's end.  x fragments are read straight from the permuted copy
+// (L1-resident: every warp of an SM streams the same few tens of KiB).
 template <int FMT, int MT, int NT>
-__global__ void __launch_bounds__(kThreadsS, LQ_STREAM_MIN_BLOCKS) gemv_stream_kernel(const __grid_constant__ SParams P) {
-    __shared__ float red[kWarps][16][(NT * 8) + 1];
-    // per warp, three x slices of one 256-column step each (binary16, fragment order)
-    extern __shared__ __align__(16) uint16_t xring[];
-    const int M = MT > 0 ? MT : P.M;
-    const int MM = MT > 0 ? MT : M;
+__global__ void __launch_bounds__(kThreadsS, LQ_STREAM_MIN_BLOCKS) gemv_stream_kernel(const __grid_constant__ FParams P) {
+    constexpr int M = MT;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    uint16_t* xw = xring + warp * 3 * 256 * MM;             // this warp's ring
+    const int64_t W = P.total_warps;
+    const int wid = blockIdx.x * kWarps + warp;
+    if (wid >= W) return;
+    const int64_t u_begin = P.total_units * wid / W, u_end = P.total_units * (wid + 1) / W;
     const int xlane = min(g, M - 1) * 16 + t * 4;            // this lane's fragment inside a block
     int tok[NT];   // x-fragment offset of each n-tile's token (clamped to the last real token)
 #pragma unroll
@@ -279,233 +300,249 @@ __global__ void __launch_bounds__(kThreadsS, LQ_STREAM_MIN_BLOCKS) gemv_stream_k
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
 
-    // The finished tile: anchors of this warp, then the K-slice reduction and the store of y.
-    int64_t T = blockIdx.x;
-    TileView CV = view_tile(P, T, warp);
-    int cstep = 0;
-    auto finish_tile = [&]() {
-        const TileView v = CV;
-        const SDesc& D = P.d[v.p];
-        const int N = D.N;
-        const int rg = (v.tile * v.rtiles + v.rt) * 16 + g, rg8 = rg + 8;
-        if (FMT == LQ_FMT_2BIT_LM_G32 && D.A > 0) {
-            const int64_t r0 = rg < N ? rg : 0, r1 = rg8 < N ? rg8 : 0;
-            const uint16_t* aw = reinterpret_cast<const uint16_t*>(reinterpret_cast<const char*>(D.anchor_w) + v.l * D.stride_anchor_w);
-            const uint16_t* awg = aw + r0 * D.ld_anchor;
-            const uint16_t* awg8 = aw + r1 * D.ld_anchor;
-            const uint16_t* xa = D.xaperm + v.l * D.xaperm_stride + xlane;
-            const int A = D.A;
-            auto pair = [&](const uint16_t* row, int a) -> uint32_t {
-                if (a >= A) return 0u;
-                const uint32_t w = ldg32(row + a);
-                return (a + 1 < A) ? w : (w & 0xFFFFu);
-            };
-            for (int ab = v.slice; ab < (A + 15) / 16; ab += v.ks) {
-                const int a = 16 * ab + 2 * t;
-                const uint32_t a0 = pair(awg, a), a2 = pair(awg, a + 8);
-                const uint32_t a1 = pair(awg8, a), a3 = pair(awg8, a + 8);
-                uint2 xb[NT];
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) xb[nt] = __ldg(reinterpret_cast<const uint2*>(xa + ab * MM * 16 + tok[nt]));
-                mma_xg<NT, MT>(acc, a0, a1, a2, a3, xb);
-            }
-        }
+    // write this warp's sums of row block `q` to its slot; the warp completing the block adds the
+    // slots in warp order and writes y
+    auto flush = [&](const Pos& q, int units) {
+        const FDesc& D = P.d[q.p];
+        const int64_t blk = q.l * D.rblocks + q.rb;
+        const int64_t first_u = D.unit_begin + blk * q.su;
+        // this warp's slot: its place among the warps that share the block
+        const int64_t w0 = first_u >= u_begin ? wid : owner_warp(first_u, W, P.total_units);
+        float* slots = D.part + blk * D.cmax * M * 16;
+        float* mine = slots + (int)(wid - w0) * M * 16;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-            const int m0 = 8 * nt + 2 * t, m1 = m0 + 1;
-            if (m0 < M) {
-                red[warp][g][m0] = acc[nt][0];
-                red[warp][g + 8][m0] = acc[nt][2];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int m = 8 * nt + 2 * t + (e & 1), r = g + (e >> 1) * 8;
+                if (m < M) __stcg(mine + m * 16 + r, acc[nt][e]);
+                acc[nt][e] = 0.f;
             }
-            if (m1 < M) {
-                red[warp][g][m1] = acc[nt][1];
-                red[warp][g + 8][m1] = acc[nt][3];
-            }
-            acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
         }
-        __syncthreads();
-        void* y = static_cast<char*>(D.y) + v.l * D.stride_y;
-        const int ks = v.ks;
-        for (int idx = threadIdx.x; idx < v.rtiles * 16 * M; idx += kThreadsS) {
-            const int rtile = idx / (16 * M), rem = idx - rtile * 16 * M;
-            const int m = rem / 16, r = rem - m * 16;
-            const int n = (v.tile * v.rtiles + rtile) * 16 + r;
-            if (n >= N) continue;
-            float sum = 0.f;
-            for (int sl = 0; sl < ks; ++sl) sum += red[rtile * ks + sl][r][m];
-            store_out(y, (size_t)m * N + n, P.y_dtype, sum);
+        __syncwarp();
+        unsigned last = 0;
+        if (lane == 0) {
+            __threadfence();
+            const unsigned old = atomicAdd(D.cnt + blk, (unsigned)units);
+            last = old + (unsigned)units == (unsigned)q.su;
         }
-        __syncthreads();
-        T += gridDim.x;
-        CV = view_tile(P, T, warp);
-        cstep = 0;
-    };
-    auto step_done = [&]() {
-        if (++cstep == CV.steps) finish_tile();
+        if (__shfl_sync(0xffffffffu, last, 0)) {
+            __threadfence();
+            const int nc = (int)(owner_warp(first_u + q.su - 1, W, P.total_units) - w0 + 1);
+            finish_block(slots, nc, M, static_cast<char*>(D.y) + q.l * D.stride_y, D.N, q.rb * 16, P.y_dtype, lane);
+        }
     };
 
-    Loader<FMT, MT> L;
-    L.open(P, blockIdx.x, warp, g, t);
-    // the x slice of a step (source `src`) goes to ring slot `slot`, one commit group per step
-    auto issue_x = [&](int slot, const uint16_t* src, bool valid) {
-        if (valid) {
-            uint16_t* dst = xw + slot * 256 * MM + lane * 8;
+    Pos q = locate(P, u_begin);
+    int64_t u = u_begin;
+    bool waited = false;   // x is read only after the pre-pass has finished
+    while (u < u_end) {
+        const FDesc& D = P.d[q.p];
+        const int64_t left = u_end - u;
+        const int n = left < (int64_t)(q.su - q.s) ? (int)left : q.su - q.s;
+        const int s_end = q.s + n, code_end = min(s_end, q.steps);
+        const int N = D.N, K = D.K;
+        const int rg = q.rb * 16 + g, rg8 = rg + 8;
+        const int64_t r0 = rg < N ? rg : N - 1, r1 = rg8 < N ? rg8 : N - 1;   // rows past N: never stored
+        const uint16_t* xb0 = D.xperm + q.l * D.xperm_stride + xlane;
+        if (FMT == LQ_FMT_2BIT_LM_G32) {
+            if (q.s < code_end) {
+                const uint8_t* cb = D.codes + q.l * D.stride_codes + 16 * t;
+                const uint8_t* c0p = cb + r0 * (K / 4);
+                const uint8_t* c1p = cb + r1 * (K / 4);
+                const uint16_t* s16 = reinterpret_cast<const uint16_t*>(static_cast<const char*>(D.scales) + q.l * D.stride_scales) + 2 * t;
+                const uint16_t* o16 = reinterpret_cast<const uint16_t*>(reinterpret_cast<const char*>(D.offsets) + q.l * D.stride_offsets) + 2 * t;
+                const uint16_t *s0p = s16 + r0 * (K / 32), *s1p = s16 + r1 * (K / 32);
+                const uint16_t *z0p = o16 + r0 * (K / 32), *z1p = o16 + r1 * (K / 32);
+                auto load = [&](Step2& f, int s) {
+                    f.c0 = ldg128(c0p + 64 * s);
+                    f.c1 = ldg128(c1p + 64 * s);
+                    f.s0 = ldg32(s0p + 8 * s);
+                    f.z0 = ldg32(z0p + 8 * s);
+                    f.s1 = ldg32(s1p + 8 * s);
+                    f.z1 = ldg32(z1p + 8 * s);
+                };
+                auto compute = [&](const Step2& f, int s) {
+                    const uint16_t* xs = xb0 + (int64_t)s * 256 * M;
+                    uint32_t RA[4], RB[4];
+                    lut2_bits((uint16_t)f.s0, (uint16_t)f.z0, RA[0], RB[0]);
+                    lut2_bits((uint16_t)(f.s0 >> 16), (uint16_t)(f.z0 >> 16), RA[1], RB[1]);
+                    lut2_bits((uint16_t)f.s1, (uint16_t)f.z1, RA[2], RB[2]);
+                    lut2_bits((uint16_t)(f.s1 >> 16), (uint16_t)(f.z1 >> 16), RA[3], RB[3]);
+                    const uint32_t w0[4] = {f.c0.x, f.c0.y, f.c0.z, f.c0.w};
+                    const uint32_t w1[4] = {f.c1.x, f.c1.y, f.c1.z, f.c1.w};
 #pragma unroll
-            for (int c = 0; c < MM; ++c) cp_async16(dst + c * 256, src + c * 256);
+                    for (int ii = 0; ii < 4; ++ii) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            uint32_t a0, a1, a2, a3;
+                            expand2_fast(w0[ii], j, RA[ii >> 1], RB[ii >> 1], a0, a2);
+                            expand2_fast(w1[ii], j, RA[2 + (ii >> 1)], RB[2 + (ii >> 1)], a1, a3);
+                            uint2 xb[NT];
+#pragma unroll
+                            for (int nt = 0; nt < NT; ++nt)
+                                xb[nt] = __ldg(reinterpret_cast<const uint2*>(xs + (ii * 4 + j) * M * 16 + tok[nt]));
+                            mma_xg<NT, MT>(acc, a0, a1, a2, a3, xb);
+                        }
+                    }
+                };
+                int s = q.s;
+                Step2 fa, fb;
+                load(fa, s);
+                if (!waited) {
+                    pdl_wait();
+                    waited = true;
+                }
+                for (;;) {
+                    if (s + 1 < code_end) load(fb, s + 1);
+                    compute(fa, s);
+                    if (++s >= code_end) break;
+                    if (s + 1 < code_end) load(fa, s + 1);
+                    compute(fb, s);
+                    if (++s >= code_end) break;
+                }
+            }
+            const int anchor_begin = q.s > q.steps ? q.s : q.steps;   // this segment's first anchor unit
+            if (anchor_begin < s_end) {
+                // anchor units: binary16 anchor weights (zero past A) against x at the anchor columns
+                if (!waited) {
+                    pdl_wait();
+                    waited = true;
+                }
+                const int A = D.A;
+                const uint16_t* aw = reinterpret_cast<const uint16_t*>(reinterpret_cast<const char*>(D.anchor_w) + q.l * D.stride_anchor_w);
+                const uint16_t* awg = aw + r0 * D.ld_anchor;
+                const uint16_t* awg8 = aw + r1 * D.ld_anchor;
+                const uint16_t* xab = D.xaperm + q.l * D.xaperm_stride + xlane;
+                auto pair = [&](const uint16_t* row, int a) -> uint32_t {
+                    if (a >= A) return 0u;
+                    const uint32_t w = ldg32(row + a);
+                    return (a + 1 < A) ? w : (w & 0xFFFFu);
+                };
+                auto load = [&](Step2& f, int s) {
+                    const int a = (s - q.steps) * kAnchorCols + 2 * t;
+                    f.c0 = make_uint4(pair(awg, a), pair(awg8, a), pair(awg, a + 8), pair(awg8, a + 8));
+                    f.c1 = make_uint4(pair(awg, a + 16), pair(awg8, a + 16), pair(awg, a + 24), pair(awg8, a + 24));
+                    f.s0 = pair(awg, a + 32);
+                    f.z0 = pair(awg8, a + 32);
+                    f.s1 = pair(awg, a + 40);
+                    f.z1 = pair(awg8, a + 40);
+                };
+                auto compute = [&](const Step2& f, int s) {
+                    const uint16_t* xs = xab + (int64_t)(s - q.steps) * kAnchorCols * M;
+                    uint2 xb[3][NT];
+#pragma unroll
+                    for (int kb = 0; kb < 3; ++kb)
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) xb[kb][nt] = __ldg(reinterpret_cast<const uint2*>(xs + kb * M * 16 + tok[nt]));
+                    mma_xg<NT, MT>(acc, f.c0.x, f.c0.y, f.c0.z, f.c0.w, xb[0]);
+                    mma_xg<NT, MT>(acc, f.c1.x, f.c1.y, f.c1.z, f.c1.w, xb[1]);
+                    mma_xg<NT, MT>(acc, f.s0, f.z0, f.s1, f.z1, xb[2]);
+                };
+                int s = anchor_begin;
+                Step2 fa, fb;
+                load(fa, s);
+                for (;;) {
+                    if (s + 1 < s_end) load(fb, s + 1);
+                    compute(fa, s);
+                    if (++s >= s_end) break;
+                    if (s + 1 < s_end) load(fa, s + 1);
+                    compute(fb, s);
+                    if (++s >= s_end) break;
+                }
+            }
+        } else {
+            const uint8_t* cb = D.codes + q.l * D.stride_codes + 8 * t;
+            const uint8_t* c0p = cb + r0 * (K / 2);
+            const uint8_t* c1p = cb + r1 * (K / 2);
+            const float* am = reinterpret_cast<const float*>(static_cast<const char*>(D.scales) + q.l * D.stride_scales);
+            const float *a0p = am + r0 * (K / 64), *a1p = am + r1 * (K / 64);
+            uint32_t TL[4], TH[4];
+            nf4_tables(TL, TH);
+            auto load = [&](StepNF4& f, int s) {
+#pragma unroll
+                for (int nb = 0; nb < 4; ++nb) {
+                    f.c0[nb] = ldg64(c0p + 128 * s + 32 * nb);
+                    f.c1[nb] = ldg64(c1p + 128 * s + 32 * nb);
+                    f.a0[nb] = __ldg(a0p + 4 * s + nb);
+                    f.a1[nb] = __ldg(a1p + 4 * s + nb);
+                }
+            };
+            auto compute = [&](const StepNF4& f, int s) {
+                const uint16_t* xs = xb0 + (int64_t)s * 256 * M;
+#pragma unroll
+                for (int nb = 0; nb < 4; ++nb) {
+                    uint2 xb[4][NT];
+#pragma unroll
+                    for (int b = 0; b < 4; ++b)
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) xb[b][nt] = __ldg(reinterpret_cast<const uint2*>(xs + (nb * 4 + b) * M * 16 + tok[nt]));
+                    float part[NT][4];
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) part[nt][0] = part[nt][1] = part[nt][2] = part[nt][3] = 0.f;
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) {
+                        uint32_t a0, a1, a2, a3;
+                        expand_nf4_fast(b < 2 ? f.c0[nb].x : f.c0[nb].y, b & 1, TL, TH, a0, a2);
+                        expand_nf4_fast(b < 2 ? f.c1[nb].x : f.c1[nb].y, b & 1, TL, TH, a1, a3);
+                        mma_xg<NT, MT>(part, a0, a1, a2, a3, xb[b]);
+                    }
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        acc[nt][0] = __fmaf_rn(f.a0[nb], part[nt][0], acc[nt][0]);
+                        acc[nt][1] = __fmaf_rn(f.a0[nb], part[nt][1], acc[nt][1]);
+                        acc[nt][2] = __fmaf_rn(f.a1[nb], part[nt][2], acc[nt][2]);
+                        acc[nt][3] = __fmaf_rn(f.a1[nb], part[nt][3], acc[nt][3]);
+                    }
+                }
+            };
+            int s = q.s;
+            StepNF4 fa, fb;
+            load(fa, s);
+            if (!waited) {
+                pdl_wait();
+                waited = true;
+            }
+            for (;;) {
+                if (s + 1 < s_end) load(fb, s + 1);
+                compute(fa, s);
+                if (++s >= s_end) break;
+                if (s + 1 < s_end) load(fa, s + 1);
+                compute(fb, s);
+                if (++s >= s_end) break;
+            }
         }
-        cp_async_commit();
-    };
-
-    if (FMT == LQ_FMT_2BIT_LM_G32) {
-        auto issue_w = [&](Step2& f) {
-            if (!L.valid) return;
-            f.c0 = ldg128(L.cg);
-            f.c1 = ldg128(L.cg8);
-            f.s0 = ldg32(L.sg);
-            f.z0 = ldg32(L.zg);
-            f.s1 = ldg32(L.sg8);
-            f.z1 = ldg32(L.zg8);
-            L.advance(P, warp, g, t);
-        };
-        auto issue = [&](Step2& f, int slot) {
-            issue_x(slot, L.xsrc, L.valid);
-            issue_w(f);
-        };
-        auto compute = [&](const Step2& f, int slot) {
-            cp_async_wait<2>();   // this step's x slice has landed (the two later ones may be in flight)
-            __syncwarp();
-            const uint16_t* xs = xw + slot * 256 * MM + xlane;
-            uint32_t RA[4], RB[4];
-            lut2_bits((uint16_t)f.s0, (uint16_t)f.z0, RA[0], RB[0]);
-            lut2_bits((uint16_t)(f.s0 >> 16), (uint16_t)(f.z0 >> 16), RA[1], RB[1]);
-            lut2_bits((uint16_t)f.s1, (uint16_t)f.z1, RA[2], RB[2]);
-            lut2_bits((uint16_t)(f.s1 >> 16), (uint16_t)(f.z1 >> 16), RA[3], RB[3]);
-            const uint32_t w0[4] = {f.c0.x, f.c0.y, f.c0.z, f.c0.w};
-            const uint32_t w1[4] = {f.c1.x, f.c1.y, f.c1.z, f.c1.w};
-#pragma unroll
-            for (int ii = 0; ii < 4; ++ii) {
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    uint32_t a0, a1, a2, a3;
-                    expand2_fast(w0[ii], j, RA[ii >> 1], RB[ii >> 1], a0, a2);
-                    expand2_fast(w1[ii], j, RA[2 + (ii >> 1)], RB[2 + (ii >> 1)], a1, a3);
-                    uint2 xb[NT];
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt)
-                        xb[nt] = *reinterpret_cast<const uint2*>(xs + (ii * 4 + j) * MM * 16 + tok[nt]);
-                    mma_xg<NT, MT>(acc, a0, a1, a2, a3, xb);
-                }
-            }
-            __syncwarp();   // every lane has read this slot before it is refilled
-            step_done();
-        };
-        // three register buffers (and x slots), two steps in flight across tile boundaries,
-        // unrolled so the buffers never move
-        Step2 fa, fb, fc;
-        // weights of the first two steps before waiting for the x pre-pass, then their x slices
-        const uint16_t* xs0 = L.xsrc;
-        const bool v0 = L.valid;
-        issue_w(fa);
-        const uint16_t* xs1 = L.xsrc;
-        const bool v1 = L.valid;
-        issue_w(fb);
-        pdl_wait();
-        issue_x(0, xs0, v0);
-        issue_x(1, xs1, v1);
-        for (;;) {
-            if (!CV.valid) break;
-            issue(fc, 2);
-            compute(fa, 0);
-            if (!CV.valid) break;
-            issue(fa, 0);
-            compute(fb, 1);
-            if (!CV.valid) break;
-            issue(fb, 1);
-            compute(fc, 2);
-        }
-    } else {
-        uint32_t TL[4], TH[4];
-        nf4_tables(TL, TH);
-        auto issue_w = [&](StepNF4& f) {
-            if (!L.valid) return;
-            const float* ag = reinterpret_cast<const float*>(L.sg);
-            const float* ag8 = reinterpret_cast<const float*>(L.sg8);
-#pragma unroll
-            for (int nb = 0; nb < 4; ++nb) {
-                f.c0[nb] = ldg64(L.cg + 32 * nb);
-                f.c1[nb] = ldg64(L.cg8 + 32 * nb);
-                f.a0[nb] = __ldg(ag + nb);
-                f.a1[nb] = __ldg(ag8 + nb);
-            }
-            L.advance(P, warp, g, t);
-        };
-        auto issue = [&](StepNF4& f, int slot) {
-            issue_x(slot, L.xsrc, L.valid);
-            issue_w(f);
-        };
-        auto compute = [&](const StepNF4& f, int slot) {
-            cp_async_wait<1>();
-            __syncwarp();
-            const uint16_t* xs = xw + slot * 256 * MM + xlane;
-#pragma unroll
-            for (int nb = 0; nb < 4; ++nb) {
-                uint2 xb[4][NT];
-#pragma unroll
-                for (int b = 0; b < 4; ++b)
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) xb[b][nt] = *reinterpret_cast<const uint2*>(xs + (nb * 4 + b) * MM * 16 + tok[nt]);
-                float part[NT][4];
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) part[nt][0] = part[nt][1] = part[nt][2] = part[nt][3] = 0.f;
-#pragma unroll
-                for (int b = 0; b < 4; ++b) {
-                    uint32_t a0, a1, a2, a3;
-                    expand_nf4_fast(b < 2 ? f.c0[nb].x : f.c0[nb].y, b & 1, TL, TH, a0, a2);
-                    expand_nf4_fast(b < 2 ? f.c1[nb].x : f.c1[nb].y, b & 1, TL, TH, a1, a3);
-                    mma_xg<NT, MT>(part, a0, a1, a2, a3, xb[b]);
-                }
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    acc[nt][0] = __fmaf_rn(f.a0[nb], part[nt][0], acc[nt][0]);
-                    acc[nt][1] = __fmaf_rn(f.a0[nb], part[nt][1], acc[nt][1]);
-                    acc[nt][2] = __fmaf_rn(f.a1[nb], part[nt][2], acc[nt][2]);
-                    acc[nt][3] = __fmaf_rn(f.a1[nb], part[nt][3], acc[nt][3]);
-                }
-            }
-            __syncwarp();
-            step_done();
-        };
-        StepNF4 fa, fb;
-        const uint16_t* xs0 = L.xsrc;
-        const bool v0 = L.valid;
-        issue_w(fa);
-        pdl_wait();
-        issue_x(0, xs0, v0);
-        for (;;) {
-            if (!CV.valid) break;
-            issue(fb, 1);
-            compute(fa, 0);
-            if (!CV.valid) break;
-            issue(fa, 0);
-            compute(fb, 1);
+        flush(q, n);
+        u += n;
+        if (u < u_end) {
+            q.s = 0;
+            next_block(P, q);
         }
     }
 }
 
 template <int FMT, int MT, int NT>
-lq_status launch_s(const SParams& P, int64_t tiles, int num_sms, cudaStream_t stream) {
-    const size_t smem = (size_t)kWarps * 3 * 256 * P.M * sizeof(uint16_t);   // x rings
-    static int per_sm = 0;   // resident CTAs per SM for this instantiation (same smem for a given M)
-    static size_t per_sm_smem = 0;
-    if (per_sm == 0 || per_sm_smem != smem) {
-        // static reduction buffer + dynamic x rings may pass the 48 KiB default: always opt in
+size_t ring_smem(int) { return 0; }
+
+// Resident CTAs per SM of one instantiation (queried once; the x-ring size is fixed by M).
+template <int FMT, int MT, int NT>
+int resident_ctas(int M) {
+    static int per_sm = 0;
+    if (per_sm == 0) {
+        const size_t smem = ring_smem<FMT, MT, NT>(M);
         if (cudaFuncSetAttribute(gemv_stream_kernel<FMT, MT, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-            return LQ_ERR_CUDA;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_stream_kernel<FMT, MT, NT>, kThreadsS, smem) != cudaSuccess)
-            return LQ_ERR_CUDA;
-        per_sm_smem = smem;
+            return -1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gemv_stream_kernel<FMT, MT, NT>, kThreadsS, smem) != cudaSuccess)
+            return -1;
+        per_sm = std::max(1, n);
     }
-    const int64_t grid = std::min<int64_t>(tiles, (int64_t)num_sms * std::max(1, per_sm));
+    return per_sm;
+}
+
+template <int FMT, int MT, int NT>
+lq_status launch_s(const FParams& P, int64_t grid, cudaStream_t stream) {
+    const size_t smem = ring_smem<FMT, MT, NT>(P.M);
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof(cfg));
     cfg.gridDim = dim3((unsigned)grid);
@@ -522,33 +559,50 @@ lq_status launch_s(const SParams& P, int64_t tiles, int num_sms, cudaStream_t st
 }
 
 template <int FMT>
-lq_status launch_s_fmt(const SParams& P, int64_t tiles, int num_sms, cudaStream_t stream) {
+lq_status launch_s_fmt(const FParams& P, int64_t grid, cudaStream_t stream) {
     switch (P.M) {
-        case 1: return launch_s<FMT, 1, 1>(P, tiles, num_sms, stream);
-        case 2: return launch_s<FMT, 2, 1>(P, tiles, num_sms, stream);
-        case 3: return launch_s<FMT, 3, 1>(P, tiles, num_sms, stream);
-        case 4: return launch_s<FMT, 4, 1>(P, tiles, num_sms, stream);
-        case 5: return launch_s<FMT, 5, 1>(P, tiles, num_sms, stream);
-        case 6: return launch_s<FMT, 6, 1>(P, tiles, num_sms, stream);
-        case 7: return launch_s<FMT, 7, 1>(P, tiles, num_sms, stream);
-        case 8: return launch_s<FMT, 8, 1>(P, tiles, num_sms, stream);
+        case 1: return launch_s<FMT, 1, 1>(P, grid, stream);
+        case 2: return launch_s<FMT, 2, 1>(P, grid, stream);
+        case 3: return launch_s<FMT, 3, 1>(P, grid, stream);
+        case 4: return launch_s<FMT, 4, 1>(P, grid, stream);
+        case 5: return launch_s<FMT, 5, 1>(P, grid, stream);
+        case 6: return launch_s<FMT, 6, 1>(P, grid, stream);
+        case 7: return launch_s<FMT, 7, 1>(P, grid, stream);
+        case 8: return launch_s<FMT, 8, 1>(P, grid, stream);
         default: return LQ_ERR_UNSUPPORTED;   // more than 8 tokens: the split-K kernel
+    }
+}
+
+template <int FMT>
+int resident_fmt(int M) {
+    switch (M) {
+        case 1: return resident_ctas<FMT, 1, 1>(M);
+        case 2: return resident_ctas<FMT, 2, 1>(M);
+        case 3: return resident_ctas<FMT, 3, 1>(M);
+        case 4: return resident_ctas<FMT, 4, 1>(M);
+        case 5: return resident_ctas<FMT, 5, 1>(M);
+        case 6: return resident_ctas<FMT, 6, 1>(M);
+        case 7: return resident_ctas<FMT, 7, 1>(M);
+        case 8: return resident_ctas<FMT, 8, 1>(M);
+        default: return -1;
     }
 }
 
 int round_up(int a, int b) { return (a + b - 1) / b * b; }
 
+size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
+
 }  // namespace
 
 bool gemv_stream_eligible(const lq_problem* probs, int count) {
-    if (probs[0].M > 8) return false;   // the x rings (3 steps x M tokens per warp) must stay small
+    if (probs[0].M > 8) return false;   // the x rings (3 units x M tokens per warp) must stay small
     for (int i = 0; i < count; ++i)
         if (probs[i].K % 256 != 0) return false;
     return true;
 }
 
 lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* probs, int count, cudaStream_t stream) {
-    SParams P;
+    FParams P;
     PrepParams Q;
     memset(&P, 0, sizeof(P));
     memset(&Q, 0, sizeof(Q));
@@ -560,15 +614,12 @@ lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* probs, i
     Q.format = fmt;
     Q.x_bf16 = probs[0].x_dtype == LQ_BF16;
 
-    int64_t blocks = 0, prep = 0, xhalves = 0;
-    int max_k = 0;
-    // minimum K steps per warp (LQ_GEMV_STEPS_PER_WARP overrides, for tuning experiments)
-    int spw = 8;
-    if (const char* e = getenv("LQ_GEMV_STEPS_PER_WARP")) spw = std::max(1, atoi(e));
+    int64_t units = 0, jobs = 0;
+    size_t ws_bytes = 0;
     for (int i = 0; i < count; ++i) {
         const lq_problem& q = probs[i];
         const int A = fmt == LQ_FMT_2BIT_LM_G32 ? q.A : 0;
-        SDesc& d = P.d[i];
+        FDesc& d = P.d[i];
         PrepDesc& e = Q.d[i];
         d.codes = q.codes;
         d.scales = q.scales;
@@ -585,18 +636,15 @@ lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* probs, i
         d.A = A;
         d.ld_anchor = q.ld_anchor;
         d.batch = q.batch;
-        // warps per row tile (K slices): as many as keep >= spw steps of 256 columns per warp
-        const int steps = q.K / 256;
-        d.ks = 8;
-        while (d.ks > 1 && steps < spw * d.ks) d.ks /= 2;
-        const int rows_per_cta = 16 * (kWarps / d.ks);
-        d.tiles = (q.N + rows_per_cta - 1) / rows_per_cta;
-        d.tile_begin = blocks;
-        blocks += (int64_t)q.batch * d.tiles;
-        const int a_pad = A > 0 ? round_up(A, 64) : 0;
+        const int a_pad = A > 0 ? round_up(A, kAnchorCols) : 0;
+        d.steps = q.K / 256;
+        d.su = d.steps + a_pad / kAnchorCols;
+        d.rblocks = (q.N + 15) / 16;
+        d.unit_begin = units;
+        units += (int64_t)q.batch * d.rblocks * d.su;
         d.xperm_stride = (int64_t)M * q.K;
         d.xaperm_stride = (int64_t)M * a_pad;
-        xhalves += (int64_t)q.batch * (d.xperm_stride + d.xaperm_stride) + 2 * 128;
+        ws_bytes += align256((size_t)q.batch * d.xperm_stride * 2) + align256((size_t)q.batch * d.xaperm_stride * 2);
         e.x = static_cast<const uint16_t*>(q.x);
         e.stride_x = q.stride_x;
         e.anchor_idx = A > 0 ? q.anchor_idx : nullptr;
@@ -607,35 +655,55 @@ lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* probs, i
         e.batch = q.batch;
         e.xperm_stride = d.xperm_stride;
         e.xaperm_stride = d.xaperm_stride;
-        const int64_t items = ((int64_t)M * q.K + (int64_t)M * a_pad) / 8;
-        e.ctas = (int)((items + kPrepItems - 1) / kPrepItems);
-        e.cta_begin = prep;
-        prep += (int64_t)q.batch * e.ctas;
-        max_k = std::max(max_k, q.K);
+        e.jobs = q.K / 256 + (a_pad + 255) / 256;
+        e.job_begin = jobs;
+        jobs += (int64_t)q.batch * e.jobs;
     }
-    if (blocks > 0x7fffffffLL) return LQ_ERR_UNSUPPORTED;
-    if ((size_t)((xhalves + 1) / 2 + 64) > ws.partial_floats) return LQ_ERR_WORKSPACE;
-    uint16_t* xp = reinterpret_cast<uint16_t*>((reinterpret_cast<uintptr_t>(ws.partials) + 255) & ~uintptr_t(255));
+    if (units == 0) return LQ_OK;
+    // the warp partition fixes how many warps can meet in one row block
+    const int per_sm = fmt == LQ_FMT_2BIT_LM_G32 ? resident_fmt<LQ_FMT_2BIT_LM_G32>(M) : resident_fmt<LQ_FMT_NF4_B64>(M);
+    if (per_sm < 0) return LQ_ERR_CUDA;
+    const int64_t want = (units + kWarps - 1) / kWarps;   // no more warps than units
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)ws.num_sms * per_sm));
+    // at most one warp per unit, so every warp of the partition owns at least one unit and the
+    // warps meeting in a row block are exactly those from its first unit's owner to its last's
+    const int64_t W = std::min<int64_t>(grid * kWarps, units);
+    const int64_t min_run = units / W;   // every warp's run has at least this many units (>= 1)
     for (int i = 0; i < count; ++i) {
-        P.d[i].xperm = Q.d[i].xperm = xp;
-        xp += (int64_t)probs[i].batch * P.d[i].xperm_stride;
-        xp = reinterpret_cast<uint16_t*>((reinterpret_cast<uintptr_t>(xp) + 255) & ~uintptr_t(255));
-        P.d[i].xaperm = Q.d[i].xaperm = xp;
-        xp += (int64_t)probs[i].batch * P.d[i].xaperm_stride;
-        xp = reinterpret_cast<uint16_t*>((reinterpret_cast<uintptr_t>(xp) + 255) & ~uintptr_t(255));
+        FDesc& d = P.d[i];
+        d.cmax = (int)std::min<int64_t>(d.su / min_run + 2, d.su);
+        ws_bytes += align256((size_t)probs[i].batch * d.rblocks * d.cmax * M * 16 * 4) +
+                    align256((size_t)probs[i].batch * d.rblocks * 4);
     }
-    Q.total_ctas = prep;
-    if (blocks == 0) return LQ_OK;
+    if (ws_bytes + 256 > ws.partial_floats * sizeof(float)) return LQ_ERR_WORKSPACE;
+    // workspace: per problem x (permuted), x at the anchors, partial-sum slots, arrival counts
+    char* wp = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(ws.partials) + 255) & ~uintptr_t(255));
+    int nz = 0;
+    for (int i = 0; i < count; ++i) {
+        FDesc& d = P.d[i];
+        const lq_problem& q = probs[i];
+        d.xperm = Q.d[i].xperm = reinterpret_cast<uint16_t*>(wp);
+        wp += align256((size_t)q.batch * d.xperm_stride * 2);
+        d.xaperm = Q.d[i].xaperm = reinterpret_cast<uint16_t*>(wp);
+        wp += align256((size_t)q.batch * d.xaperm_stride * 2);
+        d.part = reinterpret_cast<float*>(wp);
+        wp += align256((size_t)q.batch * d.rblocks * d.cmax * M * 16 * 4);
+        d.cnt = reinterpret_cast<unsigned*>(wp);
+        wp += align256((size_t)q.batch * d.rblocks * 4);
+        Q.z[nz++] = ZeroTask{d.cnt, (int64_t)q.batch * d.rblocks, 0, 1};
+    }
+    Q.zero_tasks = nz;
+    Q.total_jobs = jobs;
+    P.total_units = units;
+    P.total_warps = W;
 
-    // x pre-pass, then the main kernel, chained by programmatic dependent launch
-    if (Q.total_ctas > 0x7fffffffLL) return LQ_ERR_UNSUPPORTED;
-    const size_t prep_smem = sizeof(uint32_t) * (size_t)std::max(1, max_k / 32);
-    if (prep_smem > 48 * 1024) return LQ_ERR_UNSUPPORTED;
-    xprep_kernel<<<(unsigned)Q.total_ctas, 256, prep_smem, stream>>>(Q);
+    // x pre-pass (and zeroing), then the main kernel, chained by programmatic dependent launch
+    const int64_t prep_ctas = (jobs + kPrepWarps - 1) / kPrepWarps;
+    if (prep_ctas > 0x7fffffffLL) return LQ_ERR_UNSUPPORTED;
+    xprep_kernel<<<(unsigned)prep_ctas, 32 * kPrepWarps, 0, stream>>>(Q);
     if (cudaPeekAtLastError() != cudaSuccess) return LQ_ERR_CUDA;
-    P.total_tiles = blocks;
-    if (fmt == LQ_FMT_2BIT_LM_G32) return launch_s_fmt<LQ_FMT_2BIT_LM_G32>(P, blocks, ws.num_sms, stream);
-    return launch_s_fmt<LQ_FMT_NF4_B64>(P, blocks, ws.num_sms, stream);
+    if (fmt == LQ_FMT_2BIT_LM_G32) return launch_s_fmt<LQ_FMT_2BIT_LM_G32>(P, grid, stream);
+    return launch_s_fmt<LQ_FMT_NF4_B64>(P, grid, stream);
 }
 
 }  // namespace lq
