@@ -192,10 +192,12 @@ struct FDesc {
     int steps, su, rblocks;     // code units per row block; units per row block (code + anchor)
     int cmax;                   // most warps that can share one row block
     int64_t unit_begin;         // first unit of this problem in the launch
+    int64_t xoff;               // first half of this problem's x copies in the x buffer
 };
 
 struct FParams {
     FDesc d[kMaxGroup];
+    const uint16_t* xbuf;       // all x copies: per problem, per member [x in fragment order | x at the anchors]
     int count, M, y_dtype;
     int64_t total_units, total_warps;
 };
@@ -283,12 +285,30 @@ struct StepNF4 {
 // pointers only move), then the anchor units; the row block's sums leave through
 // flush() at the segment's end.  x fragments are read straight from the permuted copy
 // (L1-resident: every warp of an SM streams the same few tens of KiB).
-template <int FMT, int MT, int NT>
+template <int FMT, int MT, int NT, bool STAGED>
 __global__ void __launch_bounds__(kThreadsS, LQ_STREAM_MIN_BLOCKS) gemv_stream_kernel(const __grid_constant__ FParams P) {
+    // STAGED: the x span this CTA's units read is copied to shared memory once
+    extern __shared__ __align__(16) uint16_t xsm[];
     constexpr int M = MT;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
     const int64_t W = P.total_warps;
     const int wid = blockIdx.x * kWarps + warp;
+    int64_t span0 = 0;
+    if (STAGED) {
+        const int64_t w_lo = (int64_t)blockIdx.x * kWarps, w_hi = (w_lo + kWarps < W) ? w_lo + kWarps : W;
+        if (w_lo >= W) return;   // the whole CTA is idle
+        const int64_t uc0 = P.total_units * w_lo / W, uc1 = P.total_units * w_hi / W;
+        const Pos a = locate(P, uc0), b = locate(P, uc1 - 1);
+        const FDesc& Da = P.d[a.p];
+        const FDesc& Db = P.d[b.p];
+        span0 = Da.xoff + a.l * Da.xperm_stride;
+        const int64_t span1 = Db.xoff + (b.l + 1) * Db.xperm_stride;
+        pdl_wait();
+        const uint4* src = reinterpret_cast<const uint4*>(P.xbuf + span0);
+        uint4* dst = reinterpret_cast<uint4*>(xsm);
+        for (int64_t i = threadIdx.x; i < (span1 - span0) / 8; i += kThreadsS) dst[i] = __ldg(src + i);
+        __syncthreads();
+    }
     if (wid >= W) return;
     const int64_t u_begin = P.total_units * wid / W, u_end = P.total_units * (wid + 1) / W;
     const int xlane = min(g, M - 1) * 16 + t * 4;            // this lane's fragment inside a block
@@ -344,7 +364,7 @@ __global__ void __launch_bounds__(kThreadsS, LQ_STREAM_MIN_BLOCKS) gemv_stream_k
         const int N = D.N, K = D.K;
         const int rg = q.rb * 16 + g, rg8 = rg + 8;
         const int64_t r0 = rg < N ? rg : N - 1, r1 = rg8 < N ? rg8 : N - 1;   // rows past N: never stored
-        const uint16_t* xb0 = D.xperm + q.l * D.xperm_stride + xlane;
+        const uint16_t* xb0 = (STAGED ? xsm + (D.xoff + q.l * D.xperm_stride - span0) : D.xperm + q.l * D.xperm_stride) + xlane;
         if (FMT == LQ_FMT_2BIT_LM_G32) {
             if (q.s < code_end) {
                 const uint8_t* cb = D.codes + q.l * D.stride_codes + 16 * t;
@@ -381,31 +401,36 @@ __global__ void __launch_bounds__(kThreadsS, LQ_STREAM_MIN_BLOCKS) gemv_stream_k
                             uint2 xb[NT];
 #pragma unroll
                             for (int nt = 0; nt < NT; ++nt)
-                                xb[nt] = __ldg(reinterpret_cast<const uint2*>(xs + (ii * 4 + j) * M * 16 + tok[nt]));
+                                xb[nt] = *reinterpret_cast<const uint2*>(xs + (ii * 4 + j) * M * 16 + tok[nt]);
                             mma_xg<NT, MT>(acc, a0, a1, a2, a3, xb);
                         }
                     }
                 };
+                // three buffers: two units of loads in flight
                 int s = q.s;
-                Step2 fa, fb;
+                Step2 fa, fb, fc;
                 load(fa, s);
-                if (!waited) {
+                if (s + 1 < code_end) load(fb, s + 1);
+                if (!STAGED && !waited) {
                     pdl_wait();
                     waited = true;
                 }
                 for (;;) {
-                    if (s + 1 < code_end) load(fb, s + 1);
+                    if (s + 2 < code_end) load(fc, s + 2);
                     compute(fa, s);
                     if (++s >= code_end) break;
-                    if (s + 1 < code_end) load(fa, s + 1);
+                    if (s + 2 < code_end) load(fa, s + 2);
                     compute(fb, s);
+                    if (++s >= code_end) break;
+                    if (s + 2 < code_end) load(fb, s + 2);
+                    compute(fc, s);
                     if (++s >= code_end) break;
                 }
             }
             const int anchor_begin = q.s > q.steps ? q.s : q.steps;   // this segment's first anchor unit
             if (anchor_begin < s_end) {
                 // anchor units: binary16 anchor weights (zero past A) against x at the anchor columns
-                if (!waited) {
+                if (!STAGED && !waited) {
                     pdl_wait();
                     waited = true;
                 }
@@ -413,7 +438,8 @@ __global__ void __launch_bounds__(kThreadsS, LQ_STREAM_MIN_BLOCKS) gemv_stream_k
                 const uint16_t* aw = reinterpret_cast<const uint16_t*>(reinterpret_cast<const char*>(D.anchor_w) + q.l * D.stride_anchor_w);
                 const uint16_t* awg = aw + r0 * D.ld_anchor;
                 const uint16_t* awg8 = aw + r1 * D.ld_anchor;
-                const uint16_t* xab = D.xaperm + q.l * D.xaperm_stride + xlane;
+                const uint16_t* xab = (STAGED ? xsm + (D.xoff + q.l * D.xperm_stride - span0) + (int64_t)M * K
+                                              : D.xaperm + q.l * D.xaperm_stride) + xlane;
                 auto pair = [&](const uint16_t* row, int a) -> uint32_t {
                     if (a >= A) return 0u;
                     const uint32_t w = ldg32(row + a);
@@ -434,7 +460,7 @@ __global__ void __launch_bounds__(kThreadsS, LQ_STREAM_MIN_BLOCKS) gemv_stream_k
 #pragma unroll
                     for (int kb = 0; kb < 3; ++kb)
 #pragma unroll
-                        for (int nt = 0; nt < NT; ++nt) xb[kb][nt] = __ldg(reinterpret_cast<const uint2*>(xs + kb * M * 16 + tok[nt]));
+                        for (int nt = 0; nt < NT; ++nt) xb[kb][nt] = *reinterpret_cast<const uint2*>(xs + kb * M * 16 + tok[nt]);
                     mma_xg<NT, MT>(acc, f.c0.x, f.c0.y, f.c0.z, f.c0.w, xb[0]);
                     mma_xg<NT, MT>(acc, f.c1.x, f.c1.y, f.c1.z, f.c1.w, xb[1]);
                     mma_xg<NT, MT>(acc, f.s0, f.z0, f.s1, f.z1, xb[2]);
@@ -476,7 +502,7 @@ __global__ void __launch_bounds__(kThreadsS, LQ_STREAM_MIN_BLOCKS) gemv_stream_k
 #pragma unroll
                     for (int b = 0; b < 4; ++b)
 #pragma unroll
-                        for (int nt = 0; nt < NT; ++nt) xb[b][nt] = __ldg(reinterpret_cast<const uint2*>(xs + (nb * 4 + b) * M * 16 + tok[nt]));
+                        for (int nt = 0; nt < NT; ++nt) xb[b][nt] = *reinterpret_cast<const uint2*>(xs + (nb * 4 + b) * M * 16 + tok[nt]);
                     float part[NT][4];
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) part[nt][0] = part[nt][1] = part[nt][2] = part[nt][3] = 0.f;
@@ -499,7 +525,7 @@ __global__ void __launch_bounds__(kThreadsS, LQ_STREAM_MIN_BLOCKS) gemv_stream_k
             int s = q.s;
             StepNF4 fa, fb;
             load(fa, s);
-            if (!waited) {
+            if (!STAGED && !waited) {
                 pdl_wait();
                 waited = true;
             }
@@ -521,28 +547,25 @@ __global__ void __launch_bounds__(kThreadsS, LQ_STREAM_MIN_BLOCKS) gemv_stream_k
     }
 }
 
-template <int FMT, int MT, int NT>
-size_t ring_smem(int) { return 0; }
-
-// Resident CTAs per SM of one instantiation (queried once; the x-ring size is fixed by M).
-template <int FMT, int MT, int NT>
-int resident_ctas(int M) {
+// Resident CTAs per SM of one instantiation at a given dynamic shared-memory size.
+template <int FMT, int MT, int NT, bool STAGED>
+int resident_ctas(size_t smem) {
+    static size_t set_smem = (size_t)-1;
     static int per_sm = 0;
-    if (per_sm == 0) {
-        const size_t smem = ring_smem<FMT, MT, NT>(M);
-        if (cudaFuncSetAttribute(gemv_stream_kernel<FMT, MT, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    if (set_smem != smem) {
+        if (cudaFuncSetAttribute(gemv_stream_kernel<FMT, MT, NT, STAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
             return -1;
         int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gemv_stream_kernel<FMT, MT, NT>, kThreadsS, smem) != cudaSuccess)
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gemv_stream_kernel<FMT, MT, NT, STAGED>, kThreadsS, smem) != cudaSuccess)
             return -1;
-        per_sm = std::max(1, n);
+        per_sm = n;
+        set_smem = smem;
     }
     return per_sm;
 }
 
-template <int FMT, int MT, int NT>
-lq_status launch_s(const FParams& P, int64_t grid, cudaStream_t stream) {
-    const size_t smem = ring_smem<FMT, MT, NT>(P.M);
+template <int FMT, int MT, int NT, bool STAGED>
+lq_status launch_one(const FParams& P, int64_t grid, size_t smem, cudaStream_t stream) {
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof(cfg));
     cfg.gridDim = dim3((unsigned)grid);
@@ -554,38 +577,47 @@ lq_status launch_s(const FParams& P, int64_t grid, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, gemv_stream_kernel<FMT, MT, NT>, P) != cudaSuccess) return LQ_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, gemv_stream_kernel<FMT, MT, NT, STAGED>, P) != cudaSuccess) return LQ_ERR_CUDA;
     return cudaPeekAtLastError() == cudaSuccess ? LQ_OK : LQ_ERR_CUDA;
 }
 
+// mode 0: occupancy query (returns CTAs per SM through *per_sm); mode 1: launch
+template <int FMT, int MT, int NT>
+lq_status dispatch_mt(int mode, bool staged, const FParams& P, int64_t grid, size_t smem, int* per_sm, cudaStream_t stream) {
+    if (mode == 0) {
+        *per_sm = staged ? resident_ctas<FMT, MT, NT, true>(smem) : resident_ctas<FMT, MT, NT, false>(smem);
+        return *per_sm < 0 ? LQ_ERR_CUDA : LQ_OK;
+    }
+    return staged ? launch_one<FMT, MT, NT, true>(P, grid, smem, stream) : launch_one<FMT, MT, NT, false>(P, grid, smem, stream);
+}
+
 template <int FMT>
-lq_status launch_s_fmt(const FParams& P, int64_t grid, cudaStream_t stream) {
+lq_status dispatch_fmt(int mode, bool staged, const FParams& P, int64_t grid, size_t smem, int* per_sm, cudaStream_t stream) {
     switch (P.M) {
-        case 1: return launch_s<FMT, 1, 1>(P, grid, stream);
-        case 2: return launch_s<FMT, 2, 1>(P, grid, stream);
-        case 3: return launch_s<FMT, 3, 1>(P, grid, stream);
-        case 4: return launch_s<FMT, 4, 1>(P, grid, stream);
-        case 5: return launch_s<FMT, 5, 1>(P, grid, stream);
-        case 6: return launch_s<FMT, 6, 1>(P, grid, stream);
-        case 7: return launch_s<FMT, 7, 1>(P, grid, stream);
-        case 8: return launch_s<FMT, 8, 1>(P, grid, stream);
+        case 1: return dispatch_mt<FMT, 1, 1>(mode, staged, P, grid, smem, per_sm, stream);
+        case 2: return dispatch_mt<FMT, 2, 1>(mode, staged, P, grid, smem, per_sm, stream);
+        case 3: return dispatch_mt<FMT, 3, 1>(mode, staged, P, grid, smem, per_sm, stream);
+        case 4: return dispatch_mt<FMT, 4, 1>(mode, staged, P, grid, smem, per_sm, stream);
+        case 5: return dispatch_mt<FMT, 5, 1>(mode, staged, P, grid, smem, per_sm, stream);
+        case 6: return dispatch_mt<FMT, 6, 1>(mode, staged, P, grid, smem, per_sm, stream);
+        case 7: return dispatch_mt<FMT, 7, 1>(mode, staged, P, grid, smem, per_sm, stream);
+        case 8: return dispatch_mt<FMT, 8, 1>(mode, staged, P, grid, smem, per_sm, stream);
         default: return LQ_ERR_UNSUPPORTED;   // more than 8 tokens: the split-K kernel
     }
 }
 
-template <int FMT>
-int resident_fmt(int M) {
-    switch (M) {
-        case 1: return resident_ctas<FMT, 1, 1>(M);
-        case 2: return resident_ctas<FMT, 2, 1>(M);
-        case 3: return resident_ctas<FMT, 3, 1>(M);
-        case 4: return resident_ctas<FMT, 4, 1>(M);
-        case 5: return resident_ctas<FMT, 5, 1>(M);
-        case 6: return resident_ctas<FMT, 6, 1>(M);
-        case 7: return resident_ctas<FMT, 7, 1>(M);
-        case 8: return resident_ctas<FMT, 8, 1>(M);
-        default: return -1;
-    }
+lq_status dispatch(int fmt, int mode, bool staged, const FParams& P, int64_t grid, size_t smem, int* per_sm,
+                   cudaStream_t stream) {
+    return fmt == LQ_FMT_2BIT_LM_G32 ? dispatch_fmt<LQ_FMT_2BIT_LM_G32>(mode, staged, P, grid, smem, per_sm, stream)
+                                     : dispatch_fmt<LQ_FMT_NF4_B64>(mode, staged, P, grid, smem, per_sm, stream);
+}
+
+// Host copy of the kernel's unit lookup (problem and member of unit u).
+void host_locate(const FParams& P, int64_t u, int& p, int64_t& l) {
+    p = 0;
+    while (p + 1 < P.count && u >= P.d[p + 1].unit_begin) ++p;
+    const FDesc& D = P.d[p];
+    l = (u - D.unit_begin) / ((int64_t)D.rblocks * D.su);
 }
 
 int round_up(int a, int b) { return (a + b - 1) / b * b; }
@@ -614,7 +646,7 @@ lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* probs, i
     Q.format = fmt;
     Q.x_bf16 = probs[0].x_dtype == LQ_BF16;
 
-    int64_t units = 0, jobs = 0;
+    int64_t units = 0, jobs = 0, xhalves = 0;
     size_t ws_bytes = 0;
     for (int i = 0; i < count; ++i) {
         const lq_problem& q = probs[i];
@@ -642,9 +674,10 @@ lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* probs, i
         d.rblocks = (q.N + 15) / 16;
         d.unit_begin = units;
         units += (int64_t)q.batch * d.rblocks * d.su;
-        d.xperm_stride = (int64_t)M * q.K;
-        d.xaperm_stride = (int64_t)M * a_pad;
-        ws_bytes += align256((size_t)q.batch * d.xperm_stride * 2) + align256((size_t)q.batch * d.xaperm_stride * 2);
+        // per member: [x in fragment order (M*K) | x at the anchors (M*a_pad)]
+        d.xperm_stride = d.xaperm_stride = (int64_t)M * (q.K + a_pad);
+        d.xoff = xhalves;
+        xhalves += (int64_t)q.batch * d.xperm_stride;
         e.x = static_cast<const uint16_t*>(q.x);
         e.stride_x = q.stride_x;
         e.anchor_idx = A > 0 ? q.anchor_idx : nullptr;
@@ -660,14 +693,34 @@ lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* probs, i
         jobs += (int64_t)q.batch * e.jobs;
     }
     if (units == 0) return LQ_OK;
-    // the warp partition fixes how many warps can meet in one row block
-    const int per_sm = fmt == LQ_FMT_2BIT_LM_G32 ? resident_fmt<LQ_FMT_2BIT_LM_G32>(M) : resident_fmt<LQ_FMT_NF4_B64>(M);
-    if (per_sm < 0) return LQ_ERR_CUDA;
-    const int64_t want = (units + kWarps - 1) / kWarps;   // no more warps than units
-    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)ws.num_sms * per_sm));
-    // at most one warp per unit, so every warp of the partition owns at least one unit and the
-    // warps meeting in a row block are exactly those from its first unit's owner to its last's
-    const int64_t W = std::min<int64_t>(grid * kWarps, units);
+    ws_bytes += align256((size_t)xhalves * 2);
+    // first without staging, to size the grid; the warp partition then fixes the x span of each CTA
+    int per_sm = 0;
+    if (dispatch(fmt, 0, false, P, 0, 0, &per_sm, stream) != LQ_OK) return LQ_ERR_CUDA;
+    int64_t grid = std::max<int64_t>(1, std::min<int64_t>((units + kWarps - 1) / kWarps, (int64_t)ws.num_sms * std::max(1, per_sm)));
+    int64_t W = std::min<int64_t>(grid * kWarps, units);
+    P.total_units = units;
+    P.total_warps = W;
+    int64_t max_span = 0;
+    for (int64_t b = 0; b < grid; ++b) {
+        const int64_t w_lo = b * kWarps, w_hi = std::min<int64_t>(w_lo + kWarps, W);
+        if (w_lo >= W) break;
+        int pa, pb;
+        int64_t la, lb;
+        host_locate(P, units * w_lo / W, pa, la);
+        host_locate(P, units * w_hi / W - 1, pb, lb);
+        max_span = std::max<int64_t>(max_span, P.d[pb].xoff + (lb + 1) * P.d[pb].xperm_stride - (P.d[pa].xoff + la * P.d[pa].xperm_stride));
+    }
+    // stage x in shared memory when the widest span fits beside a second resident CTA
+    // (off unless LQ_GEMV_STAGE=1: on this part the L1-resident reads measured ~1% faster)
+    const size_t smem = (size_t)max_span * 2;
+    const char* st_env = getenv("LQ_GEMV_STAGE");
+    bool staged = smem <= (size_t)std::min(ws.max_smem_optin, 110 * 1024) && st_env && atoi(st_env) == 1;
+    if (staged) {
+        int per_sm_s = 0;
+        if (dispatch(fmt, 0, true, P, 0, smem, &per_sm_s, stream) != LQ_OK) return LQ_ERR_CUDA;
+        staged = per_sm_s >= per_sm;   // staging must not cost occupancy
+    }
     const int64_t min_run = units / W;   // every warp's run has at least this many units (>= 1)
     for (int i = 0; i < count; ++i) {
         FDesc& d = P.d[i];
@@ -676,16 +729,17 @@ lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* probs, i
                     align256((size_t)probs[i].batch * d.rblocks * 4);
     }
     if (ws_bytes + 256 > ws.partial_floats * sizeof(float)) return LQ_ERR_WORKSPACE;
-    // workspace: per problem x (permuted), x at the anchors, partial-sum slots, arrival counts
+    // workspace: all x copies, then per problem partial-sum slots and arrival counts
     char* wp = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(ws.partials) + 255) & ~uintptr_t(255));
+    uint16_t* xbuf = reinterpret_cast<uint16_t*>(wp);
+    wp += align256((size_t)xhalves * 2);
+    P.xbuf = xbuf;
     int nz = 0;
     for (int i = 0; i < count; ++i) {
         FDesc& d = P.d[i];
         const lq_problem& q = probs[i];
-        d.xperm = Q.d[i].xperm = reinterpret_cast<uint16_t*>(wp);
-        wp += align256((size_t)q.batch * d.xperm_stride * 2);
-        d.xaperm = Q.d[i].xaperm = reinterpret_cast<uint16_t*>(wp);
-        wp += align256((size_t)q.batch * d.xaperm_stride * 2);
+        d.xperm = Q.d[i].xperm = xbuf + d.xoff;
+        d.xaperm = Q.d[i].xaperm = xbuf + d.xoff + (int64_t)M * q.K;
         d.part = reinterpret_cast<float*>(wp);
         wp += align256((size_t)q.batch * d.rblocks * d.cmax * M * 16 * 4);
         d.cnt = reinterpret_cast<unsigned*>(wp);
@@ -694,16 +748,14 @@ lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* probs, i
     }
     Q.zero_tasks = nz;
     Q.total_jobs = jobs;
-    P.total_units = units;
-    P.total_warps = W;
 
     // x pre-pass (and zeroing), then the main kernel, chained by programmatic dependent launch
     const int64_t prep_ctas = (jobs + kPrepWarps - 1) / kPrepWarps;
     if (prep_ctas > 0x7fffffffLL) return LQ_ERR_UNSUPPORTED;
     xprep_kernel<<<(unsigned)prep_ctas, 32 * kPrepWarps, 0, stream>>>(Q);
     if (cudaPeekAtLastError() != cudaSuccess) return LQ_ERR_CUDA;
-    if (fmt == LQ_FMT_2BIT_LM_G32) return launch_s_fmt<LQ_FMT_2BIT_LM_G32>(P, grid, stream);
-    return launch_s_fmt<LQ_FMT_NF4_B64>(P, grid, stream);
+    int unused = 0;
+    return dispatch(fmt, 1, staged, P, grid, staged ? smem : 0, &unused, stream);
 }
 
 }  // namespace lq
