@@ -177,6 +177,39 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+CFG1_SETS = 32768   # distinct 512x256 weight sets of the single-linear config (1.9 GB, far beyond L2)
+
+
+def config1_batched(lq, torch, h, device: str, steps: int, warmup: int):
+    """The 512x256 single linear (2-bit, A = 8) over CFG1_SETS distinct weight sets in one launch."""
+    L, N, K, A = CFG1_SETS, 512, 256, 8
+    big = synth.random_packed_2bit_sets(L, N, K, A, seed=1, cfg=1)
+    w = lq.QuantWeights.from_host(big, lq.FMT_2BIT, device=device)
+    del big
+    x = torch.from_numpy(synth.activations(L, K, "f16", seed=1, cfg=1)).view(torch.float16).to(device).view(L, 1, K)
+    y = torch.empty((L, 1, N), dtype=torch.float32, device=device)
+    ld = 8
+    strides = dict(codes=N * K // 4, scales=N * K // 32 * 2, offsets=N * K // 32 * 2, anchor_idx=4 * A,
+                   anchor_w=N * ld * 2, x=K * 2, y=N * 4)
+    prob = [h.problem(w, x[0], y[0], batch=L, strides=strides)]
+    per_set = N * K // 4 + 2 * 2 * N * (K // 32) + 2 * N * A + 4 * A + 2 * K + 4 * N
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        h.gemv_grouped(prob, stream=stream)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        h.gemv_grouped(prob, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    return {"workload": f"512x256 single linear, 2-bit G=32 + 8 fp16 anchors, M=1, {L} distinct weight sets in one launch",
+            "value": round(L * per_set / (ms * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_launch": round(ms, 4),
+            "bytes_per_launch": L * per_set}
+
+
 GEMM_M = 2048
 GEMM_WORKLOAD = "14b decoder layer prefill, M=2048 bf16 tokens, 7 projections, one lq_gemm call each"
 
@@ -341,6 +374,9 @@ def run_lq(args):
     e2e_ms = e0.elapsed_time(e1) / args.steps
     e2e_val = world * layer_bytes / (e2e_ms * 1e-3) / 1e9
 
+    cfg1 = config1_batched(lq, torch, h, f"cuda:{local}", 20, 3)
+    cfg1["frac_of_hbm"] = round(cfg1["value"] / hbm, 4)
+
     gemm = None
     if not args.no_gemm:
         dev = f"cuda:{local}"
@@ -379,6 +415,7 @@ def run_lq(args):
             "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": 2 * args.steps,   # x pre-pass + streaming GEMV per grouped call
             "clocks": clk.summary(),
+            "config1_batched": cfg1,
             "gemm": gemm,
         }
         print(json.dumps(line), flush=True)

@@ -285,11 +285,12 @@ struct StepNF4 {
 // pointers only move), then the anchor units; the row block's sums leave through
 // flush() at the segment's end.  x fragments are read straight from the permuted copy
 // (L1-resident: every warp of an SM streams the same few tens of KiB).
+// (more than two n-tiles of accumulators need the register file of a whole SM per CTA)
 template <int FMT, int MT, int NT, bool STAGED>
-__global__ void __launch_bounds__(kThreadsS, LQ_STREAM_MIN_BLOCKS) gemv_stream_kernel(const __grid_constant__ FParams P) {
+__global__ void __launch_bounds__(kThreadsS, NT <= 2 ? LQ_STREAM_MIN_BLOCKS : 1) gemv_stream_kernel(const __grid_constant__ FParams P) {
     // STAGED: the x span this CTA's units read is copied to shared memory once
     extern __shared__ __align__(16) uint16_t xsm[];
-    constexpr int M = MT;
+    const int M = MT > 0 ? MT : P.M;   // MT 0: token count at run time (9..32 tokens, NT n-tiles of 8)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
     const int64_t W = P.total_warps;
     const int wid = blockIdx.x * kWarps + warp;
@@ -324,6 +325,21 @@ __global__ void __launch_bounds__(kThreadsS, LQ_STREAM_MIN_BLOCKS) gemv_stream_k
     // slots in warp order and writes y
     auto flush = [&](const Pos& q, int units) {
         const FDesc& D = P.d[q.p];
+        if (units == q.su) {
+            // the whole row block is this warp's: y straight from the accumulators
+            void* y = static_cast<char*>(D.y) + q.l * D.stride_y;
+            const int rg = q.rb * 16 + g;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int m = 8 * nt + 2 * t + (e & 1), row = rg + (e >> 1) * 8;
+                    if (m < M && row < D.N) store_out(y, (size_t)m * D.N + row, P.y_dtype, acc[nt][e]);
+                    acc[nt][e] = 0.f;
+                }
+            }
+            return;
+        }
         const int64_t blk = q.l * D.rblocks + q.rb;
         const int64_t first_u = D.unit_begin + blk * q.su;
         // this warp's slot: its place among the warps that share the block
@@ -602,7 +618,11 @@ lq_status dispatch_fmt(int mode, bool staged, const FParams& P, int64_t grid, si
         case 6: return dispatch_mt<FMT, 6, 1>(mode, staged, P, grid, smem, per_sm, stream);
         case 7: return dispatch_mt<FMT, 7, 1>(mode, staged, P, grid, smem, per_sm, stream);
         case 8: return dispatch_mt<FMT, 8, 1>(mode, staged, P, grid, smem, per_sm, stream);
-        default: return LQ_ERR_UNSUPPORTED;   // more than 8 tokens: the split-K kernel
+        default:
+            if (P.M <= 16) return dispatch_mt<FMT, 0, 2>(mode, staged, P, grid, smem, per_sm, stream);
+            if (P.M <= 24) return dispatch_mt<FMT, 0, 3>(mode, staged, P, grid, smem, per_sm, stream);
+            if (P.M <= 32) return dispatch_mt<FMT, 0, 4>(mode, staged, P, grid, smem, per_sm, stream);
+            return LQ_ERR_UNSUPPORTED;
     }
 }
 
@@ -627,7 +647,7 @@ size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
 }  // namespace
 
 bool gemv_stream_eligible(const lq_problem* probs, int count) {
-    if (probs[0].M > 8) return false;   // the x rings (3 units x M tokens per warp) must stay small
+    if (probs[0].M > 32) return false;
     for (int i = 0; i < count; ++i)
         if (probs[i].K % 256 != 0) return false;
     return true;

@@ -20,7 +20,7 @@ import numpy as np
 __all__ = [
     "rng", "weights", "outlier_channels", "channel_sigma", "activations",
     "f32_to_f16_bits", "f32_to_bf16_bits", "bits_to_f32",
-    "random_packed_2bit", "random_packed_nf4", "LAYER_SHAPES",
+    "random_packed_2bit", "random_packed_nf4", "random_packed_2bit_sets", "LAYER_SHAPES",
 ]
 
 # (name, N_out, K_in) per decoder layer, the shapes of the workload table.
@@ -135,3 +135,28 @@ def random_packed_nf4(N: int, K: int, sigma: float = 0.02, seed: int = 0, cfg: i
     codes = g.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
     absmax = (sigma * g.uniform(2.0, 4.0, size=(N, K // 64))).astype(np.float32)
     return dict(codes=codes, absmax=absmax, N=N, K=K)
+
+
+def random_packed_2bit_sets(L: int, N: int, K: int, A: int, sigma: float = 0.02, seed: int = 0, cfg: int = 0) -> dict:
+    """L independent weight sets of one shape in the 2-bit storage layout, stacked on a
+    leading axis (codes [L][N][K/4], scales/offsets [L][N][K/32], anchor_idx [L][A],
+    anchor_w [L][N][ld_anchor]); random draws of the right sizes and magnitudes."""
+    g = rng(seed, cfg, 50_000)
+    ld = max(8, (A + 7) // 8 * 8)
+    # codes: a random block of up to 1024 sets, tiled with a distinct XOR byte per tile (every set
+    # differs; drawing the full size byte by byte takes tens of seconds)
+    T = min(L, 1024)
+    base = g.integers(0, 2**32, size=T * N * (K // 4) // 4, dtype=np.uint32).view(np.uint8).reshape(T, N, K // 4)
+    codes = np.empty((L, N, K // 4), dtype=np.uint8)
+    for i in range(0, L, T):
+        n = min(T, L - i)
+        np.bitwise_xor(base[:n], np.uint8(((i // T) * 0x9D) & 0xFF), out=codes[i:i + n])
+    scales = f32_to_f16_bits(sigma * (np.float32(0.8) + np.float32(0.4) * g.random((L, N, K // 32), dtype=np.float32)))
+    offsets = f32_to_f16_bits(np.float32(sigma / np.sqrt(32.0)) * g.standard_normal((L, N, K // 32), dtype=np.float32))
+    # A distinct sorted columns per set: the A smallest of K random keys
+    keys = g.random((L, K), dtype=np.float32)
+    anchor_idx = np.sort(np.argpartition(keys, A, axis=1)[:, :A], axis=1).astype(np.int32)
+    anchor_w = np.zeros((L, N, ld), dtype=np.uint16)
+    anchor_w[:, :, :A] = f32_to_f16_bits(np.float32(sigma) * g.standard_normal((L, N, A), dtype=np.float32))
+    return dict(codes=codes, scales=scales, offsets=offsets, anchor_idx=anchor_idx, anchor_w=anchor_w,
+                A=A, ld_anchor=ld, N=N, K=K, L=L)

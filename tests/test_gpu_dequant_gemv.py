@@ -220,6 +220,27 @@ def test_gemv_batched_distinct_weight_sets(lqm, handle):
         assert_within(y[l].cpu().numpy(), yref, E, GEMV_TOL, f"batch member {l}")
 
 
+def test_gemv_config1_batched_full_size_sampled(lqm, handle):
+    """The 512x256 single linear as the bench runs it: 32768 distinct weight sets in one launch."""
+    L, N, K, A = 32768, 512, 256, 8
+    big = synth.random_packed_2bit_sets(L, N, K, A, seed=11, cfg=1)
+    w = lqm.QuantWeights.from_host(big, lqm.FMT_2BIT)
+    xb = synth.activations(L, K, "f16", seed=11, cfg=1)
+    x = dev_x(xb.reshape(L, 1, K), "f16")
+    y = torch.empty((L, 1, N), dtype=torch.float32, device="cuda")
+    strides = dict(codes=N * K // 4, scales=N * K // 32 * 2, offsets=N * K // 32 * 2, anchor_idx=4 * A,
+                   anchor_w=N * big["ld_anchor"] * 2, x=K * 2, y=N * 4)
+    handle.gemv_grouped([handle.problem(w, x[0], y[0], batch=L, strides=strides)])
+    yc = y.cpu().numpy()
+    g = np.random.default_rng(3)
+    for l in sorted(set(g.choice(L, 6, replace=False).tolist()) | {0, L - 1}):
+        one = {k: (v[l] if isinstance(v, np.ndarray) else v) for k, v in big.items()}
+        xl = xb[l:l + 1]
+        yref = O.gemv_2bit_rows(one, xl, "f16", 0, N)
+        E = O.row_error_scale(O.dequant_2bit(one), xl, "f16")
+        assert_within(yc[l], yref, E, GEMV_TOL, f"set {l}")
+
+
 # ---------------------------------------------------------------- full workload sizes, sampled rows
 
 def _sampled_rows(N, k=24, seed=0):
@@ -237,7 +258,7 @@ def _check_sampled_2bit(packed, xbits, xdt, y, rows, tol=GEMV_TOL, what=""):
         assert_within(y[:, n:n + 1], yr, E, tol, f"{what} row {n}")
 
 
-@pytest.mark.parametrize("layer,M", [("7b", 1), ("70b", 8)])
+@pytest.mark.parametrize("layer,M", [("7b", 1), ("70b", 8), ("70b", 32)])
 def test_gemv_full_layer_sampled(lqm, handle, layer, M):
     """The bench's launch: one grouped call over a whole decoder layer at full size."""
     sigma = 0.02 if layer == "7b" else 0.015
