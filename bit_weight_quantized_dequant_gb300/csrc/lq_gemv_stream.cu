@@ -64,17 +64,9 @@ struct PrepDesc {
     int64_t job_begin;         // first job of this problem
 };
 
-// A region the pre-pass clears: `batch` runs of `words` 4-byte words, `stride` words apart.
-struct ZeroTask {
-    uint32_t* p;
-    int64_t words, stride;
-    int batch;
-};
-
 struct PrepParams {
     PrepDesc d[kMaxGroup];
-    ZeroTask z[2 * kMaxGroup];
-    int count, M, x_bf16, format, zero_tasks;
+    int count, M, x_bf16, format;
     int64_t total_jobs;
 };
 
@@ -88,15 +80,6 @@ __global__ void __launch_bounds__(32 * kPrepWarps) xprep_kernel(const __grid_con
     __shared__ uint32_t step_bits[kPrepWarps][8];
     pdl_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // the arrival counts and sums the main kernel adds into
-    for (int zt = 0; zt < P.zero_tasks; ++zt) {
-        const ZeroTask& Z = P.z[zt];
-        const int64_t total = Z.words * Z.batch;
-        for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
-            const int64_t b = i / Z.words;
-            Z.p[b * Z.stride + (i - b * Z.words)] = 0u;
-        }
-    }
     const int64_t job = (int64_t)blockIdx.x * kPrepWarps + warp;
     if (job >= P.total_jobs) return;
     int p = 0;
@@ -111,8 +94,32 @@ __global__ void __launch_bounds__(32 * kPrepWarps) xprep_kernel(const __grid_con
                                 : nullptr;
     const int steps = K / 256;
     if (jb < steps) {
-        // anchor columns of this step, as 8 words of bits
         const int k0 = jb * 256;
+        uint16_t* dst = D.xperm + l * D.xperm_stride + (int64_t)k0 * M;
+        // column of element e of item `it` inside this step (fragment order)
+        auto col = [&](int it, int e) {
+            const int d0 = 8 * it, line = d0 >> 4, pos = (d0 & 15) + e;
+            const int bl = line / M, tt = pos >> 2, hh = pos & 3;   // mma block inside the step
+            return P.format == LQ_FMT_2BIT_LM_G32 ? tt * 64 + ((bl >> 2) & 3) * 16 + hh * 4 + (bl & 3)
+                                                   : (bl >> 2) * 64 + tt * 16 + (bl & 3) * 4 + hh;
+        };
+        auto tok = [&](int it) { const int line = (8 * it) >> 4; return line - (line / M) * M; };
+        // x loads of the first items go out before the anchor bitmap is built: no dependence
+        constexpr int C = 4;   // items per lane held in registers at a time
+        uint16_t v[C][8];
+        auto load = [&](int it0) {
+#pragma unroll
+            for (int c = 0; c < C; ++c) {
+                const int it = it0 + 32 * c + lane;
+                if (it < 32 * M) {
+                    const int m = tok(it);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) v[c][e] = x[(int64_t)m * K + k0 + col(it, e)];
+                }
+            }
+        };
+        load(0);
+        // anchor columns of this step, as 8 words of bits
         if (lane < 8) step_bits[warp][lane] = 0u;
         __syncwarp();
         for (int a0 = 0; a0 < A; a0 += 8 * 32) {
@@ -127,21 +134,26 @@ __global__ void __launch_bounds__(32 * kPrepWarps) xprep_kernel(const __grid_con
                 if (kk[j] >= 0 && kk[j] < 256) atomicOr(&step_bits[warp][kk[j] >> 5], 1u << (kk[j] & 31));
         }
         __syncwarp();
-        uint16_t* dst = D.xperm + l * D.xperm_stride + (int64_t)k0 * M;
-        for (int it = lane; it < 32 * M; it += 32) {
-            const int d0 = 8 * it, line = d0 >> 4, pos0 = d0 & 15;
-            const int bl = line / M, m = line - bl * M;   // mma block inside the step, token
-            uint16_t v[8];
+        for (int it0 = 0; it0 < 32 * M; it0 += 32 * C) {
+            if (it0 > 0) load(it0);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int pos = pos0 + e, tt = pos >> 2, hh = pos & 3;
-                const int kl = P.format == LQ_FMT_2BIT_LM_G32 ? tt * 64 + ((bl >> 2) & 3) * 16 + hh * 4 + (bl & 3)
-                                                               : (bl >> 2) * 64 + tt * 16 + (bl & 3) * 4 + hh;
-                const bool anchor = (step_bits[warp][kl >> 5] >> (kl & 31)) & 1u;
-                v[e] = anchor ? (uint16_t)0 : to_half_bits(x[(int64_t)m * K + k0 + kl], P.x_bf16);
+            for (int c = 0; c < C; ++c) {
+                const int it = it0 + 32 * c + lane;
+                if (it >= 32 * M) continue;
+                uint32_t w[4];
+#pragma unroll
+                for (int e2 = 0; e2 < 4; ++e2) {
+                    uint32_t pr = 0;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int e = 2 * e2 + h, kl = col(it, e);
+                        const bool anchor = (step_bits[warp][kl >> 5] >> (kl & 31)) & 1u;
+                        pr |= (uint32_t)(anchor ? (uint16_t)0 : to_half_bits(v[c][e], P.x_bf16)) << (16 * h);
+                    }
+                    w[e2] = pr;
+                }
+                *reinterpret_cast<uint4*>(dst + 8 * it) = make_uint4(w[0], w[1], w[2], w[3]);
             }
-            *reinterpret_cast<uint4*>(dst + d0) = make_uint4((uint32_t)v[0] | ((uint32_t)v[1] << 16), (uint32_t)v[2] | ((uint32_t)v[3] << 16),
-                                                            (uint32_t)v[4] | ((uint32_t)v[5] << 16), (uint32_t)v[6] | ((uint32_t)v[7] << 16));
         }
     } else {
         // x gathered at anchor slots [256 * j, 256 * j + 256) (zero past A)
@@ -193,12 +205,17 @@ struct FDesc {
     int cmax;                   // most warps that can share one row block
     int64_t unit_begin;         // first unit of this problem in the launch
     int64_t xoff;               // first half of this problem's x copies in the x buffer
+    const uint16_t* x;          // the caller's x [batch][M][K] (16-bit) and anchor columns, for
+    int64_t stride_x;           //   the in-kernel build of the fragment-ordered copy (bytes)
+    const int32_t* anchor_idx;
+    int64_t stride_anchor_idx;  // bytes
 };
 
 struct FParams {
     FDesc d[kMaxGroup];
     const uint16_t* xbuf;       // all x copies: per problem, per member [x in fragment order | x at the anchors]
-    int count, M, y_dtype;
+    int count, M, y_dtype, x_bf16, format;
+    int bitmap_words;           // STAGED: shared-memory words of the anchor bitmap (max K / 32)
     int64_t total_units, total_warps;
 };
 
@@ -280,6 +297,46 @@ struct StepNF4 {
     float a0[4], a1[4];
 };
 
+// The fragment-ordered copy of one member's x (anchor columns zeroed) and x gathered at
+// its anchor columns, written by the whole CTA into shared memory at `dst` (the same
+// layout the pre-pass writes to global memory).  `bits` is K/32 words of scratch.
+__device__ __forceinline__ void build_member_x(const FParams& P, const FDesc& D, int64_t l, uint16_t* dst, uint32_t* bits) {
+    const int M = P.M, K = D.K, A = D.A, a_pad = (int)(D.xperm_stride / M) - K;
+    const uint16_t* x = reinterpret_cast<const uint16_t*>(reinterpret_cast<const char*>(D.x) + l * D.stride_x);
+    const int32_t* aidx = A > 0 ? reinterpret_cast<const int32_t*>(reinterpret_cast<const char*>(D.anchor_idx) + l * D.stride_anchor_idx)
+                                : nullptr;
+    for (int i = threadIdx.x; i < K / 32; i += blockDim.x) bits[i] = 0u;
+    __syncthreads();
+    for (int a = threadIdx.x; a < A; a += blockDim.x) {
+        const int k = __ldg(aidx + a);
+        atomicOr(&bits[k >> 5], 1u << (k & 31));
+    }
+    __syncthreads();
+    const int items = M * K / 8, aitems = M * a_pad / 8;
+    for (int it = threadIdx.x; it < items + aitems; it += blockDim.x) {
+        const bool code = it < items;
+        const int d0 = 8 * (code ? it : it - items), line = d0 >> 4, pos0 = d0 & 15;
+        const int bi = line / M, m = line - bi * M;   // mma block, token
+        uint16_t v[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int pos = pos0 + e, tt = pos >> 2, hh = pos & 3;
+            if (code) {
+                const int k = P.format == LQ_FMT_2BIT_LM_G32 ? (bi >> 4) * 256 + tt * 64 + ((bi >> 2) & 3) * 16 + hh * 4 + (bi & 3)
+                                                             : (bi >> 2) * 64 + tt * 16 + (bi & 3) * 4 + hh;
+                v[e] = ((bits[k >> 5] >> (k & 31)) & 1u) ? (uint16_t)0 : to_half_bits(x[(int64_t)m * K + k], P.x_bf16);
+            } else {
+                const int a = 16 * bi + 2 * tt + (hh & 1) + 8 * (hh >> 1);
+                v[e] = a < A ? to_half_bits(x[(int64_t)m * K + __ldg(aidx + a)], P.x_bf16) : (uint16_t)0;
+            }
+        }
+        *reinterpret_cast<uint4*>(dst + (code ? 0 : (int64_t)M * K) + d0) =
+            make_uint4((uint32_t)v[0] | ((uint32_t)v[1] << 16), (uint32_t)v[2] | ((uint32_t)v[3] << 16),
+                       (uint32_t)v[4] | ((uint32_t)v[5] << 16), (uint32_t)v[6] | ((uint32_t)v[7] << 16));
+    }
+    __syncthreads();   // the bitmap is reused by the next member
+}
+
 // A warp walks its range as segments: the units of its range inside one row block.
 // Inside a segment the code units run in a tight loop (one unit of loads in flight,
 // pointers only move), then the anchor units; the row block's sums leave through
@@ -304,11 +361,14 @@ __global__ void __launch_bounds__(kThreadsS, NT <= 2 ? LQ_STREAM_MIN_BLOCKS : 1)
         const FDesc& Db = P.d[b.p];
         span0 = Da.xoff + a.l * Da.xperm_stride;
         const int64_t span1 = Db.xoff + (b.l + 1) * Db.xperm_stride;
-        pdl_wait();
-        const uint4* src = reinterpret_cast<const uint4*>(P.xbuf + span0);
-        uint4* dst = reinterpret_cast<uint4*>(xsm);
-        for (int64_t i = threadIdx.x; i < (span1 - span0) / 8; i += kThreadsS) dst[i] = __ldg(src + i);
-        __syncthreads();
+        uint32_t* bits = reinterpret_cast<uint32_t*>(xsm + (span1 - span0));
+        pdl_wait();   // x may come from the kernel before; the workspace is free once it is done
+        for (int p = a.p; p <= b.p; ++p) {
+            const FDesc& D = P.d[p];
+            const int64_t l0 = p == a.p ? a.l : 0, l1 = p == b.p ? b.l : D.batch - 1;
+            for (int64_t l = l0; l <= l1; ++l) build_member_x(P, D, l, xsm + (D.xoff + l * D.xperm_stride - span0), bits);
+        }
+        (void)Db;
     }
     if (wid >= W) return;
     const int64_t u_begin = P.total_units * wid / W, u_end = P.total_units * (wid + 1) / W;
@@ -364,6 +424,7 @@ __global__ void __launch_bounds__(kThreadsS, NT <= 2 ? LQ_STREAM_MIN_BLOCKS : 1)
         }
         if (__shfl_sync(0xffffffffu, last, 0)) {
             __threadfence();
+            if (lane == 0) D.cnt[blk] = 0u;   // counts start at zero for the next launch
             const int nc = (int)(owner_warp(first_u + q.su - 1, W, P.total_units) - w0 + 1);
             finish_block(slots, nc, M, static_cast<char*>(D.y) + q.l * D.stride_y, D.N, q.rb * 16, P.y_dtype, lane);
         }
@@ -663,11 +724,11 @@ lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* probs, i
     P.count = Q.count = count;
     P.M = Q.M = M;
     P.y_dtype = probs[0].y_dtype;
-    Q.format = fmt;
-    Q.x_bf16 = probs[0].x_dtype == LQ_BF16;
+    P.format = Q.format = fmt;
+    P.x_bf16 = Q.x_bf16 = probs[0].x_dtype == LQ_BF16;
 
-    int64_t units = 0, jobs = 0, xhalves = 0;
-    size_t ws_bytes = 0;
+    int64_t units = 0, jobs = 0, xhalves = 0, blocks = 0;
+    int max_k = 0;
     for (int i = 0; i < count; ++i) {
         const lq_problem& q = probs[i];
         const int A = fmt == LQ_FMT_2BIT_LM_G32 ? q.A : 0;
@@ -688,19 +749,24 @@ lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* probs, i
         d.A = A;
         d.ld_anchor = q.ld_anchor;
         d.batch = q.batch;
+        d.x = static_cast<const uint16_t*>(q.x);
+        d.stride_x = q.stride_x;
+        d.anchor_idx = A > 0 ? q.anchor_idx : nullptr;
+        d.stride_anchor_idx = q.stride_anchor_idx;
         const int a_pad = A > 0 ? round_up(A, kAnchorCols) : 0;
         d.steps = q.K / 256;
         d.su = d.steps + a_pad / kAnchorCols;
         d.rblocks = (q.N + 15) / 16;
         d.unit_begin = units;
         units += (int64_t)q.batch * d.rblocks * d.su;
+        blocks += (int64_t)q.batch * d.rblocks;
         // per member: [x in fragment order (M*K) | x at the anchors (M*a_pad)]
         d.xperm_stride = d.xaperm_stride = (int64_t)M * (q.K + a_pad);
         d.xoff = xhalves;
         xhalves += (int64_t)q.batch * d.xperm_stride;
-        e.x = static_cast<const uint16_t*>(q.x);
+        e.x = d.x;
         e.stride_x = q.stride_x;
-        e.anchor_idx = A > 0 ? q.anchor_idx : nullptr;
+        e.anchor_idx = d.anchor_idx;
         e.stride_anchor_idx = q.stride_anchor_idx;
         e.K = q.K;
         e.A = A;
@@ -711,17 +777,19 @@ lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* probs, i
         e.jobs = q.K / 256 + (a_pad + 255) / 256;
         e.job_begin = jobs;
         jobs += (int64_t)q.batch * e.jobs;
+        max_k = std::max(max_k, q.K);
     }
     if (units == 0) return LQ_OK;
-    ws_bytes += align256((size_t)xhalves * 2);
-    // first without staging, to size the grid; the warp partition then fixes the x span of each CTA
+    // arrival counts live in the counter area, which every kernel leaves at zero
+    if ((size_t)blocks > ws.num_counters) return LQ_ERR_UNSUPPORTED;
+    // size the grid; the warp partition then fixes the x span of each CTA
     int per_sm = 0;
     if (dispatch(fmt, 0, false, P, 0, 0, &per_sm, stream) != LQ_OK) return LQ_ERR_CUDA;
-    int64_t grid = std::max<int64_t>(1, std::min<int64_t>((units + kWarps - 1) / kWarps, (int64_t)ws.num_sms * std::max(1, per_sm)));
-    int64_t W = std::min<int64_t>(grid * kWarps, units);
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>((units + kWarps - 1) / kWarps, (int64_t)ws.num_sms * std::max(1, per_sm)));
+    const int64_t W = std::min<int64_t>(grid * kWarps, units);
     P.total_units = units;
     P.total_warps = W;
-    int64_t max_span = 0;
+    int64_t max_span = 0, max_members = 0;
     for (int64_t b = 0; b < grid; ++b) {
         const int64_t w_lo = b * kWarps, w_hi = std::min<int64_t>(w_lo + kWarps, W);
         if (w_lo >= W) break;
@@ -730,31 +798,36 @@ lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* probs, i
         host_locate(P, units * w_lo / W, pa, la);
         host_locate(P, units * w_hi / W - 1, pb, lb);
         max_span = std::max<int64_t>(max_span, P.d[pb].xoff + (lb + 1) * P.d[pb].xperm_stride - (P.d[pa].xoff + la * P.d[pa].xperm_stride));
+        int64_t members = 0;
+        for (int p = pa; p <= pb; ++p) members += (p == pb ? lb : P.d[p].batch - 1) - (p == pa ? la : 0) + 1;
+        max_members = std::max(max_members, members);
     }
-    // stage x in shared memory when the widest span fits beside a second resident CTA
-    // (off unless LQ_GEMV_STAGE=1: on this part the L1-resident reads measured ~1% faster)
-    const size_t smem = (size_t)max_span * 2;
+    // With LQ_GEMV_STAGE=1 each CTA builds the x its units read in shared memory when that
+    // span is small (a few members, room for a second resident CTA), and no pre-pass runs;
+    // by default the pre-pass does it once for all CTAs (measured faster on this part).
+    P.bitmap_words = std::max(1, max_k / 32);
+    const size_t smem = (size_t)max_span * 2 + (size_t)P.bitmap_words * 4;
     const char* st_env = getenv("LQ_GEMV_STAGE");
-    bool staged = smem <= (size_t)std::min(ws.max_smem_optin, 110 * 1024) && st_env && atoi(st_env) == 1;
+    bool staged = max_members <= 4 && smem <= (size_t)std::min(ws.max_smem_optin, 110 * 1024) && st_env && atoi(st_env) == 1;
     if (staged) {
         int per_sm_s = 0;
         if (dispatch(fmt, 0, true, P, 0, smem, &per_sm_s, stream) != LQ_OK) return LQ_ERR_CUDA;
         staged = per_sm_s >= per_sm;   // staging must not cost occupancy
     }
     const int64_t min_run = units / W;   // every warp's run has at least this many units (>= 1)
+    size_t ws_bytes = staged ? 0 : align256((size_t)xhalves * 2);
     for (int i = 0; i < count; ++i) {
         FDesc& d = P.d[i];
         d.cmax = (int)std::min<int64_t>(d.su / min_run + 2, d.su);
-        ws_bytes += align256((size_t)probs[i].batch * d.rblocks * d.cmax * M * 16 * 4) +
-                    align256((size_t)probs[i].batch * d.rblocks * 4);
+        ws_bytes += align256((size_t)probs[i].batch * d.rblocks * d.cmax * M * 16 * 4);
     }
     if (ws_bytes + 256 > ws.partial_floats * sizeof(float)) return LQ_ERR_WORKSPACE;
-    // workspace: all x copies, then per problem partial-sum slots and arrival counts
+    // workspace: x copies (pre-pass only), then per problem the partial-sum slots
     char* wp = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(ws.partials) + 255) & ~uintptr_t(255));
     uint16_t* xbuf = reinterpret_cast<uint16_t*>(wp);
-    wp += align256((size_t)xhalves * 2);
+    if (!staged) wp += align256((size_t)xhalves * 2);
     P.xbuf = xbuf;
-    int nz = 0;
+    unsigned* cnt = ws.counters;
     for (int i = 0; i < count; ++i) {
         FDesc& d = P.d[i];
         const lq_problem& q = probs[i];
@@ -762,20 +835,21 @@ lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* probs, i
         d.xaperm = Q.d[i].xaperm = xbuf + d.xoff + (int64_t)M * q.K;
         d.part = reinterpret_cast<float*>(wp);
         wp += align256((size_t)q.batch * d.rblocks * d.cmax * M * 16 * 4);
-        d.cnt = reinterpret_cast<unsigned*>(wp);
-        wp += align256((size_t)q.batch * d.rblocks * 4);
-        Q.z[nz++] = ZeroTask{d.cnt, (int64_t)q.batch * d.rblocks, 0, 1};
+        d.cnt = cnt;
+        cnt += (int64_t)q.batch * d.rblocks;
     }
-    Q.zero_tasks = nz;
+    if (ws.clear_counters && cudaMemsetAsync(ws.counters, 0, sizeof(unsigned) * (size_t)blocks, stream) != cudaSuccess)
+        return LQ_ERR_CUDA;
     Q.total_jobs = jobs;
+    int unused = 0;
+    if (staged) return dispatch(fmt, 1, true, P, grid, smem, &unused, stream);
 
-    // x pre-pass (and zeroing), then the main kernel, chained by programmatic dependent launch
+    // x pre-pass, then the main kernel, chained by programmatic dependent launch
     const int64_t prep_ctas = (jobs + kPrepWarps - 1) / kPrepWarps;
     if (prep_ctas > 0x7fffffffLL) return LQ_ERR_UNSUPPORTED;
     xprep_kernel<<<(unsigned)prep_ctas, 32 * kPrepWarps, 0, stream>>>(Q);
     if (cudaPeekAtLastError() != cudaSuccess) return LQ_ERR_CUDA;
-    int unused = 0;
-    return dispatch(fmt, 1, staged, P, grid, staged ? smem : 0, &unused, stream);
+    return dispatch(fmt, 1, false, P, grid, 0, &unused, stream);
 }
 
 }  // namespace lq
