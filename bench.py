@@ -12,8 +12,9 @@ weights + anchor indices + x + y) / time; `roofline.frac` against the measured
 HBM copy bandwidth; equivalent tok/s of a 32-layer stack.
 
 Second figure (`gemm`): prefill of a 14B-shaped layer (q/k/v/o 5120x5120,
-gate/up 13824x5120, down 5120x13824) at M = 2048 bf16 tokens, one lq_gemm
-call per projection, for 2-bit G=32 + anchors and for NF4 block 64; TFLOP/s =
+gate/up 13824x5120, down 5120x13824) at M = 2048 bf16 tokens, the seven
+projections in one lq_gemm_grouped launch, for 2-bit G=32 + anchors and for
+NF4 block 64; TFLOP/s =
 2*M*N*K summed over the layer / step time, against the measured dense bf16
 peak.
 
@@ -211,7 +212,7 @@ def config1_batched(lq, torch, h, device: str, steps: int, warmup: int):
 
 
 GEMM_M = 2048
-GEMM_WORKLOAD = "14b decoder layer prefill, M=2048 bf16 tokens, 7 projections, one lq_gemm call each"
+GEMM_WORKLOAD = "14b decoder layer prefill, M=2048 bf16 tokens, 7 projections in one lq_gemm_grouped launch"
 
 
 def gemm_layer(lq, torch, h, fmt: str, device: str, steps: int, warmup: int):
@@ -232,10 +233,10 @@ def gemm_layer(lq, torch, h, fmt: str, device: str, steps: int, warmup: int):
         mats.append((name, w, x, y))
         flops += 2 * GEMM_M * N * K
     stream = torch.cuda.current_stream()
+    probs = [h.problem(w, x, y) for _, w, x, y in mats]
 
     def step():
-        for _, w, x, y in mats:
-            h.gemm(w, x, y, stream=stream)
+        h.gemm_grouped(probs, stream=stream)
 
     for _ in range(warmup):
         step()
@@ -262,7 +263,7 @@ def gemm_layer(lq, torch, h, fmt: str, device: str, steps: int, warmup: int):
     torch.cuda.synchronize()
     one_ms = a0.elapsed_time(a1) / reps
     one_flops = 2 * GEMM_M * w.N * w.K
-    launches = sum(3 if fmt == "2bit" else 1 for _ in mats)   # 2-bit: bitmap memset + anchor gather + GEMM
+    launches = 3 if fmt == "2bit" else 1   # 2-bit: bitmap memset + anchor gather + GEMM
     return {"fmt": fmt, "value": round(flops / (ms * 1e-3) / 1e12, 1), "unit": "TFLOP/s", "ms_per_layer": round(ms, 4),
             "largest": {"name": name, "N": w.N, "K": w.K, "ms": round(one_ms, 4),
                         "tflops": round(one_flops / (one_ms * 1e-3) / 1e12, 1)},

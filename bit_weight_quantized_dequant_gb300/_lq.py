@@ -15,7 +15,7 @@ F32, F16, BF16 = 0, 1, 2
 
 #: every entry point include/lq.h declares
 EXPORTED = ("lq_create", "lq_destroy", "lq_status_string", "lq_sync", "lq_dequant", "lq_gemv",
-            "lq_gemv_grouped", "lq_gemm", "lq_gemv_noalloc")
+            "lq_gemv_grouped", "lq_gemm", "lq_gemm_grouped", "lq_gemv_noalloc")
 
 _LIB = None
 
@@ -77,6 +77,8 @@ def load_library(build_if_missing: bool = True):
     L.lq_gemv_noalloc.restype = I
     L.lq_gemv_grouped.argtypes = [P, ctypes.POINTER(lq_problem), I, P]
     L.lq_gemv_grouped.restype = I
+    L.lq_gemm_grouped.argtypes = [P, ctypes.POINTER(lq_problem), I, P]
+    L.lq_gemm_grouped.restype = I
     _LIB = L
     return L
 
@@ -228,3 +230,10 @@ class Handle:
         st = self._lib.lq_gemv_grouped(self._h, arr, len(problems), _stream(stream))
         if st != LQ_OK:
             raise LQError(st, "lq_gemv_grouped")
+
+    def gemm_grouped(self, problems, stream=None):
+        """Several prefill products (same format and x dtype) in one tensor-core launch."""
+        arr = (lq_problem * len(problems))(*problems)
+        st = self._lib.lq_gemm_grouped(self._h, arr, len(problems), _stream(stream))
+        if st != LQ_OK:
+            raise LQError(st, "lq_gemm_grouped")

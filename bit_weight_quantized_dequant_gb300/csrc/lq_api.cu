@@ -170,15 +170,18 @@ LQ_API lq_status lq_create(lq_handle* out, int device, size_t workspace_bytes) {
         return LQ_ERR_CUDA;
     }
     h->workspace_bytes = bytes;
-    // layout: [status word (256 B) | counters (1/16 of the rest) | partial sums]
+    // layout: [status word (256 B) | counters (1/16 of the rest) | partial sums | GEMM tile lists (1/64)]
     char* base = static_cast<char*>(h->workspace);
     h->status_flag = reinterpret_cast<int*>(base);
     const size_t rest = bytes - 256;
     const size_t counter_bytes = (rest / 16) & ~size_t(255);
+    const size_t sched_bytes = (rest / 64) & ~size_t(255);
     h->counters = reinterpret_cast<unsigned*>(base + 256);
     h->num_counters = counter_bytes / sizeof(unsigned);
     h->partials = reinterpret_cast<float*>(base + 256 + counter_bytes);
-    h->partial_floats = (rest - counter_bytes) / sizeof(float);
+    h->partial_floats = (rest - counter_bytes - sched_bytes) / sizeof(float);
+    h->sched = reinterpret_cast<int*>(base + bytes - sched_bytes);
+    h->sched_ints = sched_bytes / sizeof(int);
     *out = h;
     return LQ_OK;
 }
@@ -273,6 +276,27 @@ LQ_API lq_status lq_gemm(lq_handle h, int format, const uint8_t* codes, const vo
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if ((s = check_anchor_order(anchor_idx, A, K, st)) != LQ_OK) return s;
     return lq::launch_gemm(h, p, st);
+}
+
+LQ_API lq_status lq_gemm_grouped(lq_handle h, const lq_problem* problems, int count, void* stream) {
+    if (!h || !problems || count < 1) return LQ_ERR_INVALID_ARG;
+    if (count > lq::kMaxGemmGroup) return LQ_ERR_UNSUPPORTED;
+    for (int i = 0; i < count; ++i) {
+        const lq_problem& p = problems[i];
+        const lq_status s = check_problem(p);
+        if (s != LQ_OK) return s;
+        if (p.M < 1 || p.batch != 1) return LQ_ERR_UNSUPPORTED;
+        if (p.K % 64 != 0) return LQ_ERR_UNSUPPORTED;
+        if (p.format != problems[0].format || p.x_dtype != problems[0].x_dtype) return LQ_ERR_UNSUPPORTED;
+    }
+    DeviceGuard guard(h->device);
+    if (!guard.ok) return LQ_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    for (int i = 0; i < count; ++i) {
+        const lq_status s = check_anchor_order(problems[i].anchor_idx, problems[i].A, problems[i].K, st);
+        if (s != LQ_OK) return s;
+    }
+    return lq::launch_gemm_grouped(h, problems, count, st);
 }
 
 // ---- the allocation-free GEMV entry point ---------------------------------------

@@ -26,6 +26,7 @@
 #include <algorithm>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "lq_common.cuh"
 #include "lq_dq.cuh"
@@ -76,7 +77,8 @@ struct GemmLayout {
     static constexpr int kSmemBytes = 1024 + kBarOff + kNumBars * 8;
 };
 
-struct GemmParams {
+// One problem of a (grouped) launch: tensor maps, pointers and shape.
+struct GemmProb {
     CUtensorMap xmap;          // x [M][K] 16-bit, box 64 x 256, 128-byte swizzle
     CUtensorMap xamap;         // x at the anchor columns [M][a_pad], same box
     CUtensorMap awmap;         // anchor weights [N][ld_anchor] binary16, box 64 x 128, 128-byte swizzle
@@ -87,10 +89,31 @@ struct GemmParams {
     const uint16_t* offsets;
     const uint32_t* anchor_bits;   // [K/32 + 8] anchor columns of each 32-column half block
     void* y;
-    int M, N, K, A, a_pad, bf16, y_dtype, meta_tma;
-    int tiles_m, total_tiles;
+    int M, N, K, A, a_pad, y_dtype, meta_tma;
+    int tiles_m, tile_begin;   // token tiles per row tile; first tile of this problem in the launch
+};
+
+struct GemmParams {
+    GemmProb d[kMaxGemmGroup];
+    int count, bf16, total_tiles;
+    const int* sched_off;      // tile list of CTA b: sched_tiles[sched_off[b] .. sched_off[b+1]) (null: round robin)
+    const int* sched_tiles;
     int* status;
 };
+
+// Tiles of this CTA, the i-th of them, and the problem a tile belongs to.
+__device__ __forceinline__ int cta_tiles(const GemmParams& P) {
+    if (P.sched_off) return P.sched_off[blockIdx.x + 1] - P.sched_off[blockIdx.x];
+    return (int)blockIdx.x < P.total_tiles ? (P.total_tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+}
+__device__ __forceinline__ int tile_id(const GemmParams& P, int i) {
+    return P.sched_off ? __ldg(P.sched_tiles + P.sched_off[blockIdx.x] + i) : (int)blockIdx.x + i * (int)gridDim.x;
+}
+__device__ __forceinline__ int tile_prob(const GemmParams& P, int gt) {
+    int p = 0;
+    while (p + 1 < P.count && gt >= P.d[p + 1].tile_begin) ++p;
+    return p;
+}
 
 __device__ __forceinline__ uint32_t pack2(float lo, float hi, int bf16) {
     uint32_t d;
@@ -123,17 +146,6 @@ __device__ __forceinline__ void dq2_word(uint32_t w, uint32_t P01, uint32_t P23,
     c1[2] = prmt(P01, P23, sc >> 16);
     c1[3] = prmt(P01, P23, sd >> 16);
 }
-
-// Position in this CTA's sequence of work items: (output tile, K-block), K-blocks innermost.
-struct Item {
-    int tile, kb;
-    __device__ __forceinline__ void next(int nkb) {
-        if (++kb == nkb) {
-            kb = 0;
-            tile += gridDim.x;
-        }
-    }
-};
 
 struct Ring {
     int s = 0, ph = 0;
@@ -186,29 +198,33 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     tc_fence_after();
     const uint32_t tmem = s_tmem;
 
-    const int KB = P.K / kBK, NKB = KB + P.a_pad / kBK, NCH = (KB + kChunk - 1) / kChunk;
+    const int ntiles = cta_tiles(P);
     int own_abort = 0;
     volatile int* abort = &own_abort;
 
     if (warp == 0) {
-        // ---------------------------------------------------------------- TMA: x tiles, anchor weight tiles
+        // ---------------------------------------------------------------- TMA: x tiles
         if (lane == 0) {
-            prefetch_tensormap(&P.xmap);
-            if (P.a_pad) prefetch_tensormap(&P.xamap);
+            for (int p = 0; p < P.count; ++p) {
+                prefetch_tensormap(&P.d[p].xmap);
+                if (P.d[p].a_pad) prefetch_tensormap(&P.d[p].xamap);
+            }
             Ring rb;
-            for (Item it{(int)blockIdx.x, 0}; it.tile < P.total_tiles; it.next(NKB)) {
-                const int m0 = (it.tile % P.tiles_m) * kBN;
-                if (!mbar_wait_bounded(b_empty0 + 8 * rb.s, rb.ph ^ 1, abort, P.status)) break;
-                const uint32_t fb = b_full0 + 8 * rb.s;
-                if (it.kb < KB) {
+            for (int i = 0; i < ntiles; ++i) {
+                const int gt = tile_id(P, i);
+                const GemmProb& D = P.d[tile_prob(P, gt)];
+                const int lt = gt - D.tile_begin, m0 = (lt % D.tiles_m) * kBN;
+                const int KB = D.K / kBK, NKB = KB + D.a_pad / kBK;
+                bool ok = true;
+                for (int kb = 0; kb < NKB; ++kb) {
+                    if (!(ok = mbar_wait_bounded(b_empty0 + 8 * rb.s, rb.ph ^ 1, abort, P.status))) break;
+                    const uint32_t fb = b_full0 + 8 * rb.s;
                     mbar_arrive_expect_tx(fb, kBTile);
-                    tma_load_2d(smem_u32(btile + rb.s * kBTile), &P.xmap, it.kb * kBK, m0, fb);
-                } else {
-                    // anchor K-block: x gathered at the anchor columns
-                    mbar_arrive_expect_tx(fb, kBTile);
-                    tma_load_2d(smem_u32(btile + rb.s * kBTile), &P.xamap, (it.kb - KB) * kBK, m0, fb);
+                    if (kb < KB) tma_load_2d(smem_u32(btile + rb.s * kBTile), &D.xmap, kb * kBK, m0, fb);
+                    else tma_load_2d(smem_u32(btile + rb.s * kBTile), &D.xamap, (kb - KB) * kBK, m0, fb);   // x at the anchors
+                    rb.next(kStagesB);
                 }
-                rb.next(kStagesB);
+                if (!ok) break;
             }
         }
     } else if (warp == 1) {
@@ -217,10 +233,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
             const uint32_t idesc = idesc_f16(P.bf16 != 0, kBM, kBN);
             Ring ra, rb;
             bool ok = true;
-            for (int tile = blockIdx.x, lt = 0; ok && tile < P.total_tiles; tile += gridDim.x, ++lt) {
-                const int acc = lt & 1;
+            for (int i = 0; ok && i < ntiles; ++i) {
+                const GemmProb& D = P.d[tile_prob(P, tile_id(P, i))];
+                const int NKB = D.K / kBK + D.a_pad / kBK;
+                const int acc = i & 1;
                 // the epilogue has drained this accumulator (two tiles ago)
-                if (!(ok = mbar_wait_bounded(acc_empty0 + 8 * acc, ((lt >> 1) & 1) ^ 1, abort, P.status))) break;
+                if (!(ok = mbar_wait_bounded(acc_empty0 + 8 * acc, ((i >> 1) & 1) ^ 1, abort, P.status))) break;
                 tc_fence_after();
                 const uint32_t d = tmem + acc * kBN;
                 for (int kb = 0; kb < NKB; ++kb) {
@@ -244,26 +262,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     } else if (warp == 2) {
         // ---------------------------------------------------------------- metadata: codes, scales, anchor bits
         if (lane == 0) {
-            prefetch_tensormap(&P.cmap);
-            if (P.meta_tma) {
-                prefetch_tensormap(&P.smap);
-                if (!L::kNF4Fmt) prefetch_tensormap(&P.omap);
+            for (int p = 0; p < P.count; ++p) {
+                prefetch_tensormap(&P.d[p].cmap);
+                if (P.d[p].meta_tma) {
+                    prefetch_tensormap(&P.d[p].smap);
+                    if (!L::kNF4Fmt) prefetch_tensormap(&P.d[p].omap);
+                }
+                if (P.d[p].a_pad) prefetch_tensormap(&P.d[p].awmap);
             }
-            if (P.a_pad) prefetch_tensormap(&P.awmap);
         }
         Ring rm;
-        for (int tile = blockIdx.x; tile < P.total_tiles; tile += gridDim.x) {
-            const int n0 = (tile / P.tiles_m) * kBM;
+        for (int i = 0; i < ntiles; ++i) {
+            const int gt = tile_id(P, i);
+            const GemmProb& D = P.d[tile_prob(P, gt)];
+            const int lt = gt - D.tile_begin, n0 = (lt / D.tiles_m) * kBM;
+            const int KB = D.K / kBK, NCH = (KB + kChunk - 1) / kChunk;
             for (int c = 0; c < NCH; ++c) {
                 if (!__all_sync(0xffffffffu, mbar_wait_bounded(m_empty0 + 8 * rm.s, rm.ph ^ 1, abort, P.status)))
                     goto meta_done;
                 uint8_t* ch = meta + rm.s * L::kChunkBytes;
                 const uint32_t fb = m_full0 + 8 * rm.s;
                 const int kb0 = c * kChunk;
-                if (!L::kNF4Fmt && P.A > 0) {
+                if (!L::kNF4Fmt && D.A > 0) {
                     // anchor columns of the chunk's K-blocks and the per-word keep masks
-                    const uint4 b01 = *reinterpret_cast<const uint4*>(P.anchor_bits + 2 * kb0);
-                    const uint4 b23 = *reinterpret_cast<const uint4*>(P.anchor_bits + 2 * kb0 + 4);
+                    const uint4 b01 = *reinterpret_cast<const uint4*>(D.anchor_bits + 2 * kb0);
+                    const uint4 b23 = *reinterpret_cast<const uint4*>(D.anchor_bits + 2 * kb0 + 4);
                     const uint32_t bw[8] = {b01.x, b01.y, b01.z, b01.w, b23.x, b23.y, b23.z, b23.w};
                     if (lane == 0) {
                         reinterpret_cast<uint4*>(ch + L::kBitsOff)[0] = b01;
@@ -276,19 +299,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                         reinterpret_cast<uint32_t*>(ch + L::kMaskOff + j * 128)[lane] = keep;
                     }
                 }
-                if (!P.meta_tma) {
+                if (!D.meta_tma) {
                     // scale rows are not 16-byte aligned: 4-byte loads, four rows per lane
                     const int nk = min(kChunk, KB - kb0);
                     for (int rr = lane; rr < kBM; rr += 32) {
-                        const int64_t nr = min(n0 + rr, P.N - 1);
+                        const int64_t nr = min(n0 + rr, D.N - 1);
                         if (L::kNF4Fmt) {
-                            const float* src = static_cast<const float*>(P.scales) + nr * (P.K / 64) + kb0;
+                            const float* src = static_cast<const float*>(D.scales) + nr * (D.K / 64) + kb0;
                             for (int i = 0; i < nk; ++i)
                                 reinterpret_cast<float*>(ch + L::kScaleOff + rr * 16)[i] = __ldg(src + i);
                         } else {
-                            const int64_t g = nr * (P.K / 32) + 2 * kb0;
-                            const uint32_t* ss = reinterpret_cast<const uint32_t*>(static_cast<const uint16_t*>(P.scales) + g);
-                            const uint32_t* so = reinterpret_cast<const uint32_t*>(P.offsets + g);
+                            const int64_t g = nr * (D.K / 32) + 2 * kb0;
+                            const uint32_t* ss = reinterpret_cast<const uint32_t*>(static_cast<const uint16_t*>(D.scales) + g);
+                            const uint32_t* so = reinterpret_cast<const uint32_t*>(D.offsets + g);
                             for (int i = 0; i < nk; ++i) {
                                 reinterpret_cast<uint32_t*>(ch + L::kScaleOff + rr * 16)[i] = __ldg(ss + i);
                                 reinterpret_cast<uint32_t*>(ch + L::kOffsetOff + rr * 16)[i] = __ldg(so + i);
@@ -298,13 +321,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                 }
                 if (lane == 0) {
                     uint32_t tx = L::kCodesBytes;
-                    if (P.meta_tma) tx += L::kNF4Fmt ? kBM * 16 : 2 * kBM * 16;
+                    if (D.meta_tma) tx += L::kNF4Fmt ? kBM * 16 : 2 * kBM * 16;
                     mbar_arrive_expect_tx(fb, tx);
-                    tma_load_2d(smem_u32(ch), &P.cmap, kb0 * (L::kNF4Fmt ? 32 : 16), n0, fb);
-                    if (P.meta_tma) {
-                        tma_load_2d(smem_u32(ch + L::kScaleOff), &P.smap, kb0 * (L::kNF4Fmt ? 1 : 2), n0, fb);
+                    tma_load_2d(smem_u32(ch), &D.cmap, kb0 * (L::kNF4Fmt ? 32 : 16), n0, fb);
+                    if (D.meta_tma) {
+                        tma_load_2d(smem_u32(ch + L::kScaleOff), &D.smap, kb0 * (L::kNF4Fmt ? 1 : 2), n0, fb);
                         if (!L::kNF4Fmt)
-                            tma_load_2d(smem_u32(ch + L::kOffsetOff), &P.omap, kb0 * 2, n0, fb);
+                            tma_load_2d(smem_u32(ch + L::kOffsetOff), &D.omap, kb0 * 2, n0, fb);
                     }
                 } else {
                     mbar_arrive(fb);
@@ -312,13 +335,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                 rm.next(2);
             }
             // anchor weight tiles of this tile, one per slot
-            for (int a = 0; a < P.a_pad / kBK; ++a) {
+            for (int a = 0; a < D.a_pad / kBK; ++a) {
                 if (!__all_sync(0xffffffffu, mbar_wait_bounded(m_empty0 + 8 * rm.s, rm.ph ^ 1, abort, P.status)))
                     goto meta_done;
                 const uint32_t fb = m_full0 + 8 * rm.s;
                 if (lane == 0) {
                     mbar_arrive_expect_tx(fb, kATile);
-                    tma_load_2d(smem_u32(meta + rm.s * L::kChunkBytes), &P.awmap, a * kBK, n0, fb);
+                    tma_load_2d(smem_u32(meta + rm.s * L::kChunkBytes), &D.awmap, a * kBK, n0, fb);
                 } else {
                     mbar_arrive(fb);
                 }
@@ -334,18 +357,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         const int sw = r & 7;
         const float C0 = -1.52f, C1 = -0.45f, C2 = 0.45f, C3 = 1.52f;
         Ring ra, rm;
-        for (Item it{(int)blockIdx.x, 0}; it.tile < P.total_tiles; it.next(NKB)) {
-            const bool mine = (it.kb & 1) == g;
+        for (int i = 0; i < ntiles; ++i) {
+          const GemmProb& D = P.d[tile_prob(P, tile_id(P, i))];
+          const int KB = D.K / kBK, NKB = KB + D.a_pad / kBK;
+          for (int kb = 0; kb < NKB; ++kb) {
+            const bool mine = (kb & 1) == g;
             uint8_t* arow = atile + ra.s * kATile + r * 128;
-            if (it.kb < KB) {
-                const int j = it.kb % kChunk;
+            if (kb < KB) {
+                const int j = kb % kChunk;
                 // every warp waits for each metadata chunk and releases it at its end, so a
                 // release never runs ahead of the load it frees (count: all dequant warps)
                 if (j == 0 && !__all_sync(0xffffffffu, mbar_wait_bounded(m_full0 + 8 * rm.s, rm.ph, abort, P.status)))
-                    break;
+                    goto dq_done;
                 if (mine) {
                     if (!__all_sync(0xffffffffu, mbar_wait_bounded(a_empty0 + 8 * ra.s, ra.ph ^ 1, abort, P.status)))
-                        break;
+                        goto dq_done;
                     const uint8_t* ch = meta + rm.s * L::kChunkBytes;
                     uint32_t c[32];   // c[4q + k]: columns 8q + 2k, 8q + 2k + 1
                     if (FMT == LQ_FMT_2BIT_LM_G32) {
@@ -362,7 +388,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                         dq2_word(cw.y, A01, A23, *reinterpret_cast<uint32_t(*)[4]>(c + 8), *reinterpret_cast<uint32_t(*)[4]>(c + 12));
                         dq2_word(cw.z, B01, B23, *reinterpret_cast<uint32_t(*)[4]>(c + 16), *reinterpret_cast<uint32_t(*)[4]>(c + 20));
                         dq2_word(cw.w, B01, B23, *reinterpret_cast<uint32_t(*)[4]>(c + 24), *reinterpret_cast<uint32_t(*)[4]>(c + 28));
-                        if (P.A > 0) {
+                        if (D.A > 0) {
                             // anchor columns replace the 2-bit weights: clear them with the chunk's keep
                             // masks, only in the 16-column words that hold one (the bitmap is warp-uniform)
                             const uint2 bw = *reinterpret_cast<const uint2*>(ch + L::kBitsOff + 8 * j);
@@ -410,20 +436,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                     __syncwarp();
                     if (lane == 0) mbar_arrive(a_full0 + 8 * ra.s);
                 }
-                if (j == kChunk - 1 || it.kb == KB - 1) {
+                if (j == kChunk - 1 || kb == KB - 1) {
                     if (lane == 0) mbar_arrive(m_empty0 + 8 * rm.s);
                     rm.next(2);
                 }
             } else {
                 // anchor block: the metadata slot holds 64 binary16 anchor weights per row; the
                 // owning group copies them into the stage, zero past A, in bf16 when x is bf16
-                if (!__all_sync(0xffffffffu, mbar_wait_bounded(m_full0 + 8 * rm.s, rm.ph, abort, P.status))) break;
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(m_full0 + 8 * rm.s, rm.ph, abort, P.status))) goto dq_done;
                 if (mine) {
                     if (!__all_sync(0xffffffffu, mbar_wait_bounded(a_empty0 + 8 * ra.s, ra.ph ^ 1, abort, P.status)))
-                        break;
+                        goto dq_done;
                     const uint8_t* srow = meta + rm.s * L::kChunkBytes + r * 128;
-                    const int a0 = (it.kb - KB) * kBK;
-                    const bool fix = P.bf16 || a0 + kBK > P.A;
+                    const int a0 = (kb - KB) * kBK;
+                    const bool fix = P.bf16 || a0 + kBK > D.A;
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
                         const int off = (q ^ sw) << 4;
@@ -433,8 +459,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
 #pragma unroll
                             for (int i = 0; i < 4; ++i) {
                                 const int a = a0 + 8 * q + 2 * i;
-                                uint32_t w = a < P.A ? v[i] : 0u;
-                                if (a + 1 >= P.A) w &= 0xFFFFu;
+                                uint32_t w = a < D.A ? v[i] : 0u;
+                                if (a + 1 >= D.A) w &= 0xFFFFu;
                                 if (P.bf16)
                                     w = pack2(half_bits_to_float((uint16_t)w), half_bits_to_float((uint16_t)(w >> 16)), 1);
                                 v[i] = w;
@@ -451,38 +477,43 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                 rm.next(2);
             }
             ra.next(SA);
+          }
         }
+    dq_done:;
     } else {
         // ---------------------------------------------------------------- epilogue: TMEM -> y
         const int quarter = warp & 3;   // the TMEM lane quarter this warp may read
-        for (int tile = blockIdx.x, lt = 0; tile < P.total_tiles; tile += gridDim.x, ++lt) {
-            const int acc = lt & 1;
-            if (!__all_sync(0xffffffffu, mbar_wait_bounded(acc_full0 + 8 * acc, (lt >> 1) & 1, abort, P.status))) break;
+        for (int i = 0; i < ntiles; ++i) {
+            const int gt = tile_id(P, i);
+            const GemmProb& D = P.d[tile_prob(P, gt)];
+            const int acc = i & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(acc_full0 + 8 * acc, (i >> 1) & 1, abort, P.status))) break;
             tc_fence_after();
-            const int n0 = (tile / P.tiles_m) * kBM, m0 = (tile % P.tiles_m) * kBN;
+            const int lt = gt - D.tile_begin;
+            const int n0 = (lt / D.tiles_m) * kBM, m0 = (lt % D.tiles_m) * kBN;
             const int n = n0 + 32 * quarter + lane;
 #pragma unroll 1
             for (int cc = 0; cc < kBN / 32; ++cc) {
                 uint32_t v[32];
                 tmem_ld32(tmem + ((uint32_t)(32 * quarter) << 16) + acc * kBN + 32 * cc, v);
-                if (n < P.N) {
-                    const int mb = m0 + 32 * cc, mcount = min(32, P.M - mb);
-                    const size_t o = (size_t)mb * P.N + n;
-                    if (P.y_dtype == LQ_BF16) {
-                        __nv_bfloat16* yp = static_cast<__nv_bfloat16*>(P.y) + o;
+                if (n < D.N) {
+                    const int mb = m0 + 32 * cc, mcount = min(32, D.M - mb);
+                    const size_t o = (size_t)mb * D.N + n;
+                    if (D.y_dtype == LQ_BF16) {
+                        __nv_bfloat16* yp = static_cast<__nv_bfloat16*>(D.y) + o;
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
-                            if (j < mcount) yp[(size_t)j * P.N] = __float2bfloat16_rn(__uint_as_float(v[j]));
-                    } else if (P.y_dtype == LQ_F16) {
-                        __half* yp = static_cast<__half*>(P.y) + o;
+                            if (j < mcount) yp[(size_t)j * D.N] = __float2bfloat16_rn(__uint_as_float(v[j]));
+                    } else if (D.y_dtype == LQ_F16) {
+                        __half* yp = static_cast<__half*>(D.y) + o;
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
-                            if (j < mcount) yp[(size_t)j * P.N] = __float2half_rn(__uint_as_float(v[j]));
+                            if (j < mcount) yp[(size_t)j * D.N] = __float2half_rn(__uint_as_float(v[j]));
                     } else {
-                        float* yp = static_cast<float*>(P.y) + o;
+                        float* yp = static_cast<float*>(D.y) + o;
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
-                            if (j < mcount) yp[(size_t)j * P.N] = __uint_as_float(v[j]);
+                            if (j < mcount) yp[(size_t)j * D.N] = __uint_as_float(v[j]);
                     }
                 }
             }
@@ -497,20 +528,32 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-// x gathered at the anchor columns ([M][a_pad], zero past A) and the anchor bitmap
-__global__ void __launch_bounds__(256) gemm_prep_kernel(const uint16_t* __restrict__ x, int M, int K,
-                                                        const int32_t* __restrict__ anchor_idx, int A, int a_pad,
-                                                        uint16_t* __restrict__ xa, unsigned long long* bits) {
-    const int64_t total = (int64_t)M * a_pad;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total || i < A;
+// x gathered at the anchor columns ([M][a_pad], zero past A) and the anchor bitmap of
+// each problem (blockIdx.y); the bitmaps are cleared before this runs.
+struct PrepProb {
+    const uint16_t* x;
+    const int32_t* anchor_idx;
+    uint16_t* xa;
+    unsigned long long* bits;
+    int M, K, A, a_pad;
+};
+
+struct GemmPrepParams {
+    PrepProb d[kMaxGemmGroup];
+};
+
+__global__ void __launch_bounds__(256) gemm_prep_kernel(const __grid_constant__ GemmPrepParams Q) {
+    const PrepProb& D = Q.d[blockIdx.y];
+    const int64_t total = (int64_t)D.M * D.a_pad;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total || i < D.A;
          i += (int64_t)gridDim.x * blockDim.x) {
-        if (i < A) {
-            const int k = anchor_idx[i];
-            atomicOr(bits + (k >> 6), 1ull << (k & 63));
+        if (i < D.A) {
+            const int k = D.anchor_idx[i];
+            atomicOr(D.bits + (k >> 6), 1ull << (k & 63));
         }
         if (i < total) {
-            const int m = (int)(i / a_pad), a = (int)(i - (int64_t)m * a_pad);
-            xa[i] = a < A ? x[(int64_t)m * K + anchor_idx[a]] : (uint16_t)0;
+            const int m = (int)(i / D.a_pad), a = (int)(i - (int64_t)m * D.a_pad);
+            D.xa[i] = a < D.A ? D.x[(int64_t)m * D.K + D.anchor_idx[a]] : (uint16_t)0;
         }
     }
 }
@@ -556,73 +599,152 @@ lq_status launch_fmt(const GemmParams& P, int grid, cudaStream_t stream) {
 
 }  // namespace
 
-lq_status launch_gemm(lq_handle h, const lq_problem& p, cudaStream_t stream) {
-    GemmParams P;
-    memset(&P, 0, sizeof(P));
-    const int A = p.format == LQ_FMT_2BIT_LM_G32 ? p.A : 0;
-    const int a_pad = A > 0 ? (A + kBK - 1) / kBK * kBK : 0;
-    P.scales = p.scales;
-    P.offsets = p.offsets;
-    P.y = p.y;
-    P.M = p.M;
-    P.N = p.N;
-    P.K = p.K;
-    P.A = A;
-    P.a_pad = a_pad;
-    P.bf16 = p.x_dtype == LQ_BF16;
-    P.y_dtype = p.y_dtype;
-    P.meta_tma = p.K % 256 == 0;   // scale rows 16-byte aligned: TMA boxes; else 4-byte loads
-    P.tiles_m = (p.M + kBN - 1) / kBN;
-    const int64_t tiles = (int64_t)P.tiles_m * ((p.N + kBM - 1) / kBM);
-    if (tiles > 0x7fffffffLL) return LQ_ERR_UNSUPPORTED;
-    P.total_tiles = (int)tiles;
-    P.status = h->status_flag;
+// Longest-processing-time assignment of the launch's tiles to `grid` CTAs (each tile
+// costs its K-blocks), as per-CTA lists; kept on the device between calls with the same shapes.
+static lq_status upload_schedule(lq_handle h, const GemmParams& P, int grid, cudaStream_t stream) {
+    std::vector<int64_t> key = {grid, P.count};
+    for (int p = 0; p < P.count; ++p) {
+        const GemmProb& D = P.d[p];
+        key.insert(key.end(), {D.M, D.N, D.K, D.a_pad, D.tiles_m});
+    }
+    if (key == h->sched_key) return LQ_OK;
+    struct Job {
+        int cost, tile;
+    };
+    std::vector<Job> jobs;
+    jobs.reserve(P.total_tiles);
+    for (int p = 0; p < P.count; ++p) {
+        const GemmProb& D = P.d[p];
+        const int ntl = (p + 1 < P.count ? P.d[p + 1].tile_begin : P.total_tiles) - D.tile_begin;
+        for (int t = 0; t < ntl; ++t) jobs.push_back({D.K / kBK + D.a_pad / kBK, D.tile_begin + t});
+    }
+    std::stable_sort(jobs.begin(), jobs.end(), [](const Job& a, const Job& b) { return a.cost > b.cost; });
+    std::vector<std::vector<int>> lists(grid);
+    std::vector<std::pair<int64_t, int>> heap;   // (load, cta), min-heap
+    for (int b = 0; b < grid; ++b) heap.push_back({0, b});
+    auto cmp = [](const std::pair<int64_t, int>& a, const std::pair<int64_t, int>& b) { return a > b; };
+    std::make_heap(heap.begin(), heap.end(), cmp);
+    for (const Job& j : jobs) {
+        std::pop_heap(heap.begin(), heap.end(), cmp);
+        heap.back().first += j.cost;
+        lists[heap.back().second].push_back(j.tile);
+        std::push_heap(heap.begin(), heap.end(), cmp);
+    }
+    std::vector<int> flat(grid + 1);
+    for (int b = 0; b < grid; ++b) flat[b + 1] = flat[b] + (int)lists[b].size();
+    for (int b = 0; b < grid; ++b) flat.insert(flat.end(), lists[b].begin(), lists[b].end());
+    if (flat.size() > h->sched_ints) return LQ_ERR_WORKSPACE;
+    if (cudaMemcpyAsync(h->sched, flat.data(), flat.size() * sizeof(int), cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess)
+        return LQ_ERR_CUDA;
+    h->sched_key = key;
+    return LQ_OK;
+}
 
-    // workspace: anchor bitmap [K/64 + 4] (a chunk past the last K-block is read whole) | x at the anchor columns [M][a_pad]
+lq_status launch_gemm_grouped(lq_handle h, const lq_problem* probs, int count, cudaStream_t stream) {
+    if (count < 1 || count > kMaxGemmGroup) return LQ_ERR_UNSUPPORTED;
+    GemmParams P;
+    GemmPrepParams Q;
+    memset(&P, 0, sizeof(P));
+    memset(&Q, 0, sizeof(Q));
+    const int fmt = probs[0].format;
+    const bool nf4 = fmt == LQ_FMT_NF4_B64;
+    P.count = count;
+    P.bf16 = probs[0].x_dtype == LQ_BF16;
+    P.status = h->status_flag;
+    // workspace per problem: anchor bitmap [K/64 + 4] (a chunk past the last K-block is read whole),
+    // all bitmaps first so one memset clears them, then x at the anchor columns [M][a_pad]
     char* ws = reinterpret_cast<char*>(h->partials);
-    const size_t bits_bytes = ((size_t)(p.K / 64 + kChunk) * 8 + 255) & ~size_t(255);
-    const size_t xa_bytes = (size_t)p.M * a_pad * 2;
-    if (bits_bytes + xa_bytes + 256 > h->partial_floats * sizeof(float)) return LQ_ERR_WORKSPACE;
-    unsigned long long* bits = reinterpret_cast<unsigned long long*>(ws);
-    uint16_t* xa = reinterpret_cast<uint16_t*>(ws + bits_bytes);
-    P.anchor_bits = reinterpret_cast<const uint32_t*>(bits);
-    if (!map_16bit(&P.xmap, p.x, (uint64_t)p.K, (uint64_t)p.M, (uint64_t)p.K, kBN)) return LQ_ERR_CUDA;
-    const bool nf4 = p.format == LQ_FMT_NF4_B64;
-    {
+    size_t used = 0, bits_total = 0;
+    int tiles = 0, max_prep = 1, prep_count = 0;
+    size_t bits_off[kMaxGemmGroup];
+    for (int i = 0; i < count; ++i) {
+        const lq_problem& p = probs[i];
+        if (p.format != fmt || (p.x_dtype == LQ_BF16) != (P.bf16 != 0)) return LQ_ERR_UNSUPPORTED;
+        bits_off[i] = bits_total;
+        bits_total += ((size_t)(p.K / 64 + kChunk) * 8 + 255) & ~size_t(255);
+    }
+    used = bits_total;
+    for (int i = 0; i < count; ++i) {
+        const lq_problem& p = probs[i];
+        GemmProb& D = P.d[i];
+        const int A = nf4 ? 0 : p.A;
+        const int a_pad = A > 0 ? (A + kBK - 1) / kBK * kBK : 0;
+        D.scales = p.scales;
+        D.offsets = p.offsets;
+        D.y = p.y;
+        D.M = p.M;
+        D.N = p.N;
+        D.K = p.K;
+        D.A = A;
+        D.a_pad = a_pad;
+        D.y_dtype = p.y_dtype;
+        D.meta_tma = p.K % 256 == 0;   // scale rows 16-byte aligned: TMA boxes; else 4-byte loads
+        D.tiles_m = (p.M + kBN - 1) / kBN;
+        D.tile_begin = tiles;
+        const int64_t t = (int64_t)D.tiles_m * ((p.N + kBM - 1) / kBM);
+        if (tiles + t > 0x7fffffffLL) return LQ_ERR_UNSUPPORTED;
+        tiles += (int)t;
+        unsigned long long* bits = reinterpret_cast<unsigned long long*>(ws + bits_off[i]);
+        D.anchor_bits = reinterpret_cast<const uint32_t*>(bits);
+        uint16_t* xa = reinterpret_cast<uint16_t*>(ws + used);
+        used += ((size_t)p.M * a_pad * 2 + 255) & ~size_t(255);
+        if (!map_16bit(&D.xmap, p.x, (uint64_t)p.K, (uint64_t)p.M, (uint64_t)p.K, kBN)) return LQ_ERR_CUDA;
         const uint64_t cbytes = (uint64_t)p.K / (nf4 ? 2 : 4);
-        if (!map_2d(&P.cmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.codes, cbytes, (uint64_t)p.N, cbytes,
+        if (!map_2d(&D.cmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.codes, cbytes, (uint64_t)p.N, cbytes,
                     kChunk * (nf4 ? 32 : 16), kBM, nf4 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B))
             return LQ_ERR_CUDA;
-    }
-    if (P.meta_tma) {
-        if (nf4) {
-            if (!map_2d(&P.smap, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, p.scales, (uint64_t)p.K / 64, (uint64_t)p.N,
-                        (uint64_t)p.K / 64, 4, kBM, CU_TENSOR_MAP_SWIZZLE_NONE))
+        if (D.meta_tma) {
+            if (nf4) {
+                if (!map_2d(&D.smap, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, p.scales, (uint64_t)p.K / 64, (uint64_t)p.N,
+                            (uint64_t)p.K / 64, 4, kBM, CU_TENSOR_MAP_SWIZZLE_NONE))
+                    return LQ_ERR_CUDA;
+            } else {
+                if (!map_2d(&D.smap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, p.scales, (uint64_t)p.K / 32, (uint64_t)p.N,
+                            (uint64_t)p.K / 32, 8, kBM, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+                    !map_2d(&D.omap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, p.offsets, (uint64_t)p.K / 32, (uint64_t)p.N,
+                            (uint64_t)p.K / 32, 8, kBM, CU_TENSOR_MAP_SWIZZLE_NONE))
+                    return LQ_ERR_CUDA;
+            }
+        }
+        if (A > 0) {
+            if (!map_16bit(&D.xamap, xa, (uint64_t)a_pad, (uint64_t)p.M, (uint64_t)a_pad, kBN)) return LQ_ERR_CUDA;
+            if (!map_16bit(&D.awmap, p.anchor_w, (uint64_t)p.ld_anchor, (uint64_t)p.N, (uint64_t)p.ld_anchor, kBM))
                 return LQ_ERR_CUDA;
-        } else {
-            if (!map_2d(&P.smap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, p.scales, (uint64_t)p.K / 32, (uint64_t)p.N,
-                        (uint64_t)p.K / 32, 8, kBM, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-                !map_2d(&P.omap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, p.offsets, (uint64_t)p.K / 32, (uint64_t)p.N,
-                        (uint64_t)p.K / 32, 8, kBM, CU_TENSOR_MAP_SWIZZLE_NONE))
-                return LQ_ERR_CUDA;
+            PrepProb& e = Q.d[prep_count++];
+            e.x = static_cast<const uint16_t*>(p.x);
+            e.anchor_idx = p.anchor_idx;
+            e.xa = xa;
+            e.bits = bits;
+            e.M = p.M;
+            e.K = p.K;
+            e.A = A;
+            e.a_pad = a_pad;
+            max_prep = (int)std::max<int64_t>(max_prep, std::max<int64_t>((int64_t)p.M * a_pad, A));
         }
     }
-    if (A > 0) {
-        if (!map_16bit(&P.xamap, xa, (uint64_t)a_pad, (uint64_t)p.M, (uint64_t)a_pad, kBN)) return LQ_ERR_CUDA;
-        if (!map_16bit(&P.awmap, p.anchor_w, (uint64_t)p.ld_anchor, (uint64_t)p.N, (uint64_t)p.ld_anchor, kBM))
-            return LQ_ERR_CUDA;
-        if (cudaMemsetAsync(bits, 0, bits_bytes, stream) != cudaSuccess) return LQ_ERR_CUDA;
-        const int64_t work = std::max<int64_t>((int64_t)p.M * a_pad, A);
-        const int grid = (int)std::min<int64_t>((work + 255) / 256, (int64_t)h->num_sms * 8);
-        gemm_prep_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(p.x), p.M, p.K, p.anchor_idx, A, a_pad,
-                                                   xa, bits);
+    if (used + 256 > h->partial_floats * sizeof(float)) return LQ_ERR_WORKSPACE;
+    P.total_tiles = tiles;
+    if (tiles == 0) return LQ_OK;
+    if (prep_count > 0) {
+        if (cudaMemsetAsync(ws, 0, bits_total, stream) != cudaSuccess) return LQ_ERR_CUDA;
+        const int gx = (int)std::min<int64_t>((max_prep + 255) / 256, (int64_t)h->num_sms * 8);
+        gemm_prep_kernel<<<dim3(gx, prep_count), 256, 0, stream>>>(Q);
         if (cudaPeekAtLastError() != cudaSuccess) return LQ_ERR_CUDA;
     }
-
     const int smem = nf4 ? GemmLayout<LQ_FMT_NF4_B64>::kSmemBytes : GemmLayout<LQ_FMT_2BIT_LM_G32>::kSmemBytes;
     if (smem > h->max_smem_optin) return LQ_ERR_UNSUPPORTED;
-    const int grid = (int)std::min<int64_t>(tiles, h->num_sms);
+    const int grid = std::min(tiles, h->num_sms);
+    if (count > 1) {
+        // problems of different lengths: balance the CTAs' K-blocks
+        const lq_status s = upload_schedule(h, P, grid, stream);
+        if (s != LQ_OK) return s;
+        P.sched_off = h->sched;
+        P.sched_tiles = h->sched + grid + 1;
+    }
     return nf4 ? launch_fmt<LQ_FMT_NF4_B64>(P, grid, stream) : launch_fmt<LQ_FMT_2BIT_LM_G32>(P, grid, stream);
 }
+
+lq_status launch_gemm(lq_handle h, const lq_problem& p, cudaStream_t stream) { return launch_gemm_grouped(h, &p, 1, stream); }
 
 }  // namespace lq

@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <vector>
+
 #include "../../include/lq.h"
 
 struct lq_handle_s {
@@ -19,11 +21,15 @@ struct lq_handle_s {
     float* partials = nullptr;          // split-K partial sums
     size_t partial_floats = 0;
     int* status_flag = nullptr;         // device word: nonzero after a bounded wait ran out
+    int* sched = nullptr;               // grouped-GEMM tile lists, kept between calls with the same shapes
+    size_t sched_ints = 0;
+    std::vector<int64_t> sched_key;     // the shapes `sched` was built for
 };
 
 namespace lq {
 
 constexpr int kMaxGroup = 16;           // problems per grouped GEMV launch
+constexpr int kMaxGemmGroup = 8;        // problems per grouped GEMM launch
 constexpr int kGemvStripRows = 64;      // output rows per GEMV thread block (4 warps x 16)
 constexpr int kGemvThreads = 128;
 
@@ -84,5 +90,6 @@ lq_status launch_gemv_regs(const GemvWorkspace& ws, const lq_problem* problems, 
 lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* problems, int count, cudaStream_t stream);
 
 lq_status launch_gemm(lq_handle h, const lq_problem& p, cudaStream_t stream);
+lq_status launch_gemm_grouped(lq_handle h, const lq_problem* problems, int count, cudaStream_t stream);
 
 }  // namespace lq

@@ -187,6 +187,19 @@ LQ_API lq_status lq_gemm(lq_handle h, int format,
                          int M, int N, int K, void* stream);
 
 /*
+ * lq_gemm_grouped — several lq_gemm problems (e.g. the seven projections of one
+ * decoder layer at prefill) in ONE persistent launch.  `problems` is a host
+ * array of `count` (1..8) entries, read before the call returns; batch must be
+ * 1 (strides ignored).  All problems share format and x_dtype; M, N, K, anchors
+ * and y_dtype may differ.  The CTAs' tile lists balance the problems' K-blocks
+ * (longest first); the lists are built on the host and kept in the handle's
+ * workspace, so the first call with new shapes waits for their upload (the
+ * stream is synchronized once) and later calls with the same shapes do not.
+ * Errors as lq_gemm; LQ_ERR_UNSUPPORTED for count > 8 or mixed format/x_dtype.
+ */
+LQ_API lq_status lq_gemm_grouped(lq_handle h, const lq_problem* problems, int count, void* stream);
+
+/*
  * lq_gemv_noalloc — lq_gemv for callers that cannot allocate device memory.
  * The paper has no counterpart to this entry point; it exists for deployment.
  *

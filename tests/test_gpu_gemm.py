@@ -112,3 +112,33 @@ def test_gemm_14b_layer_prefill_sampled(lqm, handle, fmt):
                 E = O.row_error_scale(O.dequant_nf4(dict(codes=pk["codes"][n:n + 1], absmax=pk["absmax"][n:n + 1],
                                                          N=1, K=K)), xb, "bf16")
             assert_within(y[:, n:n + 1], yr, E, TOL["bf16"], f"{fmt} {name} row {n}")
+
+
+@pytest.mark.parametrize("fmt", ["2bit", "nf4"])
+def test_gemm_grouped_mixed_shapes(lqm, handle, fmt):
+    """Problems of different N, K (and anchor counts) in one launch: each matches the oracle, and
+    bit for bit its own lq_gemm call (every tile computes the same way on whichever CTA runs it)."""
+    shapes = [(300, 200, 1088), (300, 384, 640), (300, 128, 256)]
+    mats, probs = [], []
+    for i, (M, N, K) in enumerate(shapes):
+        if fmt == "2bit":
+            p, outl = quantized_2bit(N, K, seed=40 + i)
+            w = lqm.QuantWeights.from_host(p, lqm.FMT_2BIT)
+            Weff = O.dequant_2bit(p)
+        else:
+            p, outl = quantized_nf4(N, K, seed=40 + i), None
+            w = lqm.QuantWeights.from_host(p, lqm.FMT_NF4)
+            Weff = O.dequant_nf4(p)
+        xb = x_for(M, K, "bf16", outl, seed=40 + i)
+        x = dev_x(xb, "bf16")
+        y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        mats.append((w, x, y, xb, Weff))
+        probs.append(handle.problem(w, x, y))
+    for _ in range(2):   # the second call reuses the resident schedule
+        handle.gemm_grouped(probs)
+        torch.cuda.synchronize()
+        for (w, x, y, xb, Weff) in mats:
+            yref, E = O.matmul_ref(Weff, xb, "bf16")
+            assert_within(y.cpu().numpy(), yref, E, TOL["bf16"], f"grouped {fmt}")
+            y1 = handle.gemm(w, x)
+            assert torch.equal(y1, y)
