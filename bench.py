@@ -48,6 +48,15 @@ ROTATE = 8          # distinct layer copies in HBM (8 x 90 MB > 129 MB L2)
 STACK_LAYERS = 32   # layers of the 7B stack for the tok/s equivalent
 
 
+def _traffic(key):
+    """DRAM bytes per launch from the committed ncu summary (profiles/traffic.json)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        return json.load(f).get(key)
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -388,14 +397,11 @@ def run_lq(args):
                 "roofline": {"bound": "tensor", "achieved": g2["largest"]["tflops"], "peak": bf16, "unit": "TFLOP/s",
                              "frac": round(g2["largest"]["tflops"] / bf16, 4), "peak_kind": peak_kind + " bf16 burst",
                              "kernel": "gemm_kernel<2bit> on the largest projection, timed alone",
-                             "traffic": None},
+                             "traffic": None,
+                             "layer_traffic_bytes": _traffic("gemm_14b_layer_2bit_bytes_per_launch")},
                 "frac_of_bf16_peak": {"2bit": round(g2["value"] / bf16, 4), "nf4": round(g4["value"] / bf16, 4)}}
 
-    traffic = None
-    tpath = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tpath):
-        with open(tpath) as f:
-            traffic = json.load(f).get("gemv_7b_layer_m1_bytes_per_launch")
+    traffic = _traffic("gemv_7b_layer_m1_bytes_per_launch")
 
     if rank == 0:
         cpu_v, sample = cpu_baseline(host_copy0)
@@ -410,7 +416,7 @@ def run_lq(args):
             "tok_s_32_layer_stack": round(1e3 / (ms_per_step * STACK_LAYERS), 1),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm, "unit": "GB/s",
                          "frac": round(achieved / hbm, 4), "traffic": traffic, "peak_kind": peak_kind,
-                         "kernel": "gemv_kernel<1,2bit> (one grouped launch per layer)",
+                         "kernel": "xprep_kernel + gemv_stream_kernel (one grouped call per layer; the event pair brackets both)",
                          "algorithmic_bytes_per_launch": layer_bytes},
             "cpu_baseline": {"value": round(cpu_v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
