@@ -431,6 +431,47 @@ def run_lq(args):
         dist.destroy_process_group()
 
 
+def run_case(args):
+    """One workload, three calls, nothing timed: the command line the ncu summaries in profiles/ capture."""
+    import torch
+
+    import bit_weight_quantized_dequant_gb300 as lq
+    lq.build()
+    h = lq.Handle(0)
+    if args.case == "gemv7b":
+        mats = []
+        for name, pk, xb in layer_packs(1, 0):
+            w = lq.QuantWeights.from_host(pk, lq.FMT_2BIT)
+            x = torch.from_numpy(xb).view(torch.float16).cuda()
+            y = torch.empty((1, pk["N"]), dtype=torch.float32, device="cuda")
+            mats.append((w, x, y))
+        probs = [h.problem(w, x, y) for w, x, y in mats]
+        for _ in range(3):
+            h.gemv_grouped(probs)
+    else:
+        from math import floor
+        fmt = args.case.split("-")[1]
+        mats = []
+        for i, (name, N, K) in enumerate(synth.LAYER_SHAPES["14b"]):
+            if fmt == "2bit":
+                pk = synth.random_packed_2bit(N, K, int(floor(0.035 * K)), sigma=0.02, seed=500, cfg=5, matrix_id=i)
+                w = lq.QuantWeights.from_host(pk, lq.FMT_2BIT)
+            else:
+                pk = synth.random_packed_nf4(N, K, sigma=0.02, seed=500, cfg=5, matrix_id=i)
+                w = lq.QuantWeights.from_host(pk, lq.FMT_NF4)
+            xb = synth.activations(GEMM_M, K, "bf16", synth.channel_sigma(K, synth.outlier_channels(K, 0.01, seed=500, cfg=5), 20.0),
+                                   seed=500, cfg=5, matrix_id=i)
+            x = torch.from_numpy(xb).view(torch.bfloat16).cuda()
+            y = torch.empty((GEMM_M, N), dtype=torch.bfloat16, device="cuda")
+            mats.append((w, x, y))
+        probs = [h.problem(w, x, y) for w, x, y in mats]
+        for _ in range(3):
+            h.gemm_grouped(probs)
+    torch.cuda.synchronize()
+    h.close()
+    print(json.dumps({"case": args.case, "calls": 3}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -439,10 +480,14 @@ def main():
     ap.add_argument("--impl", default="lq", choices=["lq", "reference"])
     ap.add_argument("--gemm-steps", type=int, default=20)
     ap.add_argument("--no-gemm", action="store_true")
+    ap.add_argument("--case", choices=["gemv7b", "gemm14b-2bit", "gemm14b-nf4"],
+                    help="run one workload three times, untimed (what the profiles capture)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.case:
+        run_case(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_lq(args)
