@@ -48,6 +48,14 @@ ROTATE = 8          # distinct layer copies in HBM (8 x 90 MB > 129 MB L2)
 STACK_LAYERS = 32   # layers of the 7B stack for the tok/s equivalent
 
 
+def max_over_ranks(value: float, dist, device) -> float:
+    """The slowest rank's time: every rank's replica must have finished for the job to be done."""
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def _traffic(key):
     """DRAM bytes per launch from the committed ncu summary (profiles/traffic.json)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
@@ -348,9 +356,7 @@ def run_lq(args):
     total_ms = t_all0.elapsed_time(t_all1)
     launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     if dist:
-        t = torch.tensor([total_ms], device=f"cuda:{local}")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+        total_ms = max_over_ranks(total_ms, dist, f"cuda:{local}")
     ms_per_step = total_ms / args.steps
     value = world * layer_bytes / (ms_per_step * 1e-3) / 1e9
     kern_ms = statistics.mean(launch_ms)

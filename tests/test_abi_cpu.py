@@ -107,3 +107,29 @@ def test_create_without_device_reports_error(lib):
     h = ctypes.c_void_p()
     st = L.lq_create(ctypes.byref(h), 0, 0)
     assert st in (_lq.LQ_ERR_CUDA, _lq.LQ_ERR_INVALID_ARG) and not h.value
+
+
+def test_gemm_grouped_validation(lib):
+    """lq_gemm_grouped rejects bad groups on the host, before the handle or a device is touched."""
+    L, _ = lib
+    h = _fake_handle()
+    A16 = 0x10000
+
+    def prob(fmt=1, K=256, batch=1, xdt=2):
+        p = _lq.lq_problem()
+        p.format, p.M, p.N, p.K = fmt, 256, 128, K
+        p.codes = p.scales = p.x = p.y = A16
+        p.offsets = A16 if fmt == 1 else None
+        p.x_dtype, p.y_dtype, p.batch = xdt, 0, batch
+        return p
+
+    def call(ps):
+        arr = (_lq.lq_problem * len(ps))(*ps)
+        return L.lq_gemm_grouped(h, arr, len(ps), None)
+
+    assert L.lq_gemm_grouped(h, None, 1, None) == _lq.LQ_ERR_INVALID_ARG
+    assert call([prob() for _ in range(9)]) == _lq.LQ_ERR_UNSUPPORTED          # more than 8 problems
+    assert call([prob(), prob(fmt=2)]) == _lq.LQ_ERR_UNSUPPORTED                # mixed formats
+    assert call([prob(), prob(xdt=1)]) == _lq.LQ_ERR_UNSUPPORTED                # mixed x dtypes
+    assert call([prob(batch=2)]) == _lq.LQ_ERR_UNSUPPORTED                      # batched members
+    assert call([prob(K=96)]) == _lq.LQ_ERR_UNSUPPORTED                         # the tensor-core path needs K % 64
