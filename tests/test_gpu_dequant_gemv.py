@@ -327,7 +327,7 @@ def test_errors_on_device_launch_nothing(lqm, handle):
 @pytest.mark.parametrize("kernel", ["regs", "stream"])
 @pytest.mark.parametrize("M", [1, 8, 32])
 def test_gemv_kernel_choice_same_results(lqm, handle, monkeypatch, kernel, M):
-    """The register-fed and the TMA-fed kernels both meet the bound on a K % 256 == 0 shape."""
+    """The split-K and the streaming kernels both meet the bound on a K % 256 == 0 shape."""
     monkeypatch.setenv("LQ_GEMV_KERNEL", kernel)
     N, K = 300, 3072
     p, outl = quantized_2bit(N, K, seed=50 + M)
@@ -336,3 +336,16 @@ def test_gemv_kernel_choice_same_results(lqm, handle, monkeypatch, kernel, M):
     pn = quantized_nf4(N, K, seed=60 + M)
     xn = x_for(M, K, "bf16", None, seed=60 + M)
     _gemv_check(lqm, handle, pn, lqm.FMT_NF4, xn, "bf16")
+
+
+@pytest.mark.parametrize("M", [1, 4, 16])
+def test_gemv_in_kernel_x_build(lqm, handle, monkeypatch, M):
+    """LQ_GEMV_STAGE=1: the CTAs build the fragment-ordered x in shared memory (no pre-pass)."""
+    monkeypatch.setenv("LQ_GEMV_STAGE", "1")
+    for i, (N, K) in enumerate([(300, 3072), (80, 256)]):
+        p, outl = quantized_2bit(N, K, seed=70 + M + i)
+        xb = x_for(M, K, "f16", outl, seed=70 + M + i)
+        _gemv_check(lqm, handle, p, lqm.FMT_2BIT, xb, "f16")
+        pn = quantized_nf4(N, K, seed=80 + M + i)
+        xn = x_for(M, K, "bf16", None, seed=80 + M + i)
+        _gemv_check(lqm, handle, pn, lqm.FMT_NF4, xn, "bf16")
