@@ -266,6 +266,14 @@ __device__ __forceinline__ bool next_pos(const FParams& P, Pos& q) {
     return true;
 }
 
+// Arrival count update with release and acquire semantics at GPU scope (one instruction, no
+// separate membar on either side).
+__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* p, unsigned v) {
+    unsigned old;
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
 // The warp whose range [U*w/W, U*(w+1)/W) holds unit u.
 __device__ __noinline__ int64_t owner_warp(int64_t u, int64_t W, int64_t U) { return ((u + 1) * W - 1) / U; }
 
@@ -415,15 +423,15 @@ __global__ void __launch_bounds__(kThreadsS, NT <= 2 ? LQ_STREAM_MIN_BLOCKS : 1)
                 acc[nt][e] = 0.f;
             }
         }
-        __syncwarp();
+        __syncwarp();   // orders the warp's slot stores before lane 0's release below
         unsigned last = 0;
         if (lane == 0) {
-            __threadfence();
-            const unsigned old = atomicAdd(D.cnt + blk, (unsigned)units);
+            // release: this slot is visible with the count; acquire: so are the slots counted before
+            const unsigned old = atom_add_acq_rel_gpu(D.cnt + blk, (unsigned)units);
             last = old + (unsigned)units == (unsigned)q.su;
         }
         if (__shfl_sync(0xffffffffu, last, 0)) {
-            __threadfence();
+            __syncwarp();   // lane 0's acquire orders the other lanes' slot loads too
             if (lane == 0) D.cnt[blk] = 0u;   // counts start at zero for the next launch
             const int nc = (int)(owner_warp(first_u + q.su - 1, W, P.total_units) - w0 + 1);
             finish_block(slots, nc, M, static_cast<char*>(D.y) + q.l * D.stride_y, D.N, q.rb * 16, P.y_dtype, lane);
