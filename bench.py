@@ -287,6 +287,60 @@ def gemm_layer(lq, torch, h, fmt: str, device: str, steps: int, warmup: int):
             "launches_per_layer": launches, "clocks": clk.summary()}
 
 
+QUANT_WORKLOAD = "7b decoder layer (q,k,v,o 4096x4096; gate,up 11008x4096; down 4096x11008), fp32 weights on the device"
+
+
+def quantizer_layer(lq, torch, h, device: str, reps: int = 3):
+    """Time the GPU quantizers over one 7B layer: anchors + 2-bit G=32, and NF4 block 64."""
+    from math import floor
+    g = torch.Generator(device=device)
+    g.manual_seed(77)
+    mats = []
+    for i, (name, N, K) in enumerate(synth.LAYER_SHAPES["7b"]):
+        W = torch.randn((N, K), generator=g, device=device, dtype=torch.float32) * 0.02
+        outl = synth.outlier_channels(K, 0.01, seed=77, cfg=2)
+        prof = torch.from_numpy(np.sqrt(2.0 / np.pi) * synth.channel_sigma(K, outl, 20.0)).to(device)
+        mats.append((W, prof))
+    weights = sum(W.numel() for W, _ in mats)
+    stream = torch.cuda.current_stream()
+
+    def two_bit():
+        for W, prof in mats:
+            h.quantize_2bit(W, h.select_anchors(W, profile=prof, stream=stream), stream=stream)
+
+    def nf4():
+        for W, _ in mats:
+            h.quantize_nf4(W, stream=stream)
+
+    out = {}
+    for name, fn in (("2bit", two_bit), ("nf4", nf4)):
+        fn()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        out[name] = {"ms_per_layer": round(ms, 3), "gweights_per_s": round(weights / (ms * 1e-3) / 1e9, 2),
+                     "fp32_read_gb_s": round(4 * weights / (ms * 1e-3) / 1e9, 1)}
+    # the oracle's quantizer on a row sample of the gate projection, for scale
+    from oracle import oracle as O
+    N, K = 256, 4096
+    Wh = synth.weights(N, K, 0.02, seed=77, cfg=2)
+    ai = O.select_anchors(Wh, np.ones(K))
+    t0 = time.perf_counter()
+    O.quantize_2bit(Wh, ai)
+    cpu_s = time.perf_counter() - t0
+    out["cpu_baseline"] = {"value": round(N * K / cpu_s / 1e9, 4), "unit": "Gweights/s", "cores": 1, "kind": "oracle",
+                           "sample": f"oracle 2-bit quantizer on {N}x{K} (anchors given)"}
+    out.update({"workload": QUANT_WORKLOAD, "weights_per_layer": weights,
+                "bound": "fp64 arithmetic (every decision in fp64 to match the oracle bit for bit)"})
+    return out
+
+
 def run_lq(args):
     import torch
 
@@ -407,6 +461,8 @@ def run_lq(args):
                              "layer_traffic_bytes": _traffic("gemm_14b_layer_2bit_bytes_per_launch")},
                 "frac_of_bf16_peak": {"2bit": round(g2["value"] / bf16, 4), "nf4": round(g4["value"] / bf16, 4)}}
 
+    quant = quantizer_layer(lq, torch, h, f"cuda:{local}") if not args.no_quant else None
+
     traffic = _traffic("gemv_7b_layer_m1_bytes_per_launch")
 
     if rank == 0:
@@ -430,6 +486,7 @@ def run_lq(args):
             "clocks": clk.summary(),
             "config1_batched": cfg1,
             "gemm": gemm,
+            "quantizer": quant,
         }
         print(json.dumps(line), flush=True)
     h.close()
@@ -444,7 +501,9 @@ def run_case(args):
     import bit_weight_quantized_dequant_gb300 as lq
     lq.build()
     h = lq.Handle(0)
-    if args.case == "gemv7b":
+    if args.case == "quant7b":
+        quantizer_layer(lq, torch, h, "cuda", reps=2)
+    elif args.case == "gemv7b":
         mats = []
         for name, pk, xb in layer_packs(1, 0):
             w = lq.QuantWeights.from_host(pk, lq.FMT_2BIT)
@@ -486,7 +545,8 @@ def main():
     ap.add_argument("--impl", default="lq", choices=["lq", "reference"])
     ap.add_argument("--gemm-steps", type=int, default=20)
     ap.add_argument("--no-gemm", action="store_true")
-    ap.add_argument("--case", choices=["gemv7b", "gemm14b-2bit", "gemm14b-nf4"],
+    ap.add_argument("--no-quant", action="store_true")
+    ap.add_argument("--case", choices=["gemv7b", "gemm14b-2bit", "gemm14b-nf4", "quant7b"],
                     help="run one workload three times, untimed (what the profiles capture)")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -15,7 +15,8 @@ F32, F16, BF16 = 0, 1, 2
 
 #: every entry point include/lq.h declares
 EXPORTED = ("lq_create", "lq_destroy", "lq_status_string", "lq_sync", "lq_dequant", "lq_gemv",
-            "lq_gemv_grouped", "lq_gemm", "lq_gemm_grouped", "lq_gemv_noalloc")
+            "lq_gemv_grouped", "lq_gemm", "lq_gemm_grouped", "lq_gemv_noalloc",
+            "lq_select_anchors", "lq_quantize_2bit", "lq_quantize_nf4")
 
 _LIB = None
 
@@ -79,6 +80,12 @@ def load_library(build_if_missing: bool = True):
     L.lq_gemv_grouped.restype = I
     L.lq_gemm_grouped.argtypes = [P, ctypes.POINTER(lq_problem), I, P]
     L.lq_gemm_grouped.restype = I
+    L.lq_select_anchors.argtypes = [P, P, I, I, P, I, P, P]
+    L.lq_select_anchors.restype = I
+    L.lq_quantize_2bit.argtypes = [P, P, I, I, P, I, P, P, P, P, I, P]
+    L.lq_quantize_2bit.restype = I
+    L.lq_quantize_nf4.argtypes = [P, P, I, I, P, P, P]
+    L.lq_quantize_nf4.restype = I
     _LIB = L
     return L
 
@@ -230,6 +237,61 @@ class Handle:
         st = self._lib.lq_gemv_grouped(self._h, arr, len(problems), _stream(stream))
         if st != LQ_OK:
             raise LQError(st, "lq_gemv_grouped")
+
+    # ---- quantizers (the converter step; include/lq.h gives the definitions) ----
+
+    @staticmethod
+    def _weights_arg(W):
+        import torch
+        if W.dtype != torch.float32 or W.dim() != 2 or not W.is_contiguous() or not W.is_cuda:
+            raise ValueError("W must be a contiguous fp32 [N][K] CUDA tensor")
+        return W.shape[0], W.shape[1]
+
+    def select_anchors(self, W, A=None, profile=None, stream=None):
+        """Anchor columns of W: the A largest ||W[:,c]||_2 * profile_c (ties to the lower
+        column), ascending, as an int32 CUDA tensor.  A defaults to floor(0.035 K);
+        profile is an fp64 [K] CUDA tensor (None: all ones)."""
+        import math
+        import torch
+        N, K = self._weights_arg(W)
+        A = int(math.floor(0.035 * K)) if A is None else int(A)
+        idx = torch.empty(max(A, 0), dtype=torch.int32, device=W.device)
+        if profile is not None and (profile.dtype != torch.float64 or profile.numel() != K or not profile.is_contiguous()):
+            raise ValueError("profile must be a contiguous fp64 [K] tensor")
+        st = self._lib.lq_select_anchors(self._h, _ptr(W), N, K, _ptr(profile), A, _ptr(idx) if A > 0 else None,
+                                         _stream(stream))
+        if st != LQ_OK:
+            raise LQError(st, "lq_select_anchors")
+        return idx
+
+    def quantize_2bit(self, W, anchor_idx=None, ld_anchor=None, stream=None) -> QuantWeights:
+        """The 2-bit Lloyd-Max G=32 quantizer of W (fp32 [N][K] on the device), with the given
+        anchor columns (int32 CUDA tensor, ascending) kept in binary16."""
+        import torch
+        N, K = self._weights_arg(W)
+        A = 0 if anchor_idx is None else int(anchor_idx.numel())
+        ld = (int(ld_anchor) if ld_anchor is not None else max(8, (A + 7) // 8 * 8)) if A > 0 else 0
+        dev = W.device
+        codes = torch.empty((N, K // 4), dtype=torch.uint8, device=dev)
+        scales = torch.empty((N, K // 32), dtype=torch.float16, device=dev)
+        offsets = torch.empty((N, K // 32), dtype=torch.float16, device=dev)
+        anchor_w = torch.empty((N, ld), dtype=torch.float16, device=dev) if A > 0 else None
+        st = self._lib.lq_quantize_2bit(self._h, _ptr(W), N, K, _ptr(anchor_idx) if A > 0 else None, A, _ptr(codes),
+                                        _ptr(scales), _ptr(offsets), _ptr(anchor_w), ld, _stream(stream))
+        if st != LQ_OK:
+            raise LQError(st, "lq_quantize_2bit")
+        return QuantWeights(FMT_2BIT, N, K, codes, scales, offsets, anchor_idx if A > 0 else None, anchor_w, A, ld)
+
+    def quantize_nf4(self, W, stream=None) -> QuantWeights:
+        """The NF4 block-64 quantizer of W (fp32 [N][K] on the device)."""
+        import torch
+        N, K = self._weights_arg(W)
+        codes = torch.empty((N, K // 2), dtype=torch.uint8, device=W.device)
+        absmax = torch.empty((N, max(K // 64, 1)), dtype=torch.float32, device=W.device)
+        st = self._lib.lq_quantize_nf4(self._h, _ptr(W), N, K, _ptr(codes), _ptr(absmax), _stream(stream))
+        if st != LQ_OK:
+            raise LQError(st, "lq_quantize_nf4")
+        return QuantWeights(FMT_NF4, N, K, codes, absmax)
 
     def gemm_grouped(self, problems, stream=None):
         """Several prefill products (same format and x dtype) in one tensor-core launch."""

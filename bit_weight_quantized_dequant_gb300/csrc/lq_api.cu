@@ -299,6 +299,50 @@ LQ_API lq_status lq_gemm_grouped(lq_handle h, const lq_problem* problems, int co
     return lq::launch_gemm_grouped(h, problems, count, st);
 }
 
+// ---- quantizers ------------------------------------------------------------------
+
+LQ_API lq_status lq_select_anchors(lq_handle h, const float* W, int N, int K, const double* profile, int A,
+                                   int32_t* anchor_idx, void* stream) {
+    if (!h || !W || N < 1 || K < 1 || A < 0 || A > K) return LQ_ERR_INVALID_ARG;
+    if (A > 0 && !anchor_idx) return LQ_ERR_INVALID_ARG;
+    if (!aligned16(W) || (profile && !aligned16(profile)) || (anchor_idx && !aligned16(anchor_idx)))
+        return LQ_ERR_ALIGNMENT;
+    DeviceGuard guard(h->device);
+    if (!guard.ok) return LQ_ERR_CUDA;
+    return lq::launch_select_anchors(h, W, N, K, profile, A, anchor_idx, static_cast<cudaStream_t>(stream));
+}
+
+LQ_API lq_status lq_quantize_2bit(lq_handle h, const float* W, int N, int K, const int32_t* anchor_idx, int A,
+                                  uint8_t* codes, uint16_t* scales, uint16_t* offsets, uint16_t* anchor_w,
+                                  int ld_anchor, void* stream) {
+    if (!h || !W || !codes || !scales || !offsets) return LQ_ERR_INVALID_ARG;
+    if (N < 1 || K < 1 || K % 32 != 0 || A < 0 || A > K) return LQ_ERR_INVALID_ARG;
+    if (!aligned16(W) || !aligned16(codes) || !aligned16(scales) || !aligned16(offsets)) return LQ_ERR_ALIGNMENT;
+    if (A > 0) {
+        if (!anchor_idx || !anchor_w || ld_anchor < A) return LQ_ERR_INVALID_ARG;
+        if (!aligned16(anchor_idx) || !aligned16(anchor_w) || ld_anchor % 8 != 0) return LQ_ERR_ALIGNMENT;
+    } else if (anchor_w && (ld_anchor < 0 || ld_anchor % 8 != 0 || !aligned16(anchor_w))) {
+        return LQ_ERR_ALIGNMENT;
+    }
+    DeviceGuard guard(h->device);
+    if (!guard.ok) return LQ_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    lq_status s = check_anchor_order(anchor_idx, A, K, st);
+    if (s != LQ_OK) return s;
+    return lq::launch_quantize_2bit(h, W, N, K, anchor_idx, A, codes, scales, offsets, anchor_w, anchor_w ? ld_anchor : 0,
+                                    st);
+}
+
+LQ_API lq_status lq_quantize_nf4(lq_handle h, const float* W, int N, int K, uint8_t* codes, float* absmax,
+                                 void* stream) {
+    if (!h || !W || !codes || !absmax) return LQ_ERR_INVALID_ARG;
+    if (N < 1 || K < 1 || K % 64 != 0) return LQ_ERR_INVALID_ARG;
+    if (!aligned16(W) || !aligned16(codes) || !aligned16(absmax)) return LQ_ERR_ALIGNMENT;
+    DeviceGuard guard(h->device);
+    if (!guard.ok) return LQ_ERR_CUDA;
+    return lq::launch_quantize_nf4(W, N, K, codes, absmax, static_cast<cudaStream_t>(stream));
+}
+
 // ---- the allocation-free GEMV entry point ---------------------------------------
 //
 // Scratch for split-K partial sums and arrival counters lives in this file-scope

@@ -90,6 +90,13 @@ lq_status launch_gemv_regs(const GemvWorkspace& ws, const lq_problem* problems, 
 lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* problems, int count, cudaStream_t stream);
 
 lq_status launch_gemm(lq_handle h, const lq_problem& p, cudaStream_t stream);
+
+lq_status launch_select_anchors(lq_handle h, const float* W, int N, int K, const double* profile, int A,
+                                int32_t* anchor_idx, cudaStream_t stream);
+lq_status launch_quantize_2bit(lq_handle h, const float* W, int N, int K, const int32_t* anchor_idx, int A,
+                               uint8_t* codes, uint16_t* scales, uint16_t* offsets, uint16_t* anchor_w, int ld_anchor,
+                               cudaStream_t stream);
+lq_status launch_quantize_nf4(const float* W, int N, int K, uint8_t* codes, float* absmax, cudaStream_t stream);
 lq_status launch_gemm_grouped(lq_handle h, const lq_problem* problems, int count, cudaStream_t stream);
 
 }  // namespace lq

@@ -229,6 +229,67 @@ LQ_API lq_status lq_gemv_noalloc(int format,
                                  const void* x, int x_dtype, void* y, int y_dtype,
                                  int M, int N, int K, void* stream);
 
+/* ---- Quantizers: the converter step that produces the formats above ----------
+ *
+ * These run the quantizers of the formats' definitions on the GPU, so that a caller
+ * with fp32 weights in device memory can produce the stored formats in place.  Every
+ * output is deterministic and equal bit for bit to an fp64 evaluation of the
+ * definitions below with sums in a fixed pairwise order (eight interleaved partial
+ * sums along a group, row by row down a column).  W is fp32 [N][K] row-major, finite.
+ * Ownership, asynchrony, device and error rules are the shared ones; the selection
+ * and the 2-bit quantizer use the handle's workspace (K doubles, K/8 bytes).
+ */
+
+/*
+ * lq_select_anchors — outlier anchor columns (otf-llm 4.0.1 README, section 4):
+ *     score_c = sqrt(sum_n W[n][c]^2) * profile[c]          (fp64)
+ * the A largest scores, ties to the lower column, written to anchor_idx[A]
+ * (int32, device) in ascending column order.  profile: fp64 [K] in device memory,
+ * non-negative (mean |X_c| of a calibration profile), or NULL for all ones.  The
+ * README keeps the top 3.5 %: A = floor(0.035 * K).  0 <= A <= K; A = 0 launches
+ * nothing.  Errors: LQ_ERR_INVALID_ARG (shape, NULL), LQ_ERR_ALIGNMENT (W, profile
+ * or anchor_idx not 16-byte aligned), LQ_ERR_WORKSPACE (K doubles do not fit).
+ */
+LQ_API lq_status lq_select_anchors(lq_handle h, const float* W, int N, int K, const double* profile, int A,
+                                   int32_t* anchor_idx, void* stream);
+
+/*
+ * lq_quantize_2bit — the 2-bit Lloyd-Max G = 32 quantizer (otf-llm 4.0.1 README,
+ * sections 2-4).  For each row n and group g (columns 32g..32g+31), with V the
+ * group's columns that are not anchors:
+ *     mu = mean(W_V), sd = population std of W_V           (fp64)
+ *     z  = (W - mu) / sd, or 0 when sd == 0
+ *     q  = argmin_k |z - C_k|, C = {-1.52, -0.45, 0.45, 1.52}, lowest k on a tie
+ *     S  = sum (W - mu)(C_q - mean C_q) / (sum (C_q - mean C_q)^2 + 1e-12)
+ *     Z  = mu - S * mean C_q
+ *     scales[n][g] = binary16(S), offsets[n][g] = binary16(Z)   (round to nearest even)
+ * A group whose columns are all anchors stores S = Z = 0.  Anchor columns store
+ * code 0, and anchor_w[n][a] = binary16(W[n][anchor_idx[a]]) for a < A, 0 up to
+ * ld_anchor.  Outputs use the storage layout of LQ_FMT_2BIT_LM_G32 (codes
+ * [N][K/4], scales/offsets [N][K/32], anchor_w [N][ld_anchor]).  anchor_idx:
+ * strictly increasing columns in [0, K) (LQ_VALIDATE=1 checks them on the host;
+ * otherwise a column outside [0, K) is ignored).  Rules: K % 32 == 0, N >= 1,
+ * 0 <= A <= K, ld_anchor >= A and % 8 == 0 when A > 0 (anchor_idx and anchor_w may
+ * be NULL when A = 0).  Errors: LQ_ERR_INVALID_ARG, LQ_ERR_ALIGNMENT,
+ * LQ_ERR_WORKSPACE.
+ */
+LQ_API lq_status lq_quantize_2bit(lq_handle h, const float* W, int N, int K, const int32_t* anchor_idx, int A,
+                                  uint8_t* codes, uint16_t* scales, uint16_t* offsets, uint16_t* anchor_w,
+                                  int ld_anchor, void* stream);
+
+/*
+ * lq_quantize_nf4 — NF4 block-64 quantizer (AirQuant README, "Fundamentacao
+ * Teorica" item 2; the QLoRA NormalFloat levels T):
+ *     absmax_b = max |w| over the block (fp32, exact)
+ *     q = argmin_k |w / absmax_b - T[k]| in fp64, lowest k on a tie (0 when absmax_b = 0
+ *         gives the index of the level 0)
+ * Outputs use the LQ_FMT_NF4_B64 layout: codes uint8 [N][K/2], absmax float32
+ * [N][K/64].  Rules: K % 64 == 0, N >= 1.  Errors: LQ_ERR_INVALID_ARG,
+ * LQ_ERR_ALIGNMENT.
+ */
+LQ_API lq_status lq_quantize_nf4(lq_handle h, const float* W, int N, int K, uint8_t* codes, float* absmax,
+                                 void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -133,3 +133,25 @@ def test_gemm_grouped_validation(lib):
     assert call([prob(), prob(xdt=1)]) == _lq.LQ_ERR_UNSUPPORTED                # mixed x dtypes
     assert call([prob(batch=2)]) == _lq.LQ_ERR_UNSUPPORTED                      # batched members
     assert call([prob(K=96)]) == _lq.LQ_ERR_UNSUPPORTED                         # the tensor-core path needs K % 64
+
+
+def test_quantizer_validation(lib):
+    """The quantizer entry points reject bad shapes, pointers and alignment on the host."""
+    L, _ = lib
+    h = _fake_handle()
+    A16 = 0x10000
+    INV, ALN = _lq.LQ_ERR_INVALID_ARG, _lq.LQ_ERR_ALIGNMENT
+    assert L.lq_select_anchors(None, A16, 4, 64, None, 2, A16, None) == INV
+    assert L.lq_select_anchors(h, A16, 4, 64, None, 65, A16, None) == INV        # A > K
+    assert L.lq_select_anchors(h, A16, 4, 64, None, 2, None, None) == INV        # no output
+    assert L.lq_select_anchors(h, A16 + 4, 4, 64, None, 2, A16, None) == ALN
+    assert L.lq_select_anchors(h, A16, 4, 64, A16 + 8, 2, A16, None) == ALN      # profile
+    assert L.lq_quantize_2bit(h, A16, 4, 48, None, 0, A16, A16, A16, None, 0, None) == INV    # K % 32
+    assert L.lq_quantize_2bit(h, A16, 4, 64, None, 2, A16, A16, A16, None, 8, None) == INV    # anchors, no pointers
+    assert L.lq_quantize_2bit(h, A16, 4, 64, A16, 2, A16, A16, A16, A16, 1, None) == INV      # ld_anchor < A
+    assert L.lq_quantize_2bit(h, A16, 4, 64, A16, 2, A16, A16, A16, A16, 12, None) == ALN     # ld_anchor % 8
+    assert L.lq_quantize_2bit(h, A16, 4, 64, None, 0, A16 + 8, A16, A16, None, 0, None) == ALN
+    assert L.lq_quantize_2bit(h, A16, 0, 64, None, 0, A16, A16, A16, None, 0, None) == INV
+    assert L.lq_quantize_nf4(h, A16, 4, 96, A16, A16, None) == INV                # K % 64
+    assert L.lq_quantize_nf4(h, A16, 4, 64, A16, A16 + 4, None) == ALN
+    assert L.lq_quantize_nf4(None, A16, 4, 64, A16, A16, None) == INV
