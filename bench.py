@@ -341,6 +341,79 @@ def quantizer_layer(lq, torch, h, device: str, reps: int = 3):
     return out
 
 
+STREAM_LAYERS = 32
+
+
+def stream_stack(lq, torch, h, device: str, M: int = 1, reps: int = 3):
+    """A 32-layer 7B stack held in pinned host memory, streamed through two device slots
+    (lq_stream_run): tokens/s of one decode pass, the host-to-device rate it reached, and
+    the plain copy rate of the same bytes for comparison."""
+    distinct = 4
+    blobs, xs = [], None
+    for c in range(distinct):
+        packs = layer_packs(M, 100 + c)
+        blob, meta = lq.pack_layer([pk for _, pk, _ in packs], lq.FMT_2BIT)
+        blobs.append((blob, meta))
+        if xs is None:
+            xs = [torch.from_numpy(xb).view(torch.float16).to(device) for _, _, xb in packs]
+            ys = [torch.empty((M, pk["N"]), dtype=torch.float32, device=device) for _, pk, _ in packs]
+    layer_bytes = max(b.nbytes for b, _ in blobs)
+    stride = (layer_bytes + 4095) // 4096 * 4096
+    host = torch.empty(STREAM_LAYERS * stride, dtype=torch.uint8).pin_memory()
+    hv = host.numpy()
+    for l in range(STREAM_LAYERS):
+        b = blobs[l % distinct][0]
+        hv[l * stride:l * stride + b.nbytes] = b
+    ls = lq.LayerStream(h, stride)
+    meta = blobs[0][1]
+    probs = [ls.problem(meta[i], lq.FMT_2BIT, xs[i], ys[i]) for i in range(len(meta))]
+    stream = torch.cuda.current_stream()
+    ls.run(host, stride, layer_bytes, STREAM_LAYERS, probs, stream=stream)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        ls.run(host, stride, layer_bytes, STREAM_LAYERS, probs, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    # the copies alone, the same bytes in the same sized pieces
+    dev_buf = torch.empty(layer_bytes, dtype=torch.uint8, device=device)
+    c0 = torch.cuda.Event(enable_timing=True)
+    c1 = torch.cuda.Event(enable_timing=True)
+    c0.record(stream)
+    for l in range(STREAM_LAYERS):
+        dev_buf.copy_(host[l * stride:l * stride + layer_bytes], non_blocking=True)
+    c1.record(stream)
+    torch.cuda.synchronize()
+    copy_ms = c0.elapsed_time(c1)
+    # the kernels reading the pinned host bytes themselves (no copies)
+    direct = None
+    try:
+        ls.run_direct(host, stride, layer_bytes, STREAM_LAYERS, probs, stream=stream)
+        torch.cuda.synchronize()
+        d0 = torch.cuda.Event(enable_timing=True)
+        d1 = torch.cuda.Event(enable_timing=True)
+        d0.record(stream)
+        for _ in range(reps):
+            ls.run_direct(host, stride, layer_bytes, STREAM_LAYERS, probs, stream=stream)
+        d1.record(stream)
+        torch.cuda.synchronize()
+        dms = d0.elapsed_time(d1) / reps
+        direct = {"ms_per_token": round(dms, 3), "tok_s": round(1e3 / dms, 1),
+                  "host_read_gb_s": round(STREAM_LAYERS * layer_bytes / (dms * 1e-3) / 1e9, 1)}
+    except lq.LQError as e:
+        direct = {"unavailable": str(e)}
+    ls.close()
+    weight_bytes = STREAM_LAYERS * layer_bytes
+    return {"workload": f"{STREAM_LAYERS}-layer 7B stack, 2-bit + anchors, M={M}, weights in pinned host memory",
+            "ms_per_token": round(ms, 3), "tok_s": round(1e3 / ms, 1),
+            "h2d_gb_s_achieved": round(weight_bytes / (ms * 1e-3) / 1e9, 1),
+            "plain_copy_gb_s": round(weight_bytes / (copy_ms * 1e-3) / 1e9, 1),
+            "layer_bytes": layer_bytes, "distinct_layers": distinct, "direct_host_read": direct}
+
+
 def run_lq(args):
     import torch
 
@@ -462,6 +535,9 @@ def run_lq(args):
                 "frac_of_bf16_peak": {"2bit": round(g2["value"] / bf16, 4), "nf4": round(g4["value"] / bf16, 4)}}
 
     quant = quantizer_layer(lq, torch, h, f"cuda:{local}") if not args.no_quant else None
+    streamed = stream_stack(lq, torch, h, f"cuda:{local}") if not args.no_stream else None
+    if streamed:
+        streamed["resident_tok_s"] = round(1e3 / (ms_per_step * STACK_LAYERS), 1)
 
     traffic = _traffic("gemv_7b_layer_m1_bytes_per_launch")
 
@@ -487,6 +563,7 @@ def run_lq(args):
             "config1_batched": cfg1,
             "gemm": gemm,
             "quantizer": quant,
+            "layer_streaming": streamed,
         }
         print(json.dumps(line), flush=True)
     h.close()
@@ -546,6 +623,7 @@ def main():
     ap.add_argument("--gemm-steps", type=int, default=20)
     ap.add_argument("--no-gemm", action="store_true")
     ap.add_argument("--no-quant", action="store_true")
+    ap.add_argument("--no-stream", action="store_true")
     ap.add_argument("--case", choices=["gemv7b", "gemm14b-2bit", "gemm14b-nf4", "quant7b"],
                     help="run one workload three times, untimed (what the profiles capture)")
     args = ap.parse_args()

@@ -16,7 +16,8 @@ F32, F16, BF16 = 0, 1, 2
 #: every entry point include/lq.h declares
 EXPORTED = ("lq_create", "lq_destroy", "lq_status_string", "lq_sync", "lq_dequant", "lq_gemv",
             "lq_gemv_grouped", "lq_gemm", "lq_gemm_grouped", "lq_gemv_noalloc",
-            "lq_select_anchors", "lq_quantize_2bit", "lq_quantize_nf4")
+            "lq_select_anchors", "lq_quantize_2bit", "lq_quantize_nf4",
+            "lq_stream_create", "lq_stream_run", "lq_stream_destroy", "lq_stream_run_direct")
 
 _LIB = None
 
@@ -86,6 +87,14 @@ def load_library(build_if_missing: bool = True):
     L.lq_quantize_2bit.restype = I
     L.lq_quantize_nf4.argtypes = [P, P, I, I, P, P, P]
     L.lq_quantize_nf4.restype = I
+    L.lq_stream_create.argtypes = [ctypes.POINTER(P), P, S]
+    L.lq_stream_create.restype = I
+    L.lq_stream_run.argtypes = [P, P, S, S, I, ctypes.POINTER(lq_problem), I, ctypes.c_int64, P]
+    L.lq_stream_run.restype = I
+    L.lq_stream_destroy.argtypes = [P]
+    L.lq_stream_destroy.restype = I
+    L.lq_stream_run_direct.argtypes = [P, P, S, S, I, ctypes.POINTER(lq_problem), I, ctypes.c_int64, P]
+    L.lq_stream_run_direct.restype = I
     _LIB = L
     return L
 
@@ -299,3 +308,101 @@ class Handle:
         st = self._lib.lq_gemm_grouped(self._h, arr, len(problems), _stream(stream))
         if st != LQ_OK:
             raise LQError(st, "lq_gemm_grouped")
+
+
+# ---- layer streaming (weights in host memory, two device slots) --------------------
+
+def pack_layer(packed: list, fmt: int, align: int = 256):
+    """Lay one layer's packed host dicts (the layout of QuantWeights.from_host) out as one
+    byte blob.  Returns (blob as uint8 numpy array, per-matrix dict of byte offsets)."""
+    import numpy as np
+    parts, offs = [], []
+    pos = 0
+
+    def add(a):
+        nonlocal pos
+        b = np.ascontiguousarray(a).view(np.uint8).reshape(-1)
+        pad = (-pos) % align
+        if pad:
+            parts.append(np.zeros(pad, np.uint8))
+            pos += pad
+        o = pos
+        parts.append(b)
+        pos += b.nbytes
+        return o
+
+    for p in packed:
+        d = {"codes": add(p["codes"]), "N": int(p["N"]), "K": int(p["K"]), "A": 0, "ld_anchor": 0}
+        if fmt == FMT_2BIT:
+            d["scales"] = add(p["scales"])
+            d["offsets"] = add(p["offsets"])
+            A = int(p["A"])
+            d["A"], d["ld_anchor"] = A, (int(p["ld_anchor"]) if A > 0 else 0)
+            d["anchor_idx"] = add(p["anchor_idx"]) if A > 0 else 0
+            d["anchor_w"] = add(p["anchor_w"]) if A > 0 else 0
+        else:
+            d["scales"] = add(p["absmax"])
+            d["offsets"] = d["anchor_idx"] = d["anchor_w"] = 0
+        offs.append(d)
+    pad = (-pos) % align
+    if pad:
+        parts.append(np.zeros(pad, np.uint8))
+    return np.concatenate(parts), offs
+
+
+class LayerStream:
+    """A decode pass over a layer stack whose packed weights live in (pinned) host memory:
+    layer l+1 is copied into one of two device slots while layer l computes."""
+
+    def __init__(self, handle: Handle, slot_bytes: int):
+        self._lib = handle._lib
+        self._handle = handle
+        s = ctypes.c_void_p()
+        st = self._lib.lq_stream_create(ctypes.byref(s), handle.raw, int(slot_bytes))
+        if st != LQ_OK:
+            raise LQError(st, "lq_stream_create")
+        self._s = s
+
+    @staticmethod
+    def problem(meta: dict, fmt: int, x, y) -> lq_problem:
+        """One matrix of a layer: weight fields are byte offsets from pack_layer's `meta`."""
+        p = lq_problem()
+        p.format, p.M, p.N, p.K = fmt, int(x.shape[-2]), meta["N"], meta["K"]
+        p.codes, p.scales, p.offsets = meta["codes"], meta["scales"], meta["offsets"]
+        p.anchor_idx, p.anchor_w = meta["anchor_idx"], meta["anchor_w"]
+        p.A, p.ld_anchor = meta["A"], meta["ld_anchor"]
+        p.x, p.x_dtype, p.y, p.y_dtype = _ptr(x), _dtype_code(x), _ptr(y), _dtype_code(y)
+        p.batch = 1
+        return p
+
+    def run(self, host_layers, host_stride: int, layer_bytes: int, L: int, problems, y_layer_stride: int = 0,
+            stream=None):
+        """host_layers: a uint8 CPU tensor (pinned for overlap) holding L layers at host_stride bytes."""
+        arr = (lq_problem * len(problems))(*problems)
+        st = self._lib.lq_stream_run(self._s, int(host_layers.data_ptr()), int(host_stride), int(layer_bytes), int(L),
+                                     arr, len(problems), int(y_layer_stride), _stream(stream))
+        if st != LQ_OK:
+            raise LQError(st, "lq_stream_run")
+
+    def run_direct(self, host_layers, host_stride: int, layer_bytes: int, L: int, problems, y_layer_stride: int = 0,
+                   stream=None):
+        """The same pass with the kernels reading the pinned host bytes directly (no copies)."""
+        arr = (lq_problem * len(problems))(*problems)
+        st = self._lib.lq_stream_run_direct(self._handle.raw, int(host_layers.data_ptr()), int(host_stride),
+                                            int(layer_bytes), int(L), arr, len(problems), int(y_layer_stride),
+                                            _stream(stream))
+        if st != LQ_OK:
+            raise LQError(st, "lq_stream_run_direct")
+
+    def close(self):
+        if getattr(self, "_s", None):
+            st = self._lib.lq_stream_destroy(self._s)
+            self._s = None
+            if st != LQ_OK:
+                raise LQError(st, "lq_stream_destroy")
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -283,6 +283,9 @@ __global__ void anchor_weights_kernel(const float* __restrict__ W, int N, int K,
 
 __global__ void __launch_bounds__(256) quantize_nf4_kernel(const float* __restrict__ W, int N, int K,
                                                            uint8_t* __restrict__ codes, float* __restrict__ absmax) {
+    __shared__ double T[16];   // the levels in fp64, ascending
+    if (threadIdx.x < 16) T[threadIdx.x] = (double)kNF4[threadIdx.x];
+    __syncthreads();
     const int lane = threadIdx.x & 31;
     const int64_t blk = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int per_row = K / 64;
@@ -294,19 +297,18 @@ __global__ void __launch_bounds__(256) quantize_nf4_kernel(const float* __restri
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
     const double am = (double)m;
+    // argmin_k |r - T[k]| (lowest k on a tie) from the two levels around r: |r| <= 1 = T[15] = -T[0],
+    // and every other level is at least 0.07 further from r than the nearer of the two, far more than
+    // the fp64 rounding of a distance, so no other level can reach (or tie) their minimum.
     auto code = [&](float x) {
         const double r = am > 0.0 ? __ddiv_rn((double)x, am) : 0.0;
-        int best = 0;
-        double bd = fabs(__dsub_rn(r, (double)kNF4[0]));
+        int i = 0;   // the largest i with T[i] <= r
 #pragma unroll
-        for (int k = 1; k < 16; ++k) {
-            const double d = fabs(__dsub_rn(r, (double)kNF4[k]));
-            if (d < bd) {
-                bd = d;
-                best = k;
-            }
-        }
-        return (uint32_t)best;
+        for (int step = 8; step >= 1; step >>= 1)
+            if (T[i + step] <= r) i += step;
+        if (i == 15) return 15u;
+        const double d0 = fabs(__dsub_rn(r, T[i])), d1 = fabs(__dsub_rn(r, T[i + 1]));
+        return (uint32_t)(d1 < d0 ? i + 1 : i);
     };
     codes[n * (K / 2) + 32 * b + lane] = (uint8_t)(code(w.x) | (code(w.y) << 4));
     if (lane == 0) absmax[n * per_row + b] = m;

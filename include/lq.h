@@ -290,6 +290,51 @@ LQ_API lq_status lq_quantize_2bit(lq_handle h, const float* W, int N, int K, con
 LQ_API lq_status lq_quantize_nf4(lq_handle h, const float* W, int N, int K, uint8_t* codes, float* absmax,
                                  void* stream);
 
+/* ---- Layer streaming: decode over a stack whose weights live in host memory ------
+ *
+ * The airllm README ("Efficient Memory Usage") runs models larger than GPU memory by
+ * loading one layer at a time; the otf-llm README (section 1) notes that decode
+ * reads every weight once per token.  An lq_layer_stream holds two device slots of
+ * slot_bytes each, a copy stream and events.  lq_stream_run runs the L layers of a
+ * stack in order on `stream`:
+ *   - layer l's packed weights are the layer_bytes bytes at
+ *     host_layers + l * host_stride (host memory; pinned memory makes the copies
+ *     asynchronous and lets them overlap the computation);
+ *   - they are copied (one cudaMemcpyAsync) into slot l % 2 on the object's copy
+ *     stream, after the layer that used that slot before (l - 2) has finished, so the
+ *     copy of layer l runs while layer l - 1 computes;
+ *   - layer l then runs lq_gemv_grouped(problems) on `stream` against its slot.
+ * `problems` (count <= 16, batch 1) describe one layer: their codes, scales,
+ * offsets, anchor_idx and anchor_w fields hold BYTE OFFSETS into the layer's bytes
+ * (cast to pointers; each 16-byte aligned and inside layer_bytes); x and y are device
+ * pointers; layer l writes y at y + l * y_layer_stride bytes (0: every layer writes
+ * the same y).  Every layer has the same problem list, as in a decoder stack.
+ * lq_stream_create allocates the slots (the one allocating call besides
+ * lq_create); lq_stream_destroy waits for the copy stream and frees them.  A stream
+ * object serves one pass at a time; its handle's workspace rules apply.
+ * Errors: LQ_ERR_INVALID_ARG (shapes, offsets outside the layer),
+ * LQ_ERR_ALIGNMENT, LQ_ERR_WORKSPACE (layer_bytes > slot_bytes), LQ_ERR_UNSUPPORTED
+ * (count > 16), then those of lq_gemv_grouped; LQ_ERR_CUDA from the runtime.
+ */
+typedef struct lq_layer_stream_s* lq_layer_stream;
+
+LQ_API lq_status lq_stream_create(lq_layer_stream* out, lq_handle h, size_t slot_bytes);
+LQ_API lq_status lq_stream_run(lq_layer_stream s, const void* host_layers, size_t host_stride, size_t layer_bytes,
+                               int L, const lq_problem* problems, int count, int64_t y_layer_stride, void* stream);
+LQ_API lq_status lq_stream_destroy(lq_layer_stream s);
+
+/*
+ * lq_stream_run_direct — the same pass with no copies and no slots: the GEMV kernels
+ * read each layer's weights straight from host memory over the CPU-GPU link.
+ * host_layers must be pinned memory with a device mapping that covers the whole
+ * stack (checked with cudaPointerGetAttributes at its first and last byte; otherwise
+ * LQ_ERR_UNSUPPORTED and nothing is launched).  Other arguments and errors are those
+ * of lq_stream_run.
+ */
+LQ_API lq_status lq_stream_run_direct(lq_handle h, const void* host_layers, size_t host_stride, size_t layer_bytes,
+                                      int L, const lq_problem* problems, int count, int64_t y_layer_stride,
+                                      void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -155,3 +155,13 @@ def test_quantizer_validation(lib):
     assert L.lq_quantize_nf4(h, A16, 4, 96, A16, A16, None) == INV                # K % 64
     assert L.lq_quantize_nf4(h, A16, 4, 64, A16, A16 + 4, None) == ALN
     assert L.lq_quantize_nf4(None, A16, 4, 64, A16, A16, None) == INV
+
+
+def test_stream_null_arguments(lib):
+    """lq_stream_* reject a missing object or handle without touching a device."""
+    L, _ = lib
+    out = ctypes.c_void_p()
+    assert L.lq_stream_create(ctypes.byref(out), None, 1 << 20) == _lq.LQ_ERR_INVALID_ARG
+    assert L.lq_stream_create(None, _fake_handle(), 1 << 20) == _lq.LQ_ERR_INVALID_ARG
+    assert L.lq_stream_run(None, 0x10000, 256, 256, 1, None, 1, 0, None) == _lq.LQ_ERR_INVALID_ARG
+    assert L.lq_stream_destroy(None) == _lq.LQ_OK

@@ -135,6 +135,9 @@ def test_quantize_then_dequant_and_gemv(lqm, handle):
 def test_quantize_nf4_bit_exact(lqm, handle, N, K):
     W = synth.weights(N, K, 0.02, seed=7, cfg=3, matrix_id=K, big_frac=0.001, big_mult=10.0)
     W[1, 64:128] = 0.0                        # absmax 0: every code is the index of level 0
+    T = O.nf4_table()
+    mids = ((T[:-1].astype(np.float64) + T[1:]) / 2).astype(np.float32)
+    W[2, :64] = np.concatenate([[1.0], T, mids, -mids, 0.5 * T, [0.0]])   # levels, (near-)midpoints; absmax 1
     ref = O.quantize_nf4(W)
     got = handle.quantize_nf4(dev(W))
     torch.cuda.synchronize()
