@@ -223,9 +223,24 @@ def config1_batched(lq, torch, h, device: str, steps: int, warmup: int):
     e1.record(stream)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
+    # one weight set per call: the latency of a single small call, launches back to back
+    one = synth.random_packed_2bit(N, K, A, seed=1, cfg=1)
+    w1 = lq.QuantWeights.from_host(one, lq.FMT_2BIT, device=device)
+    x1 = x[0].clone()
+    y1 = torch.empty((1, N), dtype=torch.float32, device=device)
+    for _ in range(warmup):
+        h.gemv(w1, x1, y1, stream=stream)
+    torch.cuda.synchronize()
+    calls = 200
+    e0.record(stream)
+    for _ in range(calls):
+        h.gemv(w1, x1, y1, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    single_us = e0.elapsed_time(e1) / calls * 1e3
     return {"workload": f"512x256 single linear, 2-bit G=32 + 8 fp16 anchors, M=1, {L} distinct weight sets in one launch",
             "value": round(L * per_set / (ms * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_launch": round(ms, 4),
-            "bytes_per_launch": L * per_set}
+            "bytes_per_launch": L * per_set, "single_call_us": round(single_us, 2)}
 
 
 GEMM_M = 2048

@@ -72,19 +72,23 @@ __device__ __forceinline__ uint16_t half_bits_rn(double v) { return __half_as_us
 // ---- anchor selection -------------------------------------------------------------
 
 // score[c] = sqrt(sum_n W[n][c]^2) * profile[c] (profile NULL: 1).  W is fp32 [N][K].
-__global__ void __launch_bounds__(256) anchor_score_kernel(const float* __restrict__ W, int N, int K,
-                                                           const double* __restrict__ profile, double* score) {
+// One thread per column: the sum must run row by row, so parallelism comes from the
+// columns and from keeping 32 rows of loads in flight per thread.
+constexpr int kScoreThreads = 64;
+
+__global__ void __launch_bounds__(kScoreThreads) anchor_score_kernel(const float* __restrict__ W, int N, int K,
+                                                                     const double* __restrict__ profile, double* score) {
     const int c = blockIdx.x * blockDim.x + threadIdx.x;
     if (c >= K) return;
     const float* col = W + c;
     double acc = 0.0;
     int n = 0;
-    for (; n + 8 <= N; n += 8) {
-        float v[8];
+    for (; n + 32 <= N; n += 32) {
+        float v[32];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = __ldg(col + (size_t)(n + j) * K);
+        for (int j = 0; j < 32; ++j) v[j] = __ldg(col + (size_t)(n + j) * K);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc = __dadd_rn(acc, __dmul_rn((double)v[j], (double)v[j]));
+        for (int j = 0; j < 32; ++j) acc = __dadd_rn(acc, __dmul_rn((double)v[j], (double)v[j]));
     }
     for (; n < N; ++n) {
         const double v = (double)__ldg(col + (size_t)n * K);
@@ -192,6 +196,41 @@ __global__ void anchor_bits_kernel(const int32_t* __restrict__ anchor_idx, int A
     if (k >= 0 && k < K) atomicOr(bits + (k >> 5), 1u << (k & 31));
 }
 
+// Nearest level of z = d / sd, lowest index on a tie, exactly as the fp64 quotient and the
+// four fp64 distances decide it.  The decision only changes at the level midpoints -0.985, 0
+// and +0.985 (within a few ulps of them, where rounding can tie two distances).  d * (1/sd) is
+// within a few ulps of the quotient, so when it lies more than 1e-9 from every midpoint the
+// side it lies on is the answer; otherwise the exact quotient and distances are computed.
+// (`fast` is false when 1/sd is not a finite number, or sd is 0.)
+__device__ __forceinline__ uint32_t nearest_level(double d, double sd, double inv_sd, bool fast) {
+    if (fast) {
+        const double za = __dmul_rn(d, inv_sd);
+        const long long bits = __double_as_longlong(za);
+        const long long mag = bits & 0x7FFFFFFFFFFFFFFFll;      // |za|, ordered as an integer
+        if (mag > __double_as_longlong(1e-9) &&
+            (mag < __double_as_longlong(0.985 - 1e-9) || mag > __double_as_longlong(0.985 + 1e-9))) {
+            const uint32_t outer = mag > __double_as_longlong(0.985);
+            return bits < 0 ? 1u - outer : 2u + outer;
+        }
+    }
+    const double z = sd > 0.0 ? __ddiv_rn(d, sd) : 0.0;
+    uint32_t best = 0;
+    double bd = fabs(__dsub_rn(z, kLevels[0]));
+#pragma unroll
+    for (int k = 1; k < 4; ++k) {
+        const double dk = fabs(__dsub_rn(z, kLevels[k]));
+        if (dk < bd) {
+            bd = dk;
+            best = k;
+        }
+    }
+    return best;
+}
+
+__device__ __forceinline__ double pick4(uint32_t q, double a0, double a1, double a2, double a3) {
+    return (q & 2u) ? ((q & 1u) ? a3 : a2) : ((q & 1u) ? a1 : a0);
+}
+
 __global__ void __launch_bounds__(128) quantize_2bit_kernel(const float* __restrict__ W, int N, int K,
                                                             const uint32_t* __restrict__ bits,
                                                             uint8_t* __restrict__ codes, uint16_t* __restrict__ scales,
@@ -224,30 +263,21 @@ __global__ void __launch_bounds__(128) quantize_2bit_kernel(const float* __restr
                                          return __dmul_rn(d, d);
                                      }), dn);
         const double sd = __dsqrt_rn(var);
+        const double inv_sd = sd > 0.0 ? __ddiv_rn(1.0, sd) : 0.0;
+        const bool fast = sd > 0.0 && isfinite(inv_sd);
         uint64_t q = 0;   // code of the j-th value in bits 2j..2j+1
-        for (int j = 0; j < nv; ++j) {
-            const double z = sd > 0.0 ? __ddiv_rn(__dsub_rn((double)v[j], mu), sd) : 0.0;
-            int best = 0;
-            double bd = fabs(__dsub_rn(z, kLevels[0]));
-#pragma unroll
-            for (int k = 1; k < 4; ++k) {
-                const double d = fabs(__dsub_rn(z, kLevels[k]));
-                if (d < bd) {
-                    bd = d;
-                    best = k;
-                }
-            }
-            q |= (uint64_t)best << (2 * j);
-        }
-        auto level = [&](int j) { return kLevels[(q >> (2 * j)) & 3u]; };
-        const double cb = __ddiv_rn(pairwise_sum(nv, [&](int j) { return level(j); }), dn);
+        for (int j = 0; j < nv; ++j)
+            q |= (uint64_t)nearest_level(__dsub_rn((double)v[j], mu), sd, inv_sd, fast) << (2 * j);
+        auto code = [&](int j) { return (uint32_t)(q >> (2 * j)) & 3u; };
+        const double c0 = kLevels[0], c1 = kLevels[1], c2 = kLevels[2], c3 = kLevels[3];
+        const double cb = __ddiv_rn(pairwise_sum(nv, [&](int j) { return pick4(code(j), c0, c1, c2, c3); }), dn);
+        // C_q - cb and its square take four values per group
+        const double t0 = __dsub_rn(c0, cb), t1 = __dsub_rn(c1, cb), t2 = __dsub_rn(c2, cb), t3 = __dsub_rn(c3, cb);
+        const double s0 = __dmul_rn(t0, t0), s1 = __dmul_rn(t1, t1), s2 = __dmul_rn(t2, t2), s3 = __dmul_rn(t3, t3);
         const double num = pairwise_sum(nv, [&](int j) {
-            return __dmul_rn(__dsub_rn((double)v[j], mu), __dsub_rn(level(j), cb));
+            return __dmul_rn(__dsub_rn((double)v[j], mu), pick4(code(j), t0, t1, t2, t3));
         });
-        const double den = __dadd_rn(pairwise_sum(nv, [&](int j) {
-                                         const double d = __dsub_rn(level(j), cb);
-                                         return __dmul_rn(d, d);
-                                     }), kOlsEps);
+        const double den = __dadd_rn(pairwise_sum(nv, [&](int j) { return pick4(code(j), s0, s1, s2, s3); }), kOlsEps);
         S = __ddiv_rn(num, den);
         Z = __dsub_rn(mu, __dmul_rn(S, cb));
         // scatter the codes back to their columns (anchor columns keep code 0)
@@ -323,7 +353,7 @@ lq_status launch_select_anchors(lq_handle h, const float* W, int N, int K, const
     if (A == 0) return LQ_OK;
     if ((size_t)K * sizeof(double) > h->partial_floats * sizeof(float)) return LQ_ERR_WORKSPACE;
     double* score = reinterpret_cast<double*>(h->partials);
-    anchor_score_kernel<<<blocks_for(K, 256), 256, 0, stream>>>(W, N, K, profile, score);
+    anchor_score_kernel<<<blocks_for(K, kScoreThreads), kScoreThreads, 0, stream>>>(W, N, K, profile, score);
     if (cudaPeekAtLastError() != cudaSuccess) return LQ_ERR_CUDA;
     anchor_select_kernel<<<1, kSelThreads, 0, stream>>>(score, K, A, anchor_idx);
     return cudaPeekAtLastError() == cudaSuccess ? LQ_OK : LQ_ERR_CUDA;

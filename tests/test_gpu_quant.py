@@ -107,6 +107,8 @@ def test_quantize_2bit_degenerate_groups(lqm, handle):
 
 def test_quantize_2bit_without_anchors(lqm, handle):
     W = synth.weights(96, 512, 0.02, seed=21)
+    half = np.arange(16, dtype=np.float32) / 256          # dyadic values: every sum is exact
+    W[0, :32] = np.concatenate([half, -half])               # mean exactly 0 and one value equal to it (z = 0)
     ref = O.quantize_2bit(W, np.zeros(0, np.int32))
     got = handle.quantize_2bit(dev(W))
     torch.cuda.synchronize()
