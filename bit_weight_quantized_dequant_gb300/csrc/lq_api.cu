@@ -206,8 +206,12 @@ LQ_API lq_status lq_sync(lq_handle h) {
     int flag = 0;
     if (cudaMemcpy(&flag, h->status_flag, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return LQ_ERR_CUDA;
     if (flag != 0) {
-        const int zero = 0;
-        if (cudaMemcpy(h->status_flag, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return LQ_ERR_CUDA;
+        // a wait ran out: the launch that timed out may have left arrival counts behind, so they
+        // are cleared with the flag
+        if (cudaMemset(h->status_flag, 0, 256) != cudaSuccess ||
+            cudaMemset(h->counters, 0, h->num_counters * sizeof(unsigned)) != cudaSuccess ||
+            cudaDeviceSynchronize() != cudaSuccess)
+            return LQ_ERR_CUDA;
         return LQ_ERR_TIMEOUT;
     }
     return LQ_OK;
