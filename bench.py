@@ -359,6 +359,82 @@ def quantizer_layer(lq, torch, h, device: str, reps: int = 3):
 STREAM_LAYERS = 32
 
 
+def device_layer(lq, torch, shapes, fmt, g, device, sigma=0.02):
+    """One layer of random packed weights made on the device (throughput runs; the contents do not
+    change the kernels' work): uniform random codes, scales and offsets of the synthetic
+    magnitudes, sorted random anchor columns (2-bit), or absmax (NF4)."""
+    from math import floor
+    ws = []
+    for name, N, K in shapes:
+        if fmt == lq.FMT_2BIT:
+            A = int(floor(0.035 * K))
+            ld = max(8, (A + 7) // 8 * 8)
+            codes = torch.randint(0, 256, (N, K // 4), generator=g, device=device, dtype=torch.uint8)
+            scales = (torch.rand((N, K // 32), generator=g, device=device) * sigma + 0.5 * sigma).half()
+            offsets = (torch.randn((N, K // 32), generator=g, device=device) * 0.1 * sigma).half()
+            aidx = torch.randperm(K, generator=g, device=device)[:A].sort().values.to(torch.int32).contiguous()
+            aw = (torch.randn((N, ld), generator=g, device=device) * sigma).half()
+            ws.append(lq.QuantWeights(lq.FMT_2BIT, N, K, codes, scales, offsets, aidx, aw, A, ld))
+        else:
+            codes = torch.randint(0, 256, (N, K // 2), generator=g, device=device, dtype=torch.uint8)
+            absmax = torch.rand((N, K // 64), generator=g, device=device) * 2 * sigma + sigma
+            ws.append(lq.QuantWeights(lq.FMT_NF4, N, K, codes, absmax))
+    return ws
+
+
+def layer_weight_bytes(ws, M: int) -> int:
+    total = 0
+    for w in ws:
+        N, K = w.N, w.K
+        if w.format == 1:
+            total += N * K // 4 + 2 * 2 * N * (K // 32) + 2 * N * w.A + 4 * w.A
+        else:
+            total += N * K // 2 + 4 * N * (K // 64)
+        total += 2 * M * K + 4 * M * N
+    return total
+
+
+def decode_configs(lq, torch, h, device: str, reps: int = 5):
+    """Decode throughput of the other listed decode workloads: the 7B layer in NF4 (8 rotating
+    copies, bf16 x, M = 1, 4, 16) and an 80-layer 70B stack resident in HBM (2-bit + anchors,
+    fp16 x, M = 1, 8, 32), one grouped call per layer."""
+    g = torch.Generator(device=device)
+    g.manual_seed(303)
+    out = {}
+    stream = torch.cuda.current_stream()
+    for key, shapes, fmt, layers, Ms, xdt in (
+            ("nf4_7b_layer", synth.LAYER_SHAPES["7b"], lq.FMT_NF4, ROTATE, (1, 4, 16), torch.bfloat16),
+            ("llama70b_80_layer_stack", synth.LAYER_SHAPES["70b"], lq.FMT_2BIT, 80, (1, 8, 32), torch.float16)):
+        stack = [device_layer(lq, torch, shapes, fmt, g, device, 0.015 if "70b" in key else 0.02) for _ in range(layers)]
+        res = {}
+        for M in Ms:
+            xs = [torch.randn((M, w.K), generator=g, device=device).to(xdt) for w in stack[0]]
+            ys = [torch.empty((M, w.N), dtype=torch.float32, device=device) for w in stack[0]]
+            probs = [[h.problem(w, x, y) for w, x, y in zip(ws, xs, ys)] for ws in stack]
+            for p in probs[:3]:
+                h.gemv_grouped(p, stream=stream)
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                for p in probs:
+                    h.gemv_grouped(p, stream=stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / (reps * layers)
+            lb = layer_weight_bytes(stack[0], M)
+            res[f"M={M}"] = {"us_per_layer": round(ms * 1e3, 1), "gb_s": round(lb / (ms * 1e-3) / 1e9, 1),
+                             "tok_s_stack": round(M * 1e3 / (ms * layers), 1) if layers == 80 else None}
+        res["layer_bytes_m1"] = layer_weight_bytes(stack[0], 1)
+        res["layers"] = layers
+        out[key] = res
+        del stack
+        torch.cuda.empty_cache()
+    h.sync()
+    return out
+
+
 def stream_stack(lq, torch, h, device: str, M: int = 1, reps: int = 3):
     """A 32-layer 7B stack held in pinned host memory, streamed through two device slots
     (lq_stream_run): tokens/s of one decode pass, the host-to-device rate it reached, and
@@ -549,6 +625,7 @@ def run_lq(args):
                              "layer_traffic_bytes": _traffic("gemm_14b_layer_2bit_bytes_per_launch")},
                 "frac_of_bf16_peak": {"2bit": round(g2["value"] / bf16, 4), "nf4": round(g4["value"] / bf16, 4)}}
 
+    decode_more = decode_configs(lq, torch, h, f"cuda:{local}") if not args.no_decode_configs else None
     quant = quantizer_layer(lq, torch, h, f"cuda:{local}") if not args.no_quant else None
     streamed = stream_stack(lq, torch, h, f"cuda:{local}") if not args.no_stream else None
     if streamed:
@@ -577,6 +654,7 @@ def run_lq(args):
             "clocks": clk.summary(),
             "config1_batched": cfg1,
             "gemm": gemm,
+            "decode_configs": decode_more,
             "quantizer": quant,
             "layer_streaming": streamed,
         }
@@ -639,6 +717,7 @@ def main():
     ap.add_argument("--no-gemm", action="store_true")
     ap.add_argument("--no-quant", action="store_true")
     ap.add_argument("--no-stream", action="store_true")
+    ap.add_argument("--no-decode-configs", action="store_true")
     ap.add_argument("--case", choices=["gemv7b", "gemm14b-2bit", "gemm14b-nf4", "quant7b"],
                     help="run one workload three times, untimed (what the profiles capture)")
     args = ap.parse_args()
