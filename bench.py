@@ -195,12 +195,12 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-CFG1_SETS = 32768   # distinct 512x256 weight sets of the single-linear config (1.9 GB, far beyond L2)
+SINGLE_LINEAR_SETS = 32768   # distinct 512x256 weight sets of the single-linear workload (1.9 GB, far beyond L2)
 
 
-def config1_batched(lq, torch, h, device: str, steps: int, warmup: int):
-    """The 512x256 single linear (2-bit, A = 8) over CFG1_SETS distinct weight sets in one launch."""
-    L, N, K, A = CFG1_SETS, 512, 256, 8
+def single_linear_batched(lq, torch, h, device: str, steps: int, warmup: int):
+    """The 512x256 single linear (2-bit, A = 8) over SINGLE_LINEAR_SETS distinct weight sets in one launch."""
+    L, N, K, A = SINGLE_LINEAR_SETS, 512, 256, 8
     big = synth.random_packed_2bit_sets(L, N, K, A, seed=1, cfg=1)
     w = lq.QuantWeights.from_host(big, lq.FMT_2BIT, device=device)
     del big
@@ -394,7 +394,7 @@ def layer_weight_bytes(ws, M: int) -> int:
     return total
 
 
-def decode_configs(lq, torch, h, device: str, reps: int = 5):
+def decode_workloads(lq, torch, h, device: str, reps: int = 5):
     """Decode throughput of the other listed decode workloads: the 7B layer in NF4 (8 rotating
     copies, bf16 x, M = 1, 4, 16) and an 80-layer 70B stack resident in HBM (2-bit + anchors,
     fp16 x, M = 1, 8, 32), one grouped call per layer, one pass captured in a CUDA graph."""
@@ -651,8 +651,8 @@ def run_lq(args):
     e2e_ms = e0.elapsed_time(e1) / args.steps
     e2e_val = world * layer_bytes / (e2e_ms * 1e-3) / 1e9
 
-    cfg1 = config1_batched(lq, torch, h, f"cuda:{local}", 20, 3)
-    cfg1["frac_of_hbm"] = round(cfg1["value"] / hbm, 4)
+    single = single_linear_batched(lq, torch, h, f"cuda:{local}", 20, 3)
+    single["frac_of_hbm"] = round(single["value"] / hbm, 4)
 
     gemm = None
     if not args.no_gemm:
@@ -668,7 +668,7 @@ def run_lq(args):
                              "layer_traffic_bytes": _traffic("gemm_14b_layer_2bit_bytes_per_launch")},
                 "frac_of_bf16_peak": {"2bit": round(g2["value"] / bf16, 4), "nf4": round(g4["value"] / bf16, 4)}}
 
-    decode_more = decode_configs(lq, torch, h, f"cuda:{local}") if not args.no_decode_configs else None
+    decode_more = decode_workloads(lq, torch, h, f"cuda:{local}") if not args.no_decode_workloads else None
     quant = quantizer_layer(lq, torch, h, f"cuda:{local}") if not args.no_quant else None
     streamed = stream_stack(lq, torch, h, f"cuda:{local}") if not args.no_stream else None
     if streamed:
@@ -698,9 +698,9 @@ def run_lq(args):
             "clocks": clk.summary(),
             "direct_calls": {"value": round(world * layer_bytes / (direct_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                              "ms_per_step": round(direct_ms, 5), "note": "each step launched from the host"},
-            "config1_batched": cfg1,
+            "single_linear_512x256_batched": single,
             "gemm": gemm,
-            "decode_configs": decode_more,
+            "decode_workloads": decode_more,
             "quantizer": quant,
             "layer_streaming": streamed,
         }
@@ -763,7 +763,7 @@ def main():
     ap.add_argument("--no-gemm", action="store_true")
     ap.add_argument("--no-quant", action="store_true")
     ap.add_argument("--no-stream", action="store_true")
-    ap.add_argument("--no-decode-configs", action="store_true")
+    ap.add_argument("--no-decode-workloads", action="store_true")
     ap.add_argument("--case", choices=["gemv7b", "gemm14b-2bit", "gemm14b-nf4", "quant7b"],
                     help="run one workload three times, untimed (what the profiles capture)")
     args = ap.parse_args()

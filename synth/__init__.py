@@ -10,7 +10,7 @@ Workloads stand in for the decoder layers that the otf-llm 4.0.1 README benchmar
 AutoBot-AI #1946 issue streams ("Background"): there are no checkpoints here, so
 weights are Gaussian draws with the stated standard deviations.
 
-Random streams are keyed by (seed, config id, matrix id) through NumPy's
+Random streams are keyed by (seed, workload id, matrix id) through NumPy's
 SeedSequence, so any single matrix can be regenerated on its own.
 """
 from __future__ import annotations
@@ -35,7 +35,7 @@ LAYER_SHAPES = {
 
 
 def rng(seed: int, cfg: int = 0, matrix_id: int = 0) -> np.random.Generator:
-    """Independent generator for one (seed, config, matrix) triple."""
+    """Independent generator for one (seed, workload, matrix) triple."""
     return np.random.default_rng(np.random.SeedSequence([int(seed), int(cfg), int(matrix_id)]))
 
 

@@ -119,7 +119,7 @@ def test_gemv_2bit_shapes(lqm, handle, shape):
     _gemv_check(lqm, handle, p, lqm.FMT_2BIT, xb, "f16")
 
 
-def test_gemv_config1_exact_workload(lqm, handle):
+def test_gemv_512x256_single_linear_workload(lqm, handle):
     """K=256, N=512, M=1, sigma 0.02, 8 anchors, seed 0."""
     W = synth.weights(512, 256, 0.02, seed=0, cfg=1)
     ai = O.select_anchors(W, O.activation_profile(np.ones(256)))
@@ -196,7 +196,7 @@ def test_gemv_grouped_layer_small(lqm, handle):
 
 
 def test_gemv_batched_distinct_weight_sets(lqm, handle):
-    """Config-1 shaped problems, L distinct seeded weight sets in one launch."""
+    """512x256 single-linear problems, L distinct seeded weight sets in one launch."""
     L, N, K = 6, 512, 256
     packs = []
     for l in range(L):
@@ -220,7 +220,7 @@ def test_gemv_batched_distinct_weight_sets(lqm, handle):
         assert_within(y[l].cpu().numpy(), yref, E, GEMV_TOL, f"batch member {l}")
 
 
-def test_gemv_config1_batched_full_size_sampled(lqm, handle):
+def test_gemv_512x256_batched_full_size_sampled(lqm, handle):
     """The 512x256 single linear as the bench runs it: 32768 distinct weight sets in one launch."""
     L, N, K, A = 32768, 512, 256, 8
     big = synth.random_packed_2bit_sets(L, N, K, A, seed=11, cfg=1)
