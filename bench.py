@@ -533,18 +533,28 @@ def run_lq(args):
 
     h = lq.Handle(local)
     copies = []
+    io_bufs = []          # per layer copy: (all x of the layer in one buffer, all y in one buffer)
     host_copy0 = None
     for c in range(ROTATE):
         packs = layer_packs(M, c + 17 * rank)
         if c == 0:
             host_copy0 = packs
+        # the layer's x and y each live in one contiguous buffer (every piece starts on 16 bytes:
+        # K is a multiple of 256 and N of 16), so a step's inputs and results move in one copy each
+        xbuf = torch.empty(sum(M * pk["K"] for _, pk, _ in packs), dtype=torch.float16, device=f"cuda:{local}")
+        ybuf = torch.empty(sum(M * pk["N"] for _, pk, _ in packs), dtype=torch.float32, device=f"cuda:{local}")
         mats = []
+        xo = yo = 0
         for name, pk, xb in packs:
             w = lq.QuantWeights.from_host(pk, lq.FMT_2BIT, device=f"cuda:{local}")
-            x = torch.from_numpy(xb).view(torch.float16).to(f"cuda:{local}")
-            y = torch.empty((M, pk["N"]), dtype=torch.float32, device=f"cuda:{local}")
+            x = xbuf[xo:xo + M * pk["K"]].view(M, pk["K"])
+            x.copy_(torch.from_numpy(xb).view(torch.float16))
+            y = ybuf[yo:yo + M * pk["N"]].view(M, pk["N"])
+            xo += M * pk["K"]
+            yo += M * pk["N"]
             mats.append((w, x, y))
         copies.append([h.problem(w, x, y) for (w, x, y) in mats] + [mats])
+        io_bufs.append((xbuf, ybuf))
     layer_bytes = algorithmic_bytes(host_copy0, M)
     stream = torch.cuda.current_stream()
 
@@ -624,19 +634,17 @@ def run_lq(args):
     achieved = layer_bytes / (kern_ms * 1e-3) / 1e9
 
     # end to end through the public API: x from pinned host memory in, y back to pinned host memory, every step
-    mats0 = copies[0][-1]
-    xs_host = [x.cpu().pin_memory() for (_, x, _) in mats0]
-    ys_host = [torch.empty_like(y, device="cpu").pin_memory() for (_, _, y) in mats0]
-    h2d = sum(t.numel() * t.element_size() for t in xs_host)
-    d2h = sum(t.numel() * t.element_size() for t in ys_host)
+    # (one pinned host buffer holds a layer's x, one its y: one copy in and one copy out per step)
+    xs_host = io_bufs[0][0].cpu().pin_memory()
+    ys_host = torch.empty(io_bufs[0][1].numel(), dtype=torch.float32).pin_memory()
+    h2d = xs_host.numel() * xs_host.element_size()
+    d2h = ys_host.numel() * ys_host.element_size()
 
     def e2e_step(i):
-        c = copies[i % ROTATE]
-        for (w, x, y), xh in zip(c[-1], xs_host):
-            x.copy_(xh, non_blocking=True)
-        h.gemv_grouped(c[:-1], stream=stream)
-        for (w, x, y), yh in zip(c[-1], ys_host):
-            yh.copy_(y, non_blocking=True)
+        xbuf, ybuf = io_bufs[i % ROTATE]
+        xbuf.copy_(xs_host, non_blocking=True)
+        h.gemv_grouped(copies[i % ROTATE][:-1], stream=stream)
+        ys_host.copy_(ybuf, non_blocking=True)
 
     for i in range(args.warmup):
         e2e_step(i)
