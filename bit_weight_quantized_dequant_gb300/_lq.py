@@ -17,7 +17,8 @@ F32, F16, BF16 = 0, 1, 2
 EXPORTED = ("lq_create", "lq_destroy", "lq_status_string", "lq_sync", "lq_dequant", "lq_gemv",
             "lq_gemv_grouped", "lq_gemm", "lq_gemm_grouped", "lq_gemv_noalloc",
             "lq_select_anchors", "lq_quantize_2bit", "lq_quantize_nf4",
-            "lq_stream_create", "lq_stream_run", "lq_stream_destroy", "lq_stream_run_direct")
+            "lq_stream_create", "lq_stream_run", "lq_stream_destroy", "lq_stream_run_direct",
+            "lq_selftest_wait")
 
 _LIB = None
 
@@ -95,6 +96,8 @@ def load_library(build_if_missing: bool = True):
     L.lq_stream_destroy.restype = I
     L.lq_stream_run_direct.argtypes = [P, P, S, S, I, ctypes.POINTER(lq_problem), I, ctypes.c_int64, P]
     L.lq_stream_run_direct.restype = I
+    L.lq_selftest_wait.argtypes = [P, ctypes.c_uint, P]
+    L.lq_selftest_wait.restype = I
     _LIB = L
     return L
 
@@ -246,6 +249,13 @@ class Handle:
         st = self._lib.lq_gemv_grouped(self._h, arr, len(problems), _stream(stream))
         if st != LQ_OK:
             raise LQError(st, "lq_gemv_grouped")
+
+    def selftest_wait(self, limit_us: int, stream=None):
+        """Run the bounded-wait self-test: a wait that nothing completes gives up after
+        limit_us; the next sync() raises LQError with status LQ_ERR_TIMEOUT."""
+        st = self._lib.lq_selftest_wait(self._h, int(limit_us), _stream(stream))
+        if st != LQ_OK:
+            raise LQError(st, "lq_selftest_wait")
 
     # ---- quantizers (the converter step; include/lq.h gives the definitions) ----
 

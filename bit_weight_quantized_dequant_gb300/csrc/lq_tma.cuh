@@ -56,15 +56,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Wait for phase `parity` of barrier `bar` to complete.  Returns false (after
 // raising *abort and the global status flag) when the time limit passes, or
 // when another thread of the CTA already raised *abort.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort,
-                                                  int* status) {
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort, int* status,
+                                                  unsigned long long limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_timer_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 63u) == 0) {
             if (*abort) return false;
-            if (global_timer_ns() - t0 > kWaitLimitNs) {
+            if (global_timer_ns() - t0 > limit_ns || i >= (1u << 31)) {   // (the count is a backstop)
                 *abort = 1;
                 if (status) atomicExch(status, 1);
                 return false;

@@ -335,6 +335,17 @@ LQ_API lq_status lq_stream_run_direct(lq_handle h, const void* host_layers, size
                                       int L, const lq_problem* problems, int count, int64_t y_layer_stride,
                                       void* stream);
 
+/*
+ * lq_selftest_wait — exercises the timeout path of the kernels' bounded waits.  One
+ * thread of one CTA waits, with the routine the pipelined kernels use, on a
+ * shared-memory barrier that nothing completes.  After limit_us microseconds
+ * (1 .. 1000000) the wait gives up, raises the handle's status word and the kernel
+ * returns; the next lq_sync reports LQ_ERR_TIMEOUT and clears the status word and
+ * the arrival counters.  Nothing faults and the context stays usable.  Errors:
+ * LQ_ERR_INVALID_ARG (null handle, limit out of range), LQ_ERR_CUDA.
+ */
+LQ_API lq_status lq_selftest_wait(lq_handle h, unsigned limit_us, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -165,3 +165,10 @@ def test_stream_null_arguments(lib):
     assert L.lq_stream_create(None, _fake_handle(), 1 << 20) == _lq.LQ_ERR_INVALID_ARG
     assert L.lq_stream_run(None, 0x10000, 256, 256, 1, None, 1, 0, None) == _lq.LQ_ERR_INVALID_ARG
     assert L.lq_stream_destroy(None) == _lq.LQ_OK
+
+
+def test_selftest_wait_validation(lib):
+    L, _ = lib
+    assert L.lq_selftest_wait(None, 1000, None) == _lq.LQ_ERR_INVALID_ARG
+    assert L.lq_selftest_wait(_fake_handle(), 0, None) == _lq.LQ_ERR_INVALID_ARG
+    assert L.lq_selftest_wait(_fake_handle(), 2000000, None) == _lq.LQ_ERR_INVALID_ARG
