@@ -258,14 +258,6 @@ __device__ __forceinline__ void next_block(const FParams& P, Pos& q) {
     }
 }
 
-// Next unit; returns true when the row block changes.
-__device__ __forceinline__ bool next_pos(const FParams& P, Pos& q) {
-    if (++q.s < q.su) return false;
-    q.s = 0;
-    next_block(P, q);
-    return true;
-}
-
 // Arrival count update with release and acquire semantics at GPU scope (one instruction, no
 // separate membar on either side).
 __device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* p, unsigned v) {
@@ -797,8 +789,14 @@ lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* probs, i
     const int64_t W = std::min<int64_t>(grid * kWarps, units);
     P.total_units = units;
     P.total_warps = W;
+    // With LQ_GEMV_STAGE=1 each CTA builds the x its units read in shared memory when that
+    // span is small (a few members, room for a second resident CTA), and no pre-pass runs;
+    // by default the pre-pass does it once for all CTAs (measured faster on this part), and the
+    // per-CTA spans are not needed.
+    const char* st_env = getenv("LQ_GEMV_STAGE");
+    const bool want_stage = st_env && atoi(st_env) == 1;
     int64_t max_span = 0, max_members = 0;
-    for (int64_t b = 0; b < grid; ++b) {
+    for (int64_t b = 0; want_stage && b < grid; ++b) {
         const int64_t w_lo = b * kWarps, w_hi = std::min<int64_t>(w_lo + kWarps, W);
         if (w_lo >= W) break;
         int pa, pb;
@@ -810,13 +808,9 @@ lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* probs, i
         for (int p = pa; p <= pb; ++p) members += (p == pb ? lb : P.d[p].batch - 1) - (p == pa ? la : 0) + 1;
         max_members = std::max(max_members, members);
     }
-    // With LQ_GEMV_STAGE=1 each CTA builds the x its units read in shared memory when that
-    // span is small (a few members, room for a second resident CTA), and no pre-pass runs;
-    // by default the pre-pass does it once for all CTAs (measured faster on this part).
     P.bitmap_words = std::max(1, max_k / 32);
     const size_t smem = (size_t)max_span * 2 + (size_t)P.bitmap_words * 4;
-    const char* st_env = getenv("LQ_GEMV_STAGE");
-    bool staged = max_members <= 4 && smem <= (size_t)std::min(ws.max_smem_optin, 110 * 1024) && st_env && atoi(st_env) == 1;
+    bool staged = want_stage && max_members <= 4 && smem <= (size_t)std::min(ws.max_smem_optin, 110 * 1024);
     if (staged) {
         int per_sm_s = 0;
         if (dispatch(fmt, 0, true, P, 0, smem, &per_sm_s, stream) != LQ_OK) return LQ_ERR_CUDA;
