@@ -33,8 +33,8 @@
  * Conventions shared by every entry point
  * ---------------------------------------
  * - Ownership: the caller owns every buffer passed in.  The library owns the
- *   handle and the device workspace that lq_create allocates; no other call
- *   allocates memory.
+ *   handle and the device workspace that lq_create allocates, and the two device
+ *   slots that lq_stream_create allocates; no other call allocates memory.
  * - Asynchrony: compute calls enqueue work on `stream` (a cudaStream_t, NULL for
  *   the legacy default stream) and return without waiting.  A returned LQ_OK
  *   means the arguments were valid and the launch was accepted.
@@ -53,7 +53,12 @@
  *   binary16 x on tensor cores with fp32 accumulation (|error| <= 1e-3 *
  *   sum_k |W_eff||x|); bf16 x is converted to binary16 (exact for |x| < 65504).
  *   lq_gemm multiplies in the dtype of x (bf16 or binary16) with fp32
- *   accumulation (|error| <= 4e-3 * sum_k |W_eff||x| for bf16).
+ *   accumulation (|error| <= 4e-3 * sum_k |W_eff||x| for bf16).  The quantizers'
+ *   outputs (codes, scales, offsets, anchors, absmax) are deterministic bit
+ *   patterns.
+ * - CUDA graphs: compute calls may be captured into a graph once each shape has
+ *   been called outside capture (the first call of a kernel variant sets its
+ *   attributes; a grouped GEMM uploads its tile list when its shapes change).
  */
 #ifndef LQ_H_
 #define LQ_H_
