@@ -737,6 +737,18 @@ def run_case(args):
         probs = [h.problem(w, x, y) for w, x, y in mats]
         for _ in range(3):
             h.gemv_grouped(probs)
+    elif args.case == "gemv512x256":
+        # the single 512x256 linear over 4096 distinct weight sets (234 MB, past L2) in one launch
+        L, N, K, A = 4096, 512, 256, 8
+        big = synth.random_packed_2bit_sets(L, N, K, A, seed=1, cfg=1)
+        w = lq.QuantWeights.from_host(big, lq.FMT_2BIT)
+        x = torch.from_numpy(synth.activations(L, K, "f16", seed=1, cfg=1)).view(torch.float16).cuda().view(L, 1, K)
+        y = torch.empty((L, 1, N), dtype=torch.float32, device="cuda")
+        strides = dict(codes=N * K // 4, scales=N * K // 32 * 2, offsets=N * K // 32 * 2, anchor_idx=4 * A,
+                       anchor_w=N * 8 * 2, x=K * 2, y=N * 4)
+        prob = [h.problem(w, x[0], y[0], batch=L, strides=strides)]
+        for _ in range(3):
+            h.gemv_grouped(prob)
     else:
         from math import floor
         fmt = args.case.split("-")[1]
@@ -772,7 +784,7 @@ def main():
     ap.add_argument("--no-quant", action="store_true")
     ap.add_argument("--no-stream", action="store_true")
     ap.add_argument("--no-decode-workloads", action="store_true")
-    ap.add_argument("--case", choices=["gemv7b", "gemm14b-2bit", "gemm14b-nf4", "quant7b"],
+    ap.add_argument("--case", choices=["gemv7b", "gemv512x256", "gemm14b-2bit", "gemm14b-nf4", "quant7b"],
                     help="run one workload three times, untimed (what the profiles capture)")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -28,6 +28,7 @@
 #include <algorithm>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 
 #include "lq_common.cuh"
 #include "lq_dq.cuh"
@@ -67,8 +68,32 @@ struct PrepDesc {
 struct PrepParams {
     PrepDesc d[kMaxGroup];
     int count, M, x_bf16, format;
+    int ring;                  // write the ring kernel's x layout (see ring_x_pos)
     int64_t total_jobs;
 };
+
+// x layout of the ring kernel, per batch member: the code columns in blocks of 16 (block
+// q at q * (16 M + 4) halves; token m at m * 16 inside it; column 16q + j + 4e at position
+// 4j + e, so a lane's four x values of one mma are one 8-byte load; the 4-half pad puts
+// the blocks that the four lanes of a row read in different banks), then x at the anchor
+// columns in the pre-pass's fragment order.
+__host__ __device__ constexpr int ring_kstride(int M) { return 16 * M + 4; }
+__device__ __forceinline__ int ring_x_pos(int k, int m, int M) {
+    return (k >> 4) * ring_kstride(M) + m * 16 + 4 * (k & 3) + ((k >> 2) & 3);
+}
+
+// Sixteen binary16 x values of one token (columns 16q .. 16q+15, as loaded: word i holds
+// columns 2i, 2i+1) to the ring layout's order (output word 2j + u holds columns j + 8u and
+// j + 8u + 4).
+__device__ __forceinline__ void ring_x_transpose(const uint32_t (&w)[8], uint32_t (&o)[8]) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int c0 = j + 8 * u, c1 = c0 + 4;   // same parity: both low or both high halves
+            o[2 * j + u] = prmt(w[c0 >> 1], w[c1 >> 1], (c0 & 1) ? 0x7632u : 0x5410u);
+        }
+}
 
 constexpr int kPrepWarps = 2;   // jobs per pre-pass CTA
 
@@ -93,7 +118,38 @@ __global__ void __launch_bounds__(32 * kPrepWarps) xprep_kernel(const __grid_con
     const int32_t* aidx = A > 0 ? reinterpret_cast<const int32_t*>(reinterpret_cast<const char*>(D.anchor_idx) + l * D.stride_anchor_idx)
                                 : nullptr;
     const int steps = K / 256;
-    if (jb < steps) {
+    if (jb < steps && P.ring) {
+        // the ring layout: one item = 16 columns of one token (two 16-byte loads, one 8-word store)
+        const int k0 = jb * 256, S = ring_kstride(M);
+        if (lane < 8) step_bits[warp][lane] = 0u;
+        __syncwarp();
+        for (int a0 = 0; a0 < A; a0 += 32) {
+            const int a = a0 + lane;
+            const int kk = a < A ? __ldg(aidx + a) - k0 : -1;
+            if (kk >= 0 && kk < 256) atomicOr(&step_bits[warp][kk >> 5], 1u << (kk & 31));
+        }
+        __syncwarp();
+        uint16_t* dst = D.xperm + l * D.xperm_stride + (int64_t)(k0 / 16) * S;
+        for (int it = lane; it < 16 * M; it += 32) {
+            const int m = it >> 4, ql = it & 15;
+            const uint4* src = reinterpret_cast<const uint4*>(x + (int64_t)m * K + k0 + 16 * ql);
+            const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
+            uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w}, o[8];
+            const uint32_t amask = (step_bits[warp][ql >> 1] >> (16 * (ql & 1))) & 0xFFFFu;   // anchor columns of the block
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t lo = (amask >> (2 * i)) & 1u ? 0u : to_half_bits((uint16_t)w[i], P.x_bf16);
+                const uint32_t hi = (amask >> (2 * i + 1)) & 1u ? 0u : to_half_bits((uint16_t)(w[i] >> 16), P.x_bf16);
+                w[i] = lo | (hi << 16);
+            }
+            ring_x_transpose(w, o);
+            uint2* d2 = reinterpret_cast<uint2*>(dst + ql * S + m * 16);
+            d2[0] = make_uint2(o[0], o[1]);
+            d2[1] = make_uint2(o[2], o[3]);
+            d2[2] = make_uint2(o[4], o[5]);
+            d2[3] = make_uint2(o[6], o[7]);
+        }
+    } else if (jb < steps) {
         const int k0 = jb * 256;
         uint16_t* dst = D.xperm + l * D.xperm_stride + (int64_t)k0 * M;
         // column of element e of item `it` inside this step (fragment order)
@@ -167,7 +223,8 @@ __global__ void __launch_bounds__(32 * kPrepWarps) xprep_kernel(const __grid_con
             for (int e = 0; e < 8; ++e) {
                 const int pos = pos0 + e, tt = pos >> 2, hh = pos & 3;
                 const int a = a_base + 16 * bl + 2 * tt + (hh & 1) + 8 * (hh >> 1);
-                v[e] = a < A ? to_half_bits(x[(int64_t)m * K + __ldg(aidx + a)], P.x_bf16) : (uint16_t)0;
+                const int k = a < A ? __ldg(aidx + a) : -1;
+                v[e] = (unsigned)k < (unsigned)K ? to_half_bits(x[(int64_t)m * K + k], P.x_bf16) : (uint16_t)0;
             }
             *reinterpret_cast<uint4*>(dst + d0) = make_uint4((uint32_t)v[0] | ((uint32_t)v[1] << 16), (uint32_t)v[2] | ((uint32_t)v[3] << 16),
                                                             (uint32_t)v[4] | ((uint32_t)v[5] << 16), (uint32_t)v[6] | ((uint32_t)v[7] << 16));
@@ -205,6 +262,8 @@ struct FDesc {
     int cmax;                   // most warps that can share one row block
     int64_t unit_begin;         // first unit of this problem in the launch
     int64_t xoff;               // first half of this problem's x copies in the x buffer
+    int xa_off;                 // ring layout: halves from a member's x to its x at the anchor columns
+    int G;                      // ring kernel: anchor unit spacing inside a row block (su / anchor units)
     const uint16_t* x;          // the caller's x [batch][M][K] (16-bit) and anchor columns, for
     int64_t stride_x;           //   the in-kernel build of the fragment-ordered copy (bytes)
     const int32_t* anchor_idx;
@@ -235,10 +294,18 @@ __device__ __noinline__ Pos locate(const FParams& P, int64_t u) {
     const FDesc& D = P.d[q.p];
     int64_t loc = u - D.unit_begin;
     const int64_t per_member = (int64_t)D.rblocks * D.su;
-    q.l = loc / per_member;
-    loc -= q.l * per_member;
-    q.rb = (int)(loc / D.su);
-    q.s = (int)(loc - (int64_t)q.rb * D.su);
+    if (loc < 0x7fffffff && per_member < 0x7fffffff) {   // (32-bit divisions when the numbers fit)
+        const unsigned lu = (unsigned)loc, pm = (unsigned)per_member;
+        const unsigned l = lu / pm, rem = lu - l * pm, rb = rem / (unsigned)D.su;
+        q.l = l;
+        q.rb = (int)rb;
+        q.s = (int)(rem - rb * (unsigned)D.su);
+    } else {
+        q.l = loc / per_member;
+        loc -= q.l * per_member;
+        q.rb = (int)(loc / D.su);
+        q.s = (int)(loc - (int64_t)q.rb * D.su);
+    }
     q.steps = D.steps;
     q.su = D.su;
     return q;
@@ -270,12 +337,13 @@ __device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* p, unsigned v
 __device__ __noinline__ int64_t owner_warp(int64_t u, int64_t W, int64_t U) { return ((u + 1) * W - 1) / U; }
 
 // The last warp of a row block adds the slots of its nc contributors in order and writes y.
+// A slot holds [M][rows] fp32 sums; rows is 16 (streaming kernel) or 32 (ring kernel).
 __device__ __noinline__ void finish_block(const float* slots, int nc, int M, void* y, int N, int row0, int y_dtype,
-                                          int lane) {
-    for (int i = lane; i < 16 * M; i += 32) {
-        const int m = i >> 4, row = row0 + (i & 15);
+                                          int lane, int rows = 16) {
+    for (int i = lane; i < rows * M; i += 32) {
+        const int m = i / rows, row = row0 + (i - m * rows);
         float sum = 0.f;
-        for (int c = 0; c < nc; ++c) sum += __ldcg(slots + c * M * 16 + i);
+        for (int c = 0; c < nc; ++c) sum += __ldcg(slots + c * M * rows + i);
         if (row < N) store_out(y, (size_t)m * N + row, y_dtype, sum);
     }
 }
@@ -309,7 +377,7 @@ __device__ __forceinline__ void build_member_x(const FParams& P, const FDesc& D,
     __syncthreads();
     for (int a = threadIdx.x; a < A; a += blockDim.x) {
         const int k = __ldg(aidx + a);
-        atomicOr(&bits[k >> 5], 1u << (k & 31));
+        if ((unsigned)k < (unsigned)K) atomicOr(&bits[k >> 5], 1u << (k & 31));   // (a column outside [0, K) is ignored)
     }
     __syncthreads();
     const int items = M * K / 8, aitems = M * a_pad / 8;
@@ -327,7 +395,8 @@ __device__ __forceinline__ void build_member_x(const FParams& P, const FDesc& D,
                 v[e] = ((bits[k >> 5] >> (k & 31)) & 1u) ? (uint16_t)0 : to_half_bits(x[(int64_t)m * K + k], P.x_bf16);
             } else {
                 const int a = 16 * bi + 2 * tt + (hh & 1) + 8 * (hh >> 1);
-                v[e] = a < A ? to_half_bits(x[(int64_t)m * K + __ldg(aidx + a)], P.x_bf16) : (uint16_t)0;
+                const int k = a < A ? __ldg(aidx + a) : -1;
+                v[e] = (unsigned)k < (unsigned)K ? to_half_bits(x[(int64_t)m * K + k], P.x_bf16) : (uint16_t)0;
             }
         }
         *reinterpret_cast<uint4*>(dst + (code ? 0 : (int64_t)M * K) + d0) =
@@ -624,21 +693,456 @@ __global__ void __launch_bounds__(kThreadsS, NT <= 2 ? LQ_STREAM_MIN_BLOCKS : 1)
     }
 }
 
-// Resident CTAs per SM of one instantiation at a given dynamic shared-memory size.
-template <int FMT, int MT, int NT, bool STAGED>
-int resident_ctas(size_t smem) {
-    static size_t set_smem = (size_t)-1;
-    static int per_sm = 0;
+// ---- ring kernel (2-bit) ----------------------------------------------------------
+//
+// The same grouped launch, unit partition, x pre-pass and slot reduction as
+// gemv_stream_kernel, reorganised around what bounds decode on this part: the integer
+// pipe that turns codes into binary16 weights, and the instructions spent per unit.
+//  * A unit is 32 output rows x 256 code columns (or 32 rows x 48 anchor columns): two
+//    mma row tiles that share every x fragment, so one shared-memory x load feeds two
+//    independent accumulator chains.
+//  * Weights reach the registers through shared memory: each warp keeps two unit stages
+//    that its lanes fill with 16-byte cp.async copies, double buffered (the next unit is in
+//    flight while one is multiplied; a stage is refilled as soon as it is consumed), so
+//    loads in flight hold no registers.  One CTA of 16 warps per SM.
+//  * x: when the span of x that a CTA's warps read fits in shared memory (XS), the CTA
+//    builds it there itself (binary16, fragment order, anchor columns zeroed) and no
+//    pre-pass runs; otherwise the pre-pass writes it to global memory once per call.
+//  * Each CTA lets the next kernel in the stream launch at once (programmatic dependent
+//    launch), so a following call's weight copies start while this call finishes; every
+//    kernel waits for its predecessor before it reads x or touches the workspace or y.
+//
+// Stage layout (3072 bytes):
+//   code unit:   codes [32 rows][64 B] | scales [32 rows][8 x binary16] | offsets [32][8]
+//   anchor unit: anchor weights [32 rows][48 x binary16] (zero past A)
+
+constexpr int kRingStage = 3072;
+constexpr int kRingDepth = 2;
+constexpr int kRingRows = 32;
+
+#ifndef LQ_RING_WARPS1
+#define LQ_RING_WARPS1 16
+#endif
+__host__ __device__ constexpr int ring_warps(int NT) { return NT == 1 ? LQ_RING_WARPS1 : 16; }
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+__device__ __forceinline__ uint32_t lds32(const unsigned char* p) { return *reinterpret_cast<const uint32_t*>(p); }
+
+// Issue side of a warp's ring: the lane's source pointers for the next unit to copy and
+// the cursor (problem, member, row block, unit) that moves them.  Inside a row block the
+// pointers only advance; entering the next row block recomputes them (out of line).
+// Order of a row block's units: its na anchor units sit at positions G-1, 2G-1, ..., naG-1
+// (G = su / na) among the code units, so that any run of consecutive units holds code and
+// anchor units in about the block's proportion and equal runs cost about the same.
+struct UnitOrder {
+    int a;    // anchor units before the cursor
+    int ua;   // units from the cursor to the next anchor unit (large when none is left)
+    int G, na;
+};
+
+__device__ __forceinline__ UnitOrder unit_order(int s, int steps, int su, int G) {
+    UnitOrder o;
+    o.na = su - steps;
+    o.G = G;
+    o.a = s == 0 ? 0 : min(o.na, s / G);
+    o.ua = o.a < o.na ? (o.a + 1) * G - 1 - s : 1 << 30;
+    return o;
+}
+
+// Is the cursor's unit an anchor unit; then step the cursor past it.
+__device__ __forceinline__ bool unit_step(UnitOrder& o) {
+    if (o.ua == 0) {
+        ++o.a;
+        o.ua = o.a < o.na ? o.G - 1 : 1 << 30;
+        return true;
+    }
+    --o.ua;
+    return false;
+}
+
+struct Feed {
+    const uint8_t* c0;       // codes of row g at this lane's 16-byte slice of the next code unit
+    const uint8_t* meta;     // lane < 16: scales of rows 2i, 2i+1 (i = lane & 15); else offsets
+    const uint8_t* arow;     // anchor weights of row `lane`
+    int o8, o16, o24;        // byte offsets from c0 to the codes of rows g+8, g+16, g+24
+    int om;                  // byte offset from meta to the second row's metadata
+    int s, su;               // next unit inside the row block; all units of a row block
+    UnitOrder ord;           // where the anchor units of the row block fall
+    int left;                // units of the warp's range not yet issued
+    int A;                   // anchors of the problem
+    int fast;                // following row blocks of this member that are full (pointers only advance)
+    int dc, dm, da;          // pointer steps from the end of a full row block to the next one
+    int64_t u;               // launch-wide index of the next unit
+};
+
+// The feed cursor at unit u (left units remain in the warp's range).
+__device__ __noinline__ Feed feed_at(const FParams& P, int64_t u, int left, int lane) {
+    const Pos q = locate(P, u);
+    Feed f;
+    f.u = u;
+    f.s = q.s;
+    f.left = left;
+    const FDesc& D = P.d[q.p];
+    const int g = lane >> 2, t = lane & 3, N = D.N, K = D.K;
+    const int base = q.rb * kRingRows;
+    auto row = [&](int r) -> int64_t { return base + r < N ? base + r : N - 1; };   // rows past N: never stored
+    f.ord = unit_order(q.s, D.steps, D.su, D.G);
+    const int sc = q.s - f.ord.a;   // code units before unit s
+    const int64_t rg = row(g);
+    f.c0 = D.codes + q.l * D.stride_codes + rg * (K / 4) + 16 * t + 64 * sc;
+    f.o8 = (int)((row(g + 8) - rg) * (K / 4));
+    f.o16 = (int)((row(g + 16) - rg) * (K / 4));
+    f.o24 = (int)((row(g + 24) - rg) * (K / 4));
+    const int i = lane & 15;
+    const uint8_t* mb = lane < 16 ? static_cast<const uint8_t*>(D.scales) + q.l * D.stride_scales
+                                  : reinterpret_cast<const uint8_t*>(D.offsets) + q.l * D.stride_offsets;
+    const int64_t rm = row(2 * i);
+    f.meta = mb + rm * (K / 16) + 16 * sc;
+    f.om = (int)((row(2 * i + 1) - rm) * (K / 16));
+    f.su = D.su;
+    f.A = D.A;
+    const int full = N / kRingRows;   // row blocks with all 32 rows inside N
+    f.fast = q.rb < full ? full - 1 - q.rb : 0;
+    f.dc = (kRingRows - 1) * (K / 4);
+    f.dm = (kRingRows - 1) * (K / 16);
+    f.da = kRingRows * D.ld_anchor * 2;
+    f.arow = D.A > 0 ? reinterpret_cast<const uint8_t*>(D.anchor_w) + q.l * D.stride_anchor_w + row(lane) * D.ld_anchor * 2
+                     : D.codes;
+    return f;
+}
+
+// Copy the next unit into the stage at `st` and step the cursor; one commit group per call
+// (empty once the warp's range is exhausted).
+__device__ __forceinline__ void feed_issue(const FParams& P, Feed& f, uint32_t st, int lane) {
+    if (f.left > 0) {
+        const int g = lane >> 2, t = lane & 3;
+        const int a_unit = f.ord.a;
+        if (!unit_step(f.ord)) {
+            const uint32_t dc = st + g * 64 + 16 * t;
+            cp_async16(dc, f.c0, 16);
+            cp_async16(dc + 8 * 64, f.c0 + f.o8, 16);
+            cp_async16(dc + 16 * 64, f.c0 + f.o16, 16);
+            cp_async16(dc + 24 * 64, f.c0 + f.o24, 16);
+            const uint32_t dm = st + 2048 + (lane >> 4) * 512 + (lane & 15) * 32;
+            cp_async16(dm, f.meta, 16);
+            cp_async16(dm + 16, f.meta + f.om, 16);
+            f.c0 += 64;
+            f.meta += 16;
+        } else {
+            const int a0 = a_unit * kAnchorCols;
+            const uint32_t dst = st + lane * 96;
+#pragma unroll
+            for (int i = 0; i < 6; ++i) {
+                const int a = a0 + 8 * i;
+                const int n = f.A - a;   // anchors left from column a: copy at most 8, zero the rest
+                const uint32_t bytes = n >= 8 ? 16u : (n > 0 ? 2u * n : 0u);
+                cp_async16(dst + 16 * i, bytes ? f.arow + 2 * a : f.arow, bytes);
+            }
+        }
+        --f.left;
+        ++f.u;
+        if (++f.s == f.su && f.left > 0) {
+            if (f.fast > 0) {   // the next row block of the same member, all rows inside N
+                --f.fast;
+                f.s = 0;
+                f.c0 += f.dc;
+                f.meta += f.dm;
+                f.arow += f.A > 0 ? f.da : 0;
+                f.ord.a = 0;
+                f.ord.ua = f.ord.na > 0 ? f.ord.G - 1 : 1 << 30;
+            } else {
+                f = feed_at(P, f.u, f.left, lane);
+            }
+        }
+    }
+    cp_async_commit();
+}
+
+// Write a warp's sums of the row block at q (units: how many of the block's units it did)
+// to y directly when it did them all, else to its slot; the warp completing the block adds
+// the slots in warp order and writes y.
+template <int NT>
+__device__ __forceinline__ void ring_flush(const FParams& P, const Pos& q, int units, float (&acc)[2][NT][4], int M,
+                                           int lane) {
+    const FDesc& D = P.d[q.p];
+    const int g = lane >> 2, t = lane & 3;
+    if (units == q.su) {
+        void* y = static_cast<char*>(D.y) + q.l * D.stride_y;
+        const int rg = q.rb * kRingRows + g;
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int m = 8 * nt + 2 * t + (e & 1), row = rg + 16 * h + (e >> 1) * 8;
+                    if (m < M && row < D.N) store_out(y, (size_t)m * D.N + row, P.y_dtype, acc[h][nt][e]);
+                    acc[h][nt][e] = 0.f;
+                }
+        return;
+    }
+    const int64_t W = P.total_warps;
+    const int64_t wid = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int64_t u_begin = P.total_units * wid / W;
+    const int64_t blk = q.l * D.rblocks + q.rb;
+    const int64_t first_u = D.unit_begin + blk * q.su;
+    const int64_t w0 = first_u >= u_begin ? wid : owner_warp(first_u, W, P.total_units);
+    float* slots = D.part + blk * D.cmax * M * kRingRows;
+    float* mine = slots + (int)(wid - w0) * M * kRingRows;
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int m = 8 * nt + 2 * t + (e & 1), r = 16 * h + g + (e >> 1) * 8;
+                if (m < M) __stcg(mine + m * kRingRows + r, acc[h][nt][e]);
+                acc[h][nt][e] = 0.f;
+            }
+    __syncwarp();
+    unsigned last = 0;
+    if (lane == 0) {
+        const unsigned old = atom_add_acq_rel_gpu(D.cnt + blk, (unsigned)units);
+        last = old + (unsigned)units == (unsigned)q.su;
+    }
+    if (__shfl_sync(0xffffffffu, last, 0)) {
+        __syncwarp();
+        if (lane == 0) D.cnt[blk] = 0u;
+        const int nc = (int)(owner_warp(first_u + q.su - 1, W, P.total_units) - w0 + 1);
+        finish_block(slots, nc, M, static_cast<char*>(D.y) + q.l * D.stride_y, D.N, q.rb * kRingRows, P.y_dtype,
+                     lane, kRingRows);
+    }
+}
+
+// The x span of a CTA (members a..b of the launch, a few at most) built in shared memory
+// in the ring layout, in three passes over all members with one CTA barrier after each:
+// (1) every code column as binary16 (two 16-byte loads per 16 columns of a token);
+// (2) x at the anchor columns gathered from (1), zero past A; (3) the anchor columns of
+// (1) zeroed (the anchors replace those weights).
+__device__ __forceinline__ void build_span_x(const FParams& P, const Pos& a, const Pos& b, int64_t span0, uint16_t* xsm) {
+    const int M = P.M, tid = threadIdx.x, nth = blockDim.x, S = ring_kstride(M);
+    for (int pass = 0; pass < 3; ++pass) {
+        for (int p = a.p; p <= b.p; ++p) {
+            const FDesc& D = P.d[p];
+            const int K = D.K, A = D.A;
+            const int64_t l0 = p == a.p ? a.l : 0, l1 = p == b.p ? b.l : D.batch - 1;
+            for (int64_t l = l0; l <= l1; ++l) {
+                uint16_t* dst = xsm + (D.xoff + l * D.xperm_stride - span0);
+                const int32_t* aidx = A > 0 ? reinterpret_cast<const int32_t*>(reinterpret_cast<const char*>(D.anchor_idx) +
+                                                                                 l * D.stride_anchor_idx)
+                                            : nullptr;
+                if (pass == 0) {
+                    const uint16_t* x = reinterpret_cast<const uint16_t*>(reinterpret_cast<const char*>(D.x) + l * D.stride_x);
+                    for (int it = tid; it < M * K / 16; it += nth) {
+                        const int m = it / (K / 16), q = it - m * (K / 16);
+                        const uint4* src = reinterpret_cast<const uint4*>(x + (int64_t)m * K + 16 * q);
+                        const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
+                        uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w}, o[8];
+                        if (P.x_bf16) {
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                w[i] = (uint32_t)to_half_bits((uint16_t)w[i], 1) | ((uint32_t)to_half_bits((uint16_t)(w[i] >> 16), 1) << 16);
+                        }
+                        ring_x_transpose(w, o);
+                        uint2* d2 = reinterpret_cast<uint2*>(dst + q * S + m * 16);
+                        d2[0] = make_uint2(o[0], o[1]);
+                        d2[1] = make_uint2(o[2], o[3]);
+                        d2[2] = make_uint2(o[4], o[5]);
+                        d2[3] = make_uint2(o[6], o[7]);
+                    }
+                } else if (pass == 1) {
+                    const int a_pad = (int)(D.xperm_stride - D.xa_off) / M;
+                    uint16_t* xa = dst + D.xa_off;
+                    for (int it = tid; it < M * a_pad; it += nth) {
+                        const int m = it / a_pad, aa = it - m * a_pad;
+                        const int k = aa < A ? __ldg(aidx + aa) : -1;
+                        const int bi = aa >> 4, r = aa & 15, pos = 4 * ((r & 7) >> 1) + (r & 1) + 2 * (r >> 3);
+                        xa[(bi * M + m) * 16 + pos] = (unsigned)k < (unsigned)K ? dst[ring_x_pos(k, m, M)] : (uint16_t)0;
+                    }
+                } else {
+                    for (int it = tid; it < M * A; it += nth) {
+                        const int m = it / A, aa = it - m * A;
+                        const int k = __ldg(aidx + aa);
+                        if ((unsigned)k < (unsigned)K) dst[ring_x_pos(k, m, M)] = 0;   // (a column outside [0, K) is ignored)
+                    }
+                }
+            }
+        }
+        __syncthreads();
+    }
+}
+
+template <int MT, int NT, bool XS>
+__global__ void __launch_bounds__(32 * ring_warps(NT), 1) gemv_ring_kernel(const __grid_constant__ FParams P) {
+    constexpr int kW = ring_warps(NT);
+    extern __shared__ __align__(128) unsigned char ring_smem[];
+    const int M = MT > 0 ? MT : P.M;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int64_t W = P.total_warps;
+    const int64_t wid = (int64_t)blockIdx.x * kW + warp;
+    const bool active = wid < W;
+    if (!XS && !active) return;
+    const uint32_t ring = smem_u32(ring_smem) + warp * kRingDepth * kRingStage;
+    const unsigned char* ringp = ring_smem + warp * kRingDepth * kRingStage;
+    const int64_t u_begin = active ? P.total_units * wid / W : 0, u_end = active ? P.total_units * (wid + 1) / W : 0;
+
+    // weights do not depend on the pre-pass: the first copies go out before waiting for it
+    Feed f;
+    if (active) {
+        f = feed_at(P, u_begin, (int)(u_end - u_begin), lane);
+        feed_issue(P, f, ring, lane);
+        feed_issue(P, f, ring + kRingStage, lane);
+    }
+    pdl_launch_dependents();
+    int64_t span0 = 0;
+    uint16_t* xsm = reinterpret_cast<uint16_t*>(ring_smem + kW * kRingDepth * kRingStage);
+    if (XS) {
+        const int64_t w_lo = (int64_t)blockIdx.x * kW, w_hi = (w_lo + kW < W) ? w_lo + kW : W;
+        if (w_lo >= W) return;   // the whole CTA is idle
+        const Pos a = locate(P, P.total_units * w_lo / W), b = locate(P, P.total_units * w_hi / W - 1);
+        span0 = P.d[a.p].xoff + a.l * P.d[a.p].xperm_stride;
+        const int64_t span1 = P.d[b.p].xoff + (b.l + 1) * P.d[b.p].xperm_stride;
+        (void)span1;
+        pdl_wait();   // x may come from the kernel before
+        build_span_x(P, a, b, span0, xsm);
+        if (!active) return;
+    } else {
+        pdl_wait();
+    }
+
+    const int S = ring_kstride(M);
+    const int xlane = min(g, M - 1) * 16 + 4 * t * S;    // code columns: block 4t of each 64-column quarter
+    const int xlane_a = min(g, M - 1) * 16 + t * 4;      // anchor columns (fragment order)
+    int tok[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) tok[nt] = (min(8 * nt + g, M - 1) - min(g, M - 1)) * 16;
+    float acc[2][NT][4];
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) acc[h][nt][0] = acc[h][nt][1] = acc[h][nt][2] = acc[h][nt][3] = 0.f;
+
+    auto xbase = [&](const Pos& c) -> const uint16_t* {
+        const FDesc& D = P.d[c.p];
+        return XS ? xsm + (D.xoff + c.l * D.xperm_stride - span0) : D.xperm + c.l * D.xperm_stride;
+    };
+    Pos q = locate(P, u_begin);
+    UnitOrder ord = unit_order(q.s, q.steps, q.su, P.d[q.p].G);
+    const uint16_t* xb0 = xbase(q);
+    int seg_units = 0;
+    uint32_t cst = 0;   // byte offset of the stage to compute (the other one is being filled)
+    for (int left = (int)(u_end - u_begin); left > 0; --left) {
+        cp_async_wait<1>();
+        __syncwarp();   // every lane's copies of this unit have landed (the next unit may still be in flight)
+        const unsigned char* st = ringp + cst;
+        const int a_unit = ord.a;
+        if (!unit_step(ord)) {
+            const uint16_t* xs = xb0 + xlane + (q.s - a_unit) * 16 * S;
+#pragma unroll
+            for (int hg = 0; hg < 2; ++hg) {   // group 2t + hg: code words 2hg, 2hg+1 of each row
+                uint32_t RA[4], RB[4];
+                uint2 w[4];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const uint16_t sb = *reinterpret_cast<const uint16_t*>(st + 2048 + (g + 8 * r) * 16 + 4 * t + 2 * hg);
+                    const uint16_t zb = *reinterpret_cast<const uint16_t*>(st + 2560 + (g + 8 * r) * 16 + 4 * t + 2 * hg);
+                    lut2_bits(sb, zb, RA[r], RB[r]);
+                    w[r] = *reinterpret_cast<const uint2*>(st + (g + 8 * r) * 64 + 16 * t + 8 * hg);
+                }
+#pragma unroll
+                for (int iw = 0; iw < 2; ++iw) {
+                    const int ii = 2 * hg + iw;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        uint2 xb[NT];
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt)
+                            xb[nt] = *reinterpret_cast<const uint2*>(xs + ii * S + 4 * j + tok[nt]);
+                        uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+                        const uint32_t w0 = iw ? w[0].y : w[0].x, w1 = iw ? w[1].y : w[1].x;
+                        const uint32_t w2 = iw ? w[2].y : w[2].x, w3 = iw ? w[3].y : w[3].x;
+                        expand2_fast(w0, j, RA[0], RB[0], a0, a2);
+                        expand2_fast(w1, j, RA[1], RB[1], a1, a3);
+                        mma_xg<NT, MT>(acc[0], a0, a1, a2, a3, xb);
+                        expand2_fast(w2, j, RA[2], RB[2], b0, b2);
+                        expand2_fast(w3, j, RA[3], RB[3], b1, b3);
+                        mma_xg<NT, MT>(acc[1], b0, b1, b2, b3, xb);
+                    }
+                }
+            }
+        } else {
+            const uint16_t* xs = xb0 + xlane_a + P.d[q.p].xa_off + M * a_unit * kAnchorCols;
+            const int nkb = (P.d[q.p].A - a_unit * kAnchorCols + 15) >> 4;   // k-blocks of this unit that hold anchors
+#pragma unroll
+            for (int kb = 0; kb < 3; ++kb) {
+                if (kb > 0 && kb >= nkb) break;
+                uint2 xb[NT];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) xb[nt] = *reinterpret_cast<const uint2*>(xs + kb * M * 16 + tok[nt]);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const unsigned char* r0p = st + (16 * h + g) * 96 + 32 * kb + 4 * t;
+                    mma_xg<NT, MT>(acc[h], lds32(r0p), lds32(r0p + 8 * 96), lds32(r0p + 16), lds32(r0p + 8 * 96 + 16), xb);
+                }
+            }
+        }
+        __syncwarp();   // every lane is done with this stage: refill it two units ahead
+        feed_issue(P, f, ring + cst, lane);
+        cst ^= kRingStage;
+        ++seg_units;
+        if (++q.s == q.su || left == 1) {
+            ring_flush<NT>(P, q, seg_units, acc, M, lane);
+            seg_units = 0;
+            if (left > 1) {
+                q.s = 0;
+                const int p0 = q.p;
+                const int64_t l0 = q.l;
+                next_block(P, q);
+                ord = unit_order(0, q.steps, q.su, P.d[q.p].G);
+                if (q.p != p0 || q.l != l0) xb0 = xbase(q);
+            }
+        }
+    }
+    cp_async_wait<0>();
+}
+
+// Resident CTAs per SM of a kernel at a given dynamic shared-memory size.  The first call
+// for a size sets the kernel's shared-memory attribute; the answer is cached per kernel
+// (the lock keeps host threads that launch different sizes from racing on the cache).
+std::mutex g_occ_mutex;
+
+template <typename Kern>
+int resident_ctas_of(Kern kern, size_t smem, size_t& set_smem, int& per_sm, int threads = kThreadsS) {
+    std::lock_guard<std::mutex> lock(g_occ_mutex);
     if (set_smem != smem) {
-        if (cudaFuncSetAttribute(gemv_stream_kernel<FMT, MT, NT, STAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
             return -1;
         int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gemv_stream_kernel<FMT, MT, NT, STAGED>, kThreadsS, smem) != cudaSuccess)
-            return -1;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, smem) != cudaSuccess) return -1;
         per_sm = n;
         set_smem = smem;
     }
     return per_sm;
+}
+
+template <int FMT, int MT, int NT, bool STAGED>
+int resident_ctas(size_t smem) {
+    static size_t set_smem = (size_t)-1;
+    static int per_sm = 0;
+    return resident_ctas_of(gemv_stream_kernel<FMT, MT, NT, STAGED>, smem, set_smem, per_sm);
+}
+
+template <int MT, int NT, bool XS>
+int resident_ctas_ring(size_t smem) {
+    static size_t set_smem = (size_t)-1;
+    static int per_sm = 0;
+    return resident_ctas_of(gemv_ring_kernel<MT, NT, XS>, smem, set_smem, per_sm, 32 * ring_warps(NT));
 }
 
 template <int FMT, int MT, int NT, bool STAGED>
@@ -687,6 +1191,52 @@ lq_status dispatch_fmt(int mode, bool staged, const FParams& P, int64_t grid, si
     }
 }
 
+template <int MT, int NT, bool XS>
+lq_status ring_launch(int mode, const FParams& P, int64_t grid, size_t smem, int* per_sm, cudaStream_t stream) {
+    if (mode == 0) {
+        *per_sm = resident_ctas_ring<MT, NT, XS>(smem);
+        return *per_sm < 0 ? LQ_ERR_CUDA : LQ_OK;
+    }
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(32 * ring_warps(NT));
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, gemv_ring_kernel<MT, NT, XS>, P) != cudaSuccess) return LQ_ERR_CUDA;
+    return cudaPeekAtLastError() == cudaSuccess ? LQ_OK : LQ_ERR_CUDA;
+}
+
+template <int MT, int NT>
+lq_status ring_mt(int mode, bool xs, const FParams& P, int64_t grid, size_t smem, int* per_sm, cudaStream_t stream) {
+    return xs ? ring_launch<MT, NT, true>(mode, P, grid, smem, per_sm, stream)
+              : ring_launch<MT, NT, false>(mode, P, grid, smem, per_sm, stream);
+}
+
+lq_status dispatch_ring(int mode, bool xs, const FParams& P, int64_t grid, size_t smem, int* per_sm,
+                        cudaStream_t stream) {
+    switch (P.M) {
+        case 1: return ring_mt<1, 1>(mode, xs, P, grid, smem, per_sm, stream);
+        case 2: return ring_mt<2, 1>(mode, xs, P, grid, smem, per_sm, stream);
+        case 3: return ring_mt<3, 1>(mode, xs, P, grid, smem, per_sm, stream);
+        case 4: return ring_mt<4, 1>(mode, xs, P, grid, smem, per_sm, stream);
+        case 5: return ring_mt<5, 1>(mode, xs, P, grid, smem, per_sm, stream);
+        case 6: return ring_mt<6, 1>(mode, xs, P, grid, smem, per_sm, stream);
+        case 7: return ring_mt<7, 1>(mode, xs, P, grid, smem, per_sm, stream);
+        case 8: return ring_mt<8, 1>(mode, xs, P, grid, smem, per_sm, stream);
+        default:
+            if (P.M <= 16) return ring_mt<0, 2>(mode, xs, P, grid, smem, per_sm, stream);
+            if (P.M <= 24) return ring_mt<0, 3>(mode, xs, P, grid, smem, per_sm, stream);
+            if (P.M <= 32) return ring_mt<0, 4>(mode, xs, P, grid, smem, per_sm, stream);
+            return LQ_ERR_UNSUPPORTED;
+    }
+}
+
 lq_status dispatch(int fmt, int mode, bool staged, const FParams& P, int64_t grid, size_t smem, int* per_sm,
                    cudaStream_t stream) {
     return fmt == LQ_FMT_2BIT_LM_G32 ? dispatch_fmt<LQ_FMT_2BIT_LM_G32>(mode, staged, P, grid, smem, per_sm, stream)
@@ -726,6 +1276,14 @@ lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* probs, i
     P.y_dtype = probs[0].y_dtype;
     P.format = Q.format = fmt;
     P.x_bf16 = Q.x_bf16 = probs[0].x_dtype == LQ_BF16;
+    // 2-bit launches of up to eight tokens run the ring kernel (measured faster there); NF4
+    // and more tokens run the register-fed one.  LQ_GEMV_KERNEL=stream / ring forces either
+    // for 2-bit (comparisons and tests).
+    const char* kern_env = getenv("LQ_GEMV_KERNEL");
+    const bool use_ring = fmt == LQ_FMT_2BIT_LM_G32 && (M <= 8 || (kern_env && strcmp(kern_env, "ring") == 0)) &&
+                          !(kern_env && strcmp(kern_env, "stream") == 0);
+    const int rows_blk = use_ring ? kRingRows : 16;            // output rows per row block
+    const int cta_warps = use_ring ? ring_warps(M <= 8 ? 1 : 2) : kWarps;
 
     int64_t units = 0, jobs = 0, xhalves = 0, blocks = 0;
     int max_k = 0;
@@ -756,12 +1314,14 @@ lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* probs, i
         const int a_pad = A > 0 ? round_up(A, kAnchorCols) : 0;
         d.steps = q.K / 256;
         d.su = d.steps + a_pad / kAnchorCols;
-        d.rblocks = (q.N + 15) / 16;
+        d.G = d.su > d.steps ? d.su / (d.su - d.steps) : d.su + 1;
+        d.rblocks = (q.N + rows_blk - 1) / rows_blk;
         d.unit_begin = units;
         units += (int64_t)q.batch * d.rblocks * d.su;
         blocks += (int64_t)q.batch * d.rblocks;
-        // per member: [x in fragment order (M*K) | x at the anchors (M*a_pad)]
-        d.xperm_stride = d.xaperm_stride = (int64_t)M * (q.K + a_pad);
+        // per member: [x (fragment order, or the ring layout) | x at the anchors (M*a_pad)]
+        d.xa_off = use_ring ? (q.K / 16) * ring_kstride(M) : M * q.K;
+        d.xperm_stride = d.xaperm_stride = (int64_t)d.xa_off + (int64_t)M * a_pad;
         d.xoff = xhalves;
         xhalves += (int64_t)q.batch * d.xperm_stride;
         e.x = d.x;
@@ -782,11 +1342,16 @@ lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* probs, i
     if (units == 0) return LQ_OK;
     // arrival counts live in the counter area, which every kernel leaves at zero
     if ((size_t)blocks > ws.num_counters) return LQ_ERR_UNSUPPORTED;
+    const size_t ring_smem = (size_t)cta_warps * kRingDepth * kRingStage;
     // size the grid; the warp partition then fixes the x span of each CTA
     int per_sm = 0;
-    if (dispatch(fmt, 0, false, P, 0, 0, &per_sm, stream) != LQ_OK) return LQ_ERR_CUDA;
-    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>((units + kWarps - 1) / kWarps, (int64_t)ws.num_sms * std::max(1, per_sm)));
-    const int64_t W = std::min<int64_t>(grid * kWarps, units);
+    if (use_ring) {
+        if (dispatch_ring(0, false, P, 0, ring_smem, &per_sm, stream) != LQ_OK) return LQ_ERR_CUDA;
+    } else if (dispatch(fmt, 0, false, P, 0, 0, &per_sm, stream) != LQ_OK) {
+        return LQ_ERR_CUDA;
+    }
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>((units + cta_warps - 1) / cta_warps, (int64_t)ws.num_sms * std::max(1, per_sm)));
+    const int64_t W = std::min<int64_t>(grid * cta_warps, units);
     P.total_units = units;
     P.total_warps = W;
     // With LQ_GEMV_STAGE=1 each CTA builds the x its units read in shared memory when that
@@ -794,19 +1359,28 @@ lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* probs, i
     // by default the pre-pass does it once for all CTAs (measured faster on this part), and the
     // per-CTA spans are not needed.
     const char* st_env = getenv("LQ_GEMV_STAGE");
-    const bool want_stage = st_env && atoi(st_env) == 1;
-    int64_t max_span = 0, max_members = 0;
-    for (int64_t b = 0; want_stage && b < grid; ++b) {
-        const int64_t w_lo = b * kWarps, w_hi = std::min<int64_t>(w_lo + kWarps, W);
+    const bool want_stage = !use_ring && st_env && atoi(st_env) == 1;
+    int64_t max_span = 0, max_members = 0, max_raw = 0, max_idx = 0, max_bits = 0;
+    for (int64_t b = 0; (want_stage || use_ring) && b < grid; ++b) {
+        const int64_t w_lo = b * cta_warps, w_hi = std::min<int64_t>(w_lo + cta_warps, W);
         if (w_lo >= W) break;
         int pa, pb;
         int64_t la, lb;
         host_locate(P, units * w_lo / W, pa, la);
         host_locate(P, units * w_hi / W - 1, pb, lb);
         max_span = std::max<int64_t>(max_span, P.d[pb].xoff + (lb + 1) * P.d[pb].xperm_stride - (P.d[pa].xoff + la * P.d[pa].xperm_stride));
-        int64_t members = 0;
-        for (int p = pa; p <= pb; ++p) members += (p == pb ? lb : P.d[p].batch - 1) - (p == pa ? la : 0) + 1;
+        int64_t members = 0, raw = 0, idx = 0, bw = 0;
+        for (int p = pa; p <= pb; ++p) {
+            const int64_t n = (p == pb ? lb : P.d[p].batch - 1) - (p == pa ? la : 0) + 1;
+            members += n;
+            raw += n * M * P.d[p].K;
+            idx += n * P.d[p].A;
+            bw += n * (P.d[p].K / 32);
+        }
         max_members = std::max(max_members, members);
+        max_raw = std::max(max_raw, raw);
+        max_idx = std::max(max_idx, idx);
+        max_bits = std::max(max_bits, bw);
     }
     P.bitmap_words = std::max(1, max_k / 32);
     const size_t smem = (size_t)max_span * 2 + (size_t)P.bitmap_words * 4;
@@ -816,41 +1390,56 @@ lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* probs, i
         if (dispatch(fmt, 0, true, P, 0, smem, &per_sm_s, stream) != LQ_OK) return LQ_ERR_CUDA;
         staged = per_sm_s >= per_sm;   // staging must not cost occupancy
     }
+    // the ring kernel reads x from shared memory when each CTA's span of the x buffer fits
+    // without costing occupancy (LQ_GEMV_XS=0 keeps x in global memory)
+    const char* xs_env = getenv("LQ_GEMV_XS");
+    bool ring_xs = use_ring && max_members <= 4 && !(xs_env && xs_env[0] == '0');
+    const size_t ring_xs_smem = ring_smem + align256((size_t)max_span * 2);
+    if (ring_xs) {
+        int per_sm_x = 0;
+        if (ring_xs_smem > (size_t)ws.max_smem_optin ||
+            dispatch_ring(0, true, P, 0, ring_xs_smem, &per_sm_x, stream) != LQ_OK || per_sm_x < per_sm)
+            ring_xs = false;
+    }
     const int64_t min_run = units / W;   // every warp's run has at least this many units (>= 1)
-    size_t ws_bytes = staged ? 0 : align256((size_t)xhalves * 2);
+    const bool no_xbuf = staged || (use_ring && ring_xs);   // x is built in shared memory by each CTA
+    size_t ws_bytes = no_xbuf ? 0 : align256((size_t)xhalves * 2);
     for (int i = 0; i < count; ++i) {
         FDesc& d = P.d[i];
         d.cmax = (int)std::min<int64_t>(d.su / min_run + 2, d.su);
-        ws_bytes += align256((size_t)probs[i].batch * d.rblocks * d.cmax * M * 16 * 4);
+        ws_bytes += align256((size_t)probs[i].batch * d.rblocks * d.cmax * M * rows_blk * 4);
     }
     if (ws_bytes + 256 > ws.partial_floats * sizeof(float)) return LQ_ERR_WORKSPACE;
     // workspace: x copies (pre-pass only), then per problem the partial-sum slots
     char* wp = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(ws.partials) + 255) & ~uintptr_t(255));
     uint16_t* xbuf = reinterpret_cast<uint16_t*>(wp);
-    if (!staged) wp += align256((size_t)xhalves * 2);
+    if (!no_xbuf) wp += align256((size_t)xhalves * 2);
     P.xbuf = xbuf;
     unsigned* cnt = ws.counters;
     for (int i = 0; i < count; ++i) {
         FDesc& d = P.d[i];
         const lq_problem& q = probs[i];
         d.xperm = Q.d[i].xperm = xbuf + d.xoff;
-        d.xaperm = Q.d[i].xaperm = xbuf + d.xoff + (int64_t)M * q.K;
+        d.xaperm = Q.d[i].xaperm = xbuf + d.xoff + d.xa_off;
         d.part = reinterpret_cast<float*>(wp);
-        wp += align256((size_t)q.batch * d.rblocks * d.cmax * M * 16 * 4);
+        wp += align256((size_t)q.batch * d.rblocks * d.cmax * M * rows_blk * 4);
         d.cnt = cnt;
         cnt += (int64_t)q.batch * d.rblocks;
     }
     if (ws.clear_counters && cudaMemsetAsync(ws.counters, 0, sizeof(unsigned) * (size_t)blocks, stream) != cudaSuccess)
         return LQ_ERR_CUDA;
     Q.total_jobs = jobs;
+    Q.ring = use_ring ? 1 : 0;
     int unused = 0;
     if (staged) return dispatch(fmt, 1, true, P, grid, smem, &unused, stream);
+    if (use_ring && ring_xs) return dispatch_ring(1, true, P, grid, ring_xs_smem, &unused, stream);
 
     // x pre-pass, then the main kernel, chained by programmatic dependent launch
     const int64_t prep_ctas = (jobs + kPrepWarps - 1) / kPrepWarps;
     if (prep_ctas > 0x7fffffffLL) return LQ_ERR_UNSUPPORTED;
     xprep_kernel<<<(unsigned)prep_ctas, 32 * kPrepWarps, 0, stream>>>(Q);
     if (cudaPeekAtLastError() != cudaSuccess) return LQ_ERR_CUDA;
+    if (use_ring) return dispatch_ring(1, ring_xs, P, grid, ring_xs ? ring_xs_smem : ring_smem, &unused, stream);
     return dispatch(fmt, 1, false, P, grid, 0, &unused, stream);
 }
 

@@ -186,18 +186,6 @@ def uniform_minmax_mse(samples: np.ndarray, group: int) -> float:
     return float(np.mean((x - (lo + q * step)) ** 2))
 
 
-def lloyd_minmax_group_mse(samples: np.ndarray, group: int) -> float:
-    """MSE of the page's codebook on the same groups: normalise, nearest centroid, OLS fit."""
-    x = np.asarray(samples, dtype=np.float64)
-    x = x[: len(x) // group * group].reshape(-1, group)
-    err = 0.0
-    for row in x:
-        q = nearest_centroid(_normalise(row))
-        S, Z = ols_fit(row, np.asarray(CODEBOOK)[q])
-        err += float(np.sum((row - (S * np.asarray(CODEBOOK)[q] + Z)) ** 2))
-    return err / x.size
-
-
 # ---------------------------------------------------------------------------
 # 2-bit quantizer (sections 3 and 4)
 # ---------------------------------------------------------------------------

@@ -262,6 +262,51 @@ def test_anchor_selection_brute_force_and_ties():
     assert O.select_anchors(W2, p2).tolist() == [10, 11, 12, 13, 14, 15, 16]
 
 
+def test_activation_profile_is_mean_abs_of_gaussian_channels():
+    """mean|X_c| of zero-mean Gaussian samples with std sigma_c, against the analytic profile.
+
+    The profile enters the otf-llm README's impact score (section 4) as mean|X_c|.  Samples
+    drawn with known sigma give the mean absolute value directly; the analytic form must sit
+    within three standard errors of it for every sigma.  sqrt(pi/2)*sigma, sigma**2 or a
+    missing square root each land hundreds of standard errors away.
+    """
+    g = np.random.default_rng(31)
+    sig = np.array([0.25, 1.0, 3.0, 20.0])
+    n = 400_000
+    X = g.normal(0.0, 1.0, (n, len(sig))) * sig
+    mean_abs = np.mean(np.abs(X), axis=0)
+    se = np.std(np.abs(X), axis=0, ddof=1) / math.sqrt(n)
+    prof = O.activation_profile(sig)
+    assert np.all(np.abs(prof - mean_abs) <= 3.0 * se), (prof, mean_abs, se)
+
+
+def test_anchor_selection_with_unequal_channel_sigmas_matches_sampled_profile():
+    """Columns whose norms and activation sigmas both vary: the oracle's choice from the
+    analytic profile equals a brute-force choice from sampled mean|X_c|.
+
+    The test matrix is built so that scoring with sigma_c**2 (or a norm-only rule) picks a
+    different set: column norms fall as sigma rises, so the product decides the ranking.
+    """
+    g = np.random.default_rng(32)
+    K, N = 200, 16
+    sigma = np.linspace(0.5, 6.0, K)
+    g.shuffle(sigma)
+    W = g.normal(0.0, 1.0, (N, K))
+    W /= np.sqrt(np.sum(W * W, axis=0))                  # unit column norms
+    W *= (30.0 / sigma) ** 0.5 * (1.0 + 0.4 * g.uniform(size=K))   # norms fall as sigma rises
+    A = O.anchor_count(K)
+    n = 200_000
+    X = g.normal(0.0, 1.0, (n, K)) * sigma
+    sampled = np.mean(np.abs(X), axis=0)
+    score = [math.sqrt(sum(float(W[r, c]) ** 2 for r in range(N))) * float(sampled[c]) for c in range(K)]
+    brute = sorted(sorted(range(K), key=lambda c: (-score[c], c))[:A])
+    got = O.select_anchors(W, O.activation_profile(sigma)).tolist()
+    assert got == brute
+    # the same matrix scored with sigma squared or with the norm alone picks other columns
+    assert O.select_anchors(W, sigma ** 2).tolist() != got
+    assert O.select_anchors(W, np.ones(K)).tolist() != got
+
+
 # ---------------------------------------------------------------- packing
 
 def test_pack_2bit_worked_examples():
@@ -427,6 +472,27 @@ def test_matmul_ref_is_not_transposed():
     x[0, 3] = 2.0
     y, _ = O.matmul_ref(W, x.view(np.uint16), "f16")
     assert y.tolist() == [[0.0, 2.0]]
+
+
+def test_row_error_scale_equals_matmul_error_scale():
+    """The sampled parity tests take their tolerance scale from row_error_scale (numpy);
+    it must equal the compiled matmul_ref's E for both x dtypes, and equal |y| when every
+    product is non-negative (E is then the sum itself)."""
+    g = np.random.default_rng(33)
+    for (M, N, K) in [(1, 3, 64), (4, 7, 256), (2, 5, 512)]:
+        W = g.normal(0, 0.02, (N, K)).astype(np.float32)
+        for xdt in ("f16", "bf16"):
+            x = synth.activations(M, K, xdt, seed=K + M)
+            _, E = O.matmul_ref(W, x, xdt)
+            Er = O.row_error_scale(W, x, xdt)
+            assert Er.shape == E.shape
+            assert np.all(np.abs(Er - E) <= 1e-12 * E)
+    Wp = np.abs(g.normal(0, 1, (3, 96))).astype(np.float32)
+    xp = np.abs(g.normal(0, 1, (2, 96))).astype(np.float16).view(np.uint16)
+    y, _ = O.matmul_ref(Wp, xp, "f16")
+    assert np.all(np.abs(O.row_error_scale(Wp, xp, "f16") - y) <= 1e-12 * y)
+    # flipping the sign of W or x leaves E unchanged
+    assert np.array_equal(O.row_error_scale(-Wp, xp, "f16"), O.row_error_scale(Wp, xp, "f16"))
 
 
 def test_row_gemv_matches_full_matmul():
