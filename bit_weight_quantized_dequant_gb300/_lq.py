@@ -9,7 +9,8 @@ import ctypes
 from dataclasses import dataclass
 from pathlib import Path
 
-LQ_OK, LQ_ERR_INVALID_ARG, LQ_ERR_UNSUPPORTED, LQ_ERR_ALIGNMENT, LQ_ERR_WORKSPACE, LQ_ERR_CUDA, LQ_ERR_TIMEOUT = range(7)
+LQ_OK, LQ_ERR_INVALID_ARG, LQ_ERR_UNSUPPORTED, LQ_ERR_ALIGNMENT, LQ_ERR_WORKSPACE, LQ_ERR_CUDA, LQ_ERR_TIMEOUT, \
+    LQ_ERR_RANGE = range(8)
 FMT_2BIT, FMT_NF4 = 1, 2
 F32, F16, BF16 = 0, 1, 2
 

@@ -136,6 +136,7 @@ LQ_API const char* lq_status_string(int status) {
         case LQ_ERR_WORKSPACE: return "handle workspace too small for this call";
         case LQ_ERR_CUDA: return "CUDA error";
         case LQ_ERR_TIMEOUT: return "a bounded device-side wait ran out";
+        case LQ_ERR_RANGE: return "a dequantized weight is outside the binary16 range of the decode GEMV's operands";
         default: return "unknown status";
     }
 }
@@ -205,7 +206,7 @@ LQ_API lq_status lq_sync(lq_handle h) {
     if (cudaDeviceSynchronize() != cudaSuccess) return LQ_ERR_CUDA;
     int flag = 0;
     if (cudaMemcpy(&flag, h->status_flag, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return LQ_ERR_CUDA;
-    if (flag != 0) {
+    if (flag & 1) {
         // a wait ran out: the launch that timed out may have left arrival counts behind, so they
         // are cleared with the flag
         if (cudaMemset(h->status_flag, 0, 256) != cudaSuccess ||
@@ -213,6 +214,12 @@ LQ_API lq_status lq_sync(lq_handle h) {
             cudaDeviceSynchronize() != cudaSuccess)
             return LQ_ERR_CUDA;
         return LQ_ERR_TIMEOUT;
+    }
+    if (flag & 2) {
+        // a decode GEMV met a weight outside the binary16 range of its tensor-core operands
+        if (cudaMemset(h->status_flag, 0, 256) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess)
+            return LQ_ERR_CUDA;
+        return LQ_ERR_RANGE;
     }
     return LQ_OK;
 }
@@ -413,8 +420,8 @@ LQ_API lq_status lq_gemv_noalloc(int format, const uint8_t* codes, const void* s
     ws.num_sms = slot.num_sms;
     ws.max_smem_optin = slot.max_smem_optin;
     ws.counters = static_cast<unsigned*>(slot.base);
-    ws.num_counters = kStaticCounters - 64;              // the last words hold the timeout flag
-    ws.status = reinterpret_cast<int*>(static_cast<unsigned*>(slot.base) + kStaticCounters - 1);
+    ws.num_counters = kStaticCounters;
+    ws.status = nullptr;   // (no handle, so no lq_sync to report device-side status through)
     ws.partials = reinterpret_cast<float*>(static_cast<char*>(slot.base) + kStaticCounters * sizeof(unsigned));
     ws.partial_floats = kStaticPartialFloats;
     ws.clear_counters = true;

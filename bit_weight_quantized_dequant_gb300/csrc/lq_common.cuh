@@ -72,6 +72,29 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// ---- x in the decode kernels' binary16 operand range ---------------------------------
+//
+// bf16 x reaches the decode tensor cores as binary16.  Each token's x is first scaled by
+// the power of two 2^e that brings its largest |x| into [2^14, 2^15) (e clamped to
+// [-125, 125]; e = 0 when x is all zero); the fp32 result is multiplied by 2^-e.  Both
+// factors are exact, so the only rounding is the one to binary16, relative 2^-11 for every
+// value within 2^28 of the token's largest.  maxbits is the fp32 bit pattern of max |x|.
+__device__ __forceinline__ int x_scale_exp(uint32_t maxbits) {
+    if (maxbits == 0u) return 0;
+    const int e = 14 - ((int)(maxbits >> 23) - 127);
+    return e < -125 ? -125 : (e > 125 ? 125 : e);
+}
+__device__ __forceinline__ float x_scale(uint32_t maxbits) { return __int_as_float((x_scale_exp(maxbits) + 127) << 23); }
+__device__ __forceinline__ float x_unscale(uint32_t maxbits) { return __int_as_float((127 - x_scale_exp(maxbits)) << 23); }
+
+// bf16 bits -> binary16 bits of (value * scale), round to nearest even.
+__device__ __forceinline__ uint16_t bf16_to_half_scaled(uint16_t raw, float scale) {
+    return __half_as_ushort(__float2half_rn(__uint_as_float(((uint32_t)raw) << 16) * scale));
+}
+
+// Largest value the weight lookup tables may hold: binary16 rounds |v| >= 65520 to infinity.
+constexpr float kHalfOverflow = 65520.0f;
+
 // Store one fp32 result in the requested output dtype.
 __device__ __forceinline__ void store_out(void* y, size_t idx, int dtype, float v) {
     if (dtype == LQ_F32) {

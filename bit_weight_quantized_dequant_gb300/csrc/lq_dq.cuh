@@ -21,6 +21,16 @@ __device__ __forceinline__ void lut2_bits(uint16_t s_bits, uint16_t z_bits, uint
     P23 = pack_half2_rn(__fmaf_rn(s, 0.45f, z), __fmaf_rn(s, 1.52f, z));
 }
 
+// The same table, also raising `peak` to the group's largest |fmaf(S, C[q], Z)|, which is
+// fmaf(1.52, |S|, |Z|) exactly; a peak >= kHalfOverflow means a table value overflowed.
+__device__ __forceinline__ void lut2_bits_peak(uint16_t s_bits, uint16_t z_bits, uint32_t& P01, uint32_t& P23,
+                                               float& peak) {
+    const float s = half_bits_to_float(s_bits), z = half_bits_to_float(z_bits);
+    P01 = pack_half2_rn(__fmaf_rn(s, -1.52f, z), __fmaf_rn(s, -0.45f, z));
+    P23 = pack_half2_rn(__fmaf_rn(s, 0.45f, z), __fmaf_rn(s, 1.52f, z));
+    peak = fmaxf(peak, __fmaf_rn(1.52f, fabsf(s), fabsf(z)));
+}
+
 // Codes at bit offset 2j of the four bytes of w -> binary16 pairs (byte0, byte1) in `lo`
 // and (byte2, byte3) in `hi`.  One multiply turns each 2-bit code q into the selector
 // nibbles (2q, 2q+1) of its byte lane; the upper half of that word serves bytes 2 and 3.

@@ -81,13 +81,11 @@ __device__ __forceinline__ int xa_offset(int m, int a, int a_pad, int M, int bas
     return base + 8 * nt * a_pad + ((a >> 4) * tile_tokens(M, nt) + gg) * 16 + tt * 4 + hh;
 }
 
-__device__ __forceinline__ uint16_t x_to_half_bits(uint16_t v, int x_bf16) {
-    return x_bf16 ? __half_as_ushort(__float2half_rn(bf16_bits_to_float(v))) : v;
-}
 
 // Byte-split 4-entry table of binary16 fmaf(s, C[q], z): RA holds the low bytes, RB the high bytes.
-__device__ __forceinline__ void lut2(uint16_t s_bits, uint16_t z_bits, uint32_t& RA, uint32_t& RB) {
+__device__ __forceinline__ void lut2(uint16_t s_bits, uint16_t z_bits, uint32_t& RA, uint32_t& RB, float& peak) {
     const float s = half_bits_to_float(s_bits), z = half_bits_to_float(z_bits);
+    peak = fmaxf(peak, __fmaf_rn(1.52f, fabsf(s), fabsf(z)));   // the table's largest |value| (binary16 range check)
     const uint32_t p01 = pack_half2_rn(__fmaf_rn(s, -1.52f, z), __fmaf_rn(s, -0.45f, z));
     const uint32_t p23 = pack_half2_rn(__fmaf_rn(s, 0.45f, z), __fmaf_rn(s, 1.52f, z));
     RA = prmt(p01, p23, 0x6420);
@@ -170,12 +168,12 @@ __device__ __forceinline__ Frag2 load2(const uint8_t* cg, const uint8_t* cg8, co
 
 template <int NT>
 __device__ __forceinline__ void compute2(const Frag2& f, float (&acc)[NT][4], const uint16_t* xs, int step,
-                                         int klen_pad, int M, int g, int t) {
+                                         int klen_pad, int M, int g, int t, float& peak) {
     uint32_t RA[4], RB[4];
-    lut2((uint16_t)f.sg, (uint16_t)f.zg, RA[0], RB[0]);
-    lut2((uint16_t)(f.sg >> 16), (uint16_t)(f.zg >> 16), RA[1], RB[1]);
-    lut2((uint16_t)f.sg8, (uint16_t)f.zg8, RA[2], RB[2]);
-    lut2((uint16_t)(f.sg8 >> 16), (uint16_t)(f.zg8 >> 16), RA[3], RB[3]);
+    lut2((uint16_t)f.sg, (uint16_t)f.zg, RA[0], RB[0], peak);
+    lut2((uint16_t)(f.sg >> 16), (uint16_t)(f.zg >> 16), RA[1], RB[1], peak);
+    lut2((uint16_t)f.sg8, (uint16_t)f.zg8, RA[2], RB[2], peak);
+    lut2((uint16_t)(f.sg8 >> 16), (uint16_t)(f.zg8 >> 16), RA[3], RB[3], peak);
     const uint32_t wg[4] = {f.cg.x, f.cg.y, f.cg.z, f.cg.w};
     const uint32_t wg8[4] = {f.cg8.x, f.cg8.y, f.cg8.z, f.cg8.w};
 #pragma unroll
@@ -306,7 +304,9 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const __grid_constan
         }
     }
 
-    // ---- stage x (binary16, fragment order) and the gathered anchor columns
+    // ---- stage x (binary16, fragment order; bf16 x scaled per token, see x_scale) and the
+    // gathered anchor columns
+    const uint32_t* xmaxw = P.x_bf16 ? D.xmax + l * M : nullptr;
     if (has_codes) {
         const int chunks = klen_pad / 8;
         for (int idx = tid; idx < M * chunks; idx += kGemvThreads) {
@@ -316,8 +316,10 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const __grid_constan
             if (kk < klen) v = *reinterpret_cast<const uint4*>(x + (int64_t)m * K + k0 + kk);
             const uint16_t h[8] = {(uint16_t)v.x, (uint16_t)(v.x >> 16), (uint16_t)v.y, (uint16_t)(v.y >> 16),
                                    (uint16_t)v.z, (uint16_t)(v.z >> 16), (uint16_t)v.w, (uint16_t)(v.w >> 16)};
+            const float sc = P.x_bf16 ? x_scale(xmaxw[m]) : 1.f;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) xs[xs_offset<FMT>(m, kk + e, klen_pad, M)] = x_to_half_bits(h[e], P.x_bf16);
+            for (int e = 0; e < 8; ++e)
+                xs[xs_offset<FMT>(m, kk + e, klen_pad, M)] = P.x_bf16 ? bf16_to_half_scaled(h[e], sc) : h[e];
         }
     }
     if (FMT == LQ_FMT_2BIT_LM_G32 && do_anchors) {
@@ -326,7 +328,9 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const __grid_constan
             const int m = idx / ap;
             const int a = idx - m * ap;
             uint16_t v = 0;
-            if (a < A) v = x_to_half_bits(x[(int64_t)m * K + anchor_idx[a]], P.x_bf16);
+            const int k = a < A ? anchor_idx[a] : -1;
+            if ((unsigned)k < (unsigned)K)
+                v = P.x_bf16 ? bf16_to_half_scaled(x[(int64_t)m * K + k], x_scale(xmaxw[m])) : x[(int64_t)m * K + k];
             xs[xa_offset(m, a, a_pad, M, a_base)] = v;
         }
     }
@@ -344,6 +348,7 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const __grid_constan
     float acc[NT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+    float peak = 0.f;
 
     // ---- main loop over K
     if (has_codes) {
@@ -353,7 +358,7 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const __grid_constan
                 if (s + 1 < nsteps)
                     nxt = load2(cg + 64 * (s + 1), cg8 + 64 * (s + 1), sg + 8 * (s + 1), zg + 8 * (s + 1),
                                 sg8 + 8 * (s + 1), zg8 + 8 * (s + 1), klen - kStep * (s + 1) - 64 * t, vg, vg8, wide);
-                compute2<NT>(f2, acc, xs, s, klen_pad, M, g, t);
+                compute2<NT>(f2, acc, xs, s, klen_pad, M, g, t, peak);
                 f2 = nxt;
             }
         } else {
@@ -401,17 +406,19 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const __grid_constan
     }
 
     // ---- epilogue
+    if (FMT == LQ_FMT_2BIT_LM_G32 && peak >= kHalfOverflow && P.status) atomicOr(P.status, 2);
+    auto unscale = [&](int m) -> float { return P.x_bf16 ? x_unscale(xmaxw[m]) : 1.f; };
     if (D.parts == 1) {
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             const int m0 = 8 * nt + 2 * t, m1 = m0 + 1;
             if (vg) {
-                if (m0 < M) store_out(y, (size_t)m0 * N + rg, P.y_dtype, acc[nt][0]);
-                if (m1 < M) store_out(y, (size_t)m1 * N + rg, P.y_dtype, acc[nt][1]);
+                if (m0 < M) store_out(y, (size_t)m0 * N + rg, P.y_dtype, acc[nt][0] * unscale(m0));
+                if (m1 < M) store_out(y, (size_t)m1 * N + rg, P.y_dtype, acc[nt][1] * unscale(m1));
             }
             if (vg8) {
-                if (m0 < M) store_out(y, (size_t)m0 * N + rg8, P.y_dtype, acc[nt][2]);
-                if (m1 < M) store_out(y, (size_t)m1 * N + rg8, P.y_dtype, acc[nt][3]);
+                if (m0 < M) store_out(y, (size_t)m0 * N + rg8, P.y_dtype, acc[nt][2] * unscale(m0));
+                if (m1 < M) store_out(y, (size_t)m1 * N + rg8, P.y_dtype, acc[nt][3] * unscale(m1));
             }
         }
         return;
@@ -447,7 +454,7 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const __grid_constan
         if (n >= N) continue;
         float sum = 0.f;
         for (int pp = 0; pp < D.parts; ++pp) sum += __ldcg(strip_base + ((int64_t)pp * M + m) * kGemvStripRows + rr);
-        store_out(y, (size_t)m * N + n, P.y_dtype, sum);
+        store_out(y, (size_t)m * N + n, P.y_dtype, sum * unscale(m));
     }
     if (tid == 0) P.counters[strip_id] = 0u;
 }
@@ -585,11 +592,19 @@ lq_status launch_gemv_regs(const GemvWorkspace& ws, const lq_problem* probs, int
         kc_pad = std::max(kc_pad, round_up(d.KC, kStep));
         if (d.A > 0 && (d.S == 1 || d.parts > d.S)) a_pad = std::max(a_pad, round_up(d.A, 16));
     }
-    if ((size_t)strip > ws.num_counters || (size_t)partial_floats > ws.partial_floats) return LQ_ERR_WORKSPACE;
+    // bf16 x: one max |x| word per (member, token) row after the partial sums
+    int64_t xrows = 0;
+    for (int i = 0; i < count; ++i) {
+        P.d[i].xmax = reinterpret_cast<const uint32_t*>(ws.partials + partial_floats) + xrows;
+        xrows += (int64_t)probs[i].batch * M;
+    }
+    if (!P.x_bf16) xrows = 0;
+    if ((size_t)strip > ws.num_counters || (size_t)(partial_floats + xrows) > ws.partial_floats) return LQ_ERR_WORKSPACE;
     P.kc_pad = kc_pad;
     P.a_pad = a_pad;
     P.partials = ws.partials;
     P.counters = ws.counters;
+    P.status = ws.status;
     P.total_units = unit;
     if (unit == 0) return LQ_OK;
     if (unit > 0x7fffffffLL) return LQ_ERR_UNSUPPORTED;
@@ -598,6 +613,10 @@ lq_status launch_gemv_regs(const GemvWorkspace& ws, const lq_problem* probs, int
     if (ws.clear_counters && strip > 0 &&
         cudaMemsetAsync(ws.counters, 0, sizeof(unsigned) * (size_t)strip, stream) != cudaSuccess)
         return LQ_ERR_CUDA;
+    if (P.x_bf16) {
+        const lq_status st = launch_xmax_rows(probs, count, reinterpret_cast<uint32_t*>(ws.partials + partial_floats), stream);
+        if (st != LQ_OK) return st;
+    }
     if (P.format == LQ_FMT_2BIT_LM_G32) return run_fmt<LQ_FMT_2BIT_LM_G32>(P, smem, stream);
     return run_fmt<LQ_FMT_NF4_B64>(P, smem, stream);
 }

@@ -63,6 +63,8 @@ struct PrepDesc {
     int K, A, a_pad, batch;
     int jobs;                  // jobs per batch member: K/256 steps, then ceil(a_pad/256) anchor slices
     int64_t job_begin;         // first job of this problem
+    int xsc_off;               // halves from a member's x copy to its per-token max |x| words (bf16 x)
+    int64_t row_begin;         // first (member, token) row of this problem, for the max |x| pass
 };
 
 struct PrepParams {
@@ -70,6 +72,7 @@ struct PrepParams {
     int count, M, x_bf16, format;
     int ring;                  // write the ring kernel's x layout (see ring_x_pos)
     int64_t total_jobs;
+    int64_t total_rows;        // (member, token) rows of all problems
 };
 
 // x layout of the ring kernel, per batch member: the code columns in blocks of 16 (block
@@ -99,6 +102,44 @@ constexpr int kPrepWarps = 2;   // jobs per pre-pass CTA
 
 __device__ __forceinline__ uint16_t to_half_bits(uint16_t raw, int x_bf16) {
     return x_bf16 ? __half_as_ushort(__float2half_rn(bf16_bits_to_float(raw))) : raw;
+}
+
+// bf16 x: max |x| of each (member, token) row over its K columns, as the fp32 bit pattern,
+// into the row's word after its x copy (x_scale turns it into the conversion factor).  One
+// CTA per row.  (|bf16| bit patterns order like the magnitudes, so the maximum is taken
+// on the 15-bit patterns.)
+__global__ void __launch_bounds__(256) xmax_kernel(const __grid_constant__ PrepParams P) {
+    __shared__ uint32_t red[8];
+    const int64_t row = blockIdx.x;
+    int p = 0;
+    while (p + 1 < P.count && row >= P.d[p + 1].row_begin) ++p;
+    const PrepDesc& D = P.d[p];
+    const int64_t r = row - D.row_begin, l = r / P.M;
+    const int m = (int)(r - l * P.M), K = D.K;
+    const uint4* x = reinterpret_cast<const uint4*>(reinterpret_cast<const char*>(D.x) + l * D.stride_x) + (int64_t)m * K / 8;
+    uint32_t mx = 0;
+    for (int i = threadIdx.x; i < K / 8; i += 256) {
+        const uint4 v = __ldg(x + i);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) mx = max(mx, max(w[j] & 0x7FFFu, (w[j] >> 16) & 0x7FFFu));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int i = 1; i < 8; ++i) mx = max(mx, red[i]);
+        *reinterpret_cast<uint32_t*>(D.xperm + l * D.xperm_stride + D.xsc_off + 2 * m) = mx << 16;
+    }
+}
+
+// The conversion factor of token m of member l (1 for binary16 x).
+__device__ __forceinline__ float prep_scale(const PrepParams& P, const PrepDesc& D, int64_t l, int m) {
+    return P.x_bf16 ? x_scale(*reinterpret_cast<const uint32_t*>(D.xperm + l * D.xperm_stride + D.xsc_off + 2 * m)) : 1.f;
+}
+__device__ __forceinline__ uint16_t to_half_scaled(uint16_t raw, int x_bf16, float scale) {
+    return x_bf16 ? bf16_to_half_scaled(raw, scale) : raw;
 }
 
 __global__ void __launch_bounds__(32 * kPrepWarps) xprep_kernel(const __grid_constant__ PrepParams P) {
@@ -132,14 +173,15 @@ __global__ void __launch_bounds__(32 * kPrepWarps) xprep_kernel(const __grid_con
         uint16_t* dst = D.xperm + l * D.xperm_stride + (int64_t)(k0 / 16) * S;
         for (int it = lane; it < 16 * M; it += 32) {
             const int m = it >> 4, ql = it & 15;
+            const float sc = prep_scale(P, D, l, m);
             const uint4* src = reinterpret_cast<const uint4*>(x + (int64_t)m * K + k0 + 16 * ql);
             const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
             uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w}, o[8];
             const uint32_t amask = (step_bits[warp][ql >> 1] >> (16 * (ql & 1))) & 0xFFFFu;   // anchor columns of the block
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                const uint32_t lo = (amask >> (2 * i)) & 1u ? 0u : to_half_bits((uint16_t)w[i], P.x_bf16);
-                const uint32_t hi = (amask >> (2 * i + 1)) & 1u ? 0u : to_half_bits((uint16_t)(w[i] >> 16), P.x_bf16);
+                const uint32_t lo = (amask >> (2 * i)) & 1u ? 0u : to_half_scaled((uint16_t)w[i], P.x_bf16, sc);
+                const uint32_t hi = (amask >> (2 * i + 1)) & 1u ? 0u : to_half_scaled((uint16_t)(w[i] >> 16), P.x_bf16, sc);
                 w[i] = lo | (hi << 16);
             }
             ring_x_transpose(w, o);
@@ -196,6 +238,7 @@ __global__ void __launch_bounds__(32 * kPrepWarps) xprep_kernel(const __grid_con
             for (int c = 0; c < C; ++c) {
                 const int it = it0 + 32 * c + lane;
                 if (it >= 32 * M) continue;
+                const float sc = prep_scale(P, D, l, tok(it));
                 uint32_t w[4];
 #pragma unroll
                 for (int e2 = 0; e2 < 4; ++e2) {
@@ -204,7 +247,7 @@ __global__ void __launch_bounds__(32 * kPrepWarps) xprep_kernel(const __grid_con
                     for (int h = 0; h < 2; ++h) {
                         const int e = 2 * e2 + h, kl = col(it, e);
                         const bool anchor = (step_bits[warp][kl >> 5] >> (kl & 31)) & 1u;
-                        pr |= (uint32_t)(anchor ? (uint16_t)0 : to_half_bits(v[c][e], P.x_bf16)) << (16 * h);
+                        pr |= (uint32_t)(anchor ? (uint16_t)0 : to_half_scaled(v[c][e], P.x_bf16, sc)) << (16 * h);
                     }
                     w[e2] = pr;
                 }
@@ -218,13 +261,14 @@ __global__ void __launch_bounds__(32 * kPrepWarps) xprep_kernel(const __grid_con
         for (int it = lane; it < n_slots * M / 8; it += 32) {
             const int d0 = 8 * it, line = d0 >> 4, pos0 = d0 & 15;
             const int bl = line / M, m = line - bl * M;
+            const float sc = prep_scale(P, D, l, m);
             uint16_t v[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const int pos = pos0 + e, tt = pos >> 2, hh = pos & 3;
                 const int a = a_base + 16 * bl + 2 * tt + (hh & 1) + 8 * (hh >> 1);
                 const int k = a < A ? __ldg(aidx + a) : -1;
-                v[e] = (unsigned)k < (unsigned)K ? to_half_bits(x[(int64_t)m * K + k], P.x_bf16) : (uint16_t)0;
+                v[e] = (unsigned)k < (unsigned)K ? to_half_scaled(x[(int64_t)m * K + k], P.x_bf16, sc) : (uint16_t)0;
             }
             *reinterpret_cast<uint4*>(dst + d0) = make_uint4((uint32_t)v[0] | ((uint32_t)v[1] << 16), (uint32_t)v[2] | ((uint32_t)v[3] << 16),
                                                             (uint32_t)v[4] | ((uint32_t)v[5] << 16), (uint32_t)v[6] | ((uint32_t)v[7] << 16));
@@ -263,6 +307,8 @@ struct FDesc {
     int64_t unit_begin;         // first unit of this problem in the launch
     int64_t xoff;               // first half of this problem's x copies in the x buffer
     int xa_off;                 // ring layout: halves from a member's x to its x at the anchor columns
+    int xsc_off;                // halves from a member's x to its per-token max |x| words (bf16 x; see x_scale)
+    int a_pad;                  // anchor slots of a member's x at the anchor columns (A rounded up to 48)
     int G;                      // ring kernel: anchor unit spacing inside a row block (su / anchor units)
     const uint16_t* x;          // the caller's x [batch][M][K] (16-bit) and anchor columns, for
     int64_t stride_x;           //   the in-kernel build of the fragment-ordered copy (bytes)
@@ -271,6 +317,7 @@ struct FDesc {
 };
 
 struct FParams {
+    int* status;                // device status word: bit 2 is raised when a weight table value overflows binary16
     FDesc d[kMaxGroup];
     const uint16_t* xbuf;       // all x copies: per problem, per member [x in fragment order | x at the anchors]
     int count, M, y_dtype, x_bf16, format;
@@ -369,7 +416,7 @@ struct StepNF4 {
 // its anchor columns, written by the whole CTA into shared memory at `dst` (the same
 // layout the pre-pass writes to global memory).  `bits` is K/32 words of scratch.
 __device__ __forceinline__ void build_member_x(const FParams& P, const FDesc& D, int64_t l, uint16_t* dst, uint32_t* bits) {
-    const int M = P.M, K = D.K, A = D.A, a_pad = (int)(D.xperm_stride / M) - K;
+    const int M = P.M, K = D.K, A = D.A, a_pad = D.a_pad;
     const uint16_t* x = reinterpret_cast<const uint16_t*>(reinterpret_cast<const char*>(D.x) + l * D.stride_x);
     const int32_t* aidx = A > 0 ? reinterpret_cast<const int32_t*>(reinterpret_cast<const char*>(D.anchor_idx) + l * D.stride_anchor_idx)
                                 : nullptr;
@@ -454,6 +501,18 @@ __global__ void __launch_bounds__(kThreadsS, NT <= 2 ? LQ_STREAM_MIN_BLOCKS : 1)
     // slots in warp order and writes y
     auto flush = [&](const Pos& q, int units) {
         const FDesc& D = P.d[q.p];
+        if (P.x_bf16) {   // remove each token's x scale
+            const uint32_t* xmaxw = reinterpret_cast<const uint32_t*>(
+                (STAGED ? xsm + (D.xoff + q.l * D.xperm_stride - span0) : D.xperm + q.l * D.xperm_stride) + D.xsc_off);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const float u = x_unscale(xmaxw[min(8 * nt + 2 * t + c, M - 1)]);
+                    acc[nt][c] *= u;
+                    acc[nt][c + 2] *= u;
+                }
+        }
         if (units == q.su) {
             // the whole row block is this warp's: y straight from the accumulators
             void* y = static_cast<char*>(D.y) + q.l * D.stride_y;
@@ -501,6 +560,7 @@ __global__ void __launch_bounds__(kThreadsS, NT <= 2 ? LQ_STREAM_MIN_BLOCKS : 1)
 
     Pos q = locate(P, u_begin);
     int64_t u = u_begin;
+    float peak = 0.f;      // largest |weight table value| seen (binary16 range check)
     bool waited = false;   // x is read only after the pre-pass has finished
     while (u < u_end) {
         const FDesc& D = P.d[q.p];
@@ -531,10 +591,10 @@ __global__ void __launch_bounds__(kThreadsS, NT <= 2 ? LQ_STREAM_MIN_BLOCKS : 1)
                 auto compute = [&](const Step2& f, int s) {
                     const uint16_t* xs = xb0 + (int64_t)s * 256 * M;
                     uint32_t RA[4], RB[4];
-                    lut2_bits((uint16_t)f.s0, (uint16_t)f.z0, RA[0], RB[0]);
-                    lut2_bits((uint16_t)(f.s0 >> 16), (uint16_t)(f.z0 >> 16), RA[1], RB[1]);
-                    lut2_bits((uint16_t)f.s1, (uint16_t)f.z1, RA[2], RB[2]);
-                    lut2_bits((uint16_t)(f.s1 >> 16), (uint16_t)(f.z1 >> 16), RA[3], RB[3]);
+                    lut2_bits_peak((uint16_t)f.s0, (uint16_t)f.z0, RA[0], RB[0], peak);
+                    lut2_bits_peak((uint16_t)(f.s0 >> 16), (uint16_t)(f.z0 >> 16), RA[1], RB[1], peak);
+                    lut2_bits_peak((uint16_t)f.s1, (uint16_t)f.z1, RA[2], RB[2], peak);
+                    lut2_bits_peak((uint16_t)(f.s1 >> 16), (uint16_t)(f.z1 >> 16), RA[3], RB[3], peak);
                     const uint32_t w0[4] = {f.c0.x, f.c0.y, f.c0.z, f.c0.w};
                     const uint32_t w1[4] = {f.c1.x, f.c1.y, f.c1.z, f.c1.w};
 #pragma unroll
@@ -691,6 +751,7 @@ __global__ void __launch_bounds__(kThreadsS, NT <= 2 ? LQ_STREAM_MIN_BLOCKS : 1)
             next_block(P, q);
         }
     }
+    if (peak >= kHalfOverflow && P.status) atomicOr(P.status, 2);
 }
 
 // ---- ring kernel (2-bit) ----------------------------------------------------------
@@ -701,10 +762,10 @@ __global__ void __launch_bounds__(kThreadsS, NT <= 2 ? LQ_STREAM_MIN_BLOCKS : 1)
 //  * A unit is 32 output rows x 256 code columns (or 32 rows x 48 anchor columns): two
 //    mma row tiles that share every x fragment, so one shared-memory x load feeds two
 //    independent accumulator chains.
-//  * Weights reach the registers through shared memory: each warp keeps two unit stages
-//    that its lanes fill with 16-byte cp.async copies, double buffered (the next unit is in
-//    flight while one is multiplied; a stage is refilled as soon as it is consumed), so
-//    loads in flight hold no registers.  One CTA of 16 warps per SM.
+//  * Weights reach the registers through shared memory: each warp keeps kRingDepth unit
+//    stages that its lanes fill with 16-byte cp.async copies (the next units are in flight
+//    while one is multiplied; a stage is refilled as soon as it is consumed), so loads in
+//    flight hold no registers.  One CTA of 16 warps per SM.
 //  * x: when the span of x that a CTA's warps read fits in shared memory (XS), the CTA
 //    builds it there itself (binary16, fragment order, anchor columns zeroed) and no
 //    pre-pass runs; otherwise the pre-pass writes it to global memory once per call.
@@ -717,7 +778,10 @@ __global__ void __launch_bounds__(kThreadsS, NT <= 2 ? LQ_STREAM_MIN_BLOCKS : 1)
 //   anchor unit: anchor weights [32 rows][48 x binary16] (zero past A)
 
 constexpr int kRingStage = 3072;
-constexpr int kRingDepth = 2;
+#ifndef LQ_RING_DEPTH
+#define LQ_RING_DEPTH 2
+#endif
+constexpr int kRingDepth = LQ_RING_DEPTH;
 constexpr int kRingRows = 32;
 
 #ifndef LQ_RING_WARPS1
@@ -837,8 +901,10 @@ __device__ __forceinline__ void feed_issue(const FParams& P, Feed& f, uint32_t s
         } else {
             const int a0 = a_unit * kAnchorCols;
             const uint32_t dst = st + lane * 96;
+            const int npieces = 2 * ((f.A - a0 + 15) >> 4);   // the k-blocks that hold anchors (the rest is not read)
 #pragma unroll
             for (int i = 0; i < 6; ++i) {
+                if (i > 0 && i >= npieces) break;
                 const int a = a0 + 8 * i;
                 const int n = f.A - a;   // anchors left from column a: copy at most 8, zero the rest
                 const uint32_t bytes = n >= 8 ? 16u : (n > 0 ? 2u * n : 0u);
@@ -869,9 +935,24 @@ __device__ __forceinline__ void feed_issue(const FParams& P, Feed& f, uint32_t s
 // the slots in warp order and writes y.
 template <int NT>
 __device__ __forceinline__ void ring_flush(const FParams& P, const Pos& q, int units, float (&acc)[2][NT][4], int M,
-                                           int lane) {
+                                           int lane, const uint16_t* xmember) {
     const FDesc& D = P.d[q.p];
     const int g = lane >> 2, t = lane & 3;
+    if (P.x_bf16) {   // remove each token's x scale
+        const uint32_t* xmaxw = reinterpret_cast<const uint32_t*>(xmember + D.xsc_off);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const int m = min(8 * nt + 2 * t + c, M - 1);
+                const float u = x_unscale(xmaxw[m]);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    acc[h][nt][c] *= u;
+                    acc[h][nt][c + 2] *= u;
+                }
+            }
+    }
     if (units == q.su) {
         void* y = static_cast<char*>(D.y) + q.l * D.stride_y;
         const int rg = q.rb * kRingRows + g;
@@ -927,7 +1008,8 @@ __device__ __forceinline__ void ring_flush(const FParams& P, const Pos& q, int u
 // (1) zeroed (the anchors replace those weights).
 __device__ __forceinline__ void build_span_x(const FParams& P, const Pos& a, const Pos& b, int64_t span0, uint16_t* xsm) {
     const int M = P.M, tid = threadIdx.x, nth = blockDim.x, S = ring_kstride(M);
-    for (int pass = 0; pass < 3; ++pass) {
+    // bf16 x first takes each token's max |x| (passes -2: clear, -1: max), for its scale
+    for (int pass = P.x_bf16 ? -2 : 0; pass < 3; ++pass) {
         for (int p = a.p; p <= b.p; ++p) {
             const FDesc& D = P.d[p];
             const int K = D.K, A = D.A;
@@ -937,7 +1019,22 @@ __device__ __forceinline__ void build_span_x(const FParams& P, const Pos& a, con
                 const int32_t* aidx = A > 0 ? reinterpret_cast<const int32_t*>(reinterpret_cast<const char*>(D.anchor_idx) +
                                                                                  l * D.stride_anchor_idx)
                                             : nullptr;
-                if (pass == 0) {
+                uint32_t* xmaxw = reinterpret_cast<uint32_t*>(dst + D.xsc_off);
+                if (pass == -2) {
+                    for (int m = tid; m < M; m += nth) xmaxw[m] = 0u;
+                } else if (pass == -1) {
+                    const uint16_t* x = reinterpret_cast<const uint16_t*>(reinterpret_cast<const char*>(D.x) + l * D.stride_x);
+                    for (int it = tid; it < M * K / 16; it += nth) {
+                        const int m = it / (K / 16), q = it - m * (K / 16);
+                        const uint4* src = reinterpret_cast<const uint4*>(x + (int64_t)m * K + 16 * q);
+                        const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
+                        const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+                        uint32_t mx = 0;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) mx = max(mx, max(w[i] & 0x7FFFu, (w[i] >> 16) & 0x7FFFu));
+                        atomicMax(&xmaxw[m], mx << 16);
+                    }
+                } else if (pass == 0) {
                     const uint16_t* x = reinterpret_cast<const uint16_t*>(reinterpret_cast<const char*>(D.x) + l * D.stride_x);
                     for (int it = tid; it < M * K / 16; it += nth) {
                         const int m = it / (K / 16), q = it - m * (K / 16);
@@ -945,9 +1042,11 @@ __device__ __forceinline__ void build_span_x(const FParams& P, const Pos& a, con
                         const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
                         uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w}, o[8];
                         if (P.x_bf16) {
+                            const float sc = x_scale(xmaxw[m]);
 #pragma unroll
                             for (int i = 0; i < 8; ++i)
-                                w[i] = (uint32_t)to_half_bits((uint16_t)w[i], 1) | ((uint32_t)to_half_bits((uint16_t)(w[i] >> 16), 1) << 16);
+                                w[i] = (uint32_t)bf16_to_half_scaled((uint16_t)w[i], sc) |
+                                       ((uint32_t)bf16_to_half_scaled((uint16_t)(w[i] >> 16), sc) << 16);
                         }
                         ring_x_transpose(w, o);
                         uint2* d2 = reinterpret_cast<uint2*>(dst + q * S + m * 16);
@@ -957,7 +1056,7 @@ __device__ __forceinline__ void build_span_x(const FParams& P, const Pos& a, con
                         d2[3] = make_uint2(o[6], o[7]);
                     }
                 } else if (pass == 1) {
-                    const int a_pad = (int)(D.xperm_stride - D.xa_off) / M;
+                    const int a_pad = D.a_pad;
                     uint16_t* xa = dst + D.xa_off;
                     for (int it = tid; it < M * a_pad; it += nth) {
                         const int m = it / a_pad, aa = it - m * a_pad;
@@ -996,8 +1095,8 @@ __global__ void __launch_bounds__(32 * ring_warps(NT), 1) gemv_ring_kernel(const
     Feed f;
     if (active) {
         f = feed_at(P, u_begin, (int)(u_end - u_begin), lane);
-        feed_issue(P, f, ring, lane);
-        feed_issue(P, f, ring + kRingStage, lane);
+#pragma unroll
+        for (int i = 0; i < kRingDepth; ++i) feed_issue(P, f, ring + i * kRingStage, lane);
     }
     pdl_launch_dependents();
     int64_t span0 = 0;
@@ -1036,10 +1135,11 @@ __global__ void __launch_bounds__(32 * ring_warps(NT), 1) gemv_ring_kernel(const
     UnitOrder ord = unit_order(q.s, q.steps, q.su, P.d[q.p].G);
     const uint16_t* xb0 = xbase(q);
     int seg_units = 0;
-    uint32_t cst = 0;   // byte offset of the stage to compute (the other one is being filled)
+    float peak = 0.f;   // largest |weight table value| seen (binary16 range check)
+    uint32_t cst = 0;   // byte offset of the stage to compute (the others are being filled)
     for (int left = (int)(u_end - u_begin); left > 0; --left) {
-        cp_async_wait<1>();
-        __syncwarp();   // every lane's copies of this unit have landed (the next unit may still be in flight)
+        cp_async_wait<kRingDepth - 1>();
+        __syncwarp();   // every lane's copies of this unit have landed (the next units may still be in flight)
         const unsigned char* st = ringp + cst;
         const int a_unit = ord.a;
         if (!unit_step(ord)) {
@@ -1052,7 +1152,7 @@ __global__ void __launch_bounds__(32 * ring_warps(NT), 1) gemv_ring_kernel(const
                 for (int r = 0; r < 4; ++r) {
                     const uint16_t sb = *reinterpret_cast<const uint16_t*>(st + 2048 + (g + 8 * r) * 16 + 4 * t + 2 * hg);
                     const uint16_t zb = *reinterpret_cast<const uint16_t*>(st + 2560 + (g + 8 * r) * 16 + 4 * t + 2 * hg);
-                    lut2_bits(sb, zb, RA[r], RB[r]);
+                    lut2_bits_peak(sb, zb, RA[r], RB[r], peak);
                     w[r] = *reinterpret_cast<const uint2*>(st + (g + 8 * r) * 64 + 16 * t + 8 * hg);
                 }
 #pragma unroll
@@ -1092,12 +1192,12 @@ __global__ void __launch_bounds__(32 * ring_warps(NT), 1) gemv_ring_kernel(const
                 }
             }
         }
-        __syncwarp();   // every lane is done with this stage: refill it two units ahead
+        __syncwarp();   // every lane is done with this stage: refill it kRingDepth units ahead
         feed_issue(P, f, ring + cst, lane);
-        cst ^= kRingStage;
+        cst = cst + kRingStage == kRingDepth * kRingStage ? 0 : cst + kRingStage;
         ++seg_units;
         if (++q.s == q.su || left == 1) {
-            ring_flush<NT>(P, q, seg_units, acc, M, lane);
+            ring_flush<NT>(P, q, seg_units, acc, M, lane, xb0);
             seg_units = 0;
             if (left > 1) {
                 q.s = 0;
@@ -1110,6 +1210,7 @@ __global__ void __launch_bounds__(32 * ring_warps(NT), 1) gemv_ring_kernel(const
         }
     }
     cp_async_wait<0>();
+    if (peak >= kHalfOverflow && P.status) atomicOr(P.status, 2);
 }
 
 // Resident CTAs per SM of a kernel at a given dynamic shared-memory size.  The first call
@@ -1257,6 +1358,33 @@ size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
 
 }  // namespace
 
+lq_status launch_xmax_rows(const lq_problem* probs, int count, uint32_t* words, cudaStream_t stream) {
+    PrepParams Q;
+    memset(&Q, 0, sizeof(Q));
+    const int M = probs[0].M;
+    Q.count = count;
+    Q.M = M;
+    Q.x_bf16 = 1;
+    int64_t rows = 0;
+    for (int i = 0; i < count; ++i) {
+        PrepDesc& e = Q.d[i];
+        e.x = static_cast<const uint16_t*>(probs[i].x);
+        e.stride_x = probs[i].stride_x;
+        e.K = probs[i].K;
+        e.batch = probs[i].batch;
+        e.xperm = reinterpret_cast<uint16_t*>(words + rows);   // member l's words at 2 * M * l halves
+        e.xperm_stride = 2 * M;
+        e.xsc_off = 0;
+        e.row_begin = rows;
+        rows += (int64_t)probs[i].batch * M;
+    }
+    Q.total_rows = rows;
+    if (rows == 0) return LQ_OK;
+    if (rows > 0x7fffffffLL) return LQ_ERR_UNSUPPORTED;
+    xmax_kernel<<<(unsigned)rows, 256, 0, stream>>>(Q);
+    return cudaPeekAtLastError() == cudaSuccess ? LQ_OK : LQ_ERR_CUDA;
+}
+
 bool gemv_stream_eligible(const lq_problem* probs, int count) {
     if (probs[0].M > 32) return false;
     for (int i = 0; i < count; ++i)
@@ -1285,7 +1413,7 @@ lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* probs, i
     const int rows_blk = use_ring ? kRingRows : 16;            // output rows per row block
     const int cta_warps = use_ring ? ring_warps(M <= 8 ? 1 : 2) : kWarps;
 
-    int64_t units = 0, jobs = 0, xhalves = 0, blocks = 0;
+    int64_t units = 0, jobs = 0, xhalves = 0, blocks = 0, rows = 0;
     int max_k = 0;
     for (int i = 0; i < count; ++i) {
         const lq_problem& q = probs[i];
@@ -1321,7 +1449,9 @@ lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* probs, i
         blocks += (int64_t)q.batch * d.rblocks;
         // per member: [x (fragment order, or the ring layout) | x at the anchors (M*a_pad)]
         d.xa_off = use_ring ? (q.K / 16) * ring_kstride(M) : M * q.K;
-        d.xperm_stride = d.xaperm_stride = (int64_t)d.xa_off + (int64_t)M * a_pad;
+        d.xsc_off = d.xa_off + M * a_pad;   // then one 32-bit max |x| word per token (16-half aligned)
+        d.a_pad = a_pad;
+        d.xperm_stride = d.xaperm_stride = (int64_t)d.xsc_off + round_up(2 * M, 16);
         d.xoff = xhalves;
         xhalves += (int64_t)q.batch * d.xperm_stride;
         e.x = d.x;
@@ -1337,6 +1467,9 @@ lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* probs, i
         e.jobs = q.K / 256 + (a_pad + 255) / 256;
         e.job_begin = jobs;
         jobs += (int64_t)q.batch * e.jobs;
+        e.xsc_off = d.xsc_off;
+        e.row_begin = rows;
+        rows += (int64_t)q.batch * M;
         max_k = std::max(max_k, q.K);
     }
     if (units == 0) return LQ_OK;
@@ -1359,7 +1492,7 @@ lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* probs, i
     // by default the pre-pass does it once for all CTAs (measured faster on this part), and the
     // per-CTA spans are not needed.
     const char* st_env = getenv("LQ_GEMV_STAGE");
-    const bool want_stage = !use_ring && st_env && atoi(st_env) == 1;
+    const bool want_stage = !use_ring && st_env && atoi(st_env) == 1 && !P.x_bf16;   // (binary16 x only)
     int64_t max_span = 0, max_members = 0, max_raw = 0, max_idx = 0, max_bits = 0;
     for (int64_t b = 0; (want_stage || use_ring) && b < grid; ++b) {
         const int64_t w_lo = b * cta_warps, w_hi = std::min<int64_t>(w_lo + cta_warps, W);
@@ -1429,14 +1562,21 @@ lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* probs, i
     if (ws.clear_counters && cudaMemsetAsync(ws.counters, 0, sizeof(unsigned) * (size_t)blocks, stream) != cudaSuccess)
         return LQ_ERR_CUDA;
     Q.total_jobs = jobs;
+    Q.total_rows = rows;
     Q.ring = use_ring ? 1 : 0;
+    P.status = ws.status;
     int unused = 0;
     if (staged) return dispatch(fmt, 1, true, P, grid, smem, &unused, stream);
     if (use_ring && ring_xs) return dispatch_ring(1, true, P, grid, ring_xs_smem, &unused, stream);
 
-    // x pre-pass, then the main kernel, chained by programmatic dependent launch
+    // x pre-pass (bf16 x: after each token's max |x|), then the main kernel, chained by
+    // programmatic dependent launch
     const int64_t prep_ctas = (jobs + kPrepWarps - 1) / kPrepWarps;
-    if (prep_ctas > 0x7fffffffLL) return LQ_ERR_UNSUPPORTED;
+    if (prep_ctas > 0x7fffffffLL || rows > 0x7fffffffLL) return LQ_ERR_UNSUPPORTED;
+    if (P.x_bf16) {
+        xmax_kernel<<<(unsigned)rows, 256, 0, stream>>>(Q);
+        if (cudaPeekAtLastError() != cudaSuccess) return LQ_ERR_CUDA;
+    }
     xprep_kernel<<<(unsigned)prep_ctas, 32 * kPrepWarps, 0, stream>>>(Q);
     if (cudaPeekAtLastError() != cudaSuccess) return LQ_ERR_CUDA;
     if (use_ring) return dispatch_ring(1, ring_xs, P, grid, ring_xs ? ring_xs_smem : ring_smem, &unused, stream);

@@ -51,6 +51,7 @@ struct GemvDesc {
     int64_t unit_begin;   // first global unit of this problem
     int64_t strip_begin;  // first global strip (counters index)
     int64_t partial_begin;  // first float of this problem's split-K partial sums
+    const uint32_t* xmax; // bf16 x: max |x| word of each (member, token) row of this problem
 };
 
 struct GemvParams {
@@ -64,6 +65,7 @@ struct GemvParams {
     int a_pad;         // smem columns reserved for anchors (multiple of 16)
     float* partials;
     unsigned* counters;
+    int* status;       // device status word: bit 2 is raised when a weight table value overflows binary16
     int64_t total_units;
 };
 
@@ -88,6 +90,8 @@ lq_status launch_gemv_ws(const GemvWorkspace& ws, const lq_problem* problems, in
 bool gemv_stream_eligible(const lq_problem* problems, int count);
 lq_status launch_gemv_regs(const GemvWorkspace& ws, const lq_problem* problems, int count, cudaStream_t stream);
 lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* problems, int count, cudaStream_t stream);
+// bf16 x: each (member, token) row's max |x| (fp32 bit pattern) into words[], rows in problem order.
+lq_status launch_xmax_rows(const lq_problem* problems, int count, uint32_t* words, cudaStream_t stream);
 
 lq_status launch_gemm(lq_handle h, const lq_problem& p, cudaStream_t stream);
 

@@ -51,7 +51,15 @@
  * - Arithmetic: dequantized weights follow the definitions above exactly
  *   (lq_dequant is bit-exact).  lq_gemv multiplies binary16-rounded weights by
  *   binary16 x on tensor cores with fp32 accumulation (|error| <= 1e-3 *
- *   sum_k |W_eff||x|); bf16 x is converted to binary16 (exact for |x| < 65504).
+ *   sum_k |W_eff||x|).  bf16 x: each token's x is scaled by the power of two that
+ *   brings its largest |x| into [2^14, 2^15), rounded to binary16, and the fp32
+ *   result is scaled back (both factors exact), so bf16 x of any finite magnitude
+ *   keeps the bound.  Weight domain of lq_gemv (2-bit): the four table values
+ *   fmaf(S, C[q], Z) of a group are rounded to binary16, so they must satisfy
+ *   |S*C+Z| < 65520 (a group that breaks this raises LQ_ERR_RANGE at the next
+ *   lq_sync); values below 2^-14 keep an absolute error of at most 2^-25, so the
+ *   bound needs each row's weights to be mostly above that size (NF4: the levels
+ *   T[q] are in [-1, 1] and absmax scales in fp32; no range limit).
  *   lq_gemm multiplies in the dtype of x (bf16 or binary16) with fp32
  *   accumulation (|error| <= 4e-3 * sum_k |W_eff||x| for bf16).  The quantizers'
  *   outputs (codes, scales, offsets, anchors, absmax) are deterministic bit
@@ -83,7 +91,9 @@ typedef enum lq_status {
     LQ_ERR_ALIGNMENT = 3,     /* a pointer or leading dimension breaks the 16-byte rule */
     LQ_ERR_WORKSPACE = 4,     /* the handle's workspace is too small for this call */
     LQ_ERR_CUDA = 5,          /* a CUDA runtime call or launch failed */
-    LQ_ERR_TIMEOUT = 6        /* a bounded device-side wait ran out (reported by lq_sync) */
+    LQ_ERR_TIMEOUT = 6,       /* a bounded device-side wait ran out (reported by lq_sync) */
+    LQ_ERR_RANGE = 7          /* a decode GEMV met a weight table value |S*C+Z| >= 65520, outside the
+                                 binary16 range of its tensor-core operands (reported by lq_sync) */
 } lq_status;
 
 typedef enum lq_format {

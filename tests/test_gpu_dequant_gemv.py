@@ -258,7 +258,7 @@ def _check_sampled_2bit(packed, xbits, xdt, y, rows, tol=GEMV_TOL, what=""):
         assert_within(y[:, n:n + 1], yr, E, tol, f"{what} row {n}")
 
 
-@pytest.mark.parametrize("layer,M", [("7b", 1), ("70b", 8), ("70b", 32)])
+@pytest.mark.parametrize("layer,M", [("7b", 1), ("70b", 1), ("70b", 8), ("70b", 32)])
 def test_gemv_full_layer_sampled(lqm, handle, layer, M):
     """The bench's launch: one grouped call over a whole decoder layer at full size."""
     sigma = 0.02 if layer == "7b" else 0.015
@@ -279,7 +279,7 @@ def test_gemv_full_layer_sampled(lqm, handle, layer, M):
         _check_sampled_2bit(pk, xb, "f16", y.cpu().numpy(), _sampled_rows(pk["N"], 8, seed=i), what=f"{layer}[{i}]")
 
 
-@pytest.mark.parametrize("M", [1, 16])
+@pytest.mark.parametrize("M", [1, 4, 16])
 def test_gemv_nf4_full_layer_sampled(lqm, handle, M):
     probs, keep = [], []
     for i, (name, N, K) in enumerate(synth.LAYER_SHAPES["7b"]):
@@ -324,10 +324,11 @@ def test_errors_on_device_launch_nothing(lqm, handle):
 
 # ---------------------------------------------------------------- both decode kernels on the same shapes
 
-@pytest.mark.parametrize("kernel", ["regs", "stream"])
-@pytest.mark.parametrize("M", [1, 8, 32])
+@pytest.mark.parametrize("kernel", ["regs", "stream", "ring"])
+@pytest.mark.parametrize("M", [1, 8, 9, 32])
 def test_gemv_kernel_choice_same_results(lqm, handle, monkeypatch, kernel, M):
-    """The split-K and the streaming kernels both meet the bound on a K % 256 == 0 shape."""
+    """The split-K, the streaming and the ring kernels each meet the bound on a K % 256 == 0
+    shape, for token counts on both sides of the default switch between the last two."""
     monkeypatch.setenv("LQ_GEMV_KERNEL", kernel)
     N, K = 300, 3072
     p, outl = quantized_2bit(N, K, seed=50 + M)
@@ -349,3 +350,13 @@ def test_gemv_in_kernel_x_build(lqm, handle, monkeypatch, M):
         pn = quantized_nf4(N, K, seed=80 + M + i)
         xn = x_for(M, K, "bf16", None, seed=80 + M + i)
         _gemv_check(lqm, handle, pn, lqm.FMT_NF4, xn, "bf16")
+
+
+def test_gemv_full_projection_quantized_by_the_oracle(lqm, handle):
+    """A full 4096 x 4096 projection quantized by the oracle from the listed distribution
+    (profile-guided anchors on the x20 outlier channels), M = 1, every output checked."""
+    N = K = 4096
+    p, outl = quantized_2bit(N, K, seed=12, cfg=2)
+    assert set(outl.tolist()) <= set(p["anchor_idx"].tolist())
+    xb = x_for(1, K, "f16", outl, seed=12, cfg=2)
+    _gemv_check(lqm, handle, p, lqm.FMT_2BIT, xb, "f16")
