@@ -16,6 +16,7 @@ F32, F16, BF16 = 0, 1, 2
 
 #: every entry point include/lq.h declares
 EXPORTED = ("lq_create", "lq_destroy", "lq_status_string", "lq_sync", "lq_dequant", "lq_gemv",
+            "lq_anchor_count",
             "lq_gemv_grouped", "lq_gemm", "lq_gemm_grouped", "lq_gemv_noalloc",
             "lq_select_anchors", "lq_quantize_2bit", "lq_quantize_nf4",
             "lq_stream_create", "lq_stream_run", "lq_stream_destroy", "lq_stream_run_direct",
@@ -83,6 +84,8 @@ def load_library(build_if_missing: bool = True):
     L.lq_gemv_grouped.restype = I
     L.lq_gemm_grouped.argtypes = [P, ctypes.POINTER(lq_problem), I, P]
     L.lq_gemm_grouped.restype = I
+    L.lq_anchor_count.argtypes = [I]
+    L.lq_anchor_count.restype = I
     L.lq_select_anchors.argtypes = [P, P, I, I, P, I, P, P]
     L.lq_select_anchors.restype = I
     L.lq_quantize_2bit.argtypes = [P, P, I, I, P, I, P, P, P, P, I, P]
@@ -269,12 +272,12 @@ class Handle:
 
     def select_anchors(self, W, A=None, profile=None, stream=None):
         """Anchor columns of W: the A largest ||W[:,c]||_2 * profile_c (ties to the lower
-        column), ascending, as an int32 CUDA tensor.  A defaults to floor(0.035 K);
-        profile is an fp64 [K] CUDA tensor (None: all ones)."""
-        import math
+        column), ascending, as an int32 CUDA tensor.  A defaults to the library's
+        outlier-anchor count for K (lq_anchor_count); profile is an fp64 [K] CUDA tensor
+        (None: all ones)."""
         import torch
         N, K = self._weights_arg(W)
-        A = int(math.floor(0.035 * K)) if A is None else int(A)
+        A = self._lib.lq_anchor_count(K) if A is None else int(A)
         idx = torch.empty(max(A, 0), dtype=torch.int32, device=W.device)
         if profile is not None and (profile.dtype != torch.float64 or profile.numel() != K or not profile.is_contiguous()):
             raise ValueError("profile must be a contiguous fp64 [K] tensor")

@@ -312,9 +312,15 @@ LQ_API lq_status lq_gemm_grouped(lq_handle h, const lq_problem* problems, int co
 
 // ---- quantizers ------------------------------------------------------------------
 
+LQ_API int lq_anchor_count(int K) {
+    // the otf-llm README's top 3.5 % of input columns, floor(0.035 K), in exact integer arithmetic
+    return K > 0 ? (int)(((int64_t)K * 35) / 1000) : 0;
+}
+
 LQ_API lq_status lq_select_anchors(lq_handle h, const float* W, int N, int K, const double* profile, int A,
                                    int32_t* anchor_idx, void* stream) {
-    if (!h || !W || N < 1 || K < 1 || A < 0 || A > K) return LQ_ERR_INVALID_ARG;
+    if (A < 0) A = lq_anchor_count(K);
+    if (!h || !W || N < 1 || K < 1 || A > K) return LQ_ERR_INVALID_ARG;
     if (A > 0 && !anchor_idx) return LQ_ERR_INVALID_ARG;
     if (!aligned16(W) || (profile && !aligned16(profile)) || (anchor_idx && !aligned16(anchor_idx)))
         return LQ_ERR_ALIGNMENT;

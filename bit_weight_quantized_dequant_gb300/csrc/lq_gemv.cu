@@ -504,8 +504,9 @@ lq_status launch_gemv_ws(const GemvWorkspace& ws, const lq_problem* probs, int c
     const char* force = getenv("LQ_GEMV_KERNEL");
     const bool regs_only = force && strcmp(force, "regs") == 0;
     if (!regs_only && gemv_stream_eligible(probs, count)) {
+        // (a launch whose copies of x or row-block slots do not fit falls back to split-K)
         const lq_status s = launch_gemv_stream(ws, probs, count, stream);
-        if (s != LQ_ERR_UNSUPPORTED) return s;
+        if (s != LQ_ERR_UNSUPPORTED && s != LQ_ERR_WORKSPACE) return s;
     }
     return launch_gemv_regs(ws, probs, count, stream);
 }

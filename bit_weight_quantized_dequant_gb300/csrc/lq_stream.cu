@@ -128,8 +128,11 @@ LQ_API lq_status lq_stream_run(lq_layer_stream s, const void* host_layers, size_
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     lq_status res = LQ_OK;
     std::vector<lq_problem> abs(problems, problems + count);
-    // slots may still be read by the caller's earlier work
-    if (cudaEventRecord(s->start, st) != cudaSuccess || cudaStreamWaitEvent(s->copy, s->start, 0) != cudaSuccess)
+    // slots may still be read by the caller's earlier work, and by the last two layers of an
+    // earlier pass (which may have run on another stream): the copies wait for both
+    if (cudaEventRecord(s->start, st) != cudaSuccess || cudaStreamWaitEvent(s->copy, s->start, 0) != cudaSuccess ||
+        cudaStreamWaitEvent(s->copy, s->freed[0], 0) != cudaSuccess ||
+        cudaStreamWaitEvent(s->copy, s->freed[1], 0) != cudaSuccess)
         res = LQ_ERR_CUDA;
     for (int l = 0; l < L && res == LQ_OK; ++l) {
         const int k = l & 1;

@@ -224,18 +224,27 @@ LQ_API lq_status lq_gemm_grouped(lq_handle h, const lq_problem* problems, int co
  * caller cannot create an lq handle, because lq_create allocates the handle's
  * workspace.  This entry point takes no handle and allocates nothing (no
  * cudaMalloc, cudaFree or allocating library call).  The caller still provides
- * x, y and the packed weights; the split-K scratch is a fixed file-scope device
- * array of 8.06 MiB (16384 arrival counters + 2^21 fp32 partial sums) that every
- * GPU loading the library holds until the process exits.
+ * x, y and the packed weights; the scratch is a fixed file-scope device array of
+ * 8.06 MiB (16384 arrival counters + 2^21 fp32 words) that every GPU loading the
+ * library holds until the process exits.
  *
  * - Runs on the CURRENT device.  Its first call on a device looks up the
  *   array's device address (cudaGetSymbolAddress); make that first call before
  *   any stream capture.
- * - Problems whose split-K scratch exceeds the array return LQ_ERR_WORKSPACE
- *   before anything is launched (roughly M * N * (K-splits + 1) <= 2^21 fp32).
+ * - Scratch needs (fp32 words), as for lq_gemv: K % 256 == 0 uses a copy of x in
+ *   the kernels' layout (about M * (K + A) / 2 words; none for small problems at
+ *   up to 8 tokens, which build it in shared memory) plus one 16- or 32-row slot
+ *   of M * rows words per warp that shares a row block; otherwise the split-K
+ *   kernel uses M * 64 words per 64-row strip per K-split (plus one split for the
+ *   anchors), and one word per token for bf16 x.  A launch that does not fit the
+ *   streaming kernel's needs falls back to split-K; one that fits neither returns
+ *   LQ_ERR_WORKSPACE before anything is launched.
  * - All calls share the one array: each call clears the counters it uses on
  *   `stream` before its kernel runs, and calls that overlap on the GPU (other
  *   streams, other threads) race and give wrong results.
+ * - There is no handle and no lq_sync here, so nothing reports device-side status:
+ *   the decode kernels have no waits to time out, and a weight past the binary16
+ *   range (LQ_ERR_RANGE through lq_gemv) is not reported.
  * Arguments, layouts, results and the other errors are those of lq_gemv.
  */
 LQ_API lq_status lq_gemv_noalloc(int format,
@@ -261,10 +270,16 @@ LQ_API lq_status lq_gemv_noalloc(int format,
  * the A largest scores, ties to the lower column, written to anchor_idx[A]
  * (int32, device) in ascending column order.  profile: fp64 [K] in device memory,
  * non-negative (mean |X_c| of a calibration profile), or NULL for all ones.  The
- * README keeps the top 3.5 %: A = floor(0.035 * K).  0 <= A <= K; A = 0 launches
- * nothing.  Errors: LQ_ERR_INVALID_ARG (shape, NULL), LQ_ERR_ALIGNMENT (W, profile
- * or anchor_idx not 16-byte aligned), LQ_ERR_WORKSPACE (K doubles do not fit).
+ * README keeps the top 3.5 %: A < 0 selects lq_anchor_count(K) columns (anchor_idx
+ * must then hold that many).  0 <= A <= K otherwise; A = 0 launches nothing.
+ * Errors: LQ_ERR_INVALID_ARG (shape, NULL), LQ_ERR_ALIGNMENT (W, profile or
+ * anchor_idx not 16-byte aligned), LQ_ERR_WORKSPACE (K doubles do not fit).
  */
+/* lq_anchor_count — the otf-llm README's outlier-anchor count for K input columns
+ * (section 4, "Top-3.5%"): floor(0.035 * K), computed exactly as (35 K) / 1000;
+ * 0 for K <= 0.  Host-only, needs no device. */
+LQ_API int lq_anchor_count(int K);
+
 LQ_API lq_status lq_select_anchors(lq_handle h, const float* W, int N, int K, const double* profile, int A,
                                    int32_t* anchor_idx, void* stream);
 

@@ -35,9 +35,19 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_status_strings(lib):
     L, _ = lib
-    for s in range(7):
-        assert L.lq_status_string(s)
+    for s in range(8):
+        assert L.lq_status_string(s) != b"unknown status"
     assert L.lq_status_string(99) == b"unknown status"
+
+
+def test_anchor_count_is_the_oracles(lib):
+    """The library's default anchor count (floor of 3.5 % of K) equals the oracle's, which the
+    oracle pins test ties to the listed workloads (8 at K = 256, 143 at 4096, ...)."""
+    from oracle import oracle as O
+    L, _ = lib
+    for K in list(range(0, 2049)) + [4096, 5120, 8192, 11008, 13824, 28672, 1 << 20]:
+        assert L.lq_anchor_count(K) == (O.anchor_count(K) if K > 0 else 0), K
+    assert L.lq_anchor_count(-5) == 0
 
 
 def _fake_handle():
