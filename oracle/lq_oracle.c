@@ -18,6 +18,8 @@
  *     exactly in FP16 and replace the 2-bit reconstruction there.
  * NF4 (AirQuant README, "Fundamentacao Teorica", item 2; QLoRA data type):
  *   w = T[q] * absmax of the 64-weight block.
+ * INT4 (the same otf-llm README's v3.2 engine): w = S * q on a uniform symmetric grid,
+ *   columns in a static permutation (oracle_dequant_int4 below).
  *
  * Rounding (fixed here because the pages leave it open): the 2-bit value is one
  * fp32 fused multiply-add fmaf(S, C[q], Z) of the binary16 scale and offset; the
@@ -143,6 +145,33 @@ ORACLE_API void oracle_dequant_nf4(const uint8_t* codes, const float* absmax, co
             int q = (k % 2 == 0) ? (byte & 15) : (byte >> 4);
             out[(size_t)n * K + k] = table[q] * absmax[(size_t)n * (K / 64) + k / 64];
         }
+    }
+}
+
+/*
+ * The otf-llm README's v3.2 INT4 format ("Comparative Analysis: INT4 (v3.2) vs INT2
+ * Non-Uniform (v4.0)"): 2 weights per byte on a uniform grid with zero-point 0, input
+ * columns stored in a global static permutation, the top-1% columns kept in FP16.
+ * Dequantize one matrix to fp32 [N][K] in ORIGINAL column order:
+ *   codes     [N][K/2]   byte j holds permuted positions 2j (low nibble) and 2j+1 (high),
+ *                        each a 4-bit two's complement integer q
+ *   scales    [N][K/32]  binary16 S of the 32 consecutive permuted positions of a group
+ *   perm      [K]        perm[j] = the input column stored at permuted position j
+ *   anchor_idx[A], anchor_w [N][lda]   as for the 2-bit format (replace the grid value)
+ * w = S * q is one fp32 product (exact: 11 by 4 significant bits).
+ */
+ORACLE_API void oracle_dequant_int4(const uint8_t* codes, const uint16_t* scales, const int32_t* perm,
+                                    const int32_t* anchor_idx, const uint16_t* anchor_w, int A, int lda,
+                                    int N, int K, float* out) {
+    for (int n = 0; n < N; ++n) {
+        for (int j = 0; j < K; ++j) {
+            int byte = codes[(size_t)n * (K / 2) + j / 2];
+            int nib = (j % 2 == 0) ? (byte & 15) : (byte >> 4);
+            int q = nib >= 8 ? nib - 16 : nib;
+            out[(size_t)n * K + perm[j]] = half_to_float(scales[(size_t)n * (K / 32) + j / 32]) * (float)q;
+        }
+        for (int a = 0; a < A; ++a)
+            out[(size_t)n * K + anchor_idx[a]] = half_to_float(anchor_w[(size_t)n * lda + a]);
     }
 }
 

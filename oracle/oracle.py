@@ -24,6 +24,12 @@ Functions and what they follow
                                       (NF4, block-wise) and its QLoRA reference.
 * ``pack_nf4`` / ``unpack_nf4``      NF4 storage, 2 codes per byte.
 * ``dequant_2bit`` / ``dequant_nf4`` the reconstruction S*C[q]+Z / T[q]*absmax (C code).
+* ``int4_permutation``, ``quantize_int4``, ``pack_int4`` / ``unpack_int4``, ``dequant_int4``
+                                     the otf-llm README's v3.2 INT4 engine ("Comparative
+                                      Analysis: INT4 (v3.2) vs INT2 Non-Uniform (v4.0)" and
+                                      the "Method Comparison Table"): 2 weights per byte,
+                                      uniform grid, zero-point 0, a global static column
+                                      permutation, top-1% FP16 outlier columns.
 * ``matmul_ref``                     y = x * W_eff^T in fp64, with the error scale
                                       E = |x| * |W_eff|^T.
 
@@ -56,6 +62,12 @@ ANCHOR_FRAC = 0.035
 NF4_BLOCK = 64
 #: OLS denominator epsilon (the page writes "+ eps" without a value).
 OLS_EPS = 1e-12
+#: v3.2 INT4 engine: outlier fraction ("Top-1% FP16 Outlier Channels"), group size along the
+#: permuted columns and the symmetric grid's largest code (readings; the page gives only
+#: "2 weights / byte", "Uniform Linear Grid" and "Symmetric Zero-Point = 0").
+INT4_OUTLIER_FRAC = 0.01
+INT4_GROUP = 32
+INT4_QMAX = 7
 
 #: The NF4 levels as published with the QLoRA data type (Dettmers et al. 2023,
 #: the paper the AirQuant README cites for NF4), as float32.  ``nf4_table_construction``
@@ -124,6 +136,7 @@ def _lib():
         i = ctypes.c_int
         L.oracle_dequant_2bit.argtypes = [P, P, P, P, P, i, i, i, i, P]
         L.oracle_dequant_nf4.argtypes = [P, P, P, i, i, P]
+        L.oracle_dequant_int4.argtypes = [P, P, P, P, P, i, i, i, i, P]
         L.oracle_round_f32.argtypes = [P, ctypes.c_size_t, i, P]
         L.oracle_matmul_f64.argtypes = [P, P, i, i, i, i, P, P]
         L.oracle_gemv_2bit_rows.argtypes = [P, P, P, P, P, i, i, P, i, i, i, i, i, i, P, P]
@@ -346,6 +359,87 @@ def unpack_nf4(codes: np.ndarray) -> np.ndarray:
     q[:, 0::2] = codes & 15
     q[:, 1::2] = codes >> 4
     return q
+
+
+# ---------------------------------------------------------------------------
+# v3.2 INT4: uniform symmetric grid, global static permutation, top-1% outliers
+# ---------------------------------------------------------------------------
+
+def int4_permutation(W: np.ndarray, profile: np.ndarray) -> np.ndarray:
+    """The static column order: input columns by descending impact score
+    I_c = ||W[:,c]||_2 * profile_c (the score the v4.0 anchors use), ties to the lower
+    column.  perm[j] is the column stored at permuted position j (int32)."""
+    W = np.asarray(W, dtype=np.float64)
+    K = W.shape[1]
+    score = np.sqrt(np.sum(W * W, axis=0)) * np.asarray(profile, dtype=np.float64)
+    return np.array(sorted(range(K), key=lambda c: (-score[c], c)), dtype=np.int32)
+
+
+def quantize_int4(W: np.ndarray, perm: np.ndarray, anchor_idx: np.ndarray, lda: int | None = None) -> dict:
+    """Quantize W [N][K] to the INT4 format.
+
+    Columns are taken in the order perm; each row's permuted positions form groups of 32.
+    For a group with V = its non-anchor positions:
+      S = max |W_V| / 7 (fp64), stored as binary16 (RNE);
+      q = clamp(round_half_even(W / S16), -7, 7) with the stored S16 (q = 0 when S16 = 0);
+    anchor positions store q = 0 (exactly 0 on the zero-point-0 grid); their binary16
+    values go to anchor_w[n][a] for the ascending anchor_idx.
+    """
+    W = np.asarray(W, dtype=np.float32)
+    N, K = W.shape
+    assert K % INT4_GROUP == 0
+    perm = np.asarray(perm, dtype=np.int32)
+    anchor_idx = np.asarray(anchor_idx, dtype=np.int32)
+    A = len(anchor_idx)
+    lda = int(lda if lda is not None else max(8, (A + 7) // 8 * 8))
+    is_anchor = np.zeros(K, dtype=bool)
+    is_anchor[anchor_idx] = True
+    Wp = W[:, perm].astype(np.float64)                 # permuted columns
+    anchor_p = is_anchor[perm]
+    q = np.zeros((N, K), dtype=np.int8)
+    S16 = np.zeros((N, K // INT4_GROUP), dtype=np.float16)
+    for g in range(K // INT4_GROUP):
+        pos = np.arange(g * INT4_GROUP, (g + 1) * INT4_GROUP)
+        V = pos[~anchor_p[pos]]
+        if len(V) == 0:
+            continue
+        absmax = np.max(np.abs(Wp[:, V]), axis=1)
+        s16 = (absmax / INT4_QMAX).astype(np.float16)       # float64 -> binary16, RNE
+        S16[:, g] = s16
+        s = s16.astype(np.float64)[:, None]
+        r = np.where(s > 0, Wp[:, V] / np.where(s > 0, s, 1.0), 0.0)
+        q[:, V] = np.clip(np.rint(r), -INT4_QMAX, INT4_QMAX).astype(np.int8)
+    anchor_w = np.zeros((N, lda), dtype=np.uint16)
+    if A:
+        anchor_w[:, :A] = W[:, anchor_idx].astype(np.float16).view(np.uint16)
+    return dict(codes=pack_int4(q), q=q, scales=S16.view(np.uint16), perm=perm, anchor_idx=anchor_idx,
+                anchor_w=anchor_w, A=A, ld_anchor=lda, N=N, K=K)
+
+
+def pack_int4(q: np.ndarray) -> np.ndarray:
+    """signed codes q [N][K] in -8..7 -> bytes [N][K/2]: position 2j in the low nibble, 2j+1 in the
+    high nibble, each as 4-bit two's complement."""
+    u = (np.asarray(q, dtype=np.int16) & 15).astype(np.uint8)
+    return (u[:, 0::2] | (u[:, 1::2] << 4)).astype(np.uint8)
+
+
+def unpack_int4(codes: np.ndarray) -> np.ndarray:
+    u = unpack_nf4(codes).astype(np.int16)
+    return np.where(u >= 8, u - 16, u).astype(np.int8)
+
+
+def dequant_int4(p: dict) -> np.ndarray:
+    """fp32 W_eff [N][K] in original column order: S * q at column perm[j], anchors substituted."""
+    L = _lib()
+    N, K, A = int(p["N"]), int(p["K"]), int(p["A"])
+    out = np.empty((N, K), dtype=np.float32)
+    L.oracle_dequant_int4(_p(np.ascontiguousarray(p["codes"], dtype=np.uint8)),
+                          _p(np.ascontiguousarray(p["scales"], dtype=np.uint16)),
+                          _p(np.ascontiguousarray(p["perm"], dtype=np.int32)),
+                          _p(np.ascontiguousarray(p["anchor_idx"], dtype=np.int32)),
+                          _p(np.ascontiguousarray(p["anchor_w"], dtype=np.uint16)), A, int(p["ld_anchor"]), N, K,
+                          _p(out))
+    return out
 
 
 # ---------------------------------------------------------------------------

@@ -516,3 +516,98 @@ def test_page_decode_ceilings():
             assert abs(tps - float(claim)) / float(claim) < 0.05
         else:
             assert tps >= float(claim)
+
+
+# ---------------------------------------------------------------- v3.2 INT4 (uniform grid, permutation, 1% outliers)
+
+def test_int4_grid_points_recovered_exactly():
+    """Groups built as S16 * q with q on the symmetric grid (each group holding a +-7, so
+    its max |w| is 7 * S16) come back with the same codes and the same binary16 scale."""
+    g = np.random.default_rng(40)
+    N, K = 6, 256
+    S16 = g.uniform(0.001, 0.05, (N, K // 32)).astype(np.float16)
+    q = g.integers(-7, 8, (N, K)).astype(np.int8)
+    q[:, ::32] = np.where(g.random((N, K // 32)) < 0.5, -7, 7)
+    W = (S16.astype(np.float32).repeat(32, axis=1) * q.astype(np.float32)).astype(np.float32)
+    p = O.quantize_int4(W, np.arange(K, dtype=np.int32), np.zeros(0, np.int32))
+    assert np.array_equal(p["q"], q)
+    assert np.array_equal(p["scales"], S16.view(np.uint16))
+    assert np.array_equal(O.dequant_int4(p), W)
+
+
+def test_int4_pack_roundtrip_and_worked_byte():
+    g = np.random.default_rng(41)
+    q = g.integers(-8, 8, (5, 64)).astype(np.int8)
+    b = O.pack_int4(q)
+    assert b.shape == (5, 32) and np.array_equal(O.unpack_int4(b), q)
+    # position 0 = -1 (two's complement 0xF) in the low nibble, position 1 = 3 in the high nibble
+    assert O.pack_int4(np.array([[-1, 3]], np.int8))[0, 0] == 0x3F
+    assert O.pack_int4(np.array([[7, -8]], np.int8))[0, 0] == 0x87
+
+
+def test_int4_permutation_orders_by_score_and_inverts():
+    g = np.random.default_rng(42)
+    N, K = 9, 160
+    W = g.normal(0, 1, (N, K))
+    prof = g.uniform(0.5, 3.0, K)
+    perm = O.int4_permutation(W, prof)
+    assert sorted(perm.tolist()) == list(range(K))                     # a permutation
+    score = [math.sqrt(sum(W[n, c] ** 2 for n in range(N))) * prof[c] for c in range(K)]
+    assert all(score[perm[j]] >= score[perm[j + 1]] for j in range(K - 1))
+    inv = np.empty(K, np.int64)
+    inv[perm] = np.arange(K)
+    x = g.normal(0, 1, K)
+    assert np.array_equal(x[perm][inv], x)                              # the inverse undoes it
+    assert abs(W[:, perm] @ x[perm] - W @ x).max() < 1e-12 * np.abs(W).sum()   # y is unchanged
+    # equal scores keep the columns in order
+    assert O.int4_permutation(np.ones((2, 40)), np.ones(40)).tolist() == list(range(40))
+
+
+def test_int4_dequant_places_values_at_permuted_columns_and_keeps_zero():
+    """W_eff[n][perm[j]] = S * q[n][j]; anchors store q = 0 and are replaced by their binary16
+    value; a zero weight reconstructs to exactly 0 (zero-point 0)."""
+    K = 64
+    perm = np.r_[np.arange(32, 64), np.arange(0, 32)].astype(np.int32)
+    W = np.zeros((2, K), np.float32)
+    W[0, 40] = 0.7                     # permuted position 8, group 0
+    W[0, 3] = -0.35                    # permuted position 35, group 1
+    W[1, 33] = 5.0                     # anchor column
+    W[1, 10] = 0.02
+    anchors = np.array([33], np.int32)
+    p = O.quantize_int4(W, perm, anchors)
+    assert p["q"][1, 1] == 0           # column 33 sits at permuted position 1
+    Wd = O.dequant_int4(p)
+    assert Wd[1, 33] == np.float32(np.float16(5.0))
+    assert Wd[0, 40] == np.float32(np.float16(0.1)) * 7 and p["q"][0, 8] == 7
+    assert Wd[0, 3] == np.float32(np.float16(0.05)) * -7
+    zero_cols = [c for c in range(K) if W[0, c] == 0 and c not in (33,)]
+    assert np.all(Wd[0, zero_cols] == 0.0)
+
+
+def test_int4_rounding_error_bound():
+    """Every non-anchor weight lands within half a grid step of its reconstruction, or is
+    clipped at +-7 steps (only when the binary16 scale rounded below max|w|/7)."""
+    W = synth.weights(48, 512, 0.02, seed=43, big_frac=0.002, big_mult=10.0)
+    prof = np.ones(512)
+    perm = O.int4_permutation(W, prof)
+    ai = O.select_anchors(W, prof, frac=O.INT4_OUTLIER_FRAC)
+    p = O.quantize_int4(W, perm, ai)
+    Wd = O.dequant_int4(p).astype(np.float64)
+    S = p["scales"].view(np.float16).astype(np.float64).repeat(32, axis=1)[:, np.argsort(perm)]
+    err = np.abs(W.astype(np.float64) - Wd)
+    allow = np.maximum(S / 2, np.abs(W) - 7 * S) * (1 + 1e-12)
+    nonanchor = np.ones(512, bool)
+    nonanchor[ai] = False
+    assert np.all(err[:, nonanchor] <= allow[:, nonanchor])
+    assert np.all(Wd[:, ai] == W[:, ai].astype(np.float16).astype(np.float64))
+
+
+def test_int4_outlier_count_and_bits_per_weight():
+    """Top-1% outlier columns (floor), and 4 bits + one binary16 scale per 32 = 4.5 bits per
+    weight before the outliers (1% binary16 columns add 0.16 bit at these sizes)."""
+    for K, A in [(256, 2), (4096, 40), (11008, 110), (8192, 81), (28672, 286)]:
+        assert int(np.floor(O.INT4_OUTLIER_FRAC * K)) == A
+    N, K = 4096, 4096
+    A = int(np.floor(O.INT4_OUTLIER_FRAC * K))
+    bits = 8 * (N * K / 2 + 2 * N * K / 32 + 2 * N * A + 4 * A + 4 * K) / (N * K)
+    assert abs((4 + 16 / 32) - 4.5) < 1e-12 and abs(bits - 4.66) < 0.01
