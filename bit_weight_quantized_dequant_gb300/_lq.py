@@ -11,7 +11,7 @@ from pathlib import Path
 
 LQ_OK, LQ_ERR_INVALID_ARG, LQ_ERR_UNSUPPORTED, LQ_ERR_ALIGNMENT, LQ_ERR_WORKSPACE, LQ_ERR_CUDA, LQ_ERR_TIMEOUT, \
     LQ_ERR_RANGE = range(8)
-FMT_2BIT, FMT_NF4 = 1, 2
+FMT_2BIT, FMT_NF4, FMT_INT4 = 1, 2, 3
 F32, F16, BF16 = 0, 1, 2
 
 #: every entry point include/lq.h declares
@@ -134,8 +134,8 @@ class QuantWeights:
     N: int
     K: int
     codes: object                 # uint8 tensor
-    scales: object                # float16 [N][K/32] (2-bit) or float32 [N][K/64] (NF4)
-    offsets: object = None        # float16 [N][K/32] (2-bit)
+    scales: object                # float16 [N][K/32] (2-bit, INT4) or float32 [N][K/64] (NF4)
+    offsets: object = None        # float16 [N][K/32] (2-bit) or the int32 permutation [K] (INT4)
     anchor_idx: object = None     # int32 [A]
     anchor_w: object = None       # float16 [N][ld_anchor]
     A: int = 0
@@ -149,10 +149,11 @@ class QuantWeights:
 
         def t(a, dtype):
             return torch.from_numpy(np.ascontiguousarray(a)).view(dtype).to(device)
-        if fmt == FMT_2BIT:
+        if fmt in (FMT_2BIT, FMT_INT4):
             A = int(packed["A"])
-            return QuantWeights(FMT_2BIT, int(packed["N"]), int(packed["K"]), t(packed["codes"], torch.uint8),
-                                t(packed["scales"], torch.float16), t(packed["offsets"], torch.float16),
+            off = t(packed["offsets"], torch.float16) if fmt == FMT_2BIT else t(packed["perm"], torch.int32)
+            return QuantWeights(fmt, int(packed["N"]), int(packed["K"]), t(packed["codes"], torch.uint8),
+                                t(packed["scales"], torch.float16), off,
                                 t(packed["anchor_idx"], torch.int32) if A > 0 else None,
                                 t(packed["anchor_w"], torch.float16) if A > 0 else None, A, int(packed["ld_anchor"]))
         return QuantWeights(FMT_NF4, int(packed["N"]), int(packed["K"]), t(packed["codes"], torch.uint8),

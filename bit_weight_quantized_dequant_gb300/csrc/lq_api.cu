@@ -56,15 +56,15 @@ lq_status check_anchor_order(const int32_t* anchor_idx, int A, int K, cudaStream
 }
 
 // Shape, pointer and alignment rules shared by every compute entry point.
-lq_status check_weights(int format, const uint8_t* codes, const void* scales, const uint16_t* offsets,
+lq_status check_weights(int format, const uint8_t* codes, const void* scales, const void* offsets,
                         const int32_t* anchor_idx, const uint16_t* anchor_w, int A, int ld_anchor, int N, int K) {
-    if (format != LQ_FMT_2BIT_LM_G32 && format != LQ_FMT_NF4_B64) return LQ_ERR_INVALID_ARG;
+    if (format != LQ_FMT_2BIT_LM_G32 && format != LQ_FMT_NF4_B64 && format != LQ_FMT_INT4_G32) return LQ_ERR_INVALID_ARG;
     if (N < 1 || K < 1) return LQ_ERR_INVALID_ARG;
     if (!codes || !scales) return LQ_ERR_INVALID_ARG;
     if (!aligned16(codes) || !aligned16(scales)) return LQ_ERR_ALIGNMENT;
-    if (format == LQ_FMT_2BIT_LM_G32) {
+    if (format == LQ_FMT_2BIT_LM_G32 || format == LQ_FMT_INT4_G32) {
         if (K % 32 != 0) return LQ_ERR_INVALID_ARG;
-        if (!offsets) return LQ_ERR_INVALID_ARG;
+        if (!offsets) return LQ_ERR_INVALID_ARG;   // (binary16 Z_g, or the INT4 permutation)
         if (!aligned16(offsets)) return LQ_ERR_ALIGNMENT;
         if (A < 0 || A > K) return LQ_ERR_INVALID_ARG;
         if (A > 0) {
@@ -99,7 +99,7 @@ lq_status check_problem(const lq_problem& p) {
     return LQ_OK;
 }
 
-lq_problem make_problem(int format, const uint8_t* codes, const void* scales, const uint16_t* offsets,
+lq_problem make_problem(int format, const uint8_t* codes, const void* scales, const void* offsets,
                         const int32_t* anchor_idx, const uint16_t* anchor_w, int A, int ld_anchor, const void* x,
                         int x_dtype, void* y, int y_dtype, int M, int N, int K) {
     lq_problem p;
@@ -110,7 +110,7 @@ lq_problem make_problem(int format, const uint8_t* codes, const void* scales, co
     p.K = K;
     p.codes = codes;
     p.scales = scales;
-    p.offsets = offsets;
+    p.offsets = offsets;   // (a binary16 array, or the INT4 permutation)
     p.anchor_idx = anchor_idx;
     p.anchor_w = anchor_w;
     p.A = A;
@@ -225,7 +225,7 @@ LQ_API lq_status lq_sync(lq_handle h) {
 }
 
 LQ_API lq_status lq_dequant(lq_handle h, int format, const uint8_t* codes, const void* scales,
-                            const uint16_t* offsets, const int32_t* anchor_idx, const uint16_t* anchor_w, int A,
+                            const void* offsets, const int32_t* anchor_idx, const uint16_t* anchor_w, int A,
                             int ld_anchor, void* w_out, int out_dtype, int N, int K, void* stream) {
     if (!h) return LQ_ERR_INVALID_ARG;
     lq_status s = check_weights(format, codes, scales, offsets, anchor_idx, anchor_w, A, ld_anchor, N, K);
@@ -264,7 +264,7 @@ LQ_API lq_status lq_gemv_grouped(lq_handle h, const lq_problem* problems, int co
     return lq::launch_gemv(h, problems, count, st);
 }
 
-LQ_API lq_status lq_gemv(lq_handle h, int format, const uint8_t* codes, const void* scales, const uint16_t* offsets,
+LQ_API lq_status lq_gemv(lq_handle h, int format, const uint8_t* codes, const void* scales, const void* offsets,
                          const int32_t* anchor_idx, const uint16_t* anchor_w, int A, int ld_anchor, const void* x,
                          int x_dtype, void* y, int y_dtype, int M, int N, int K, void* stream) {
     lq_problem p = make_problem(format, codes, scales, offsets, anchor_idx, anchor_w, A, ld_anchor, x, x_dtype, y,
@@ -272,7 +272,7 @@ LQ_API lq_status lq_gemv(lq_handle h, int format, const uint8_t* codes, const vo
     return lq_gemv_grouped(h, &p, 1, stream);
 }
 
-LQ_API lq_status lq_gemm(lq_handle h, int format, const uint8_t* codes, const void* scales, const uint16_t* offsets,
+LQ_API lq_status lq_gemm(lq_handle h, int format, const uint8_t* codes, const void* scales, const void* offsets,
                          const int32_t* anchor_idx, const uint16_t* anchor_w, int A, int ld_anchor, const void* x,
                          int x_dtype, void* y, int y_dtype, int M, int N, int K, void* stream) {
     if (!h) return LQ_ERR_INVALID_ARG;
@@ -281,7 +281,7 @@ LQ_API lq_status lq_gemm(lq_handle h, int format, const uint8_t* codes, const vo
     lq_status s = check_problem(p);
     if (s != LQ_OK) return s;
     if (M < 1) return LQ_ERR_INVALID_ARG;
-    if (K % 64 != 0) return LQ_ERR_UNSUPPORTED;
+    if (K % 64 != 0 || format == LQ_FMT_INT4_G32) return LQ_ERR_UNSUPPORTED;   // (INT4: decode only)
     DeviceGuard guard(h->device);
     if (!guard.ok) return LQ_ERR_CUDA;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -297,7 +297,7 @@ LQ_API lq_status lq_gemm_grouped(lq_handle h, const lq_problem* problems, int co
         const lq_status s = check_problem(p);
         if (s != LQ_OK) return s;
         if (p.M < 1 || p.batch != 1) return LQ_ERR_UNSUPPORTED;
-        if (p.K % 64 != 0) return LQ_ERR_UNSUPPORTED;
+        if (p.K % 64 != 0 || p.format == LQ_FMT_INT4_G32) return LQ_ERR_UNSUPPORTED;
         if (p.format != problems[0].format || p.x_dtype != problems[0].x_dtype) return LQ_ERR_UNSUPPORTED;
     }
     DeviceGuard guard(h->device);
@@ -409,7 +409,7 @@ lq_status static_scratch(StaticScratchSlot& out) {
 
 }  // namespace
 
-LQ_API lq_status lq_gemv_noalloc(int format, const uint8_t* codes, const void* scales, const uint16_t* offsets,
+LQ_API lq_status lq_gemv_noalloc(int format, const uint8_t* codes, const void* scales, const void* offsets,
                                  const int32_t* anchor_idx, const uint16_t* anchor_w, int A, int ld_anchor,
                                  const void* x, int x_dtype, void* y, int y_dtype, int M, int N, int K,
                                  void* stream) {

@@ -3,6 +3,8 @@
 // 2-bit (otf-llm 4.0.1 README, sections 2-4): W_eff = fmaf(S_g, C[q], Z_g) in
 // fp32 with one rounding; anchor columns then take their binary16 value.
 // NF4 (AirQuant README, NF4 block-wise): W_eff = T[q] * absmax, one fp32 rounding.
+// INT4 (otf-llm 4.0.1 README, the v3.2 engine): W_eff[n][perm[j]] = S * q, an exact
+// fp32 product; anchor columns then take their binary16 value.
 // fp16/bf16 outputs are one round-to-nearest-even conversion of the fp32 value.
 //
 // One thread expands one 32-bit word of codes (16 two-bit or 8 four-bit codes);
@@ -128,6 +130,28 @@ __global__ void __launch_bounds__(256) dequant_nf4_kernel(const uint8_t* __restr
     }
 }
 
+// INT4: one thread per 32-bit word (8 permuted positions of one group), each value
+// written at its input column perm[j].
+template <int OUT>
+__global__ void __launch_bounds__(256) dequant_int4_kernel(const uint8_t* __restrict__ codes,
+                                                           const uint16_t* __restrict__ scales,
+                                                           const int32_t* __restrict__ perm, void* out, int N, int K) {
+    const int64_t words_per_row = K / 8;
+    const int64_t total = (int64_t)N * words_per_row;
+    for (int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; w < total; w += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t n = w / words_per_row;
+        const int64_t wk = w - n * words_per_row;
+        const uint32_t word = ldg32(codes + n * (K / 2) + wk * 4);
+        const float s = half_bits_to_float(scales[n * (K / 32) + wk / 4]);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const int q = ((int)(word << (28 - 4 * c))) >> 28;   // 4-bit two's complement
+            const int col = __ldg(perm + wk * 8 + c);
+            if ((unsigned)col < (unsigned)K) store_out(out, (size_t)(n * K + col), OUT, __fmul_rn(s, (float)q));
+        }
+    }
+}
+
 int grid_for(int64_t work, int num_sms) {
     int64_t blocks = (work + 255) / 256;
     int64_t cap = (int64_t)num_sms * 16;
@@ -135,12 +159,16 @@ int grid_for(int64_t work, int num_sms) {
 }
 
 template <int OUT>
-lq_status dequant_typed(lq_handle h, int format, const uint8_t* codes, const void* scales, const uint16_t* offsets,
+lq_status dequant_typed(lq_handle h, int format, const uint8_t* codes, const void* scales, const void* offsets,
                         const int32_t* anchor_idx, const uint16_t* anchor_w, int A, int ld_anchor, void* w_out,
                         int N, int K, cudaStream_t stream) {
-    if (format == LQ_FMT_2BIT_LM_G32) {
-        dequant_2bit_kernel<OUT><<<grid_for((int64_t)N * (K / 16), h->num_sms), 256, 0, stream>>>(
-            codes, static_cast<const uint16_t*>(scales), offsets, w_out, N, K);
+    if (format == LQ_FMT_2BIT_LM_G32 || format == LQ_FMT_INT4_G32) {
+        if (format == LQ_FMT_2BIT_LM_G32)
+            dequant_2bit_kernel<OUT><<<grid_for((int64_t)N * (K / 16), h->num_sms), 256, 0, stream>>>(
+                codes, static_cast<const uint16_t*>(scales), static_cast<const uint16_t*>(offsets), w_out, N, K);
+        else
+            dequant_int4_kernel<OUT><<<grid_for((int64_t)N * (K / 8), h->num_sms), 256, 0, stream>>>(
+                codes, static_cast<const uint16_t*>(scales), static_cast<const int32_t*>(offsets), w_out, N, K);
         if (A > 0) {
             anchor_scatter_kernel<OUT><<<grid_for((int64_t)N * A, h->num_sms), 256, 0, stream>>>(
                 anchor_idx, anchor_w, A, ld_anchor, w_out, N, K);
@@ -154,7 +182,7 @@ lq_status dequant_typed(lq_handle h, int format, const uint8_t* codes, const voi
 
 }  // namespace
 
-lq_status launch_dequant(lq_handle h, int format, const uint8_t* codes, const void* scales, const uint16_t* offsets,
+lq_status launch_dequant(lq_handle h, int format, const uint8_t* codes, const void* scales, const void* offsets,
                          const int32_t* anchor_idx, const uint16_t* anchor_w, int A, int ld_anchor, void* w_out,
                          int out_dtype, int N, int K, cudaStream_t stream) {
     switch (out_dtype) {

@@ -671,7 +671,7 @@ lq_status launch_gemm_grouped(lq_handle h, const lq_problem* probs, int count, c
         const int A = nf4 ? 0 : p.A;
         const int a_pad = A > 0 ? (A + kBK - 1) / kBK * kBK : 0;
         D.scales = p.scales;
-        D.offsets = p.offsets;
+        D.offsets = static_cast<const uint16_t*>(p.offsets);
         D.y = p.y;
         D.M = p.M;
         D.N = p.N;

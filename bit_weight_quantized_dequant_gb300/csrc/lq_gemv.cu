@@ -501,6 +501,8 @@ lq_status launch_gemv(lq_handle h, const lq_problem* probs, int count, cudaStrea
 // split-K kernel below covers the rest (any K % 32 == 0).
 // LQ_GEMV_KERNEL=regs forces the register-fed kernel (for comparisons and tests).
 lq_status launch_gemv_ws(const GemvWorkspace& ws, const lq_problem* probs, int count, cudaStream_t stream) {
+    if (probs[0].format == LQ_FMT_INT4_G32)   // INT4 decodes on the ring kernel only (K % 256 == 0)
+        return gemv_stream_eligible(probs, count) ? launch_gemv_stream(ws, probs, count, stream) : LQ_ERR_UNSUPPORTED;
     const char* force = getenv("LQ_GEMV_KERNEL");
     const bool regs_only = force && strcmp(force, "regs") == 0;
     if (!regs_only && gemv_stream_eligible(probs, count)) {
@@ -553,7 +555,7 @@ lq_status launch_gemv_regs(const GemvWorkspace& ws, const lq_problem* probs, int
         GemvDesc& d = P.d[i];
         d.codes = q.codes;
         d.scales = q.scales;
-        d.offsets = q.offsets;
+        d.offsets = static_cast<const uint16_t*>(q.offsets);
         d.anchor_idx = q.anchor_idx;
         d.anchor_w = q.anchor_w;
         d.x = q.x;

@@ -65,6 +65,8 @@ struct PrepDesc {
     int64_t job_begin;         // first job of this problem
     int xsc_off;               // halves from a member's x copy to its per-token max |x| words (bf16 x)
     int64_t row_begin;         // first (member, token) row of this problem, for the max |x| pass
+    const int32_t* perm;       // INT4: the column permutation, and its bytes per member
+    int64_t stride_perm;
 };
 
 struct PrepParams {
@@ -83,6 +85,12 @@ struct PrepParams {
 __host__ __device__ constexpr int ring_kstride(int M) { return 16 * M + 4; }
 __device__ __forceinline__ int ring_x_pos(int k, int m, int M) {
     return (k >> 4) * ring_kstride(M) + m * 16 + 4 * (k & 3) + ((k >> 2) & 3);
+}
+// INT4's order inside a block of 16 (permuted) columns: an mma takes columns c, c+4, c+1,
+// c+5 (c = 8h + 2kk) from one code word, so those four sit together at 4 * (2h + kk).
+__device__ __forceinline__ int int4_block_pos(int r) {
+    const int rr = r & 7;
+    return 4 * (2 * (r >> 3) + ((rr >> 1) & 1)) + ((rr >> 2) & 1) + 2 * (rr & 1);
 }
 
 // Sixteen binary16 x values of one token (columns 16q .. 16q+15, as loaded: word i holds
@@ -159,7 +167,34 @@ __global__ void __launch_bounds__(32 * kPrepWarps) xprep_kernel(const __grid_con
     const int32_t* aidx = A > 0 ? reinterpret_cast<const int32_t*>(reinterpret_cast<const char*>(D.anchor_idx) + l * D.stride_anchor_idx)
                                 : nullptr;
     const int steps = K / 256;
-    if (jb < steps && P.ring) {
+    if (jb < steps && P.ring && P.format == LQ_FMT_INT4_G32) {
+        // INT4 in the ring layout: x through the permutation, no column zeroed (anchor positions
+        // store q = 0); one item = 16 permuted positions of one token
+        const int k0 = jb * 256, S = ring_kstride(M);
+        const int32_t* perm = reinterpret_cast<const int32_t*>(reinterpret_cast<const char*>(D.perm) + l * D.stride_perm);
+        uint16_t* dst = D.xperm + l * D.xperm_stride + (int64_t)(k0 / 16) * S;
+        for (int it = lane; it < 16 * M; it += 32) {
+            const int m = it >> 4, ql = it & 15;
+            const float sc = prep_scale(P, D, l, m);
+            const int4* pp = reinterpret_cast<const int4*>(perm + k0 + 16 * ql);
+            uint16_t v[16];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int4 c4 = __ldg(pp + i);
+                const int cs[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int c = cs[e];
+                    v[int4_block_pos(4 * i + e)] =
+                        (unsigned)c < (unsigned)K ? to_half_scaled(x[(int64_t)m * K + c], P.x_bf16, sc) : (uint16_t)0;
+                }
+            }
+            uint2* d2 = reinterpret_cast<uint2*>(dst + ql * S + m * 16);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                d2[i] = make_uint2((uint32_t)v[4 * i] | ((uint32_t)v[4 * i + 1] << 16), (uint32_t)v[4 * i + 2] | ((uint32_t)v[4 * i + 3] << 16));
+        }
+    } else if (jb < steps && P.ring) {
         // the ring layout: one item = 16 columns of one token (two 16-byte loads, one 8-word store)
         const int k0 = jb * 256, S = ring_kstride(M);
         if (lane < 8) step_bits[warp][lane] = 0u;
@@ -309,6 +344,8 @@ struct FDesc {
     int xa_off;                 // ring layout: halves from a member's x to its x at the anchor columns
     int xsc_off;                // halves from a member's x to its per-token max |x| words (bf16 x; see x_scale)
     int a_pad;                  // anchor slots of a member's x at the anchor columns (A rounded up to 48)
+    const int32_t* perm;        // INT4: the column permutation (perm[j] = input column at position j)
+    int64_t stride_perm;        //   bytes per member
     int G;                      // ring kernel: anchor unit spacing inside a row block (su / anchor units)
     const uint16_t* x;          // the caller's x [batch][M][K] (16-bit) and anchor columns, for
     int64_t stride_x;           //   the in-kernel build of the fragment-ordered copy (bytes)
@@ -773,11 +810,14 @@ __global__ void __launch_bounds__(kThreadsS, NT <= 2 ? LQ_STREAM_MIN_BLOCKS : 1)
 //    launch), so a following call's weight copies start while this call finishes; every
 //    kernel waits for its predecessor before it reads x or touches the workspace or y.
 //
-// Stage layout (3072 bytes):
-//   code unit:   codes [32 rows][64 B] | scales [32 rows][8 x binary16] | offsets [32][8]
-//   anchor unit: anchor weights [32 rows][48 x binary16] (zero past A)
+// Stage layouts:
+//   2-bit code unit (3072 B): codes [32 rows][64 B] | scales [32][8 x binary16] | offsets [32][8]
+//   INT4 code unit (4608 B):  codes [32 rows][128 B] (16-byte chunk c of row r at chunk
+//                             c ^ (r & 1), so the lanes of a quarter-warp hit distinct banks)
+//                             | scales [32][8 x binary16]
+//   anchor unit:              anchor weights [32 rows][48 x binary16] (zero past A)
 
-constexpr int kRingStage = 3072;
+__host__ __device__ constexpr int ring_stage(int FMT) { return FMT == LQ_FMT_INT4_G32 ? 4608 : 3072; }
 #ifndef LQ_RING_DEPTH
 #define LQ_RING_DEPTH 2
 #endif
@@ -846,7 +886,9 @@ struct Feed {
 };
 
 // The feed cursor at unit u (left units remain in the warp's range).
+template <int FMT>
 __device__ __noinline__ Feed feed_at(const FParams& P, int64_t u, int left, int lane) {
+    constexpr int CB = FMT == LQ_FMT_INT4_G32 ? 2 : 4;   // codes per byte
     const Pos q = locate(P, u);
     Feed f;
     f.u = u;
@@ -859,21 +901,26 @@ __device__ __noinline__ Feed feed_at(const FParams& P, int64_t u, int left, int 
     f.ord = unit_order(q.s, D.steps, D.su, D.G);
     const int sc = q.s - f.ord.a;   // code units before unit s
     const int64_t rg = row(g);
-    f.c0 = D.codes + q.l * D.stride_codes + rg * (K / 4) + 16 * t + 64 * sc;
-    f.o8 = (int)((row(g + 8) - rg) * (K / 4));
-    f.o16 = (int)((row(g + 16) - rg) * (K / 4));
-    f.o24 = (int)((row(g + 24) - rg) * (K / 4));
-    const int i = lane & 15;
-    const uint8_t* mb = lane < 16 ? static_cast<const uint8_t*>(D.scales) + q.l * D.stride_scales
-                                  : reinterpret_cast<const uint8_t*>(D.offsets) + q.l * D.stride_offsets;
-    const int64_t rm = row(2 * i);
-    f.meta = mb + rm * (K / 16) + 16 * sc;
-    f.om = (int)((row(2 * i + 1) - rm) * (K / 16));
+    f.c0 = D.codes + q.l * D.stride_codes + rg * (K / CB) + (256 / CB / 4) * t + (256 / CB) * sc;
+    f.o8 = (int)((row(g + 8) - rg) * (K / CB));
+    f.o16 = (int)((row(g + 16) - rg) * (K / CB));
+    f.o24 = (int)((row(g + 24) - rg) * (K / CB));
+    if (FMT == LQ_FMT_INT4_G32) {   // scales of row `lane`
+        f.meta = static_cast<const uint8_t*>(D.scales) + q.l * D.stride_scales + row(lane) * (K / 16) + 16 * sc;
+        f.om = 0;
+    } else {                        // lane < 16: scales of rows 2i, 2i+1; else their offsets
+        const int i = lane & 15;
+        const uint8_t* mb = lane < 16 ? static_cast<const uint8_t*>(D.scales) + q.l * D.stride_scales
+                                      : reinterpret_cast<const uint8_t*>(D.offsets) + q.l * D.stride_offsets;
+        const int64_t rm = row(2 * i);
+        f.meta = mb + rm * (K / 16) + 16 * sc;
+        f.om = (int)((row(2 * i + 1) - rm) * (K / 16));
+    }
     f.su = D.su;
     f.A = D.A;
     const int full = N / kRingRows;   // row blocks with all 32 rows inside N
     f.fast = q.rb < full ? full - 1 - q.rb : 0;
-    f.dc = (kRingRows - 1) * (K / 4);
+    f.dc = (kRingRows - 1) * (K / CB);
     f.dm = (kRingRows - 1) * (K / 16);
     f.da = kRingRows * D.ld_anchor * 2;
     f.arow = D.A > 0 ? reinterpret_cast<const uint8_t*>(D.anchor_w) + q.l * D.stride_anchor_w + row(lane) * D.ld_anchor * 2
@@ -883,21 +930,36 @@ __device__ __noinline__ Feed feed_at(const FParams& P, int64_t u, int left, int 
 
 // Copy the next unit into the stage at `st` and step the cursor; one commit group per call
 // (empty once the warp's range is exhausted).
+template <int FMT>
 __device__ __forceinline__ void feed_issue(const FParams& P, Feed& f, uint32_t st, int lane) {
     if (f.left > 0) {
         const int g = lane >> 2, t = lane & 3;
         const int a_unit = f.ord.a;
         if (!unit_step(f.ord)) {
-            const uint32_t dc = st + g * 64 + 16 * t;
-            cp_async16(dc, f.c0, 16);
-            cp_async16(dc + 8 * 64, f.c0 + f.o8, 16);
-            cp_async16(dc + 16 * 64, f.c0 + f.o16, 16);
-            cp_async16(dc + 24 * 64, f.c0 + f.o24, 16);
-            const uint32_t dm = st + 2048 + (lane >> 4) * 512 + (lane & 15) * 32;
-            cp_async16(dm, f.meta, 16);
-            cp_async16(dm + 16, f.meta + f.om, 16);
-            f.c0 += 64;
-            f.meta += 16;
+            if (FMT == LQ_FMT_INT4_G32) {
+                // rows g + 8r: 32 bytes each (chunks 2t, 2t+1, swizzled by the row's parity)
+                const uint32_t d0 = st + g * 128 + (((2 * t) ^ (g & 1)) << 4), d1 = st + g * 128 + (((2 * t + 1) ^ (g & 1)) << 4);
+                const int off[4] = {0, f.o8, f.o16, f.o24};
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    cp_async16(d0 + r * 8 * 128, f.c0 + off[r], 16);
+                    cp_async16(d1 + r * 8 * 128, f.c0 + off[r] + 16, 16);
+                }
+                cp_async16(st + 4096 + lane * 16, f.meta, 16);
+                f.c0 += 128;
+                f.meta += 16;
+            } else {
+                const uint32_t dc = st + g * 64 + 16 * t;
+                cp_async16(dc, f.c0, 16);
+                cp_async16(dc + 8 * 64, f.c0 + f.o8, 16);
+                cp_async16(dc + 16 * 64, f.c0 + f.o16, 16);
+                cp_async16(dc + 24 * 64, f.c0 + f.o24, 16);
+                const uint32_t dm = st + 2048 + (lane >> 4) * 512 + (lane & 15) * 32;
+                cp_async16(dm, f.meta, 16);
+                cp_async16(dm + 16, f.meta + f.om, 16);
+                f.c0 += 64;
+                f.meta += 16;
+            }
         } else {
             const int a0 = a_unit * kAnchorCols;
             const uint32_t dst = st + lane * 96;
@@ -923,7 +985,7 @@ __device__ __forceinline__ void feed_issue(const FParams& P, Feed& f, uint32_t s
                 f.ord.a = 0;
                 f.ord.ua = f.ord.na > 0 ? f.ord.G - 1 : 1 << 30;
             } else {
-                f = feed_at(P, f.u, f.left, lane);
+                f = feed_at<FMT>(P, f.u, f.left, lane);
             }
         }
     }
@@ -1006,6 +1068,10 @@ __device__ __forceinline__ void ring_flush(const FParams& P, const Pos& q, int u
 // (1) every code column as binary16 (two 16-byte loads per 16 columns of a token);
 // (2) x at the anchor columns gathered from (1), zero past A; (3) the anchor columns of
 // (1) zeroed (the anchors replace those weights).
+// INT4: x is taken through the permutation (position j holds x at column perm[j]) with
+// INT4's order inside each block of 16, the anchor x comes straight from the caller's x,
+// and no column is zeroed (an anchor position stores q = 0, which is exactly 0).
+template <int FMT>
 __device__ __forceinline__ void build_span_x(const FParams& P, const Pos& a, const Pos& b, int64_t span0, uint16_t* xsm) {
     const int M = P.M, tid = threadIdx.x, nth = blockDim.x, S = ring_kstride(M);
     // bf16 x first takes each token's max |x| (passes -2: clear, -1: max), for its scale
@@ -1033,6 +1099,35 @@ __device__ __forceinline__ void build_span_x(const FParams& P, const Pos& a, con
 #pragma unroll
                         for (int i = 0; i < 8; ++i) mx = max(mx, max(w[i] & 0x7FFFu, (w[i] >> 16) & 0x7FFFu));
                         atomicMax(&xmaxw[m], mx << 16);
+                    }
+                } else if (pass == 0 && FMT == LQ_FMT_INT4_G32) {
+                    const uint16_t* x = reinterpret_cast<const uint16_t*>(reinterpret_cast<const char*>(D.x) + l * D.stride_x);
+                    const int32_t* perm = reinterpret_cast<const int32_t*>(reinterpret_cast<const char*>(D.perm) + l * D.stride_perm);
+                    for (int it = tid; it < M * K / 16; it += nth) {
+                        const int m = it / (K / 16), q = it - m * (K / 16);
+                        const float sc = P.x_bf16 ? x_scale(xmaxw[m]) : 1.f;
+                        const int4* pp = reinterpret_cast<const int4*>(perm + 16 * q);
+                        int cols[16];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int4 c4 = __ldg(pp + i);
+                            cols[4 * i] = c4.x;
+                            cols[4 * i + 1] = c4.y;
+                            cols[4 * i + 2] = c4.z;
+                            cols[4 * i + 3] = c4.w;
+                        }
+                        uint16_t v[16];
+#pragma unroll
+                        for (int r = 0; r < 16; ++r) {
+                            const int c = cols[r];
+                            const uint16_t raw = (unsigned)c < (unsigned)K ? x[(int64_t)m * K + c] : (uint16_t)0;
+                            v[int4_block_pos(r)] = to_half_scaled(raw, P.x_bf16, sc);
+                        }
+                        uint2* d2 = reinterpret_cast<uint2*>(dst + q * S + m * 16);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            d2[i] = make_uint2((uint32_t)v[4 * i] | ((uint32_t)v[4 * i + 1] << 16),
+                                               (uint32_t)v[4 * i + 2] | ((uint32_t)v[4 * i + 3] << 16));
                     }
                 } else if (pass == 0) {
                     const uint16_t* x = reinterpret_cast<const uint16_t*>(reinterpret_cast<const char*>(D.x) + l * D.stride_x);
@@ -1062,9 +1157,18 @@ __device__ __forceinline__ void build_span_x(const FParams& P, const Pos& a, con
                         const int m = it / a_pad, aa = it - m * a_pad;
                         const int k = aa < A ? __ldg(aidx + aa) : -1;
                         const int bi = aa >> 4, r = aa & 15, pos = 4 * ((r & 7) >> 1) + (r & 1) + 2 * (r >> 3);
-                        xa[(bi * M + m) * 16 + pos] = (unsigned)k < (unsigned)K ? dst[ring_x_pos(k, m, M)] : (uint16_t)0;
+                        uint16_t v = 0;
+                        if ((unsigned)k < (unsigned)K) {
+                            if (FMT == LQ_FMT_INT4_G32) {
+                                const uint16_t* x = reinterpret_cast<const uint16_t*>(reinterpret_cast<const char*>(D.x) + l * D.stride_x);
+                                v = to_half_scaled(x[(int64_t)m * K + k], P.x_bf16, P.x_bf16 ? x_scale(xmaxw[m]) : 1.f);
+                            } else {
+                                v = dst[ring_x_pos(k, m, M)];
+                            }
+                        }
+                        xa[(bi * M + m) * 16 + pos] = v;
                     }
-                } else {
+                } else if (FMT != LQ_FMT_INT4_G32) {
                     for (int it = tid; it < M * A; it += nth) {
                         const int m = it / A, aa = it - m * A;
                         const int k = __ldg(aidx + aa);
@@ -1077,9 +1181,22 @@ __device__ __forceinline__ void build_span_x(const FParams& P, const Pos& a, con
     }
 }
 
-template <int MT, int NT, bool XS>
+// INT4: two codes of a word (nibbles k and k+4, the word XORed with 0x88888888 so each
+// nibble is q + 8) -> binary16 pair (S q_k, S q_{k+4}): OR into 1024's bit pattern gives
+// 1032 + q exactly, subtracting 1032 gives q, and one product by the group's scale rounds
+// once.  (Integer ops on the ALU pipe, half-precision ops on the FMA pipe.)
+__device__ __forceinline__ uint32_t int4_pair(uint32_t wx, int k, uint32_t s2) {
+    const uint32_t v = ((k == 0 ? wx : (wx >> (4 * k))) & 0x000F000Fu) | 0x64006400u;
+    uint32_t d;
+    asm("{\n\t.reg .b32 t;\n\tsub.rn.f16x2 t, %1, %2;\n\tmul.rn.f16x2 %0, t, %3;\n\t}"
+        : "=r"(d) : "r"(v), "r"(0x64086408u), "r"(s2));
+    return d;
+}
+
+template <int FMT, int MT, int NT, bool XS>
 __global__ void __launch_bounds__(32 * ring_warps(NT), 1) gemv_ring_kernel(const __grid_constant__ FParams P) {
     constexpr int kW = ring_warps(NT);
+    constexpr int kStage = ring_stage(FMT);
     extern __shared__ __align__(128) unsigned char ring_smem[];
     const int M = MT > 0 ? MT : P.M;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
@@ -1087,20 +1204,20 @@ __global__ void __launch_bounds__(32 * ring_warps(NT), 1) gemv_ring_kernel(const
     const int64_t wid = (int64_t)blockIdx.x * kW + warp;
     const bool active = wid < W;
     if (!XS && !active) return;
-    const uint32_t ring = smem_u32(ring_smem) + warp * kRingDepth * kRingStage;
-    const unsigned char* ringp = ring_smem + warp * kRingDepth * kRingStage;
+    const uint32_t ring = smem_u32(ring_smem) + warp * kRingDepth * kStage;
+    const unsigned char* ringp = ring_smem + warp * kRingDepth * kStage;
     const int64_t u_begin = active ? P.total_units * wid / W : 0, u_end = active ? P.total_units * (wid + 1) / W : 0;
 
     // weights do not depend on the pre-pass: the first copies go out before waiting for it
     Feed f;
     if (active) {
-        f = feed_at(P, u_begin, (int)(u_end - u_begin), lane);
+        f = feed_at<FMT>(P, u_begin, (int)(u_end - u_begin), lane);
 #pragma unroll
-        for (int i = 0; i < kRingDepth; ++i) feed_issue(P, f, ring + i * kRingStage, lane);
+        for (int i = 0; i < kRingDepth; ++i) feed_issue<FMT>(P, f, ring + i * kStage, lane);
     }
     pdl_launch_dependents();
     int64_t span0 = 0;
-    uint16_t* xsm = reinterpret_cast<uint16_t*>(ring_smem + kW * kRingDepth * kRingStage);
+    uint16_t* xsm = reinterpret_cast<uint16_t*>(ring_smem + kW * kRingDepth * kStage);
     if (XS) {
         const int64_t w_lo = (int64_t)blockIdx.x * kW, w_hi = (w_lo + kW < W) ? w_lo + kW : W;
         if (w_lo >= W) return;   // the whole CTA is idle
@@ -1109,7 +1226,7 @@ __global__ void __launch_bounds__(32 * ring_warps(NT), 1) gemv_ring_kernel(const
         const int64_t span1 = P.d[b.p].xoff + (b.l + 1) * P.d[b.p].xperm_stride;
         (void)span1;
         pdl_wait();   // x may come from the kernel before
-        build_span_x(P, a, b, span0, xsm);
+        build_span_x<FMT>(P, a, b, span0, xsm);
         if (!active) return;
     } else {
         pdl_wait();
@@ -1142,7 +1259,45 @@ __global__ void __launch_bounds__(32 * ring_warps(NT), 1) gemv_ring_kernel(const
         __syncwarp();   // every lane's copies of this unit have landed (the next units may still be in flight)
         const unsigned char* st = ringp + cst;
         const int a_unit = ord.a;
-        if (!unit_step(ord)) {
+        const bool anchor_unit = unit_step(ord);
+        if (FMT == LQ_FMT_INT4_G32 && !anchor_unit) {
+            const uint16_t* xs = xb0 + xlane + (q.s - a_unit) * 16 * S;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {   // group 2t + h: 32 columns = words 4h .. 4h+3 of the lane's slice
+                uint32_t s2[4];
+                uint4 w[4];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const uint16_t sb = *reinterpret_cast<const uint16_t*>(st + 4096 + (g + 8 * r) * 16 + 4 * t + 2 * h);
+                    s2[r] = (uint32_t)sb | ((uint32_t)sb << 16);
+                    peak = fmaxf(peak, 8.f * fabsf(half_bits_to_float(sb)));   // |S q| for the widest code
+                    w[r] = *reinterpret_cast<const uint4*>(st + (g + 8 * r) * 128 + (((2 * t + h) ^ (g & 1)) << 4));
+                    w[r].x ^= 0x88888888u;
+                    w[r].y ^= 0x88888888u;
+                    w[r].z ^= 0x88888888u;
+                    w[r].w ^= 0x88888888u;
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {   // word 4h + i: block 2h + i/2, half i & 1 of it
+#pragma unroll
+                    for (int kk = 0; kk < 2; ++kk) {
+                        uint2 xb[NT];
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt)
+                            xb[nt] = *reinterpret_cast<const uint2*>(xs + (2 * h + (i >> 1)) * S + 4 * (2 * (i & 1) + kk) + tok[nt]);
+                        uint32_t wd[4];
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) wd[r] = i == 0 ? w[r].x : (i == 1 ? w[r].y : (i == 2 ? w[r].z : w[r].w));
+                        const uint32_t a0 = int4_pair(wd[0], 2 * kk, s2[0]), a2 = int4_pair(wd[0], 2 * kk + 1, s2[0]);
+                        const uint32_t a1 = int4_pair(wd[1], 2 * kk, s2[1]), a3 = int4_pair(wd[1], 2 * kk + 1, s2[1]);
+                        mma_xg<NT, MT>(acc[0], a0, a1, a2, a3, xb);
+                        const uint32_t b0 = int4_pair(wd[2], 2 * kk, s2[2]), b2 = int4_pair(wd[2], 2 * kk + 1, s2[2]);
+                        const uint32_t b1 = int4_pair(wd[3], 2 * kk, s2[3]), b3 = int4_pair(wd[3], 2 * kk + 1, s2[3]);
+                        mma_xg<NT, MT>(acc[1], b0, b1, b2, b3, xb);
+                    }
+                }
+            }
+        } else if (FMT != LQ_FMT_INT4_G32 && !anchor_unit) {
             const uint16_t* xs = xb0 + xlane + (q.s - a_unit) * 16 * S;
 #pragma unroll
             for (int hg = 0; hg < 2; ++hg) {   // group 2t + hg: code words 2hg, 2hg+1 of each row
@@ -1193,8 +1348,8 @@ __global__ void __launch_bounds__(32 * ring_warps(NT), 1) gemv_ring_kernel(const
             }
         }
         __syncwarp();   // every lane is done with this stage: refill it kRingDepth units ahead
-        feed_issue(P, f, ring + cst, lane);
-        cst = cst + kRingStage == kRingDepth * kRingStage ? 0 : cst + kRingStage;
+        feed_issue<FMT>(P, f, ring + cst, lane);
+        cst = cst + kStage == kRingDepth * kStage ? 0 : cst + kStage;
         ++seg_units;
         if (++q.s == q.su || left == 1) {
             ring_flush<NT>(P, q, seg_units, acc, M, lane, xb0);
@@ -1239,11 +1394,11 @@ int resident_ctas(size_t smem) {
     return resident_ctas_of(gemv_stream_kernel<FMT, MT, NT, STAGED>, smem, set_smem, per_sm);
 }
 
-template <int MT, int NT, bool XS>
+template <int FMT, int MT, int NT, bool XS>
 int resident_ctas_ring(size_t smem) {
     static size_t set_smem = (size_t)-1;
     static int per_sm = 0;
-    return resident_ctas_of(gemv_ring_kernel<MT, NT, XS>, smem, set_smem, per_sm, 32 * ring_warps(NT));
+    return resident_ctas_of(gemv_ring_kernel<FMT, MT, NT, XS>, smem, set_smem, per_sm, 32 * ring_warps(NT));
 }
 
 template <int FMT, int MT, int NT, bool STAGED>
@@ -1292,10 +1447,10 @@ lq_status dispatch_fmt(int mode, bool staged, const FParams& P, int64_t grid, si
     }
 }
 
-template <int MT, int NT, bool XS>
+template <int FMT, int MT, int NT, bool XS>
 lq_status ring_launch(int mode, const FParams& P, int64_t grid, size_t smem, int* per_sm, cudaStream_t stream) {
     if (mode == 0) {
-        *per_sm = resident_ctas_ring<MT, NT, XS>(smem);
+        *per_sm = resident_ctas_ring<FMT, MT, NT, XS>(smem);
         return *per_sm < 0 ? LQ_ERR_CUDA : LQ_OK;
     }
     cudaLaunchConfig_t cfg;
@@ -1309,31 +1464,39 @@ lq_status ring_launch(int mode, const FParams& P, int64_t grid, size_t smem, int
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, gemv_ring_kernel<MT, NT, XS>, P) != cudaSuccess) return LQ_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, gemv_ring_kernel<FMT, MT, NT, XS>, P) != cudaSuccess) return LQ_ERR_CUDA;
     return cudaPeekAtLastError() == cudaSuccess ? LQ_OK : LQ_ERR_CUDA;
 }
 
-template <int MT, int NT>
+template <int FMT, int MT, int NT>
 lq_status ring_mt(int mode, bool xs, const FParams& P, int64_t grid, size_t smem, int* per_sm, cudaStream_t stream) {
-    return xs ? ring_launch<MT, NT, true>(mode, P, grid, smem, per_sm, stream)
-              : ring_launch<MT, NT, false>(mode, P, grid, smem, per_sm, stream);
+    return xs ? ring_launch<FMT, MT, NT, true>(mode, P, grid, smem, per_sm, stream)
+              : ring_launch<FMT, MT, NT, false>(mode, P, grid, smem, per_sm, stream);
 }
 
 lq_status dispatch_ring(int mode, bool xs, const FParams& P, int64_t grid, size_t smem, int* per_sm,
                         cudaStream_t stream) {
+    if (P.format == LQ_FMT_INT4_G32) {   // (one token at compile time; 2..8 tokens share one instantiation)
+        if (P.M == 1) return ring_mt<LQ_FMT_INT4_G32, 1, 1>(mode, xs, P, grid, smem, per_sm, stream);
+        if (P.M <= 8) return ring_mt<LQ_FMT_INT4_G32, 0, 1>(mode, xs, P, grid, smem, per_sm, stream);
+        if (P.M <= 16) return ring_mt<LQ_FMT_INT4_G32, 0, 2>(mode, xs, P, grid, smem, per_sm, stream);
+        if (P.M <= 24) return ring_mt<LQ_FMT_INT4_G32, 0, 3>(mode, xs, P, grid, smem, per_sm, stream);
+        if (P.M <= 32) return ring_mt<LQ_FMT_INT4_G32, 0, 4>(mode, xs, P, grid, smem, per_sm, stream);
+        return LQ_ERR_UNSUPPORTED;
+    }
     switch (P.M) {
-        case 1: return ring_mt<1, 1>(mode, xs, P, grid, smem, per_sm, stream);
-        case 2: return ring_mt<2, 1>(mode, xs, P, grid, smem, per_sm, stream);
-        case 3: return ring_mt<3, 1>(mode, xs, P, grid, smem, per_sm, stream);
-        case 4: return ring_mt<4, 1>(mode, xs, P, grid, smem, per_sm, stream);
-        case 5: return ring_mt<5, 1>(mode, xs, P, grid, smem, per_sm, stream);
-        case 6: return ring_mt<6, 1>(mode, xs, P, grid, smem, per_sm, stream);
-        case 7: return ring_mt<7, 1>(mode, xs, P, grid, smem, per_sm, stream);
-        case 8: return ring_mt<8, 1>(mode, xs, P, grid, smem, per_sm, stream);
+        case 1: return ring_mt<LQ_FMT_2BIT_LM_G32, 1, 1>(mode, xs, P, grid, smem, per_sm, stream);
+        case 2: return ring_mt<LQ_FMT_2BIT_LM_G32, 2, 1>(mode, xs, P, grid, smem, per_sm, stream);
+        case 3: return ring_mt<LQ_FMT_2BIT_LM_G32, 3, 1>(mode, xs, P, grid, smem, per_sm, stream);
+        case 4: return ring_mt<LQ_FMT_2BIT_LM_G32, 4, 1>(mode, xs, P, grid, smem, per_sm, stream);
+        case 5: return ring_mt<LQ_FMT_2BIT_LM_G32, 5, 1>(mode, xs, P, grid, smem, per_sm, stream);
+        case 6: return ring_mt<LQ_FMT_2BIT_LM_G32, 6, 1>(mode, xs, P, grid, smem, per_sm, stream);
+        case 7: return ring_mt<LQ_FMT_2BIT_LM_G32, 7, 1>(mode, xs, P, grid, smem, per_sm, stream);
+        case 8: return ring_mt<LQ_FMT_2BIT_LM_G32, 8, 1>(mode, xs, P, grid, smem, per_sm, stream);
         default:
-            if (P.M <= 16) return ring_mt<0, 2>(mode, xs, P, grid, smem, per_sm, stream);
-            if (P.M <= 24) return ring_mt<0, 3>(mode, xs, P, grid, smem, per_sm, stream);
-            if (P.M <= 32) return ring_mt<0, 4>(mode, xs, P, grid, smem, per_sm, stream);
+            if (P.M <= 16) return ring_mt<LQ_FMT_2BIT_LM_G32, 0, 2>(mode, xs, P, grid, smem, per_sm, stream);
+            if (P.M <= 24) return ring_mt<LQ_FMT_2BIT_LM_G32, 0, 3>(mode, xs, P, grid, smem, per_sm, stream);
+            if (P.M <= 32) return ring_mt<LQ_FMT_2BIT_LM_G32, 0, 4>(mode, xs, P, grid, smem, per_sm, stream);
             return LQ_ERR_UNSUPPORTED;
     }
 }
@@ -1408,8 +1571,9 @@ lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* probs, i
     // and more tokens run the register-fed one.  LQ_GEMV_KERNEL=stream / ring forces either
     // for 2-bit (comparisons and tests).
     const char* kern_env = getenv("LQ_GEMV_KERNEL");
-    const bool use_ring = fmt == LQ_FMT_2BIT_LM_G32 && (M <= 8 || (kern_env && strcmp(kern_env, "ring") == 0)) &&
-                          !(kern_env && strcmp(kern_env, "stream") == 0);
+    const bool use_ring = fmt == LQ_FMT_INT4_G32 ||   // (INT4 decodes on the ring kernel only)
+                          (fmt == LQ_FMT_2BIT_LM_G32 && (M <= 8 || (kern_env && strcmp(kern_env, "ring") == 0)) &&
+                           !(kern_env && strcmp(kern_env, "stream") == 0));
     const int rows_blk = use_ring ? kRingRows : 16;            // output rows per row block
     const int cta_warps = use_ring ? ring_warps(M <= 8 ? 1 : 2) : kWarps;
 
@@ -1417,12 +1581,14 @@ lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* probs, i
     int max_k = 0;
     for (int i = 0; i < count; ++i) {
         const lq_problem& q = probs[i];
-        const int A = fmt == LQ_FMT_2BIT_LM_G32 ? q.A : 0;
+        const int A = fmt != LQ_FMT_NF4_B64 ? q.A : 0;
         FDesc& d = P.d[i];
         PrepDesc& e = Q.d[i];
         d.codes = q.codes;
         d.scales = q.scales;
-        d.offsets = q.offsets;
+        d.offsets = fmt == LQ_FMT_2BIT_LM_G32 ? static_cast<const uint16_t*>(q.offsets) : nullptr;
+        d.perm = e.perm = fmt == LQ_FMT_INT4_G32 ? static_cast<const int32_t*>(q.offsets) : nullptr;
+        d.stride_perm = e.stride_perm = q.stride_offsets;
         d.anchor_w = q.anchor_w;
         d.y = q.y;
         d.stride_codes = q.stride_codes;
@@ -1475,7 +1641,7 @@ lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* probs, i
     if (units == 0) return LQ_OK;
     // arrival counts live in the counter area, which every kernel leaves at zero
     if ((size_t)blocks > ws.num_counters) return LQ_ERR_UNSUPPORTED;
-    const size_t ring_smem = (size_t)cta_warps * kRingDepth * kRingStage;
+    const size_t ring_smem = (size_t)cta_warps * kRingDepth * ring_stage(fmt);
     // size the grid; the warp partition then fixes the x span of each CTA
     int per_sm = 0;
     if (use_ring) {

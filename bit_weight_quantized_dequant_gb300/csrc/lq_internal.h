@@ -69,7 +69,7 @@ struct GemvParams {
     int64_t total_units;
 };
 
-lq_status launch_dequant(lq_handle h, int format, const uint8_t* codes, const void* scales, const uint16_t* offsets,
+lq_status launch_dequant(lq_handle h, int format, const uint8_t* codes, const void* scales, const void* offsets,
                          const int32_t* anchor_idx, const uint16_t* anchor_w, int A, int ld_anchor, void* w_out,
                          int out_dtype, int N, int K, cudaStream_t stream);
 

@@ -22,6 +22,18 @@
  *       anchor_w   binary16[N][ld_anchor], ld_anchor >= A, ld_anchor % 8 == 0
  *   Anchor columns store code 0 in `codes`; their code is never used.
  *
+ * LQ_FMT_INT4_G32 — the same README's v3.2 engine ("Comparative Analysis: INT4
+ *   (v3.2) vs INT2 Non-Uniform (v4.0)" and the "Method Comparison Table"): 2 weights
+ *   per byte on a uniform grid with zero-point 0, input columns stored in a global
+ *   static permutation, the top-1 % columns kept in binary16.  Position j of the
+ *   permuted order holds input column perm[j]; 32 consecutive positions of a row
+ *   share a binary16 scale S:
+ *       W_eff[n][perm[j]] = S * q[n][j]     (fp32, exact; q a 4-bit two's complement)
+ *       W_eff[n][anchor_idx[a]] = anchor_w[n][a]    (replaces the grid value)
+ *   Storage: codes uint8 [N][K/2] (position 2j in the low nibble of byte j, 2j+1 in
+ *   the high nibble), scales binary16 [N][K/32], `offsets` = perm int32 [K] (each
+ *   column once), anchors as for the 2-bit format (anchor positions store q = 0).
+ *
  * LQ_FMT_NF4_B64 — the AirQuant README, "Fundamentacao Teorica" item 2 (NF4,
  *   block-wise, the QLoRA NormalFloat data type): blocks of 64 consecutive input
  *   columns share an fp32 absmax, codes index the 16 NF4 levels T:
@@ -98,7 +110,8 @@ typedef enum lq_status {
 
 typedef enum lq_format {
     LQ_FMT_2BIT_LM_G32 = 1,
-    LQ_FMT_NF4_B64 = 2
+    LQ_FMT_NF4_B64 = 2,
+    LQ_FMT_INT4_G32 = 3
 } lq_format;
 
 typedef enum lq_dtype {
@@ -120,7 +133,7 @@ typedef struct lq_problem {
     int M, N, K;
     const uint8_t* codes;
     const void* scales;        /* binary16 S_g (2-bit) or fp32 absmax (NF4) */
-    const uint16_t* offsets;   /* binary16 Z_g (2-bit) or NULL */
+    const void* offsets;       /* binary16 Z_g (2-bit), int32 perm[K] (INT4), or NULL (NF4) */
     const int32_t* anchor_idx; /* 2-bit only, may be NULL when A == 0 */
     const uint16_t* anchor_w;  /* 2-bit only, may be NULL when A == 0 */
     int A;
@@ -163,7 +176,7 @@ LQ_API lq_status lq_sync(lq_handle h);
  * Format rules: K % 32 == 0 (2-bit) or K % 64 == 0 (NF4); N >= 1; anchors as above.
  */
 LQ_API lq_status lq_dequant(lq_handle h, int format,
-                            const uint8_t* codes, const void* scales, const uint16_t* offsets,
+                            const uint8_t* codes, const void* scales, const void* offsets,
                             const int32_t* anchor_idx, const uint16_t* anchor_w, int A, int ld_anchor,
                             void* w_out, int out_dtype, int N, int K, void* stream);
 
@@ -174,7 +187,7 @@ LQ_API lq_status lq_dequant(lq_handle h, int format,
  * LQ_ERR_UNSUPPORTED for M outside 1..32.
  */
 LQ_API lq_status lq_gemv(lq_handle h, int format,
-                         const uint8_t* codes, const void* scales, const uint16_t* offsets,
+                         const uint8_t* codes, const void* scales, const void* offsets,
                          const int32_t* anchor_idx, const uint16_t* anchor_w, int A, int ld_anchor,
                          const void* x, int x_dtype, void* y, int y_dtype,
                          int M, int N, int K, void* stream);
@@ -196,7 +209,7 @@ LQ_API lq_status lq_gemv_grouped(lq_handle h, const lq_problem* problems, int co
  * y_dtype.  2-bit: K % 64 == 0; NF4: K % 64 == 0.
  */
 LQ_API lq_status lq_gemm(lq_handle h, int format,
-                         const uint8_t* codes, const void* scales, const uint16_t* offsets,
+                         const uint8_t* codes, const void* scales, const void* offsets,
                          const int32_t* anchor_idx, const uint16_t* anchor_w, int A, int ld_anchor,
                          const void* x, int x_dtype, void* y, int y_dtype,
                          int M, int N, int K, void* stream);
@@ -248,7 +261,7 @@ LQ_API lq_status lq_gemm_grouped(lq_handle h, const lq_problem* problems, int co
  * Arguments, layouts, results and the other errors are those of lq_gemv.
  */
 LQ_API lq_status lq_gemv_noalloc(int format,
-                                 const uint8_t* codes, const void* scales, const uint16_t* offsets,
+                                 const uint8_t* codes, const void* scales, const void* offsets,
                                  const int32_t* anchor_idx, const uint16_t* anchor_w, int A, int ld_anchor,
                                  const void* x, int x_dtype, void* y, int y_dtype,
                                  int M, int N, int K, void* stream);

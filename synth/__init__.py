@@ -137,6 +137,33 @@ def random_packed_nf4(N: int, K: int, sigma: float = 0.02, seed: int = 0, cfg: i
     return dict(codes=codes, absmax=absmax, N=N, K=K)
 
 
+def random_packed_int4(N: int, K: int, A: int, sigma: float = 0.02, seed: int = 0, cfg: int = 0,
+                       matrix_id: int = 0) -> dict:
+    """Random bytes in the INT4 storage layout, for runs at full size.
+
+    perm: a random permutation of the K columns (int32); codes: random bytes [N][K/2]
+    with the nibbles of the permuted positions that hold an anchor column set to 0 (the
+    layout stores code 0 there); scales ~ (sigma/4)*U(0.8, 1.2) as binary16 [N][K/32];
+    anchor_idx: A distinct sorted columns; anchor_w ~ N(0, sigma^2) binary16, zero past A.
+    """
+    g = rng(seed, cfg, 60_000 + matrix_id)
+    ld = max(8, (A + 7) // 8 * 8)
+    perm = g.permutation(K).astype(np.int32)
+    codes = g.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    anchor_idx = np.sort(g.choice(K, size=A, replace=False)).astype(np.int32) if A > 0 else np.zeros(0, np.int32)
+    if A > 0:
+        pos = np.flatnonzero(np.isin(perm, anchor_idx))          # permuted positions of anchor columns
+        keep = np.where(pos % 2 == 0, 0xF0, 0x0F).astype(np.uint8)
+        for j, m in zip(pos // 2, keep):
+            codes[:, j] &= m
+    scales = f32_to_f16_bits((sigma / 4) * g.uniform(0.8, 1.2, size=(N, K // 32)).astype(np.float32))
+    anchor_w = np.zeros((N, ld), dtype=np.uint16)
+    if A > 0:
+        anchor_w[:, :A] = f32_to_f16_bits(sigma * g.standard_normal((N, A)).astype(np.float32))
+    return dict(codes=codes, scales=scales, perm=perm, anchor_idx=anchor_idx, anchor_w=anchor_w,
+                A=A, ld_anchor=ld, N=N, K=K)
+
+
 def random_packed_2bit_sets(L: int, N: int, K: int, A: int, sigma: float = 0.02, seed: int = 0, cfg: int = 0) -> dict:
     """L independent weight sets of one shape in the 2-bit storage layout, stacked on a
     leading axis (codes [L][N][K/4], scales/offsets [L][N][K/32], anchor_idx [L][A],

@@ -39,3 +39,14 @@ def assert_within(y_gpu: np.ndarray, y_ref: np.ndarray, E: np.ndarray, rel: floa
                              f"gpu={y_gpu[tuple(i)]!r} ref={y_ref[tuple(i)]!r} E={E[tuple(i)]!r} "
                              f"max err/E={np.max(err / (E + 1e-30)):.3e}")
     return float(np.max(err / (E + 1e-30)))
+
+
+def quantized_int4(N, K, seed=0, cfg=0, mid=0, sigma=0.02, outlier_frac=0.01, outlier_mult=20.0):
+    """Synthetic W quantized by the oracle to the INT4 format: the impact-score permutation
+    and the top-1% binary16 outlier columns both from the activation profile."""
+    W = synth.weights(N, K, sigma, seed=seed, cfg=cfg, matrix_id=mid, big_frac=0.001, big_mult=10.0)
+    outl = synth.outlier_channels(K, outlier_frac, seed=seed, cfg=cfg)
+    prof = O.activation_profile(synth.channel_sigma(K, outl, outlier_mult))
+    perm = O.int4_permutation(W, prof)
+    ai = O.select_anchors(W, prof, frac=O.INT4_OUTLIER_FRAC)
+    return O.quantize_int4(W, perm, ai), outl
