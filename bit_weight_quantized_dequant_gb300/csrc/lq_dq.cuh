@@ -31,6 +31,36 @@ __device__ __forceinline__ void lut2_bits_peak(uint16_t s_bits, uint16_t z_bits,
     peak = fmaxf(peak, __fmaf_rn(1.52f, fabsf(s), fabsf(z)));
 }
 
+// The tables of two groups at once (packed fp32 fma: one instruction per table entry for
+// both; each entry still one fmaf rounding, then one RNE to binary16), raising `peak` to the
+// largest |fmaf(S, C[q], Z)| of both, which is max(|L0|, |L3|) (C is symmetric, so one of the
+// two is fmaf(1.52, |S|, |Z|) exactly).
+__device__ __forceinline__ float2 fma_f32x2(float2 a, float c, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 a, c, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 c, {%4, %4};\n\tmov.b64 b, {%5, %6};\n\t"
+        "fma.rn.f32x2 d, a, c, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(c), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+__device__ __forceinline__ void lut2_bits_x2(float2 S, float2 Z, uint32_t& A0, uint32_t& B0, uint32_t& A1,
+                                             uint32_t& B1, float& peak) {
+    const float2 L0 = fma_f32x2(S, -1.52f, Z), L1 = fma_f32x2(S, -0.45f, Z);
+    const float2 L2 = fma_f32x2(S, 0.45f, Z), L3 = fma_f32x2(S, 1.52f, Z);
+    A0 = pack_half2_rn(L0.x, L1.x);
+    B0 = pack_half2_rn(L2.x, L3.x);
+    A1 = pack_half2_rn(L0.y, L1.y);
+    B1 = pack_half2_rn(L2.y, L3.y);
+    peak = fmax3(peak, fabsf(L0.x), fabsf(L3.x));
+    peak = fmax3(peak, fabsf(L0.y), fabsf(L3.y));
+}
+
 // Codes at bit offset 2j of the four bytes of w -> binary16 pairs (byte0, byte1) in `lo`
 // and (byte2, byte3) in `hi`.  One multiply turns each 2-bit code q into the selector
 // nibbles (2q, 2q+1) of its byte lane; the upper half of that word serves bytes 2 and 3.

@@ -78,11 +78,12 @@ struct PrepParams {
 };
 
 // x layout of the ring kernel, per batch member: the code columns in blocks of 16 (block
-// q at q * (16 M + 4) halves; token m at m * 16 inside it; column 16q + j + 4e at position
-// 4j + e, so a lane's four x values of one mma are one 8-byte load; the 4-half pad puts
-// the blocks that the four lanes of a row read in different banks), then x at the anchor
-// columns in the pre-pass's fragment order.
-__host__ __device__ constexpr int ring_kstride(int M) { return 16 * M + 4; }
+// q at q * (16 M + 8) halves; token m at m * 16 inside it; column 16q + j + 4e at position
+// 4j + e, so a lane's four x values of one mma are one 8-byte load and a token's block is
+// two 16-byte loads; the 8-half pad keeps blocks 16-byte aligned and spreads the blocks that
+// the four lanes of a row read over two bank groups), then x at the anchor columns in the
+// pre-pass's fragment order.
+__host__ __device__ constexpr int ring_kstride(int M) { return 16 * M + 8; }
 __device__ __forceinline__ int ring_x_pos(int k, int m, int M) {
     return (k >> 4) * ring_kstride(M) + m * 16 + 4 * (k & 3) + ((k >> 2) & 3);
 }
@@ -360,7 +361,20 @@ struct FParams {
     int count, M, y_dtype, x_bf16, format;
     int bitmap_words;           // STAGED: shared-memory words of the anchor bitmap (max K / 32)
     int64_t total_units, total_warps;
+    int div32;                  // total_units * total_warps < 2^32: warp ranges in 32-bit arithmetic
 };
+
+// First unit of warp w's range, U * w / W (32-bit division when the product fits).
+__device__ __forceinline__ int64_t split_at(const FParams& P, int64_t w) {
+    if (P.div32) return (int64_t)((uint32_t)P.total_units * (uint32_t)w / (uint32_t)P.total_warps);
+    return P.total_units * w / P.total_warps;
+}
+
+// The warp whose range [U*w/W, U*(w+1)/W) holds unit u.
+__device__ __forceinline__ int64_t owner_of(const FParams& P, int64_t u) {
+    if (P.div32) return (int64_t)((((uint32_t)u + 1u) * (uint32_t)P.total_warps - 1u) / (uint32_t)P.total_units);
+    return ((u + 1) * P.total_warps - 1) / P.total_units;
+}
 
 
 // Position of a unit: problem, member, 16-row block, unit inside the row block, with
@@ -370,8 +384,7 @@ struct Pos {
     int64_t l;
 };
 
-// (rare paths are kept out of line: the unrolled unit loop must stay small)
-__device__ __noinline__ Pos locate(const FParams& P, int64_t u) {
+__device__ __forceinline__ Pos locate(const FParams& P, int64_t u) {
     Pos q;
     q.p = 0;
     while (q.p + 1 < P.count && u >= P.d[q.p + 1].unit_begin) ++q.p;
@@ -417,8 +430,6 @@ __device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* p, unsigned v
     return old;
 }
 
-// The warp whose range [U*w/W, U*(w+1)/W) holds unit u.
-__device__ __noinline__ int64_t owner_warp(int64_t u, int64_t W, int64_t U) { return ((u + 1) * W - 1) / U; }
 
 // The last warp of a row block adds the slots of its nc contributors in order and writes y.
 // A slot holds [M][rows] fp32 sums; rows is 16 (streaming kernel) or 32 (ring kernel).
@@ -508,7 +519,7 @@ __global__ void __launch_bounds__(kThreadsS, NT <= 2 ? LQ_STREAM_MIN_BLOCKS : 1)
     if (STAGED) {
         const int64_t w_lo = (int64_t)blockIdx.x * kWarps, w_hi = (w_lo + kWarps < W) ? w_lo + kWarps : W;
         if (w_lo >= W) return;   // the whole CTA is idle
-        const int64_t uc0 = P.total_units * w_lo / W, uc1 = P.total_units * w_hi / W;
+        const int64_t uc0 = split_at(P, w_lo), uc1 = split_at(P, w_hi);
         const Pos a = locate(P, uc0), b = locate(P, uc1 - 1);
         const FDesc& Da = P.d[a.p];
         const FDesc& Db = P.d[b.p];
@@ -524,7 +535,7 @@ __global__ void __launch_bounds__(kThreadsS, NT <= 2 ? LQ_STREAM_MIN_BLOCKS : 1)
         (void)Db;
     }
     if (wid >= W) return;
-    const int64_t u_begin = P.total_units * wid / W, u_end = P.total_units * (wid + 1) / W;
+    const int64_t u_begin = split_at(P, wid), u_end = split_at(P, wid + 1);
     const int xlane = min(g, M - 1) * 16 + t * 4;            // this lane's fragment inside a block
     int tok[NT];   // x-fragment offset of each n-tile's token (clamped to the last real token)
 #pragma unroll
@@ -568,7 +579,7 @@ __global__ void __launch_bounds__(kThreadsS, NT <= 2 ? LQ_STREAM_MIN_BLOCKS : 1)
         const int64_t blk = q.l * D.rblocks + q.rb;
         const int64_t first_u = D.unit_begin + blk * q.su;
         // this warp's slot: its place among the warps that share the block
-        const int64_t w0 = first_u >= u_begin ? wid : owner_warp(first_u, W, P.total_units);
+        const int64_t w0 = first_u >= u_begin ? wid : owner_of(P, first_u);
         float* slots = D.part + blk * D.cmax * M * 16;
         float* mine = slots + (int)(wid - w0) * M * 16;
 #pragma unroll
@@ -590,7 +601,7 @@ __global__ void __launch_bounds__(kThreadsS, NT <= 2 ? LQ_STREAM_MIN_BLOCKS : 1)
         if (__shfl_sync(0xffffffffu, last, 0)) {
             __syncwarp();   // lane 0's acquire orders the other lanes' slot loads too
             if (lane == 0) D.cnt[blk] = 0u;   // counts start at zero for the next launch
-            const int nc = (int)(owner_warp(first_u + q.su - 1, W, P.total_units) - w0 + 1);
+            const int nc = (int)(owner_of(P, first_u + q.su - 1) - w0 + 1);
             finish_block(slots, nc, M, static_cast<char*>(D.y) + q.l * D.stride_y, D.N, q.rb * 16, P.y_dtype, lane);
         }
     };
@@ -887,7 +898,7 @@ struct Feed {
 
 // The feed cursor at unit u (left units remain in the warp's range).
 template <int FMT>
-__device__ __noinline__ Feed feed_at(const FParams& P, int64_t u, int left, int lane) {
+__device__ __forceinline__ Feed feed_at(const FParams& P, int64_t u, int left, int lane) {
     constexpr int CB = FMT == LQ_FMT_INT4_G32 ? 2 : 4;   // codes per byte
     const Pos q = locate(P, u);
     Feed f;
@@ -1032,10 +1043,10 @@ __device__ __forceinline__ void ring_flush(const FParams& P, const Pos& q, int u
     }
     const int64_t W = P.total_warps;
     const int64_t wid = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    const int64_t u_begin = P.total_units * wid / W;
+    const int64_t u_begin = split_at(P, wid);
     const int64_t blk = q.l * D.rblocks + q.rb;
     const int64_t first_u = D.unit_begin + blk * q.su;
-    const int64_t w0 = first_u >= u_begin ? wid : owner_warp(first_u, W, P.total_units);
+    const int64_t w0 = first_u >= u_begin ? wid : owner_of(P, first_u);
     float* slots = D.part + blk * D.cmax * M * kRingRows;
     float* mine = slots + (int)(wid - w0) * M * kRingRows;
 #pragma unroll
@@ -1057,25 +1068,26 @@ __device__ __forceinline__ void ring_flush(const FParams& P, const Pos& q, int u
     if (__shfl_sync(0xffffffffu, last, 0)) {
         __syncwarp();
         if (lane == 0) D.cnt[blk] = 0u;
-        const int nc = (int)(owner_warp(first_u + q.su - 1, W, P.total_units) - w0 + 1);
+        const int nc = (int)(owner_of(P, first_u + q.su - 1) - w0 + 1);
         finish_block(slots, nc, M, static_cast<char*>(D.y) + q.l * D.stride_y, D.N, q.rb * kRingRows, P.y_dtype,
                      lane, kRingRows);
     }
 }
 
 // The x span of a CTA (members a..b of the launch, a few at most) built in shared memory
-// in the ring layout, in three passes over all members with one CTA barrier after each:
-// (1) every code column as binary16 (two 16-byte loads per 16 columns of a token);
-// (2) x at the anchor columns gathered from (1), zero past A; (3) the anchor columns of
-// (1) zeroed (the anchors replace those weights).
+// in the ring layout, with one CTA barrier after each pass:
+// (0) every code column as binary16 (two 16-byte loads per 16 columns of a token), and x at
+//     the anchor columns (zero past A) read from the caller's x, both in the same pass;
+// (1) the anchor columns of (0) zeroed (the anchors replace those weights).
+// bf16 x first takes each token's max |x| (passes -2: clear, -1: max), for its scale.
 // INT4: x is taken through the permutation (position j holds x at column perm[j]) with
-// INT4's order inside each block of 16, the anchor x comes straight from the caller's x,
-// and no column is zeroed (an anchor position stores q = 0, which is exactly 0).
+// INT4's order inside each block of 16, and no column is zeroed (an anchor position stores
+// q = 0, which is exactly 0), so pass (1) is not needed.
 template <int FMT>
 __device__ __forceinline__ void build_span_x(const FParams& P, const Pos& a, const Pos& b, int64_t span0, uint16_t* xsm) {
     const int M = P.M, tid = threadIdx.x, nth = blockDim.x, S = ring_kstride(M);
-    // bf16 x first takes each token's max |x| (passes -2: clear, -1: max), for its scale
-    for (int pass = P.x_bf16 ? -2 : 0; pass < 3; ++pass) {
+    const int last_pass = FMT == LQ_FMT_INT4_G32 ? 0 : 1;
+    for (int pass = P.x_bf16 ? -2 : 0; pass <= last_pass; ++pass) {
         for (int p = a.p; p <= b.p; ++p) {
             const FDesc& D = P.d[p];
             const int K = D.K, A = D.A;
@@ -1085,11 +1097,11 @@ __device__ __forceinline__ void build_span_x(const FParams& P, const Pos& a, con
                 const int32_t* aidx = A > 0 ? reinterpret_cast<const int32_t*>(reinterpret_cast<const char*>(D.anchor_idx) +
                                                                                  l * D.stride_anchor_idx)
                                             : nullptr;
+                const uint16_t* x = reinterpret_cast<const uint16_t*>(reinterpret_cast<const char*>(D.x) + l * D.stride_x);
                 uint32_t* xmaxw = reinterpret_cast<uint32_t*>(dst + D.xsc_off);
                 if (pass == -2) {
                     for (int m = tid; m < M; m += nth) xmaxw[m] = 0u;
                 } else if (pass == -1) {
-                    const uint16_t* x = reinterpret_cast<const uint16_t*>(reinterpret_cast<const char*>(D.x) + l * D.stride_x);
                     for (int it = tid; it < M * K / 16; it += nth) {
                         const int m = it / (K / 16), q = it - m * (K / 16);
                         const uint4* src = reinterpret_cast<const uint4*>(x + (int64_t)m * K + 16 * q);
@@ -1100,73 +1112,64 @@ __device__ __forceinline__ void build_span_x(const FParams& P, const Pos& a, con
                         for (int i = 0; i < 8; ++i) mx = max(mx, max(w[i] & 0x7FFFu, (w[i] >> 16) & 0x7FFFu));
                         atomicMax(&xmaxw[m], mx << 16);
                     }
-                } else if (pass == 0 && FMT == LQ_FMT_INT4_G32) {
-                    const uint16_t* x = reinterpret_cast<const uint16_t*>(reinterpret_cast<const char*>(D.x) + l * D.stride_x);
-                    const int32_t* perm = reinterpret_cast<const int32_t*>(reinterpret_cast<const char*>(D.perm) + l * D.stride_perm);
-                    for (int it = tid; it < M * K / 16; it += nth) {
-                        const int m = it / (K / 16), q = it - m * (K / 16);
-                        const float sc = P.x_bf16 ? x_scale(xmaxw[m]) : 1.f;
-                        const int4* pp = reinterpret_cast<const int4*>(perm + 16 * q);
-                        int cols[16];
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const int4 c4 = __ldg(pp + i);
-                            cols[4 * i] = c4.x;
-                            cols[4 * i + 1] = c4.y;
-                            cols[4 * i + 2] = c4.z;
-                            cols[4 * i + 3] = c4.w;
-                        }
-                        uint16_t v[16];
-#pragma unroll
-                        for (int r = 0; r < 16; ++r) {
-                            const int c = cols[r];
-                            const uint16_t raw = (unsigned)c < (unsigned)K ? x[(int64_t)m * K + c] : (uint16_t)0;
-                            v[int4_block_pos(r)] = to_half_scaled(raw, P.x_bf16, sc);
-                        }
-                        uint2* d2 = reinterpret_cast<uint2*>(dst + q * S + m * 16);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            d2[i] = make_uint2((uint32_t)v[4 * i] | ((uint32_t)v[4 * i + 1] << 16),
-                                               (uint32_t)v[4 * i + 2] | ((uint32_t)v[4 * i + 3] << 16));
-                    }
                 } else if (pass == 0) {
-                    const uint16_t* x = reinterpret_cast<const uint16_t*>(reinterpret_cast<const char*>(D.x) + l * D.stride_x);
-                    for (int it = tid; it < M * K / 16; it += nth) {
-                        const int m = it / (K / 16), q = it - m * (K / 16);
-                        const uint4* src = reinterpret_cast<const uint4*>(x + (int64_t)m * K + 16 * q);
-                        const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
-                        uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w}, o[8];
-                        if (P.x_bf16) {
-                            const float sc = x_scale(xmaxw[m]);
-#pragma unroll
-                            for (int i = 0; i < 8; ++i)
-                                w[i] = (uint32_t)bf16_to_half_scaled((uint16_t)w[i], sc) |
-                                       ((uint32_t)bf16_to_half_scaled((uint16_t)(w[i] >> 16), sc) << 16);
-                        }
-                        ring_x_transpose(w, o);
-                        uint2* d2 = reinterpret_cast<uint2*>(dst + q * S + m * 16);
-                        d2[0] = make_uint2(o[0], o[1]);
-                        d2[1] = make_uint2(o[2], o[3]);
-                        d2[2] = make_uint2(o[4], o[5]);
-                        d2[3] = make_uint2(o[6], o[7]);
-                    }
-                } else if (pass == 1) {
+                    // x at the anchor columns (fragment order), straight from the caller's x
                     const int a_pad = D.a_pad;
                     uint16_t* xa = dst + D.xa_off;
                     for (int it = tid; it < M * a_pad; it += nth) {
                         const int m = it / a_pad, aa = it - m * a_pad;
                         const int k = aa < A ? __ldg(aidx + aa) : -1;
                         const int bi = aa >> 4, r = aa & 15, pos = 4 * ((r & 7) >> 1) + (r & 1) + 2 * (r >> 3);
-                        uint16_t v = 0;
-                        if ((unsigned)k < (unsigned)K) {
-                            if (FMT == LQ_FMT_INT4_G32) {
-                                const uint16_t* x = reinterpret_cast<const uint16_t*>(reinterpret_cast<const char*>(D.x) + l * D.stride_x);
-                                v = to_half_scaled(x[(int64_t)m * K + k], P.x_bf16, P.x_bf16 ? x_scale(xmaxw[m]) : 1.f);
-                            } else {
-                                v = dst[ring_x_pos(k, m, M)];
+                        xa[(bi * M + m) * 16 + pos] =
+                            (unsigned)k < (unsigned)K ? to_half_scaled(x[(int64_t)m * K + k], P.x_bf16, P.x_bf16 ? x_scale(xmaxw[m]) : 1.f)
+                                                      : (uint16_t)0;
+                    }
+                    if (FMT == LQ_FMT_INT4_G32) {
+                        const int32_t* perm = reinterpret_cast<const int32_t*>(reinterpret_cast<const char*>(D.perm) + l * D.stride_perm);
+                        for (int it = tid; it < M * K / 16; it += nth) {
+                            const int m = it / (K / 16), q = it - m * (K / 16);
+                            const float sc = P.x_bf16 ? x_scale(xmaxw[m]) : 1.f;
+                            const int4* pp = reinterpret_cast<const int4*>(perm + 16 * q);
+                            int cols[16];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const int4 c4 = __ldg(pp + i);
+                                cols[4 * i] = c4.x;
+                                cols[4 * i + 1] = c4.y;
+                                cols[4 * i + 2] = c4.z;
+                                cols[4 * i + 3] = c4.w;
                             }
+                            uint16_t v[16];
+#pragma unroll
+                            for (int r = 0; r < 16; ++r) {
+                                const int c = cols[r];
+                                const uint16_t raw = (unsigned)c < (unsigned)K ? x[(int64_t)m * K + c] : (uint16_t)0;
+                                v[int4_block_pos(r)] = to_half_scaled(raw, P.x_bf16, sc);
+                            }
+                            uint2* d2 = reinterpret_cast<uint2*>(dst + q * S + m * 16);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                d2[i] = make_uint2((uint32_t)v[4 * i] | ((uint32_t)v[4 * i + 1] << 16),
+                                                   (uint32_t)v[4 * i + 2] | ((uint32_t)v[4 * i + 3] << 16));
                         }
-                        xa[(bi * M + m) * 16 + pos] = v;
+                    } else {
+                        for (int it = tid; it < M * K / 16; it += nth) {
+                            const int m = it / (K / 16), q = it - m * (K / 16);
+                            const uint4* src = reinterpret_cast<const uint4*>(x + (int64_t)m * K + 16 * q);
+                            const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
+                            uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w}, o[8];
+                            if (P.x_bf16) {
+                                const float sc = x_scale(xmaxw[m]);
+#pragma unroll
+                                for (int i = 0; i < 8; ++i)
+                                    w[i] = (uint32_t)bf16_to_half_scaled((uint16_t)w[i], sc) |
+                                           ((uint32_t)bf16_to_half_scaled((uint16_t)(w[i] >> 16), sc) << 16);
+                            }
+                            ring_x_transpose(w, o);
+                            uint4* d4 = reinterpret_cast<uint4*>(dst + q * S + m * 16);
+                            d4[0] = make_uint4(o[0], o[1], o[2], o[3]);
+                            d4[1] = make_uint4(o[4], o[5], o[6], o[7]);
+                        }
                     }
                 } else if (FMT != LQ_FMT_INT4_G32) {
                     for (int it = tid; it < M * A; it += nth) {
@@ -1180,6 +1183,34 @@ __device__ __forceinline__ void build_span_x(const FParams& P, const Pos& a, con
         __syncthreads();
     }
 }
+
+// binary16 half h (0: low, 1: high) of a 32-bit word, as fp32
+__device__ __forceinline__ float half_of(uint32_t v, int h) {
+    return half_bits_to_float(h == 0 ? (uint16_t)(v & 0xFFFFu) : (uint16_t)(v >> 16));
+}
+
+// One 16-column block of x for the n-tiles of a lane: with one n-tile, two 16-byte loads
+// cover the block's four mma steps (j = 0..3, 4 halves each); with more, each step loads
+// its 8 bytes when used (fewer live registers).
+template <int NT>
+struct XBlock {
+    uint4 v[2];
+    __device__ __forceinline__ void load(const uint16_t* blk, const int (&tok)[NT]) {
+        if (NT == 1) {
+            v[0] = *reinterpret_cast<const uint4*>(blk + tok[0]);
+            v[1] = *reinterpret_cast<const uint4*>(blk + 8 + tok[0]);
+        }
+    }
+    __device__ __forceinline__ void get(int j, const uint16_t* blk, const int (&tok)[NT], uint2 (&xb)[NT]) const {
+        if (NT == 1) {
+            const uint4& u = v[j >> 1];
+            xb[0] = (j & 1) ? make_uint2(u.z, u.w) : make_uint2(u.x, u.y);
+        } else {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) xb[nt] = *reinterpret_cast<const uint2*>(blk + 4 * j + tok[nt]);
+        }
+    }
+};
 
 // INT4: two codes of a word (nibbles k and k+4, the word XORed with 0x88888888 so each
 // nibble is q + 8) -> binary16 pair (S q_k, S q_{k+4}): OR into 1024's bit pattern gives
@@ -1206,7 +1237,7 @@ __global__ void __launch_bounds__(32 * ring_warps(NT), 1) gemv_ring_kernel(const
     if (!XS && !active) return;
     const uint32_t ring = smem_u32(ring_smem) + warp * kRingDepth * kStage;
     const unsigned char* ringp = ring_smem + warp * kRingDepth * kStage;
-    const int64_t u_begin = active ? P.total_units * wid / W : 0, u_end = active ? P.total_units * (wid + 1) / W : 0;
+    const int64_t u_begin = active ? split_at(P, wid) : 0, u_end = active ? split_at(P, wid + 1) : 0;
 
     // weights do not depend on the pre-pass: the first copies go out before waiting for it
     Feed f;
@@ -1221,7 +1252,7 @@ __global__ void __launch_bounds__(32 * ring_warps(NT), 1) gemv_ring_kernel(const
     if (XS) {
         const int64_t w_lo = (int64_t)blockIdx.x * kW, w_hi = (w_lo + kW < W) ? w_lo + kW : W;
         if (w_lo >= W) return;   // the whole CTA is idle
-        const Pos a = locate(P, P.total_units * w_lo / W), b = locate(P, P.total_units * w_hi / W - 1);
+        const Pos a = locate(P, split_at(P, w_lo)), b = locate(P, split_at(P, w_hi) - 1);
         span0 = P.d[a.p].xoff + a.l * P.d[a.p].xperm_stride;
         const int64_t span1 = P.d[b.p].xoff + (b.l + 1) * P.d[b.p].xperm_stride;
         (void)span1;
@@ -1277,14 +1308,14 @@ __global__ void __launch_bounds__(32 * ring_warps(NT), 1) gemv_ring_kernel(const
                     w[r].z ^= 0x88888888u;
                     w[r].w ^= 0x88888888u;
                 }
+                XBlock<NT> xk;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {   // word 4h + i: block 2h + i/2, half i & 1 of it
+                    if ((i & 1) == 0) xk.load(xs + (2 * h + (i >> 1)) * S, tok);
 #pragma unroll
                     for (int kk = 0; kk < 2; ++kk) {
                         uint2 xb[NT];
-#pragma unroll
-                        for (int nt = 0; nt < NT; ++nt)
-                            xb[nt] = *reinterpret_cast<const uint2*>(xs + (2 * h + (i >> 1)) * S + 4 * (2 * (i & 1) + kk) + tok[nt]);
+                        xk.get(2 * (i & 1) + kk, xs + (2 * h + (i >> 1)) * S, tok, xb);
                         uint32_t wd[4];
 #pragma unroll
                         for (int r = 0; r < 4; ++r) wd[r] = i == 0 ? w[r].x : (i == 1 ? w[r].y : (i == 2 ? w[r].z : w[r].w));
@@ -1299,26 +1330,32 @@ __global__ void __launch_bounds__(32 * ring_warps(NT), 1) gemv_ring_kernel(const
             }
         } else if (FMT != LQ_FMT_INT4_G32 && !anchor_unit) {
             const uint16_t* xs = xb0 + xlane + (q.s - a_unit) * 16 * S;
+            uint32_t sp[4], zp[4];   // row g + 8r: binary16 S (Z) of groups 2t (low half) and 2t+1
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                sp[r] = lds32(st + 2048 + (g + 8 * r) * 16 + 4 * t);
+                zp[r] = lds32(st + 2560 + (g + 8 * r) * 16 + 4 * t);
+            }
 #pragma unroll
             for (int hg = 0; hg < 2; ++hg) {   // group 2t + hg: code words 2hg, 2hg+1 of each row
                 uint32_t RA[4], RB[4];
                 uint2 w[4];
 #pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    const uint16_t sb = *reinterpret_cast<const uint16_t*>(st + 2048 + (g + 8 * r) * 16 + 4 * t + 2 * hg);
-                    const uint16_t zb = *reinterpret_cast<const uint16_t*>(st + 2560 + (g + 8 * r) * 16 + 4 * t + 2 * hg);
-                    lut2_bits_peak(sb, zb, RA[r], RB[r], peak);
-                    w[r] = *reinterpret_cast<const uint2*>(st + (g + 8 * r) * 64 + 16 * t + 8 * hg);
-                }
+                for (int rp = 0; rp < 4; rp += 2)   // rows g + 8rp and g + 8rp + 8 share the table arithmetic
+                    lut2_bits_x2(make_float2(half_of(sp[rp], hg), half_of(sp[rp + 1], hg)),
+                                 make_float2(half_of(zp[rp], hg), half_of(zp[rp + 1], hg)), RA[rp], RB[rp], RA[rp + 1],
+                                 RB[rp + 1], peak);
+#pragma unroll
+                for (int r = 0; r < 4; ++r) w[r] = *reinterpret_cast<const uint2*>(st + (g + 8 * r) * 64 + 16 * t + 8 * hg);
 #pragma unroll
                 for (int iw = 0; iw < 2; ++iw) {
                     const int ii = 2 * hg + iw;
+                    XBlock<NT> xk;
+                    xk.load(xs + ii * S, tok);
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         uint2 xb[NT];
-#pragma unroll
-                        for (int nt = 0; nt < NT; ++nt)
-                            xb[nt] = *reinterpret_cast<const uint2*>(xs + ii * S + 4 * j + tok[nt]);
+                        xk.get(j, xs + ii * S, tok, xb);
                         uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
                         const uint32_t w0 = iw ? w[0].y : w[0].x, w1 = iw ? w[1].y : w[1].x;
                         const uint32_t w2 = iw ? w[2].y : w[2].x, w3 = iw ? w[3].y : w[3].x;
@@ -1652,6 +1689,7 @@ lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* probs, i
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>((units + cta_warps - 1) / cta_warps, (int64_t)ws.num_sms * std::max(1, per_sm)));
     const int64_t W = std::min<int64_t>(grid * cta_warps, units);
     P.total_units = units;
+    P.div32 = (uint64_t)units * (uint64_t)W < (1ull << 32) ? 1 : 0;
     P.total_warps = W;
     // With LQ_GEMV_STAGE=1 each CTA builds the x its units read in shared memory when that
     // span is small (a few members, room for a second resident CTA), and no pre-pass runs;
