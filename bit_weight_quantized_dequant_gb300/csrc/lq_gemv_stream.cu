@@ -355,13 +355,15 @@ struct FDesc {
 };
 
 struct FParams {
+    // (read first by every warp: kept together so that the first lookups share cache lines)
+    int64_t total_units, total_warps;
+    int count, div32;           // div32: total_units * total_warps < 2^32, warp ranges in 32-bit arithmetic
+    int64_t unit_begin[kMaxGroup];   // first unit of each problem (copies of d[i].unit_begin)
     int* status;                // device status word: bit 2 is raised when a weight table value overflows binary16
     FDesc d[kMaxGroup];
     const uint16_t* xbuf;       // all x copies: per problem, per member [x in fragment order | x at the anchors]
-    int count, M, y_dtype, x_bf16, format;
+    int M, y_dtype, x_bf16, format;
     int bitmap_words;           // STAGED: shared-memory words of the anchor bitmap (max K / 32)
-    int64_t total_units, total_warps;
-    int div32;                  // total_units * total_warps < 2^32: warp ranges in 32-bit arithmetic
 };
 
 // First unit of warp w's range, U * w / W (32-bit division when the product fits).
@@ -387,7 +389,7 @@ struct Pos {
 __device__ __forceinline__ Pos locate(const FParams& P, int64_t u) {
     Pos q;
     q.p = 0;
-    while (q.p + 1 < P.count && u >= P.d[q.p + 1].unit_begin) ++q.p;
+    while (q.p + 1 < P.count && u >= P.unit_begin[q.p + 1]) ++q.p;
     const FDesc& D = P.d[q.p];
     int64_t loc = u - D.unit_begin;
     const int64_t per_member = (int64_t)D.rblocks * D.su;
@@ -1041,7 +1043,6 @@ __device__ __forceinline__ void ring_flush(const FParams& P, const Pos& q, int u
                 }
         return;
     }
-    const int64_t W = P.total_warps;
     const int64_t wid = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int64_t u_begin = split_at(P, wid);
     const int64_t blk = q.l * D.rblocks + q.rb;
@@ -1225,7 +1226,7 @@ __device__ __forceinline__ uint32_t int4_pair(uint32_t wx, int k, uint32_t s2) {
 }
 
 template <int FMT, int MT, int NT, bool XS>
-__global__ void __launch_bounds__(32 * ring_warps(NT), 1) gemv_ring_kernel(const __grid_constant__ FParams P) {
+__global__ void __launch_bounds__(32 * ring_warps(NT), 16 / ring_warps(NT)) gemv_ring_kernel(const __grid_constant__ FParams P) {
     constexpr int kW = ring_warps(NT);
     constexpr int kStage = ring_stage(FMT);
     extern __shared__ __align__(128) unsigned char ring_smem[];
@@ -1647,7 +1648,7 @@ lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* probs, i
         d.su = d.steps + a_pad / kAnchorCols;
         d.G = d.su > d.steps ? d.su / (d.su - d.steps) : d.su + 1;
         d.rblocks = (q.N + rows_blk - 1) / rows_blk;
-        d.unit_begin = units;
+        d.unit_begin = P.unit_begin[i] = units;
         units += (int64_t)q.batch * d.rblocks * d.su;
         blocks += (int64_t)q.batch * d.rblocks;
         // per member: [x (fragment order, or the ring layout) | x at the anchors (M*a_pad)]
