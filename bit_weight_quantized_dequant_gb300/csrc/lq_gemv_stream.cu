@@ -348,6 +348,7 @@ struct FDesc {
     const int32_t* perm;        // INT4: the column permutation (perm[j] = input column at position j)
     int64_t stride_perm;        //   bytes per member
     int G;                      // ring kernel: anchor unit spacing inside a row block (su / anchor units)
+    int fuse;                   // ring kernel: 1..16 anchors, carried in each row block's last code unit
     const uint16_t* x;          // the caller's x [batch][M][K] (16-bit) and anchor columns, for
     int64_t stride_x;           //   the in-kernel build of the fragment-ordered copy (bytes)
     const int32_t* anchor_idx;
@@ -360,6 +361,7 @@ struct FParams {
     int count, div32;           // div32: total_units * total_warps < 2^32, warp ranges in 32-bit arithmetic
     int64_t unit_begin[kMaxGroup];   // first unit of each problem (copies of d[i].unit_begin)
     int* status;                // device status word: bit 2 is raised when a weight table value overflows binary16
+    int stage;                  // ring kernel: bytes of one ring stage (a code unit, plus fused anchors if any)
     FDesc d[kMaxGroup];
     const uint16_t* xbuf;       // all x copies: per problem, per member [x in fragment order | x at the anchors]
     int M, y_dtype, x_bf16, format;
@@ -831,6 +833,10 @@ __global__ void __launch_bounds__(kThreadsS, NT <= 2 ? LQ_STREAM_MIN_BLOCKS : 1)
 //   anchor unit:              anchor weights [32 rows][48 x binary16] (zero past A)
 
 __host__ __device__ constexpr int ring_stage(int FMT) { return FMT == LQ_FMT_INT4_G32 ? 4608 : 3072; }
+// A problem with 1..16 anchors carries them in the last code unit of each row block (no
+// anchor units): [32 rows][16 x binary16] after the stage's code part, zero past A.
+constexpr int kFuseA = 16;
+constexpr int kFuseBytes = 32 * kFuseA * 2;
 #ifndef LQ_RING_DEPTH
 #define LQ_RING_DEPTH 2
 #endif
@@ -894,6 +900,7 @@ struct Feed {
     int left;                // units of the warp's range not yet issued
     int A;                   // anchors of the problem
     int fast;                // following row blocks of this member that are full (pointers only advance)
+    int fuse;                // the problem's anchors ride in each row block's last code unit
     int dc, dm, da;          // pointer steps from the end of a full row block to the next one
     int64_t u;               // launch-wide index of the next unit
 };
@@ -931,6 +938,7 @@ __device__ __forceinline__ Feed feed_at(const FParams& P, int64_t u, int left, i
     }
     f.su = D.su;
     f.A = D.A;
+    f.fuse = D.fuse;
     const int full = N / kRingRows;   // row blocks with all 32 rows inside N
     f.fast = q.rb < full ? full - 1 - q.rb : 0;
     f.dc = (kRingRows - 1) * (K / CB);
@@ -939,6 +947,16 @@ __device__ __forceinline__ Feed feed_at(const FParams& P, int64_t u, int left, i
     f.arow = D.A > 0 ? reinterpret_cast<const uint8_t*>(D.anchor_w) + q.l * D.stride_anchor_w + row(lane) * D.ld_anchor * 2
                      : D.codes;
     return f;
+}
+
+// Row `lane`'s anchors 0..15 (zero past A) to [dst + 32 lane, +32).
+__device__ __forceinline__ void feed_fused_anchors(const Feed& f, uint32_t dst, int lane) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int n = f.A - 8 * i;
+        const uint32_t bytes = n >= 8 ? 16u : (n > 0 ? 2u * n : 0u);
+        cp_async16(dst + lane * 32 + 16 * i, bytes ? f.arow + 16 * i : f.arow, bytes);
+    }
 }
 
 // Copy the next unit into the stage at `st` and step the cursor; one commit group per call
@@ -961,6 +979,7 @@ __device__ __forceinline__ void feed_issue(const FParams& P, Feed& f, uint32_t s
                 cp_async16(st + 4096 + lane * 16, f.meta, 16);
                 f.c0 += 128;
                 f.meta += 16;
+                if (f.fuse && f.s == f.su - 1) feed_fused_anchors(f, st + ring_stage(FMT), lane);
             } else {
                 const uint32_t dc = st + g * 64 + 16 * t;
                 cp_async16(dc, f.c0, 16);
@@ -972,6 +991,7 @@ __device__ __forceinline__ void feed_issue(const FParams& P, Feed& f, uint32_t s
                 cp_async16(dm + 16, f.meta + f.om, 16);
                 f.c0 += 64;
                 f.meta += 16;
+                if (f.fuse && f.s == f.su - 1) feed_fused_anchors(f, st + ring_stage(FMT), lane);
             }
         } else {
             const int a0 = a_unit * kAnchorCols;
@@ -1228,7 +1248,7 @@ __device__ __forceinline__ uint32_t int4_pair(uint32_t wx, int k, uint32_t s2) {
 template <int FMT, int MT, int NT, bool XS>
 __global__ void __launch_bounds__(32 * ring_warps(NT), 16 / ring_warps(NT)) gemv_ring_kernel(const __grid_constant__ FParams P) {
     constexpr int kW = ring_warps(NT);
-    constexpr int kStage = ring_stage(FMT);
+    const int kStage = P.stage;
     extern __shared__ __align__(128) unsigned char ring_smem[];
     const int M = MT > 0 ? MT : P.M;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
@@ -1282,6 +1302,7 @@ __global__ void __launch_bounds__(32 * ring_warps(NT), 16 / ring_warps(NT)) gemv
     };
     Pos q = locate(P, u_begin);
     UnitOrder ord = unit_order(q.s, q.steps, q.su, P.d[q.p].G);
+    int fuse_blk = P.d[q.p].fuse;
     const uint16_t* xb0 = xbase(q);
     int seg_units = 0;
     float peak = 0.f;   // largest |weight table value| seen (binary16 range check)
@@ -1385,6 +1406,17 @@ __global__ void __launch_bounds__(32 * ring_warps(NT), 16 / ring_warps(NT)) gemv
                 }
             }
         }
+        if (fuse_blk && !anchor_unit && q.s == q.su - 1) {   // the row block's anchors, in its last code unit
+            const uint16_t* xs = xb0 + xlane_a + P.d[q.p].xa_off;
+            uint2 xb[NT];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) xb[nt] = *reinterpret_cast<const uint2*>(xs + tok[nt]);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const unsigned char* r0p = st + ring_stage(FMT) + (16 * h + g) * 32 + 4 * t;
+                mma_xg<NT, MT>(acc[h], lds32(r0p), lds32(r0p + 8 * 32), lds32(r0p + 16), lds32(r0p + 8 * 32 + 16), xb);
+            }
+        }
         __syncwarp();   // every lane is done with this stage: refill it kRingDepth units ahead
         feed_issue<FMT>(P, f, ring + cst, lane);
         cst = cst + kStage == kRingDepth * kStage ? 0 : cst + kStage;
@@ -1398,6 +1430,7 @@ __global__ void __launch_bounds__(32 * ring_warps(NT), 16 / ring_warps(NT)) gemv
                 const int64_t l0 = q.l;
                 next_block(P, q);
                 ord = unit_order(0, q.steps, q.su, P.d[q.p].G);
+                fuse_blk = P.d[q.p].fuse;
                 if (q.p != p0 || q.l != l0) xb0 = xbase(q);
             }
         }
@@ -1616,6 +1649,7 @@ lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* probs, i
     const int cta_warps = use_ring ? ring_warps(M <= 8 ? 1 : 2) : kWarps;
 
     int64_t units = 0, jobs = 0, xhalves = 0, blocks = 0, rows = 0;
+    int any_fuse = 0;
     int max_k = 0;
     for (int i = 0; i < count; ++i) {
         const lq_problem& q = probs[i];
@@ -1645,7 +1679,9 @@ lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* probs, i
         d.stride_anchor_idx = q.stride_anchor_idx;
         const int a_pad = A > 0 ? round_up(A, kAnchorCols) : 0;
         d.steps = q.K / 256;
-        d.su = d.steps + a_pad / kAnchorCols;
+        d.fuse = use_ring && A > 0 && A <= kFuseA ? 1 : 0;
+        any_fuse |= d.fuse;
+        d.su = d.steps + (d.fuse ? 0 : a_pad / kAnchorCols);
         d.G = d.su > d.steps ? d.su / (d.su - d.steps) : d.su + 1;
         d.rblocks = (q.N + rows_blk - 1) / rows_blk;
         d.unit_begin = P.unit_begin[i] = units;
@@ -1679,7 +1715,8 @@ lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* probs, i
     if (units == 0) return LQ_OK;
     // arrival counts live in the counter area, which every kernel leaves at zero
     if ((size_t)blocks > ws.num_counters) return LQ_ERR_UNSUPPORTED;
-    const size_t ring_smem = (size_t)cta_warps * kRingDepth * ring_stage(fmt);
+    P.stage = ring_stage(fmt) + (any_fuse ? kFuseBytes : 0);
+    const size_t ring_smem = (size_t)cta_warps * kRingDepth * P.stage;
     // size the grid; the warp partition then fixes the x span of each CTA
     int per_sm = 0;
     if (use_ring) {

@@ -360,3 +360,26 @@ def test_gemv_full_projection_quantized_by_the_oracle(lqm, handle):
     assert set(outl.tolist()) <= set(p["anchor_idx"].tolist())
     xb = x_for(1, K, "f16", outl, seed=12, cfg=2)
     _gemv_check(lqm, handle, p, lqm.FMT_2BIT, xb, "f16")
+
+
+@pytest.mark.parametrize("A", [1, 7, 8, 15, 16, 17, 48, 49])
+@pytest.mark.parametrize("M", [1, 5])
+def test_gemv_anchor_counts_around_the_fused_limit(lqm, handle, A, M):
+    """Up to 16 anchors ride in the last code unit of each row block (no anchor units); 17
+    and more take anchor units of 48 columns.  Anchor counts on both sides of both limits,
+    2-bit and INT4, on a shape with a ragged row block."""
+    N, K = 150, 512
+    W = synth.weights(N, K, 0.02, seed=A, big_frac=0.002, big_mult=10.0)
+    prof = O.activation_profile(np.linspace(0.5, 3.0, K))
+    ai = O.select_anchors(W, prof, frac=(A + 0.5) / K)
+    assert len(ai) == A
+    xb = x_for(M, K, "f16", seed=A + M)
+    p2 = O.quantize_2bit(W, ai)
+    _gemv_check(lqm, handle, p2, lqm.FMT_2BIT, xb, "f16")
+    p4 = O.quantize_int4(W, O.int4_permutation(W, prof), ai)
+    w4 = lqm.QuantWeights.from_host(p4, lqm.FMT_INT4)
+    y = handle.gemv(w4, dev_x(xb, "f16"), y_dtype=torch.float32)
+    torch.cuda.synchronize()
+    yref, E = O.matmul_ref(O.dequant_int4(p4), xb, "f16")
+    assert_within(y.cpu().numpy(), yref, E, GEMV_TOL, f"int4 A={A} M={M}")
+    handle.sync()
