@@ -848,6 +848,8 @@ constexpr int kRingRows = 32;
 #endif
 __host__ __device__ constexpr int ring_warps(int NT) { return NT == 1 ? LQ_RING_WARPS1 : 16; }
 
+__device__ __forceinline__ void prefetch_l1(const void* p) { asm volatile("prefetch.global.L1 [%0];" ::"l"(p)); }
+
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
@@ -1097,13 +1099,14 @@ __device__ __forceinline__ void ring_flush(const FParams& P, const Pos& q, int u
 
 // The x span of a CTA (members a..b of the launch, a few at most) built in shared memory
 // in the ring layout, with one CTA barrier after each pass:
-// (0) every code column as binary16 (two 16-byte loads per 16 columns of a token), and x at
-//     the anchor columns (zero past A) read from the caller's x, both in the same pass;
-// (1) the anchor columns of (0) zeroed (the anchors replace those weights).
+// (0) every code column as binary16 (two 16-byte loads per 16 columns of a token);
+// (1) x at the anchor columns (zero past A) taken from (0), and those columns of (0) zeroed
+//     (the anchors replace those weights).
 // bf16 x first takes each token's max |x| (passes -2: clear, -1: max), for its scale.
 // INT4: x is taken through the permutation (position j holds x at column perm[j]) with
-// INT4's order inside each block of 16, and no column is zeroed (an anchor position stores
-// q = 0, which is exactly 0), so pass (1) is not needed.
+// INT4's order inside each block of 16, x at the anchor columns comes from the caller's x in
+// pass (0), and no column is zeroed (an anchor position stores q = 0, which is exactly 0), so
+// pass (1) is not needed.
 template <int FMT>
 __device__ __forceinline__ void build_span_x(const FParams& P, const Pos& a, const Pos& b, int64_t span0, uint16_t* xsm) {
     const int M = P.M, tid = threadIdx.x, nth = blockDim.x, S = ring_kstride(M);
@@ -1134,16 +1137,21 @@ __device__ __forceinline__ void build_span_x(const FParams& P, const Pos& a, con
                         atomicMax(&xmaxw[m], mx << 16);
                     }
                 } else if (pass == 0) {
-                    // x at the anchor columns (fragment order), straight from the caller's x
-                    const int a_pad = D.a_pad;
-                    uint16_t* xa = dst + D.xa_off;
-                    for (int it = tid; it < M * a_pad; it += nth) {
-                        const int m = it / a_pad, aa = it - m * a_pad;
-                        const int k = aa < A ? __ldg(aidx + aa) : -1;
-                        const int bi = aa >> 4, r = aa & 15, pos = 4 * ((r & 7) >> 1) + (r & 1) + 2 * (r >> 3);
-                        xa[(bi * M + m) * 16 + pos] =
-                            (unsigned)k < (unsigned)K ? to_half_scaled(x[(int64_t)m * K + k], P.x_bf16, P.x_bf16 ? x_scale(xmaxw[m]) : 1.f)
-                                                      : (uint16_t)0;
+                    if (FMT == LQ_FMT_INT4_G32) {
+                        // x at the anchor columns (fragment order), straight from the caller's x
+                        const int a_pad = D.a_pad;
+                        uint16_t* xa = dst + D.xa_off;
+                        for (int it = tid; it < M * a_pad; it += nth) {
+                            const int m = it / a_pad, aa = it - m * a_pad;
+                            const int k = aa < A ? __ldg(aidx + aa) : -1;
+                            const int bi = aa >> 4, r = aa & 15, pos = 4 * ((r & 7) >> 1) + (r & 1) + 2 * (r >> 3);
+                            xa[(bi * M + m) * 16 + pos] =
+                                (unsigned)k < (unsigned)K ? to_half_scaled(x[(int64_t)m * K + k], P.x_bf16, P.x_bf16 ? x_scale(xmaxw[m]) : 1.f)
+                                                          : (uint16_t)0;
+                        }
+                    } else {
+                        // the anchor columns are read in pass 1: bring them into L1 now
+                        for (int i = tid * 32; i < A; i += nth * 32) prefetch_l1(aidx + i);
                     }
                     if (FMT == LQ_FMT_INT4_G32) {
                         const int32_t* perm = reinterpret_cast<const int32_t*>(reinterpret_cast<const char*>(D.perm) + l * D.stride_perm);
@@ -1193,10 +1201,21 @@ __device__ __forceinline__ void build_span_x(const FParams& P, const Pos& a, con
                         }
                     }
                 } else if (FMT != LQ_FMT_INT4_G32) {
-                    for (int it = tid; it < M * A; it += nth) {
-                        const int m = it / A, aa = it - m * A;
-                        const int k = __ldg(aidx + aa);
-                        if ((unsigned)k < (unsigned)K) dst[ring_x_pos(k, m, M)] = 0;   // (a column outside [0, K) is ignored)
+                    // x at the anchor columns (fragment order, zero past A) taken from pass 0's copy,
+                    // then those columns of the copy zeroed (the item that reads a column zeroes it)
+                    const int a_pad = D.a_pad;
+                    uint16_t* xa = dst + D.xa_off;
+                    for (int it = tid; it < M * a_pad; it += nth) {
+                        const int m = it / a_pad, aa = it - m * a_pad;
+                        const int k = aa < A ? __ldg(aidx + aa) : -1;
+                        const int bi = aa >> 4, r = aa & 15, pos = 4 * ((r & 7) >> 1) + (r & 1) + 2 * (r >> 3);
+                        uint16_t v = 0;
+                        if ((unsigned)k < (unsigned)K) {   // (a column outside [0, K) is ignored)
+                            uint16_t& c = dst[ring_x_pos(k, m, M)];
+                            v = c;
+                            c = 0;
+                        }
+                        xa[(bi * M + m) * 16 + pos] = v;
                     }
                 }
             }
