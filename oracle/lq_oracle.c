@@ -175,6 +175,63 @@ ORACLE_API void oracle_dequant_int4(const uint8_t* codes, const uint16_t* scales
     }
 }
 
+/*
+ * NF4 with double quantization (QLoRA, the method the AirQuant README cites for NF4, item 2
+ * and the reference list): the fp32 block maxima are themselves stored as 8-bit floats.
+ * 8-bit float = E4M3: sign, 4 exponent bits (bias 7), 3 mantissa bits; exponent 0 holds
+ * the subnormals m/8 * 2^-6; 0x7F and 0xFF are NaN; no infinities; largest finite 448.
+ */
+ORACLE_API double oracle_e4m3_to_double(uint8_t c) {
+    int sign = (c >> 7) & 1, e = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0)
+        v = ldexp((double)m, -9);               /* m/8 * 2^-6 */
+    else
+        v = ldexp((double)(8 + m), e - 10);     /* (1 + m/8) * 2^(e-7) */
+    return sign ? -v : v;
+}
+
+/* Nearest E4M3 value to v (ties to the even mantissa), saturating at +-448; v finite. */
+ORACLE_API uint8_t oracle_double_to_e4m3(double v) {
+    uint8_t sign = v < 0 ? 0x80 : 0;
+    double a = fabs(v);
+    if (a >= 448.0) return sign | 0x7E;
+    /* candidates: every finite magnitude code 0x00..0x7E; pick the nearest, ties to even m */
+    int best = 0;
+    double bd = a;                               /* distance to code 0 (value 0) */
+    for (int c = 1; c <= 0x7E; ++c) {
+        double d = fabs(oracle_e4m3_to_double((uint8_t)c) - a);
+        if (d < bd || (d == bd && (c & 1) == 0 && (best & 1) == 1)) {
+            bd = d;
+            best = c;
+        }
+    }
+    return (uint8_t)(sign | best);
+}
+
+/*
+ * The double-quantized block maximum of first-level block i (row-major index into the
+ * [N][K/64] array): c'_i = fmaf(e4m3(acodes[i]), s2[i / 256], mean), one fp32 rounding.
+ *   second [1 + ceil(N*K/64 / 256)]: second[0] = mean, second[1 + j] = s2 of 256-block j.
+ * The weights: w = T[q] * c' (one fp32 rounding), as for plain NF4.
+ */
+ORACLE_API float oracle_nf4_dq_absmax(const uint8_t* acodes, const float* second, size_t i) {
+    return fmaf((float)oracle_e4m3_to_double(acodes[i]), second[1 + i / 256], second[0]);
+}
+
+ORACLE_API void oracle_dequant_nf4_dq(const uint8_t* codes, const uint8_t* acodes, const float* second,
+                                      const float* table, int N, int K, float* out) {
+    for (int n = 0; n < N; ++n) {
+        for (int k = 0; k < K; ++k) {
+            int byte = codes[(size_t)n * (K / 2) + k / 2];
+            int q = (k % 2 == 0) ? (byte & 15) : (byte >> 4);
+            float am = oracle_nf4_dq_absmax(acodes, second, (size_t)n * (K / 64) + k / 64);
+            out[(size_t)n * K + k] = table[q] * am;
+        }
+    }
+}
+
 /* fp32 values -> binary16 or bfloat16 bit patterns (kind 1 = f16, 2 = bf16), RNE. */
 ORACLE_API void oracle_round_f32(const float* in, size_t count, int kind, uint16_t* out) {
     for (size_t i = 0; i < count; ++i)

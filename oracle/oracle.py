@@ -30,6 +30,11 @@ Functions and what they follow
                                       the "Method Comparison Table"): 2 weights per byte,
                                       uniform grid, zero-point 0, a global static column
                                       permutation, top-1% FP16 outlier columns.
+* ``e4m3_decode`` / ``e4m3_encode``, ``double_quantize_absmax``, ``quantize_nf4_dq``,
+  ``dequant_nf4_dq``                 NF4 double quantization, from the QLoRA method the
+                                      AirQuant README cites for NF4: the fp32 block maxima
+                                      quantized again as 8-bit floats (E4M3) in blocks of
+                                      256, after subtracting their mean.
 * ``matmul_ref``                     y = x * W_eff^T in fp64, with the error scale
                                       E = |x| * |W_eff|^T.
 
@@ -137,6 +142,11 @@ def _lib():
         L.oracle_dequant_2bit.argtypes = [P, P, P, P, P, i, i, i, i, P]
         L.oracle_dequant_nf4.argtypes = [P, P, P, i, i, P]
         L.oracle_dequant_int4.argtypes = [P, P, P, P, P, i, i, i, i, P]
+        L.oracle_dequant_nf4_dq.argtypes = [P, P, P, P, i, i, P]
+        L.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+        L.oracle_e4m3_to_double.restype = ctypes.c_double
+        L.oracle_double_to_e4m3.argtypes = [ctypes.c_double]
+        L.oracle_double_to_e4m3.restype = ctypes.c_uint8
         L.oracle_round_f32.argtypes = [P, ctypes.c_size_t, i, P]
         L.oracle_matmul_f64.argtypes = [P, P, i, i, i, i, P, P]
         L.oracle_gemv_2bit_rows.argtypes = [P, P, P, P, P, i, i, P, i, i, i, i, i, i, P, P]
@@ -469,6 +479,68 @@ def dequant_nf4(p: dict) -> np.ndarray:
     T = nf4_table()
     out = np.empty((N, K), dtype=np.float32)
     L.oracle_dequant_nf4(_p(codes), _p(am), _p(T), N, K, _p(out))
+    return out
+
+
+# ---------------------------------------------------------------------------
+# NF4 with double quantization (QLoRA): the block maxima stored as 8-bit floats
+# ---------------------------------------------------------------------------
+
+NF4_DQ_BLOCK = 256          # first-level constants per second-level block
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """8-bit float (E4M3) codes -> float64 values (NaN for 0x7F / 0xFF)."""
+    L = _lib()
+    c = np.asarray(codes, dtype=np.uint8)
+    return np.array([L.oracle_e4m3_to_double(int(v)) for v in c.ravel()], dtype=np.float64).reshape(c.shape)
+
+
+def e4m3_encode(values) -> np.ndarray:
+    """float64 values -> nearest E4M3 codes (ties to the even mantissa), saturating at +-448."""
+    L = _lib()
+    v = np.asarray(values, dtype=np.float64)
+    return np.array([L.oracle_double_to_e4m3(float(x)) for x in v.ravel()], dtype=np.uint8).reshape(v.shape)
+
+
+def double_quantize_absmax(absmax: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
+    """The second quantization of the fp32 block maxima c [N][K/64].
+
+    mean = the mean of all c (fp64, rounded once to fp32); in row-major order, each run of 256
+    consecutive c (the last may be shorter) is block j with s2_j = max |c - mean| / 448 (fp64,
+    rounded once to fp32); acode_i = E4M3((c_i - mean) / s2_j) from the fp64 quotient (0 when
+    s2_j = 0).  Returns (acodes uint8 [N][K/64], second float32 [1 + blocks] = [mean, s2_0, ...]).
+    """
+    c = np.asarray(absmax, dtype=np.float32)
+    flat = c.ravel().astype(np.float64)
+    mean32 = np.float32(np.sum(flat) / flat.size)
+    nb = (flat.size + NF4_DQ_BLOCK - 1) // NF4_DQ_BLOCK
+    s2 = np.zeros(nb, dtype=np.float32)
+    codes = np.zeros(flat.size, dtype=np.uint8)
+    for j in range(nb):
+        seg = flat[j * NF4_DQ_BLOCK:(j + 1) * NF4_DQ_BLOCK] - np.float64(mean32)
+        s2[j] = np.float32(np.max(np.abs(seg)) / 448.0)
+        if s2[j] > 0:
+            codes[j * NF4_DQ_BLOCK:j * NF4_DQ_BLOCK + len(seg)] = e4m3_encode(seg / np.float64(s2[j]))
+    return codes.reshape(c.shape), np.concatenate([[mean32], s2]).astype(np.float32)
+
+
+def quantize_nf4_dq(W: np.ndarray) -> dict:
+    """NF4 codes from the fp32 block maxima (exactly as quantize_nf4), then the maxima
+    double-quantized.  Storage: codes [N][K/2], acodes uint8 [N][K/64], second fp32."""
+    p = quantize_nf4(W)
+    acodes, second = double_quantize_absmax(p["absmax"])
+    return dict(codes=p["codes"], q=p["q"], absmax=p["absmax"], acodes=acodes, second=second, N=p["N"], K=p["K"])
+
+
+def dequant_nf4_dq(p: dict) -> np.ndarray:
+    """fp32 W_eff [N][K] = T[q] * c', c' = fmaf(E4M3(acode), s2, mean) (one fp32 rounding each)."""
+    L = _lib()
+    N, K = int(p["N"]), int(p["K"])
+    out = np.empty((N, K), dtype=np.float32)
+    L.oracle_dequant_nf4_dq(_p(np.ascontiguousarray(p["codes"], dtype=np.uint8)),
+                            _p(np.ascontiguousarray(p["acodes"], dtype=np.uint8)),
+                            _p(np.ascontiguousarray(p["second"], dtype=np.float32)), _p(nf4_table()), N, K, _p(out))
     return out
 
 

@@ -611,3 +611,97 @@ def test_int4_outlier_count_and_bits_per_weight():
     A = int(np.floor(O.INT4_OUTLIER_FRAC * K))
     bits = 8 * (N * K / 2 + 2 * N * K / 32 + 2 * N * A + 4 * A + 4 * K) / (N * K)
     assert abs((4 + 16 / 32) - 4.5) < 1e-12 and abs(bits - 4.66) < 0.01
+
+
+# ---------------------------------------------------------------- NF4 double quantization (QLoRA)
+
+def _rn_f32(r: Fraction) -> np.float32:
+    """Exact rational -> nearest fp32 (ties to even), checked against both fp32 neighbours."""
+    f = np.float32(float(r))
+    cands = [np.nextafter(f, np.float32(-np.inf)), f, np.nextafter(f, np.float32(np.inf))]
+    best = min(cands, key=lambda c: (abs(Fraction(float(c)) - r), int(np.float32(c).view(np.uint32)) & 1))
+    return np.float32(best)
+
+
+def test_e4m3_decode_matches_the_library_and_the_format_definition():
+    torch = pytest.importorskip("torch")
+    lib = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).float().numpy().astype(np.float64)
+    ours = O.e4m3_decode(np.arange(256, dtype=np.uint8))
+    assert np.array_equal(np.isnan(ours), np.isnan(lib)) and np.isnan(ours).sum() == 2
+    ok = ~np.isnan(ours)
+    assert np.array_equal(ours[ok], lib[ok])
+    # the format's landmarks: largest finite, smallest normal, smallest subnormal, one, sign
+    assert ours[0x7E] == 448.0 and ours[0x08] == 2.0 ** -6 and ours[0x01] == 2.0 ** -9
+    assert ours[0x38] == 1.0 and ours[0xC0] == -2.0 and ours[0x80] == 0.0
+
+
+def test_e4m3_encode_is_the_nearest_code_with_ties_to_even():
+    torch = pytest.importorskip("torch")
+    g = np.random.default_rng(7)
+    vals = np.concatenate([g.standard_normal(3000) * 10.0 ** g.uniform(-4, 2.5, 3000),
+                           (O.e4m3_decode(np.arange(1, 0x7E)) + O.e4m3_decode(np.arange(2, 0x7F))) / 2,  # midpoints
+                           [0.0, 2.0 ** -10, 3 * 2.0 ** -10, 463.99, -463.99]])
+    vals = vals[np.abs(vals) < 464.0]
+    ours = O.e4m3_encode(vals)
+    lib = torch.from_numpy(vals).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    # (+-0: the library keeps the sign of a value that rounds to zero; compare magnitudes there)
+    zero = O.e4m3_decode(ours) == 0
+    assert np.array_equal(ours[~zero], lib[~zero]) and np.all(lib[zero] & 0x7F == 0)
+    # beyond the largest finite value the reading saturates (the library gives NaN there)
+    assert O.e4m3_encode(np.array([448.0, 464.0, 1e6, -1e6])).tolist() == [0x7E, 0x7E, 0x7E, 0xFE]
+
+
+def test_nf4_double_quant_blocks_mean_and_error_bound():
+    """Second-level blocks are 256 consecutive maxima in row-major order; each element is
+    reconstructed within half an E4M3 step of (c - mean) / s2, times s2, plus fp32 rounding."""
+    N, KB = 96, 8                                   # 768 first-level maxima -> 3 blocks
+    g = np.random.default_rng(3)
+    c = (0.01 + 0.05 * g.random((N, KB))).astype(np.float32)
+    c[32:64] *= 4                                   # rows 32..63 are block 1 (256 = 32 rows x 8)
+    acodes, second = O.double_quantize_absmax(c)
+    mean = np.float32(np.sum(c.astype(np.float64)) / c.size)
+    assert second[0] == mean and len(second) == 1 + 3
+    flat = c.ravel().astype(np.float64)
+    for j in range(3):
+        seg = flat[256 * j:256 * (j + 1)] - np.float64(mean)
+        assert second[1 + j] == np.float32(np.max(np.abs(seg)) / 448.0)
+    assert second[2] > 2 * max(second[1], second[3])
+    v = (flat - np.float64(mean)) / np.repeat(second[1:].astype(np.float64), 256)
+    dec = O.e4m3_decode(acodes.ravel())
+    half_step = np.where(np.abs(v) >= 2.0 ** -6, 2.0 ** (np.floor(np.log2(np.maximum(np.abs(v), 2.0 ** -6))) - 4), 2.0 ** -10)
+    assert np.all(np.abs(dec - v) <= half_step * (1 + 1e-12))
+    # the block maximum maps to +-448 exactly
+    for j in range(3):
+        i = 256 * j + int(np.argmax(np.abs(v[256 * j:256 * (j + 1)])))
+        assert abs(dec[i]) == 448.0
+
+
+def test_nf4_double_quant_dequant_is_two_exact_roundings():
+    """W = RN32(T[q] * RN32(E4M3(acode) * s2 + mean)) on every element of a small case,
+    the roundings done here on exact rationals."""
+    W = synth.weights(6, 128, 0.02, seed=11, big_frac=0.01, big_mult=10.0)
+    p = O.quantize_nf4_dq(W)
+    got = O.dequant_nf4_dq(p)
+    T = O.nf4_table()
+    q = O.unpack_nf4(p["codes"])
+    dec = O.e4m3_decode(p["acodes"])
+    mean, s2 = p["second"][0], p["second"][1:]
+    for n in range(6):
+        for k in range(128):
+            i = n * 2 + k // 64
+            cp = _rn_f32(Fraction(float(dec[n, k // 64])) * Fraction(float(s2[i // 256])) + Fraction(float(mean)))
+            w = _rn_f32(Fraction(float(T[q[n, k]])) * Fraction(float(cp)))
+            assert got[n, k] == w, (n, k)
+
+
+def test_nf4_double_quant_degenerate_blocks_and_bits_per_weight():
+    # every maximum equal to the mean: s2 = 0, codes 0, reconstruction = the mean exactly
+    c = np.full((4, 64), 0.037, dtype=np.float32)
+    acodes, second = O.double_quantize_absmax(c)
+    assert np.all(acodes == 0) and np.all(second[1:] == 0)
+    p = dict(codes=np.zeros((4, 2048), np.uint8) + 0x77, acodes=acodes, second=second, N=4, K=4096)
+    assert np.all(O.dequant_nf4_dq(p) == np.float32(O.nf4_table()[7]) * np.float32(0.037))
+    # storage: 4 bits + 8 bits per 64 + 32 bits per 64*256 (+ one mean) = 4.127 bits per weight
+    N, K = 4096, 4096
+    bits = 8 * (N * K / 2 + N * K / 64 + 4 * (N * K / 64 / 256 + 1)) / (N * K)
+    assert abs(bits - (4 + 8 / 64 + 32 / (64 * 256))) < 1e-5 and abs(bits - 4.127) < 1e-3
