@@ -379,8 +379,9 @@ STREAM_LAYERS = 32
 def device_layer(lq, torch, shapes, fmt, g, device, sigma=0.02):
     """One layer of random packed weights made on the device (throughput runs; the contents do not
     change the kernels' work): uniform random codes, scales and offsets of the synthetic
-    magnitudes, sorted random anchor columns (2-bit), absmax (NF4), or scales, a random
-    column permutation and 1 % anchor columns (INT4)."""
+    magnitudes, sorted random anchor columns (2-bit), absmax (NF4), scales, a random
+    column permutation and 1 % anchor columns (INT4), or 8-bit float maxima and their
+    second-level constants (NF4 with double quantization)."""
     from math import floor
     ws = []
     for name, N, K in shapes:
@@ -402,6 +403,13 @@ def device_layer(lq, torch, shapes, fmt, g, device, sigma=0.02):
             aidx = torch.randperm(K, generator=g, device=device)[:A].sort().values.to(torch.int32).contiguous()
             aw = (torch.randn((N, ld), generator=g, device=device) * sigma).half()
             ws.append(lq.QuantWeights(lq.FMT_INT4, N, K, codes, scales, perm, aidx, aw, A, ld))
+        elif fmt == lq.FMT_NF4_DQ:
+            codes = torch.randint(0, 256, (N, K // 2), generator=g, device=device, dtype=torch.uint8)
+            acodes = torch.randint(0, 0x7F, (N, K // 64), generator=g, device=device, dtype=torch.uint8)
+            nb = (N * (K // 64) + 255) // 256
+            second = torch.rand((1 + nb,), generator=g, device=device) * sigma / 448.0
+            second[0] = 3 * sigma
+            ws.append(lq.QuantWeights(lq.FMT_NF4_DQ, N, K, codes, acodes, second))
         else:
             codes = torch.randint(0, 256, (N, K // 2), generator=g, device=device, dtype=torch.uint8)
             absmax = torch.rand((N, K // 64), generator=g, device=device) * 2 * sigma + sigma
@@ -417,6 +425,8 @@ def layer_weight_bytes(ws, M: int) -> int:
             total += N * K // 4 + 2 * 2 * N * (K // 32) + 2 * N * w.A + 4 * w.A
         elif w.format == 3:   # INT4: codes, binary16 scales, anchors, the permutation
             total += N * K // 2 + 2 * N * (K // 32) + 2 * N * w.A + 4 * w.A + 4 * K
+        elif w.format == 4:   # NF4 with double quantization: codes, 8-bit maxima, second level
+            total += N * K // 2 + N * (K // 64) + 4 * (1 + (N * (K // 64) + 255) // 256)
         else:
             total += N * K // 2 + 4 * N * (K // 64)
         total += 2 * M * K + 4 * M * N
@@ -425,7 +435,8 @@ def layer_weight_bytes(ws, M: int) -> int:
 
 def decode_workloads(lq, torch, h, device: str, reps: int = 5):
     """Decode throughput of the other listed decode workloads: the 7B layer in NF4 (8 rotating
-    copies, bf16 x, M = 1, 4, 16), the same layer in the INT4 format (fp16 x) and an 80-layer 70B stack resident in HBM (2-bit + anchors,
+    copies, bf16 x, M = 1, 4, 16), the same layer in the INT4 format (fp16 x) and in NF4 with
+    double quantization (bf16 x), and an 80-layer 70B stack resident in HBM (2-bit + anchors,
     fp16 x, M = 1, 8, 32), one grouped call per layer, one pass captured in a CUDA graph."""
     g = torch.Generator(device=device)
     g.manual_seed(303)
@@ -434,6 +445,7 @@ def decode_workloads(lq, torch, h, device: str, reps: int = 5):
     for key, shapes, fmt, layers, Ms, xdt in (
             ("nf4_7b_layer", synth.LAYER_SHAPES["7b"], lq.FMT_NF4, ROTATE, (1, 4, 16), torch.bfloat16),
             ("int4_7b_layer", synth.LAYER_SHAPES["7b"], lq.FMT_INT4, ROTATE, (1, 4, 16), torch.float16),
+            ("nf4_dq_7b_layer", synth.LAYER_SHAPES["7b"], lq.FMT_NF4_DQ, ROTATE, (1, 4, 16), torch.bfloat16),
             ("llama70b_80_layer_stack", synth.LAYER_SHAPES["70b"], lq.FMT_2BIT, 80, (1, 8, 32), torch.float16)):
         stack = [device_layer(lq, torch, shapes, fmt, g, device, 0.015 if "70b" in key else 0.02) for _ in range(layers)]
         res = {}

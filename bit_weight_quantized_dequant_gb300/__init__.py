@@ -13,7 +13,7 @@ from __future__ import annotations
 
 from ._lq import (  # noqa: F401
     LQ_OK, LQ_ERR_INVALID_ARG, LQ_ERR_UNSUPPORTED, LQ_ERR_ALIGNMENT, LQ_ERR_WORKSPACE, LQ_ERR_CUDA,
-    LQ_ERR_TIMEOUT, LQ_ERR_RANGE, FMT_2BIT, FMT_NF4, FMT_INT4, F32, F16, BF16, LQError, QuantWeights, Handle, load_library,
+    LQ_ERR_TIMEOUT, LQ_ERR_RANGE, FMT_2BIT, FMT_NF4, FMT_INT4, FMT_NF4_DQ, F32, F16, BF16, LQError, QuantWeights, Handle, load_library,
     library_path, exported_symbols, EXPORTED, LayerStream, pack_layer,
 )
 from .build import build  # noqa: F401

@@ -11,7 +11,7 @@ from pathlib import Path
 
 LQ_OK, LQ_ERR_INVALID_ARG, LQ_ERR_UNSUPPORTED, LQ_ERR_ALIGNMENT, LQ_ERR_WORKSPACE, LQ_ERR_CUDA, LQ_ERR_TIMEOUT, \
     LQ_ERR_RANGE = range(8)
-FMT_2BIT, FMT_NF4, FMT_INT4 = 1, 2, 3
+FMT_2BIT, FMT_NF4, FMT_INT4, FMT_NF4_DQ = 1, 2, 3, 4
 F32, F16, BF16 = 0, 1, 2
 
 #: every entry point include/lq.h declares
@@ -134,8 +134,8 @@ class QuantWeights:
     N: int
     K: int
     codes: object                 # uint8 tensor
-    scales: object                # float16 [N][K/32] (2-bit, INT4) or float32 [N][K/64] (NF4)
-    offsets: object = None        # float16 [N][K/32] (2-bit) or the int32 permutation [K] (INT4)
+    scales: object                # float16 [N][K/32] (2-bit, INT4), float32 [N][K/64] (NF4) or uint8 [N][K/64] (NF4-DQ)
+    offsets: object = None        # float16 [N][K/32] (2-bit), int32 permutation [K] (INT4) or float32 second level (NF4-DQ)
     anchor_idx: object = None     # int32 [A]
     anchor_w: object = None       # float16 [N][ld_anchor]
     A: int = 0
@@ -156,6 +156,9 @@ class QuantWeights:
                                 t(packed["scales"], torch.float16), off,
                                 t(packed["anchor_idx"], torch.int32) if A > 0 else None,
                                 t(packed["anchor_w"], torch.float16) if A > 0 else None, A, int(packed["ld_anchor"]))
+        if fmt == FMT_NF4_DQ:
+            return QuantWeights(FMT_NF4_DQ, int(packed["N"]), int(packed["K"]), t(packed["codes"], torch.uint8),
+                                t(packed["acodes"], torch.uint8), t(packed["second"], torch.float32))
         return QuantWeights(FMT_NF4, int(packed["N"]), int(packed["K"]), t(packed["codes"], torch.uint8),
                             t(packed["absmax"], torch.float32))
 

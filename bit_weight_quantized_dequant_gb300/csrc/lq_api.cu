@@ -58,7 +58,9 @@ lq_status check_anchor_order(const int32_t* anchor_idx, int A, int K, cudaStream
 // Shape, pointer and alignment rules shared by every compute entry point.
 lq_status check_weights(int format, const uint8_t* codes, const void* scales, const void* offsets,
                         const int32_t* anchor_idx, const uint16_t* anchor_w, int A, int ld_anchor, int N, int K) {
-    if (format != LQ_FMT_2BIT_LM_G32 && format != LQ_FMT_NF4_B64 && format != LQ_FMT_INT4_G32) return LQ_ERR_INVALID_ARG;
+    if (format != LQ_FMT_2BIT_LM_G32 && format != LQ_FMT_NF4_B64 && format != LQ_FMT_INT4_G32 &&
+        format != LQ_FMT_NF4_DQ)
+        return LQ_ERR_INVALID_ARG;
     if (N < 1 || K < 1) return LQ_ERR_INVALID_ARG;
     if (!codes || !scales) return LQ_ERR_INVALID_ARG;
     if (!aligned16(codes) || !aligned16(scales)) return LQ_ERR_ALIGNMENT;
@@ -75,6 +77,10 @@ lq_status check_weights(int format, const uint8_t* codes, const void* scales, co
     } else {
         if (K % 64 != 0) return LQ_ERR_INVALID_ARG;
         if (A != 0 || anchor_idx || anchor_w) return LQ_ERR_INVALID_ARG;
+        if (format == LQ_FMT_NF4_DQ) {   // (offsets: the second-level constants [mean, s2_0, ...])
+            if (!offsets) return LQ_ERR_INVALID_ARG;
+            if (!aligned16(offsets)) return LQ_ERR_ALIGNMENT;
+        }
     }
     return LQ_OK;
 }
@@ -281,7 +287,8 @@ LQ_API lq_status lq_gemm(lq_handle h, int format, const uint8_t* codes, const vo
     lq_status s = check_problem(p);
     if (s != LQ_OK) return s;
     if (M < 1) return LQ_ERR_INVALID_ARG;
-    if (K % 64 != 0 || format == LQ_FMT_INT4_G32) return LQ_ERR_UNSUPPORTED;   // (INT4: decode only)
+    if (K % 64 != 0 || format == LQ_FMT_INT4_G32 || format == LQ_FMT_NF4_DQ)   // (INT4, NF4-DQ: decode only)
+        return LQ_ERR_UNSUPPORTED;
     DeviceGuard guard(h->device);
     if (!guard.ok) return LQ_ERR_CUDA;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -297,7 +304,7 @@ LQ_API lq_status lq_gemm_grouped(lq_handle h, const lq_problem* problems, int co
         const lq_status s = check_problem(p);
         if (s != LQ_OK) return s;
         if (p.M < 1 || p.batch != 1) return LQ_ERR_UNSUPPORTED;
-        if (p.K % 64 != 0 || p.format == LQ_FMT_INT4_G32) return LQ_ERR_UNSUPPORTED;
+        if (p.K % 64 != 0 || p.format == LQ_FMT_INT4_G32 || p.format == LQ_FMT_NF4_DQ) return LQ_ERR_UNSUPPORTED;
         if (p.format != problems[0].format || p.x_dtype != problems[0].x_dtype) return LQ_ERR_UNSUPPORTED;
     }
     DeviceGuard guard(h->device);

@@ -95,6 +95,21 @@ __device__ __forceinline__ uint16_t bf16_to_half_scaled(uint16_t raw, float scal
 // Largest value the weight lookup tables may hold: binary16 rounds |v| >= 65520 to infinity.
 constexpr float kHalfOverflow = 65520.0f;
 
+// An 8-bit float (E4M3: sign, 4 exponent bits with bias 7, 3 mantissa bits; exponent 0
+// holds the subnormals m/8 * 2^-6; 0x7F / 0xFF are NaN) as fp32, exactly.
+__device__ __forceinline__ float e4m3_to_float(uint32_t c) {
+    const uint32_t e = (c >> 3) & 15u, m = c & 7u;
+    float v = e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : (float)m * 0.001953125f;   // (2^-9)
+    if (e == 15u && m == 7u) v = __uint_as_float(0x7fc00000u);
+    return (c & 0x80u) ? -v : v;
+}
+
+// NF4 with double quantization: the block maximum of first-level block i (row-major in
+// [N][K/64]) is fmaf(E4M3(acodes[i]), second[1 + i / 256], second[0]), one fp32 rounding.
+__device__ __forceinline__ float nf4_dq_absmax(const uint8_t* acodes, const float* second, int64_t i) {
+    return __fmaf_rn(e4m3_to_float(__ldg(acodes + i)), __ldg(second + 1 + (i >> 8)), __ldg(second));
+}
+
 // Store one fp32 result in the requested output dtype.
 __device__ __forceinline__ void store_out(void* y, size_t idx, int dtype, float v) {
     if (dtype == LQ_F32) {

@@ -2,7 +2,8 @@
 //
 // 2-bit (otf-llm 4.0.1 README, sections 2-4): W_eff = fmaf(S_g, C[q], Z_g) in
 // fp32 with one rounding; anchor columns then take their binary16 value.
-// NF4 (AirQuant README, NF4 block-wise): W_eff = T[q] * absmax, one fp32 rounding.
+// NF4 (AirQuant README, NF4 block-wise): W_eff = T[q] * absmax, one fp32 rounding; with
+// double quantization (QLoRA) the maxima are decoded from their 8-bit float codes first.
 // INT4 (otf-llm 4.0.1 README, the v3.2 engine): W_eff[n][perm[j]] = S * q, an exact
 // fp32 product; anchor columns then take their binary16 value.
 // fp16/bf16 outputs are one round-to-nearest-even conversion of the fp32 value.
@@ -109,9 +110,12 @@ __global__ void __launch_bounds__(256) anchor_scatter_kernel(const int32_t* __re
     }
 }
 
+// NF4; with `second` set (double quantization), `absmax` holds the E4M3 codes of the
+// block maxima and each maximum is decoded as fmaf(E4M3(code), s2, mean).
 template <int OUT>
 __global__ void __launch_bounds__(256) dequant_nf4_kernel(const uint8_t* __restrict__ codes,
-                                                          const float* __restrict__ absmax, void* out, int N,
+                                                          const void* __restrict__ absmax,
+                                                          const float* __restrict__ second, void* out, int N,
                                                           int K) {
     __shared__ float table[16];
     if (threadIdx.x < 16) table[threadIdx.x] = kNF4[threadIdx.x];
@@ -122,7 +126,9 @@ __global__ void __launch_bounds__(256) dequant_nf4_kernel(const uint8_t* __restr
         const int64_t n = w / words_per_row;
         const int64_t wk = w - n * words_per_row;
         const uint32_t word = ldg32(codes + n * (K / 2) + wk * 4);
-        const float am = absmax[n * (K / 64) + wk / 8];
+        const int64_t blk = n * (K / 64) + wk / 8;
+        const float am = second ? nf4_dq_absmax(static_cast<const uint8_t*>(absmax), second, blk)
+                                : static_cast<const float*>(absmax)[blk];
         float v[8];
 #pragma unroll
         for (int c = 0; c < 8; ++c) v[c] = __fmul_rn(table[(word >> (4 * c)) & 15u], am);
@@ -175,7 +181,7 @@ lq_status dequant_typed(lq_handle h, int format, const uint8_t* codes, const voi
         }
     } else {
         dequant_nf4_kernel<OUT><<<grid_for((int64_t)N * (K / 8), h->num_sms), 256, 0, stream>>>(
-            codes, static_cast<const float*>(scales), w_out, N, K);
+            codes, scales, format == LQ_FMT_NF4_DQ ? static_cast<const float*>(offsets) : nullptr, w_out, N, K);
     }
     return cudaPeekAtLastError() == cudaSuccess ? LQ_OK : LQ_ERR_CUDA;
 }

@@ -189,16 +189,23 @@ __device__ __forceinline__ void compute2(const Frag2& f, float (&acc)[NT][4], co
     }
 }
 
-__device__ __forceinline__ FragNF4 load_nf4(const uint8_t* cg, const uint8_t* cg8, const float* ag, const float* ag8,
-                                            int valid_blocks, bool vg, bool vg8) {
+// ig, ig8: index of the first block maximum (row-major in [N][K/64]); with `second` set
+// (double quantization) `am` holds the maxima's E4M3 codes, else the fp32 maxima.
+__device__ __forceinline__ FragNF4 load_nf4(const uint8_t* cg, const uint8_t* cg8, const void* am, const float* second,
+                                            int64_t ig, int64_t ig8, int valid_blocks, bool vg, bool vg8) {
     FragNF4 f;
 #pragma unroll
     for (int nb = 0; nb < 4; ++nb) {
         const bool v = nb < valid_blocks;
         f.cg[nb] = (v && vg) ? ldg64(cg + 32 * nb) : make_uint2(0, 0);
         f.cg8[nb] = (v && vg8) ? ldg64(cg8 + 32 * nb) : make_uint2(0, 0);
-        f.ag[nb] = (v && vg) ? __ldg(ag + nb) : 0.f;
-        f.ag8[nb] = (v && vg8) ? __ldg(ag8 + nb) : 0.f;
+        if (second) {
+            f.ag[nb] = (v && vg) ? nf4_dq_absmax(static_cast<const uint8_t*>(am), second, ig + nb) : 0.f;
+            f.ag8[nb] = (v && vg8) ? nf4_dq_absmax(static_cast<const uint8_t*>(am), second, ig8 + nb) : 0.f;
+        } else {
+            f.ag[nb] = (v && vg) ? __ldg(static_cast<const float*>(am) + ig + nb) : 0.f;
+            f.ag8[nb] = (v && vg8) ? __ldg(static_cast<const float*>(am) + ig8 + nb) : 0.f;
+        }
     }
     return f;
 }
@@ -279,7 +286,10 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const __grid_constan
     FragNF4 f4;
     const uint8_t *cg = nullptr, *cg8 = nullptr;
     const uint16_t *sg = nullptr, *zg = nullptr, *sg8 = nullptr, *zg8 = nullptr;
-    const float *ag = nullptr, *ag8 = nullptr;
+    int64_t ig = 0, ig8 = 0;   // NF4: first block-maximum index of rows rg, rg + 8
+    const float* second = P.format == LQ_FMT_NF4_DQ
+                              ? reinterpret_cast<const float*>(reinterpret_cast<const char*>(D.offsets) + l * D.stride_offsets)
+                              : nullptr;
     const int nsteps = klen_pad / kStep;
     if (has_codes) {
         if (FMT == LQ_FMT_2BIT_LM_G32) {
@@ -294,13 +304,12 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const __grid_constan
             zg8 = of + rg8c * (K / 32) + k0 / 32 + 2 * t;
             f2 = load2(cg, cg8, sg, zg, sg8, zg8, klen - 64 * t, vg, vg8, wide);
         } else {
-            const float* am = reinterpret_cast<const float*>(scales);
             const int64_t rgc = vg ? rg : 0, rg8c = vg8 ? rg8 : 0;
             cg = codes + rgc * (K / 2) + k0 / 2 + 8 * t;
             cg8 = codes + rg8c * (K / 2) + k0 / 2 + 8 * t;
-            ag = am + rgc * (K / 64) + k0 / 64;
-            ag8 = am + rg8c * (K / 64) + k0 / 64;
-            f4 = load_nf4(cg, cg8, ag, ag8, klen / 64, vg, vg8);
+            ig = rgc * (K / 64) + k0 / 64;
+            ig8 = rg8c * (K / 64) + k0 / 64;
+            f4 = load_nf4(cg, cg8, scales, second, ig, ig8, klen / 64, vg, vg8);
         }
     }
 
@@ -373,8 +382,8 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const __grid_constan
             for (int s = 0; s < nsteps; ++s) {
                 FragNF4 nxt;
                 if (s + 1 < nsteps)
-                    nxt = load_nf4(cg + 128 * (s + 1), cg8 + 128 * (s + 1), ag + 4 * (s + 1), ag8 + 4 * (s + 1),
-                                   klen / 64 - 4 * (s + 1), vg, vg8);
+                    nxt = load_nf4(cg + 128 * (s + 1), cg8 + 128 * (s + 1), scales, second, ig + 4 * (s + 1),
+                                   ig8 + 4 * (s + 1), klen / 64 - 4 * (s + 1), vg, vg8);
                 compute_nf4<NT>(f4, acc, TL, TH, xs, s, klen_pad, M, g, t);
                 f4 = nxt;
             }

@@ -739,8 +739,15 @@ __global__ void __launch_bounds__(kThreadsS, NT <= 2 ? LQ_STREAM_MIN_BLOCKS : 1)
             const uint8_t* cb = D.codes + q.l * D.stride_codes + 8 * t;
             const uint8_t* c0p = cb + r0 * (K / 2);
             const uint8_t* c1p = cb + r1 * (K / 2);
-            const float* am = reinterpret_cast<const float*>(static_cast<const char*>(D.scales) + q.l * D.stride_scales);
-            const float *a0p = am + r0 * (K / 64), *a1p = am + r1 * (K / 64);
+            // the rows' block maxima: fp32, or (double quantization) E4M3 codes, four blocks (one
+            // 256-column step) per 32-bit word sharing one second-level scale (256 is a multiple of 4)
+            const float* second = FMT == LQ_FMT_NF4_DQ
+                                      ? reinterpret_cast<const float*>(reinterpret_cast<const char*>(D.offsets) + q.l * D.stride_offsets)
+                                      : nullptr;
+            const int mb = FMT == LQ_FMT_NF4_DQ ? 1 : 4;   // bytes per block maximum
+            const char* am = static_cast<const char*>(D.scales) + q.l * D.stride_scales;
+            const char* a0p = am + r0 * (K / 64) * mb;
+            const char* a1p = am + r1 * (K / 64) * mb;
             uint32_t TL[4], TH[4];
             nf4_tables(TL, TH);
             auto load = [&](StepNF4& f, int s) {
@@ -748,8 +755,23 @@ __global__ void __launch_bounds__(kThreadsS, NT <= 2 ? LQ_STREAM_MIN_BLOCKS : 1)
                 for (int nb = 0; nb < 4; ++nb) {
                     f.c0[nb] = ldg64(c0p + 128 * s + 32 * nb);
                     f.c1[nb] = ldg64(c1p + 128 * s + 32 * nb);
-                    f.a0[nb] = __ldg(a0p + 4 * s + nb);
-                    f.a1[nb] = __ldg(a1p + 4 * s + nb);
+                }
+                if (FMT == LQ_FMT_NF4_DQ) {
+                    const uint32_t w0 = ldg32(a0p + 4 * s), w1 = ldg32(a1p + 4 * s);
+                    const float s0 = __ldg(second + 1 + ((r0 * (K / 64) + 4 * s) >> 8));
+                    const float s1 = __ldg(second + 1 + ((r1 * (K / 64) + 4 * s) >> 8));
+                    const float mean = __ldg(second);
+#pragma unroll
+                    for (int nb = 0; nb < 4; ++nb) {
+                        f.a0[nb] = __fmaf_rn(e4m3_to_float((w0 >> (8 * nb)) & 0xFFu), s0, mean);
+                        f.a1[nb] = __fmaf_rn(e4m3_to_float((w1 >> (8 * nb)) & 0xFFu), s1, mean);
+                    }
+                } else {
+#pragma unroll
+                    for (int nb = 0; nb < 4; ++nb) {
+                        f.a0[nb] = __ldg(reinterpret_cast<const float*>(a0p) + 4 * s + nb);
+                        f.a1[nb] = __ldg(reinterpret_cast<const float*>(a1p) + 4 * s + nb);
+                    }
                 }
             };
             auto compute = [&](const StepNF4& f, int s) {
@@ -1593,6 +1615,14 @@ lq_status dispatch_ring(int mode, bool xs, const FParams& P, int64_t grid, size_
 
 lq_status dispatch(int fmt, int mode, bool staged, const FParams& P, int64_t grid, size_t smem, int* per_sm,
                    cudaStream_t stream) {
+    if (fmt == LQ_FMT_NF4_DQ) {   // (fewer instantiations: one token at compile time, the rest by n-tiles)
+        if (P.M == 1) return dispatch_mt<LQ_FMT_NF4_DQ, 1, 1>(mode, staged, P, grid, smem, per_sm, stream);
+        if (P.M <= 8) return dispatch_mt<LQ_FMT_NF4_DQ, 0, 1>(mode, staged, P, grid, smem, per_sm, stream);
+        if (P.M <= 16) return dispatch_mt<LQ_FMT_NF4_DQ, 0, 2>(mode, staged, P, grid, smem, per_sm, stream);
+        if (P.M <= 24) return dispatch_mt<LQ_FMT_NF4_DQ, 0, 3>(mode, staged, P, grid, smem, per_sm, stream);
+        if (P.M <= 32) return dispatch_mt<LQ_FMT_NF4_DQ, 0, 4>(mode, staged, P, grid, smem, per_sm, stream);
+        return LQ_ERR_UNSUPPORTED;
+    }
     return fmt == LQ_FMT_2BIT_LM_G32 ? dispatch_fmt<LQ_FMT_2BIT_LM_G32>(mode, staged, P, grid, smem, per_sm, stream)
                                      : dispatch_fmt<LQ_FMT_NF4_B64>(mode, staged, P, grid, smem, per_sm, stream);
 }
@@ -1672,12 +1702,12 @@ lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* probs, i
     int max_k = 0;
     for (int i = 0; i < count; ++i) {
         const lq_problem& q = probs[i];
-        const int A = fmt != LQ_FMT_NF4_B64 ? q.A : 0;
+        const int A = fmt == LQ_FMT_2BIT_LM_G32 || fmt == LQ_FMT_INT4_G32 ? q.A : 0;
         FDesc& d = P.d[i];
         PrepDesc& e = Q.d[i];
         d.codes = q.codes;
         d.scales = q.scales;
-        d.offsets = fmt == LQ_FMT_2BIT_LM_G32 ? static_cast<const uint16_t*>(q.offsets) : nullptr;
+        d.offsets = fmt == LQ_FMT_2BIT_LM_G32 || fmt == LQ_FMT_NF4_DQ ? static_cast<const uint16_t*>(q.offsets) : nullptr;
         d.perm = e.perm = fmt == LQ_FMT_INT4_G32 ? static_cast<const int32_t*>(q.offsets) : nullptr;
         d.stride_perm = e.stride_perm = q.stride_offsets;
         d.anchor_w = q.anchor_w;

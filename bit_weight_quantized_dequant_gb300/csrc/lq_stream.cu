@@ -46,7 +46,8 @@ lq_status check_layer(const lq_problem* problems, int count, size_t layer_bytes)
     for (int i = 0; i < count; ++i) {
         const lq_problem& p = problems[i];
         if (p.batch != 1 || p.N < 1 || p.K < 1) return LQ_ERR_INVALID_ARG;
-        if (p.format == LQ_FMT_INT4_G32) return LQ_ERR_UNSUPPORTED;   // (the stream object carries 2-bit and NF4 layers)
+        if (p.format == LQ_FMT_INT4_G32 || p.format == LQ_FMT_NF4_DQ)
+            return LQ_ERR_UNSUPPORTED;   // (the stream object carries 2-bit and NF4 layers)
         if (p.format != LQ_FMT_2BIT_LM_G32 && p.format != LQ_FMT_NF4_B64) return LQ_ERR_INVALID_ARG;
         if (p.K % (p.format == LQ_FMT_2BIT_LM_G32 ? 32 : 64) != 0 || p.A < 0 || p.ld_anchor < 0) return LQ_ERR_INVALID_ARG;
         uint64_t ext[5];

@@ -42,6 +42,17 @@
  *   the high nibble), scales = absmax float32 [N][K/64]; offsets, anchor_idx and
  *   anchor_w are NULL and A = 0.
  *
+ * LQ_FMT_NF4_DQ — NF4 with double quantization (QLoRA, the method the AirQuant README
+ *   cites for NF4): the block maxima themselves are stored as 8-bit floats (E4M3: bias
+ *   7, 3 mantissa bits, no infinities, largest 448).  The maxima of a matrix, in
+ *   row-major order of [N][K/64], form blocks of 256; with `second` = [mean, s2_0,
+ *   s2_1, ...] (fp32):
+ *       c'_i = fmaf(E4M3(acode_i), s2_(i/256), mean)   (fp32, one rounding)
+ *       W_eff[n][k] = T[q] * c'_(n*(K/64) + k/64)      (fp32, one rounding)
+ *   Storage: codes as for NF4; scales = acode uint8 [N][K/64]; offsets = second
+ *   float32 [1 + ceil(N*K/64 / 256)]; anchor_idx and anchor_w NULL and A = 0.
+ *   Decode (lq_gemv) needs K % 256 == 0; lq_gemm does not take this format.
+ *
  * Conventions shared by every entry point
  * ---------------------------------------
  * - Ownership: the caller owns every buffer passed in.  The library owns the
@@ -111,7 +122,8 @@ typedef enum lq_status {
 typedef enum lq_format {
     LQ_FMT_2BIT_LM_G32 = 1,
     LQ_FMT_NF4_B64 = 2,
-    LQ_FMT_INT4_G32 = 3
+    LQ_FMT_INT4_G32 = 3,
+    LQ_FMT_NF4_DQ = 4
 } lq_format;
 
 typedef enum lq_dtype {

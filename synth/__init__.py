@@ -164,6 +164,19 @@ def random_packed_int4(N: int, K: int, A: int, sigma: float = 0.02, seed: int = 
                 A=A, ld_anchor=ld, N=N, K=K)
 
 
+def random_packed_nf4_dq(N: int, K: int, sigma: float = 0.02, seed: int = 0, cfg: int = 0,
+                         matrix_id: int = 0) -> dict:
+    """Random bytes in the double-quantized NF4 layout: codes [N][K/2]; acodes uint8 [N][K/64]
+    (8-bit float codes of either sign, the two NaN codes excluded); second = [mean, s2_0, ...]
+    float32 with mean ~ 3 sigma and s2 ~ sigma * U(0.5, 1) / 448."""
+    g = rng(seed, cfg, 70_000 + matrix_id)
+    codes = g.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    acodes = (g.integers(0, 0x7F, size=(N, K // 64)) | (g.integers(0, 2, size=(N, K // 64)) << 7)).astype(np.uint8)
+    nb = (N * (K // 64) + 255) // 256
+    second = np.concatenate([[3 * sigma], sigma * g.uniform(0.5, 1.0, nb) / 448.0]).astype(np.float32)
+    return dict(codes=codes, acodes=acodes, second=second, N=N, K=K)
+
+
 def random_packed_2bit_sets(L: int, N: int, K: int, A: int, sigma: float = 0.02, seed: int = 0, cfg: int = 0) -> dict:
     """L independent weight sets of one shape in the 2-bit storage layout, stacked on a
     leading axis (codes [L][N][K/4], scales/offsets [L][N][K/32], anchor_idx [L][A],
