@@ -257,7 +257,9 @@ def single_linear_batched(lq, torch, h, device: str, steps: int, warmup: int):
     single_us = e0.elapsed_time(e1) / calls * 1e3
     return {"workload": f"512x256 single linear, 2-bit G=32 + 8 fp16 anchors, M=1, {L} distinct weight sets in one launch",
             "value": round(L * per_set / (ms * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_launch": round(ms, 4),
-            "bytes_per_launch": L * per_set, "single_call_us": round(single_us, 2)}
+            "bytes_per_launch": L * per_set, "single_call_us": round(single_us, 2),
+            # DRAM bytes of the same kernel over 4096 sets (ncu), scaled to this launch's sets
+            "traffic": (lambda t: None if t is None else int(t * L // 4096))(_traffic("gemv_ring_512x256_4096_sets_bytes_per_launch"))}
 
 
 GEMM_M = 2048
@@ -724,7 +726,7 @@ def run_lq(args):
     if streamed:
         streamed["resident_tok_s"] = round(1e3 / (ms_per_step * STACK_LAYERS), 1)
 
-    traffic = _traffic("gemv_7b_layer_m1_bytes_per_launch")
+    traffic = _traffic("gemv_ring_7b_layer_m1_bytes_per_launch")
 
     if rank == 0:
         cores = host_cores()
