@@ -641,8 +641,52 @@ static lq_status upload_schedule(lq_handle h, const GemmParams& P, int grid, cud
     return LQ_OK;
 }
 
+lq_status launch_gemm_grouped_limited(lq_handle h, const lq_problem* probs, int count, cudaStream_t stream,
+                                      size_t ws_bytes);
+
+// NF4 with double quantization, prefill: the block maxima decoded once into fp32 (one
+// fmaf each, as the decode kernels do in registers), then the NF4 GEMM reads them.
+__global__ void __launch_bounds__(256) nf4_dq_decode_kernel(const uint8_t* __restrict__ acodes,
+                                                            const float* __restrict__ second, float* __restrict__ out,
+                                                            int64_t n) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        out[i] = nf4_dq_absmax(acodes, second, i);
+}
+
 lq_status launch_gemm_grouped(lq_handle h, const lq_problem* probs, int count, cudaStream_t stream) {
     if (count < 1 || count > kMaxGemmGroup) return LQ_ERR_UNSUPPORTED;
+    if (probs[0].format == LQ_FMT_NF4_DQ) {
+        // decode each problem's maxima into the workspace's tail, then run the NF4 GEMM on copies of
+        // the problems that point there
+        lq_problem q[kMaxGemmGroup];
+        size_t need = 0;
+        for (int i = 0; i < count; ++i) {
+            if (probs[i].format != LQ_FMT_NF4_DQ) return LQ_ERR_UNSUPPORTED;
+            need += ((size_t)probs[i].N * (probs[i].K / 64) * 4 + 255) & ~size_t(255);
+        }
+        const size_t cap = h->partial_floats * sizeof(float);
+        if (need + (size_t(1) << 20) > cap) return LQ_ERR_WORKSPACE;
+        char* tail = reinterpret_cast<char*>(h->partials) + ((cap - need) & ~size_t(255));
+        for (int i = 0; i < count; ++i) {
+            q[i] = probs[i];
+            const int64_t n = (int64_t)probs[i].N * (probs[i].K / 64);
+            float* dec = reinterpret_cast<float*>(tail);
+            tail += ((size_t)n * 4 + 255) & ~size_t(255);
+            const int g = (int)std::min<int64_t>((n + 255) / 256, (int64_t)h->num_sms * 16);
+            nf4_dq_decode_kernel<<<std::max(g, 1), 256, 0, stream>>>(static_cast<const uint8_t*>(probs[i].scales),
+                                                                      static_cast<const float*>(probs[i].offsets), dec, n);
+            if (cudaPeekAtLastError() != cudaSuccess) return LQ_ERR_CUDA;
+            q[i].format = LQ_FMT_NF4_B64;
+            q[i].scales = dec;
+            q[i].offsets = nullptr;
+        }
+        return launch_gemm_grouped_limited(h, q, count, stream, (cap - need) & ~size_t(255));
+    }
+    return launch_gemm_grouped_limited(h, probs, count, stream, h->partial_floats * sizeof(float));
+}
+
+lq_status launch_gemm_grouped_limited(lq_handle h, const lq_problem* probs, int count, cudaStream_t stream,
+                                      size_t ws_bytes) {
     GemmParams P;
     GemmPrepParams Q;
     memset(&P, 0, sizeof(P));
@@ -723,7 +767,7 @@ lq_status launch_gemm_grouped(lq_handle h, const lq_problem* probs, int count, c
             max_prep = (int)std::max<int64_t>(max_prep, std::max<int64_t>((int64_t)p.M * a_pad, A));
         }
     }
-    if (used + 256 > h->partial_floats * sizeof(float)) return LQ_ERR_WORKSPACE;
+    if (used + 256 > ws_bytes) return LQ_ERR_WORKSPACE;
     P.total_tiles = tiles;
     if (tiles == 0) return LQ_OK;
     if (prep_count > 0) {

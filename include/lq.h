@@ -51,7 +51,8 @@
  *       W_eff[n][k] = T[q] * c'_(n*(K/64) + k/64)      (fp32, one rounding)
  *   Storage: codes as for NF4; scales = acode uint8 [N][K/64]; offsets = second
  *   float32 [1 + ceil(N*K/64 / 256)]; anchor_idx and anchor_w NULL and A = 0.
- *   Decode (lq_gemv) needs K % 256 == 0; lq_gemm does not take this format.
+ *   Decode (lq_gemv) needs K % 256 == 0.  lq_gemm decodes the maxima into fp32 in the
+ *   handle's workspace (one small kernel per problem) and runs the NF4 GEMM on them.
  *
  * Conventions shared by every entry point
  * ---------------------------------------

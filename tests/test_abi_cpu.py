@@ -87,12 +87,12 @@ def test_validation_rejects_before_launch(lib):
     # gemm: K % 64
     assert L.lq_gemm(h, 1, A16, A16, A16, None, None, 0, 0, A16, 2, A16, 0, 256, 4, 96, None) == _lq.LQ_ERR_UNSUPPORTED
     # NF4 with double quantization (format 4): needs the second-level constants, 16-byte
-    # aligned, and no anchors; decode only
+    # aligned, and no anchors
     assert L.lq_dequant(h, 4, A16, A16, None, None, None, 0, 0, A16, 0, 4, 64, None) == _lq.LQ_ERR_INVALID_ARG
     assert L.lq_dequant(h, 4, A16, A16, A16 + 4, None, None, 0, 0, A16, 0, 4, 64, None) == _lq.LQ_ERR_ALIGNMENT
     assert L.lq_dequant(h, 4, A16, A16, A16, A16, A16, 1, 8, A16, 0, 4, 64, None) == _lq.LQ_ERR_INVALID_ARG
     assert L.lq_dequant(h, 4, A16, A16, A16, None, None, 0, 0, A16, 0, 4, 96, None) == _lq.LQ_ERR_INVALID_ARG
-    assert L.lq_gemm(h, 4, A16, A16, A16, None, None, 0, 0, A16, 2, A16, 0, 256, 4, 64, None) == _lq.LQ_ERR_UNSUPPORTED
+    assert L.lq_gemm(h, 4, A16, A16, A16, None, None, 0, 0, A16, 2, A16, 0, 256, 4, 96, None) == _lq.LQ_ERR_INVALID_ARG
 
 
 def test_grouped_validation(lib):

@@ -5,7 +5,9 @@ maxima, 8-bit floats in blocks of 256) against the CPU oracle, through the C ABI
 * lq_gemv: |y - y_ref| <= 1e-3 * sum_k |W_eff||x| per output on the streaming kernel
   (K % 256 == 0) and the split-K kernel, 1..32 tokens, binary16 and bf16 x, batched, and a
   whole 7B decoder layer at full size on sampled rows;
-* lq_gemm and the layer stream answer LQ_ERR_UNSUPPORTED for this format.
+* lq_gemm (the maxima decoded into the workspace, then the NF4 tcgen05 GEMM) within
+  4e-3 * E (bf16 operands) or 1e-3 * E (fp16), single and grouped;
+* the layer stream does not take this format.
 """
 import numpy as np
 import pytest
@@ -149,10 +151,58 @@ def test_gemv_nf4_dq_7b_layer_sampled(lqm, handle, M):
             assert_within(yc[:, n:n + 1], yref, E, GEMV_TOL, f"7b[{i}] row {n}")
 
 
-def test_nf4_dq_unsupported_paths(lqm, handle):
-    p = packed(128, 256, seed=1)
+@pytest.mark.parametrize("xdt", ["bf16", "f16"])
+@pytest.mark.parametrize("shape", [(256, 128, 256), (300, 200, 1088), (17, 64, 128)])
+def test_gemm_nf4_dq(lqm, handle, xdt, shape):
+    """Prefill: the maxima decoded into the workspace, then the tcgen05 NF4 GEMM (4e-3 * E
+    with bf16 operands, 1e-3 * E with fp16)."""
+    M, N, K = shape
+    p = packed(N, K, seed=M + N + K)
     w = lqm.QuantWeights.from_host(p, lqm.FMT_NF4_DQ)
-    with pytest.raises(lqm.LQError) as e:
-        handle.gemm(w, dev_x(x_for(64, 256, "bf16"), "bf16"))
-    assert e.value.status == lqm.LQ_ERR_UNSUPPORTED
+    xb = x_for(M, K, xdt, seed=M)
+    y = handle.gemm(w, dev_x(xb, xdt), y_dtype=torch.float32)
+    torch.cuda.synchronize()
+    yref, E = O.matmul_ref(O.dequant_nf4_dq(p), xb, xdt)
+    assert_within(y.cpu().numpy(), yref, E, 4e-3 if xdt == "bf16" else 1e-3, f"gemm nf4-dq {shape} {xdt}")
+    handle.sync()
+
+
+def test_gemm_nf4_dq_grouped(lqm, handle):
+    shapes = [(256, 192, 512), (256, 64, 1024)]
+    probs, keep = [], []
+    for i, (M, N, K) in enumerate(shapes):
+        p = packed(N, K, seed=70 + i)
+        w = lqm.QuantWeights.from_host(p, lqm.FMT_NF4_DQ)
+        xb = x_for(M, K, "bf16", seed=70 + i)
+        x = dev_x(xb, "bf16")
+        y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        probs.append(handle.problem(w, x, y))
+        keep.append((p, xb, y, w, x))
+    handle.gemm_grouped(probs)
+    torch.cuda.synchronize()
+    for i, (p, xb, y, _, _) in enumerate(keep):
+        yref, E = O.matmul_ref(O.dequant_nf4_dq(p), xb, "bf16")
+        assert_within(y.cpu().numpy(), yref, E, 4e-3, f"grouped nf4-dq {i}")
+    handle.sync()
+
+
+def test_nf4_dq_layer_stream_refused(lqm, handle):
+    """The layer stream carries 2-bit and NF4 layers only: a double-quantized layer is refused
+    before any copy."""
+    from bit_weight_quantized_dequant_gb300._lq import lq_problem
+    N, K, M = 64, 256, 1
+    p = lq_problem()
+    p.format, p.M, p.N, p.K = lqm.FMT_NF4_DQ, M, N, K
+    p.codes, p.scales, p.offsets = 0, 1024, 2048            # byte offsets into the layer blob
+    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    x = torch.zeros((M, K), dtype=torch.bfloat16, device="cuda")
+    p.x, p.x_dtype, p.y, p.y_dtype, p.batch = x.data_ptr(), lqm.BF16, y.data_ptr(), lqm.F32, 1
+    host = torch.zeros(4096, dtype=torch.uint8).pin_memory()
+    s = lqm.LayerStream(handle, 1 << 20)
+    try:
+        with pytest.raises(lqm.LQError) as e:
+            s.run(host, 4096, 4096, 1, [p])
+        assert e.value.status == lqm.LQ_ERR_UNSUPPORTED
+    finally:
+        s.close()
     handle.sync()
