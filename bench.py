@@ -274,6 +274,12 @@ def gemm_layer(lq, torch, h, fmt: str, device: str, steps: int, warmup: int):
         if fmt == "2bit":
             pk = synth.random_packed_2bit(N, K, int(floor(0.035 * K)), sigma=0.02, seed=500, cfg=5, matrix_id=i)
             w = lq.QuantWeights.from_host(pk, lq.FMT_2BIT, device=device)
+        elif fmt == "int4":
+            pk = synth.random_packed_int4(N, K, int(floor(0.01 * K)), sigma=0.02, seed=500, cfg=5, matrix_id=i)
+            w = lq.QuantWeights.from_host(pk, lq.FMT_INT4, device=device)
+        elif fmt == "nf4_dq":
+            pk = synth.random_packed_nf4_dq(N, K, sigma=0.02, seed=500, cfg=5, matrix_id=i)
+            w = lq.QuantWeights.from_host(pk, lq.FMT_NF4_DQ, device=device)
         else:
             pk = synth.random_packed_nf4(N, K, sigma=0.02, seed=500, cfg=5, matrix_id=i)
             w = lq.QuantWeights.from_host(pk, lq.FMT_NF4, device=device)
@@ -314,7 +320,9 @@ def gemm_layer(lq, torch, h, fmt: str, device: str, steps: int, warmup: int):
     torch.cuda.synchronize()
     one_ms = a0.elapsed_time(a1) / reps
     one_flops = 2 * GEMM_M * w.N * w.K
-    launches = 3 if fmt == "2bit" else 1   # 2-bit: bitmap memset + anchor gather + GEMM
+    # 2-bit: bitmap memset + anchor gather + GEMM; INT4: + one x permutation per projection;
+    # NF4-DQ: one block-maximum decode per projection + GEMM
+    launches = {"2bit": 3, "nf4": 1, "int4": 3 + len(mats), "nf4_dq": 1 + len(mats)}[fmt]
     return {"fmt": fmt, "value": round(flops / (ms * 1e-3) / 1e12, 1), "unit": "TFLOP/s", "ms_per_layer": round(ms, 4),
             "largest": {"name": name, "N": w.N, "K": w.K, "ms": round(one_ms, 4),
                         "tflops": round(one_flops / (one_ms * 1e-3) / 1e12, 1)},
@@ -711,14 +719,17 @@ def run_lq(args):
         dev = f"cuda:{local}"
         g2 = gemm_layer(lq, torch, h, "2bit", dev, args.gemm_steps, 3)
         g4 = gemm_layer(lq, torch, h, "nf4", dev, args.gemm_steps, 3)
+        gi4 = gemm_layer(lq, torch, h, "int4", dev, args.gemm_steps, 3)
+        gdq = gemm_layer(lq, torch, h, "nf4_dq", dev, args.gemm_steps, 3)
         gemm = {"workload": GEMM_WORKLOAD, "metric": "dequant-GEMM TFLOP/s", "dtype": "bf16 x bf16 -> f32 accumulate",
-                "2bit": g2, "nf4": g4,
+                "2bit": g2, "nf4": g4, "int4": gi4, "nf4_dq": gdq,
                 "roofline": {"bound": "tensor", "achieved": g2["value"], "peak": bf16, "unit": "TFLOP/s",
                              "frac": round(g2["value"] / bf16, 4), "peak_kind": peak_kind + " bf16 burst",
                              "kernel": "gemm_kernel<2bit>, one lq_gemm_grouped launch over the layer's 7 projections",
                              "traffic": _traffic("gemm_14b_layer_2bit_bytes_per_launch"),
                              "largest_projection_alone_tflops": g2["largest"]["tflops"]},
-                "frac_of_bf16_peak": {"2bit": round(g2["value"] / bf16, 4), "nf4": round(g4["value"] / bf16, 4)}}
+                "frac_of_bf16_peak": {"2bit": round(g2["value"] / bf16, 4), "nf4": round(g4["value"] / bf16, 4),
+                                      "int4": round(gi4["value"] / bf16, 4), "nf4_dq": round(gdq["value"] / bf16, 4)}}
 
     decode_more = decode_workloads(lq, torch, h, f"cuda:{local}") if not args.no_decode_workloads else None
     quant = quantizer_layer(lq, torch, h, f"cuda:{local}") if not args.no_quant else None

@@ -287,7 +287,7 @@ LQ_API lq_status lq_gemm(lq_handle h, int format, const uint8_t* codes, const vo
     lq_status s = check_problem(p);
     if (s != LQ_OK) return s;
     if (M < 1) return LQ_ERR_INVALID_ARG;
-    if (K % 64 != 0 || format == LQ_FMT_INT4_G32) return LQ_ERR_UNSUPPORTED;   // (INT4: decode only)
+    if (K % 64 != 0) return LQ_ERR_UNSUPPORTED;
     DeviceGuard guard(h->device);
     if (!guard.ok) return LQ_ERR_CUDA;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -303,7 +303,7 @@ LQ_API lq_status lq_gemm_grouped(lq_handle h, const lq_problem* problems, int co
         const lq_status s = check_problem(p);
         if (s != LQ_OK) return s;
         if (p.M < 1 || p.batch != 1) return LQ_ERR_UNSUPPORTED;
-        if (p.K % 64 != 0 || p.format == LQ_FMT_INT4_G32) return LQ_ERR_UNSUPPORTED;
+        if (p.K % 64 != 0) return LQ_ERR_UNSUPPORTED;
         if (p.format != problems[0].format || p.x_dtype != problems[0].x_dtype) return LQ_ERR_UNSUPPORTED;
     }
     DeviceGuard guard(h->device);

@@ -56,18 +56,21 @@ constexpr int kTmemCols = 2 * kBN;       // two accumulators: the epilogue drain
 template <int FMT>
 struct GemmLayout {
     static constexpr bool kNF4Fmt = FMT == LQ_FMT_NF4_B64;
-    static constexpr int kStagesA = kNF4Fmt ? 3 : 4;
+    static constexpr bool kInt4Fmt = FMT == LQ_FMT_INT4_G32;
+    static constexpr bool kNib = kNF4Fmt || kInt4Fmt;   // 4-bit codes, 32 bytes per row and K-block
+    static constexpr int kStagesA = kNib ? 3 : 4;
     // one metadata chunk (kChunk K-blocks of 128 rows):
     //   2-bit: codes [128][64 B] (64-byte swizzle) | scales [128][8 x f16] | offsets [128][8 x f16] |
     //          anchor bits [4][u64] | keep masks [4][32 x u32] (word w clears the halves of anchor columns 2w, 2w+1)
     //   NF4:   codes [128][128 B] (128-byte swizzle) | absmax [128][4 x f32]
-    static constexpr int kCodesBytes = kBM * kChunk * (kNF4Fmt ? 32 : 16);
+    //   INT4:  codes [128][128 B] (128-byte swizzle; permuted positions) | scales [128][8 x f16]
+    static constexpr int kCodesBytes = kBM * kChunk * (kNib ? 32 : 16);
     static constexpr int kScaleOff = kCodesBytes;
     static constexpr int kOffsetOff = kScaleOff + kBM * 16;
-    static constexpr int kBitsOff = kOffsetOff + (kNF4Fmt ? 0 : kBM * 16);
+    static constexpr int kBitsOff = kOffsetOff + (kNib ? 0 : kBM * 16);
     static constexpr int kMaskOff = kBitsOff + 32;
-    // a 2-bit slot also carries one anchor weight tile [128][64 x f16] (128-byte swizzle)
-    static constexpr int kMetaBytes = ((kNF4Fmt ? kBitsOff : kMaskOff + kChunk * 128) + 1023) / 1024 * 1024;
+    // a 2-bit or INT4 slot also carries one anchor weight tile [128][64 x f16] (128-byte swizzle)
+    static constexpr int kMetaBytes = ((kNib ? kBitsOff : kMaskOff + kChunk * 128) + 1023) / 1024 * 1024;
     static constexpr int kChunkBytes = kNF4Fmt ? kMetaBytes : (kMetaBytes > kATile ? kMetaBytes : kATile);
     static constexpr int kAOff = 0;
     static constexpr int kBOff = kAOff + kStagesA * kATile;
@@ -266,7 +269,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                 prefetch_tensormap(&P.d[p].cmap);
                 if (P.d[p].meta_tma) {
                     prefetch_tensormap(&P.d[p].smap);
-                    if (!L::kNF4Fmt) prefetch_tensormap(&P.d[p].omap);
+                    if (!L::kNib) prefetch_tensormap(&P.d[p].omap);
                 }
                 if (P.d[p].a_pad) prefetch_tensormap(&P.d[p].awmap);
             }
@@ -283,7 +286,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                 uint8_t* ch = meta + rm.s * L::kChunkBytes;
                 const uint32_t fb = m_full0 + 8 * rm.s;
                 const int kb0 = c * kChunk;
-                if (!L::kNF4Fmt && D.A > 0) {
+                if (!L::kNib && D.A > 0) {
                     // anchor columns of the chunk's K-blocks and the per-word keep masks
                     const uint4 b01 = *reinterpret_cast<const uint4*>(D.anchor_bits + 2 * kb0);
                     const uint4 b23 = *reinterpret_cast<const uint4*>(D.anchor_bits + 2 * kb0 + 4);
@@ -308,6 +311,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                             const float* src = static_cast<const float*>(D.scales) + nr * (D.K / 64) + kb0;
                             for (int i = 0; i < nk; ++i)
                                 reinterpret_cast<float*>(ch + L::kScaleOff + rr * 16)[i] = __ldg(src + i);
+                        } else if (L::kInt4Fmt) {
+                            const uint32_t* ss = reinterpret_cast<const uint32_t*>(static_cast<const uint16_t*>(D.scales) +
+                                                                                   nr * (D.K / 32) + 2 * kb0);
+                            for (int i = 0; i < nk; ++i) reinterpret_cast<uint32_t*>(ch + L::kScaleOff + rr * 16)[i] = __ldg(ss + i);
                         } else {
                             const int64_t g = nr * (D.K / 32) + 2 * kb0;
                             const uint32_t* ss = reinterpret_cast<const uint32_t*>(static_cast<const uint16_t*>(D.scales) + g);
@@ -321,12 +328,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                 }
                 if (lane == 0) {
                     uint32_t tx = L::kCodesBytes;
-                    if (D.meta_tma) tx += L::kNF4Fmt ? kBM * 16 : 2 * kBM * 16;
+                    if (D.meta_tma) tx += L::kNib ? kBM * 16 : 2 * kBM * 16;
                     mbar_arrive_expect_tx(fb, tx);
-                    tma_load_2d(smem_u32(ch), &D.cmap, kb0 * (L::kNF4Fmt ? 32 : 16), n0, fb);
+                    tma_load_2d(smem_u32(ch), &D.cmap, kb0 * (L::kNib ? 32 : 16), n0, fb);
                     if (D.meta_tma) {
                         tma_load_2d(smem_u32(ch + L::kScaleOff), &D.smap, kb0 * (L::kNF4Fmt ? 1 : 2), n0, fb);
-                        if (!L::kNF4Fmt)
+                        if (!L::kNib)
                             tma_load_2d(smem_u32(ch + L::kOffsetOff), &D.omap, kb0 * 2, n0, fb);
                     }
                 } else {
@@ -407,6 +414,37 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                                     c[8 * wi + 6] &= m1.z;
                                     c[8 * wi + 7] &= m1.w;
                                 }
+                            }
+                        }
+                    } else if (FMT == LQ_FMT_INT4_G32) {
+                        // two 32-position groups: each group's 16 values S * q (q the nibble as a 4-bit
+                        // two's complement integer; exact in fp32, then one rounding) in byte-split registers
+                        const uint8_t* crow = ch + r * 128;
+                        const uint4 cw0 = *reinterpret_cast<const uint4*>(crow + (((2 * j) ^ sw) << 4));
+                        const uint4 cw1 = *reinterpret_cast<const uint4*>(crow + (((2 * j + 1) ^ sw) << 4));
+                        const uint32_t s2 = *reinterpret_cast<const uint32_t*>(ch + L::kScaleOff + r * 16 + 4 * j);
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh) {
+                            const float sg = half_bits_to_float((uint16_t)(hh ? s2 >> 16 : s2 & 0xFFFFu));
+                            uint32_t BL[4], BH[4];
+#pragma unroll
+                            for (int q4 = 0; q4 < 4; ++q4) {
+                                float v[4];
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const int nib = 4 * q4 + e;
+                                    v[e] = __fmul_rn((float)(nib < 8 ? nib : nib - 16), sg);
+                                }
+                                const uint32_t p01 = pack2(v[0], v[1], P.bf16), p23 = pack2(v[2], v[3], P.bf16);
+                                BL[q4] = prmt(p01, p23, 0x6420);
+                                BH[q4] = prmt(p01, p23, 0x7531);
+                            }
+                            const uint4& cw = hh ? cw1 : cw0;
+                            const uint32_t ws[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+                            for (int wi = 0; wi < 4; ++wi) {
+                                expand_nf4_fast(ws[wi], 0, BL, BH, c[16 * hh + 4 * wi + 0], c[16 * hh + 4 * wi + 1]);
+                                expand_nf4_fast(ws[wi], 1, BL, BH, c[16 * hh + 4 * wi + 2], c[16 * hh + 4 * wi + 3]);
                             }
                         }
                     } else {
@@ -558,6 +596,27 @@ __global__ void __launch_bounds__(256) gemm_prep_kernel(const __grid_constant__ 
     }
 }
 
+// INT4 prefill: x in the permuted column order, xp[m][j] = x[m][perm[j]] (zero for a column
+// outside [0, K)); one thread per 8 consecutive positions of a token.
+__global__ void __launch_bounds__(256) gemm_permute_x_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm,
+                                                             uint16_t* __restrict__ xp, int M, int K) {
+    const int64_t n8 = (int64_t)M * (K / 8);
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t m = i / (K / 8);
+        const int j0 = (int)(i - m * (K / 8)) * 8;
+        const int4 c0 = __ldg(reinterpret_cast<const int4*>(perm + j0)), c1 = __ldg(reinterpret_cast<const int4*>(perm + j0 + 4));
+        const int cols[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+        uint32_t v[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int a = cols[2 * e], b = cols[2 * e + 1];
+            const uint32_t lo = (unsigned)a < (unsigned)K ? x[m * K + a] : 0u, hi = (unsigned)b < (unsigned)K ? x[m * K + b] : 0u;
+            v[e] = lo | (hi << 16);
+        }
+        *reinterpret_cast<uint4*>(xp + m * K + j0) = make_uint4(v[0], v[1], v[2], v[3]);
+    }
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn_g() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
@@ -692,7 +751,15 @@ lq_status launch_gemm_grouped_limited(lq_handle h, const lq_problem* probs, int 
     memset(&P, 0, sizeof(P));
     memset(&Q, 0, sizeof(Q));
     const int fmt = probs[0].format;
-    const bool nf4 = fmt == LQ_FMT_NF4_B64;
+    const bool nf4 = fmt == LQ_FMT_NF4_B64, int4 = fmt == LQ_FMT_INT4_G32;
+    const bool nib = nf4 || int4;   // 4-bit codes
+    struct PermJob {
+        const uint16_t* x;
+        const int32_t* perm;
+        uint16_t* xp;
+        int M, K;
+    } perm_jobs[kMaxGemmGroup];
+    int nperm = 0;
     P.count = count;
     P.bf16 = probs[0].x_dtype == LQ_BF16;
     P.status = h->status_flag;
@@ -715,7 +782,7 @@ lq_status launch_gemm_grouped_limited(lq_handle h, const lq_problem* probs, int 
         const int A = nf4 ? 0 : p.A;
         const int a_pad = A > 0 ? (A + kBK - 1) / kBK * kBK : 0;
         D.scales = p.scales;
-        D.offsets = static_cast<const uint16_t*>(p.offsets);
+        D.offsets = int4 ? nullptr : static_cast<const uint16_t*>(p.offsets);
         D.y = p.y;
         D.M = p.M;
         D.N = p.N;
@@ -733,10 +800,18 @@ lq_status launch_gemm_grouped_limited(lq_handle h, const lq_problem* probs, int 
         D.anchor_bits = reinterpret_cast<const uint32_t*>(bits);
         uint16_t* xa = reinterpret_cast<uint16_t*>(ws + used);
         used += ((size_t)p.M * a_pad * 2 + 255) & ~size_t(255);
-        if (!map_16bit(&D.xmap, p.x, (uint64_t)p.K, (uint64_t)p.M, (uint64_t)p.K, kBN)) return LQ_ERR_CUDA;
-        const uint64_t cbytes = (uint64_t)p.K / (nf4 ? 2 : 4);
+        const void* xsrc = p.x;
+        if (int4) {   // INT4: x in the weights' permuted column order, gathered once into the workspace
+            uint16_t* xp = reinterpret_cast<uint16_t*>(ws + used);
+            used += ((size_t)p.M * p.K * 2 + 255) & ~size_t(255);
+            perm_jobs[nperm++] = PermJob{static_cast<const uint16_t*>(p.x), static_cast<const int32_t*>(p.offsets), xp, p.M,
+                                         p.K};
+            xsrc = xp;
+        }
+        if (!map_16bit(&D.xmap, xsrc, (uint64_t)p.K, (uint64_t)p.M, (uint64_t)p.K, kBN)) return LQ_ERR_CUDA;
+        const uint64_t cbytes = (uint64_t)p.K / (nib ? 2 : 4);
         if (!map_2d(&D.cmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.codes, cbytes, (uint64_t)p.N, cbytes,
-                    kChunk * (nf4 ? 32 : 16), kBM, nf4 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B))
+                    kChunk * (nib ? 32 : 16), kBM, nib ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B))
             return LQ_ERR_CUDA;
         if (D.meta_tma) {
             if (nf4) {
@@ -745,9 +820,10 @@ lq_status launch_gemm_grouped_limited(lq_handle h, const lq_problem* probs, int 
                     return LQ_ERR_CUDA;
             } else {
                 if (!map_2d(&D.smap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, p.scales, (uint64_t)p.K / 32, (uint64_t)p.N,
-                            (uint64_t)p.K / 32, 8, kBM, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-                    !map_2d(&D.omap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, p.offsets, (uint64_t)p.K / 32, (uint64_t)p.N,
                             (uint64_t)p.K / 32, 8, kBM, CU_TENSOR_MAP_SWIZZLE_NONE))
+                    return LQ_ERR_CUDA;
+                if (!int4 && !map_2d(&D.omap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, p.offsets, (uint64_t)p.K / 32,
+                                     (uint64_t)p.N, (uint64_t)p.K / 32, 8, kBM, CU_TENSOR_MAP_SWIZZLE_NONE))
                     return LQ_ERR_CUDA;
             }
         }
@@ -776,7 +852,16 @@ lq_status launch_gemm_grouped_limited(lq_handle h, const lq_problem* probs, int 
         gemm_prep_kernel<<<dim3(gx, prep_count), 256, 0, stream>>>(Q);
         if (cudaPeekAtLastError() != cudaSuccess) return LQ_ERR_CUDA;
     }
-    const int smem = nf4 ? GemmLayout<LQ_FMT_NF4_B64>::kSmemBytes : GemmLayout<LQ_FMT_2BIT_LM_G32>::kSmemBytes;
+    for (int i = 0; i < nperm; ++i) {
+        const PermJob& jb = perm_jobs[i];
+        const int64_t n8 = (int64_t)jb.M * (jb.K / 8);
+        const int g = (int)std::min<int64_t>((n8 + 255) / 256, (int64_t)h->num_sms * 16);
+        gemm_permute_x_kernel<<<std::max(g, 1), 256, 0, stream>>>(jb.x, jb.perm, jb.xp, jb.M, jb.K);
+        if (cudaPeekAtLastError() != cudaSuccess) return LQ_ERR_CUDA;
+    }
+    const int smem = nf4    ? GemmLayout<LQ_FMT_NF4_B64>::kSmemBytes
+                     : int4 ? GemmLayout<LQ_FMT_INT4_G32>::kSmemBytes
+                            : GemmLayout<LQ_FMT_2BIT_LM_G32>::kSmemBytes;
     if (smem > h->max_smem_optin) return LQ_ERR_UNSUPPORTED;
     const int grid = std::min(tiles, h->num_sms);
     if (count > 1) {
@@ -786,7 +871,9 @@ lq_status launch_gemm_grouped_limited(lq_handle h, const lq_problem* probs, int 
         P.sched_off = h->sched;
         P.sched_tiles = h->sched + grid + 1;
     }
-    return nf4 ? launch_fmt<LQ_FMT_NF4_B64>(P, grid, stream) : launch_fmt<LQ_FMT_2BIT_LM_G32>(P, grid, stream);
+    if (nf4) return launch_fmt<LQ_FMT_NF4_B64>(P, grid, stream);
+    if (int4) return launch_fmt<LQ_FMT_INT4_G32>(P, grid, stream);
+    return launch_fmt<LQ_FMT_2BIT_LM_G32>(P, grid, stream);
 }
 
 lq_status launch_gemm(lq_handle h, const lq_problem& p, cudaStream_t stream) { return launch_gemm_grouped(h, &p, 1, stream); }

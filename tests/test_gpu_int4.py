@@ -7,7 +7,8 @@
   memory and by the pre-pass, grouped and batched problems, a whole 7B decoder layer at
   full size on sampled rows, bf16 x far outside binary16's range, and the weight range
   limit (8 |S| >= 65520 reports LQ_ERR_RANGE);
-* K % 256 != 0 and the prefill GEMM answer LQ_ERR_UNSUPPORTED without launching.
+* lq_gemm (prefill on tcgen05): 4e-3 * E (bf16) / 1e-3 * E (fp16), single and grouped;
+* a decode with K % 256 != 0 answers LQ_ERR_UNSUPPORTED without launching.
 """
 import numpy as np
 import pytest
@@ -229,21 +230,59 @@ def test_gemv_int4_weight_range_limit(lqm, handle):
     gemv_check(lqm, handle, p, xb, "f16", "after the range error")
 
 
+# ---------------------------------------------------------------- prefill (tcgen05 GEMM)
+
+@pytest.mark.parametrize("xdt", ["bf16", "f16"])
+@pytest.mark.parametrize("shape", [(256, 128, 256), (300, 200, 1088), (17, 64, 128), (513, 384, 640)])
+def test_gemm_int4(lqm, handle, xdt, shape):
+    """x permuted once into the workspace, two 16-entry S*q tables per 64-column block in the
+    producer warps, the outlier columns as extra K-blocks: 4e-3 * E with bf16 operands, 1e-3 * E
+    with fp16 (the weights are rounded once to the operand type)."""
+    M, N, K = shape
+    p, outl = quantized_int4(N, K, seed=M + N + K)
+    w = lqm.QuantWeights.from_host(p, lqm.FMT_INT4)
+    xb = x_for(M, K, xdt, outl, seed=M)
+    y = handle.gemm(w, dev_x(xb, xdt), y_dtype=torch.float32)
+    torch.cuda.synchronize()
+    yref, E = O.matmul_ref(O.dequant_int4(p), xb, xdt)
+    assert_within(y.cpu().numpy(), yref, E, 4e-3 if xdt == "bf16" else 1e-3, f"gemm int4 {shape} {xdt}")
+    handle.sync()
+
+
+def test_gemm_int4_grouped_and_all_codes(lqm, handle):
+    """Two problems in one launch; the second holds every nibble (-8 included) at every position."""
+    probs, keep = [], []
+    p0, outl = quantized_int4(192, 512, seed=90)
+    N, K = 64, 256
+    q = ((np.arange(N)[:, None] + np.arange(K)[None, :]) % 16 - 8).astype(np.int8)
+    g = np.random.default_rng(9)
+    p1 = dict(codes=O.pack_int4(q), scales=(g.uniform(0.5, 2.0, size=(N, K // 32)) * 1e-2).astype(np.float16).view(np.uint16),
+              perm=g.permutation(K).astype(np.int32), anchor_idx=np.zeros(0, np.int32), anchor_w=np.zeros((N, 8), np.uint16),
+              A=0, ld_anchor=8, N=N, K=K)
+    for i, p in enumerate((p0, p1)):
+        w = lqm.QuantWeights.from_host(p, lqm.FMT_INT4)
+        xb = x_for(256, p["K"], "bf16", outl if i == 0 else None, seed=91 + i)
+        x = dev_x(xb, "bf16")
+        y = torch.empty((256, p["N"]), dtype=torch.float32, device="cuda")
+        probs.append(handle.problem(w, x, y))
+        keep.append((p, xb, y, w, x))
+    handle.gemm_grouped(probs)
+    torch.cuda.synchronize()
+    for i, (p, xb, y, _, _) in enumerate(keep):
+        yref, E = O.matmul_ref(O.dequant_int4(p), xb, "bf16")
+        assert_within(y.cpu().numpy(), yref, E, 4e-3, f"grouped int4 {i}")
+    handle.sync()
+
+
 # ---------------------------------------------------------------- what INT4 does not take
 
 def test_int4_unsupported_paths_launch_nothing(lqm, handle):
-    p, outl = quantized_int4(64, 2592, seed=1)             # K % 256 != 0
+    p, outl = quantized_int4(64, 2592, seed=1)             # K % 256 != 0: no decode kernel takes it
     w = lqm.QuantWeights.from_host(p, lqm.FMT_INT4)
     y = torch.full((1, 64), 7.0, device="cuda")
     x = dev_x(x_for(1, 2592, "f16", outl), "f16")
     with pytest.raises(lqm.LQError) as e:
         handle.gemv(w, x, y=y)
-    assert e.value.status == lqm.LQ_ERR_UNSUPPORTED
-    p2, outl2 = quantized_int4(128, 256, seed=2)
-    w2 = lqm.QuantWeights.from_host(p2, lqm.FMT_INT4)
-    x2 = dev_x(x_for(64, 256, "f16", outl2), "f16")
-    with pytest.raises(lqm.LQError) as e:
-        handle.gemm(w2, x2)
     assert e.value.status == lqm.LQ_ERR_UNSUPPORTED
     torch.cuda.synchronize()
     assert torch.all(y == 7.0)
