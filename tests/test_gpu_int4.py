@@ -274,6 +274,24 @@ def test_gemm_int4_grouped_and_all_codes(lqm, handle):
     handle.sync()
 
 
+def test_gemm_int4_14b_prefill_sampled(lqm, handle):
+    """M = 2048 prefill over the 14B layer's down projection (5120 x 13824) and gate (13824 x 5120),
+    sampled rows against the oracle."""
+    g = np.random.default_rng(8)
+    for i, (name, N, K) in enumerate([s for s in synth.LAYER_SHAPES["14b"] if s[0] in ("down", "gate")]):
+        M = 2048
+        outl = synth.outlier_channels(K, 0.01, seed=8)
+        xb = synth.activations(M, K, "bf16", synth.channel_sigma(K, outl, 20.0), seed=8, matrix_id=i)
+        pk = synth.random_packed_int4(N, K, int(np.floor(O.INT4_OUTLIER_FRAC * K)), seed=8, matrix_id=i)
+        w = lqm.QuantWeights.from_host(pk, lqm.FMT_INT4)
+        y = handle.gemm(w, dev_x(xb, "bf16")).float().cpu().numpy()
+        for n in sorted(set(g.choice(N, 4, replace=False).tolist()) | {0, N - 1}):
+            one = dict(pk, codes=pk["codes"][n:n + 1], scales=pk["scales"][n:n + 1], anchor_w=pk["anchor_w"][n:n + 1], N=1)
+            yref, E = O.matmul_ref(O.dequant_int4(one), xb, "bf16")
+            assert_within(y[:, n:n + 1], yref, E, 4e-3, f"int4 {name} row {n}")
+    handle.sync()
+
+
 # ---------------------------------------------------------------- what INT4 does not take
 
 def test_int4_unsupported_paths_launch_nothing(lqm, handle):

@@ -17,7 +17,8 @@ import numpy as np
 import pytest
 
 from oracle import oracle as O
-from tests._util import quantized_2bit, x_for
+import synth
+from tests._util import quantized_2bit, quantized_int4, x_for
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -36,7 +37,8 @@ def lqm():
 
 def _noalloc(L, w, x, y, stream=None):
     fmt, c, s, o, ai, aw, A, ld = w.args()
-    return L.lq_gemv_noalloc(fmt, c, s, o, ai, aw, A, ld, x.data_ptr(), 1, y.data_ptr(), 0, x.shape[0], w.N, w.K,
+    xdt = 2 if x.dtype == torch.bfloat16 else 1
+    return L.lq_gemv_noalloc(fmt, c, s, o, ai, aw, A, ld, x.data_ptr(), xdt, y.data_ptr(), 0, x.shape[0], w.N, w.K,
                              stream)
 
 
@@ -61,6 +63,33 @@ def test_noalloc_matches_the_oracle_on_two_calls_in_a_row(lqm, N, K, M):
         assert np.all(np.isfinite(got)), f"call {call}: unwritten outputs"
         err = np.abs(got - y_ref)
         assert np.all(err <= TOL * E + 1e-30), f"call {call}: max err/E = {np.max(err / (E + 1e-30)):.3e}"
+
+
+@pytest.mark.parametrize("fmt", ["int4", "nf4_dq"])
+def test_noalloc_other_formats_match_the_oracle(lqm, fmt):
+    """INT4 (the ring kernel, x gathered through the permutation) and NF4 with double
+    quantization (the streaming kernel) through the same entry point."""
+    L = lqm.load_library()
+    N, K, M = 700, 4096, 4
+    if fmt == "int4":
+        p, outl = quantized_int4(N, K, seed=5)
+        w = lqm.QuantWeights.from_host(p, lqm.FMT_INT4)
+        W = O.dequant_int4(p)
+    else:
+        p = O.quantize_nf4_dq(synth.weights(N, K, 0.02, seed=6, big_frac=0.001, big_mult=10.0))
+        outl = None
+        w = lqm.QuantWeights.from_host(p, lqm.FMT_NF4_DQ)
+        W = O.dequant_nf4_dq(p)
+    xb = x_for(M, K, "bf16", outl, seed=7)
+    x = torch.from_numpy(xb).view(torch.bfloat16).cuda()
+    y_ref, E = O.matmul_ref(W, xb, "bf16")
+    for call in range(2):
+        y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+        st = _noalloc(L, w, x, y)
+        assert st == lqm.LQ_OK, L.lq_status_string(st)
+        torch.cuda.synchronize()
+        err = np.abs(y.cpu().numpy().astype(np.float64) - y_ref)
+        assert np.all(err <= TOL * E + 1e-30), f"{fmt} call {call}: max err/E = {np.max(err / (E + 1e-30)):.3e}"
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch(lqm):
