@@ -462,7 +462,15 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const __grid_constan
         const int n = strip * kGemvStripRows + rr;
         if (n >= N) continue;
         float sum = 0.f;
-        for (int pp = 0; pp < D.parts; ++pp) sum += __ldcg(strip_base + ((int64_t)pp * M + m) * kGemvStripRows + rr);
+        for (int p0 = 0; p0 < D.parts; p0 += 8) {   // eight loads in flight, then the adds in part order
+            float v[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                v[k] = p0 + k < D.parts ? __ldcg(strip_base + ((int64_t)(p0 + k) * M + m) * kGemvStripRows + rr) : 0.f;
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                if (p0 + k < D.parts) sum += v[k];
+        }
         store_out(y, (size_t)m * N + n, P.y_dtype, sum * unscale(m));
     }
     if (tid == 0) P.counters[strip_id] = 0u;

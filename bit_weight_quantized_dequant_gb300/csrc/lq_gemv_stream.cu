@@ -442,7 +442,14 @@ __device__ __noinline__ void finish_block(const float* slots, int nc, int M, voi
     for (int i = lane; i < rows * M; i += 32) {
         const int m = i / rows, row = row0 + (i - m * rows);
         float sum = 0.f;
-        for (int c = 0; c < nc; ++c) sum += __ldcg(slots + c * M * rows + i);
+        for (int c0 = 0; c0 < nc; c0 += 8) {   // eight loads in flight, then the adds in slot order
+            float v[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v[k] = c0 + k < nc ? __ldcg(slots + (c0 + k) * M * rows + i) : 0.f;
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                if (c0 + k < nc) sum += v[k];
+        }
         if (row < N) store_out(y, (size_t)m * N + row, y_dtype, sum);
     }
 }
