@@ -1308,29 +1308,33 @@ __global__ void __launch_bounds__(32 * ring_warps(NT), 16 / ring_warps(NT)) gemv
     const unsigned char* ringp = ring_smem + warp * kRingDepth * kStage;
     const int64_t u_begin = active ? split_at(P, wid) : 0, u_end = active ? split_at(P, wid + 1) : 0;
 
-    // weights do not depend on the pre-pass: the first copies go out before waiting for it
+    // Weights do not depend on the kernel before: the first unit's copies go out before
+    // waiting for it, after the cheap lookups (the warp's cursor, the CTA's x span) and before
+    // the x build; the second unit's copies go out after the build, so that the build's loads
+    // do not queue behind both.
     Feed f;
-    if (active) {
-        f = feed_at<FMT>(P, u_begin, (int)(u_end - u_begin), lane);
-#pragma unroll
-        for (int i = 0; i < kRingDepth; ++i) feed_issue<FMT>(P, f, ring + i * kStage, lane);
-    }
-    pdl_launch_dependents();
+    if (active) f = feed_at<FMT>(P, u_begin, (int)(u_end - u_begin), lane);
     int64_t span0 = 0;
     uint16_t* xsm = reinterpret_cast<uint16_t*>(ring_smem + kW * kRingDepth * kStage);
+    Pos a, b;
+    const int64_t w_lo = (int64_t)blockIdx.x * kW, w_hi = (w_lo + kW < W) ? w_lo + kW : W;
     if (XS) {
-        const int64_t w_lo = (int64_t)blockIdx.x * kW, w_hi = (w_lo + kW < W) ? w_lo + kW : W;
         if (w_lo >= W) return;   // the whole CTA is idle
-        const Pos a = locate(P, split_at(P, w_lo)), b = locate(P, split_at(P, w_hi) - 1);
+        a = locate(P, split_at(P, w_lo));
+        b = locate(P, split_at(P, w_hi) - 1);
         span0 = P.d[a.p].xoff + a.l * P.d[a.p].xperm_stride;
-        const int64_t span1 = P.d[b.p].xoff + (b.l + 1) * P.d[b.p].xperm_stride;
-        (void)span1;
+    }
+    if (active) feed_issue<FMT>(P, f, ring, lane);
+    pdl_launch_dependents();
+    if (XS) {
         pdl_wait();   // x may come from the kernel before
         build_span_x<FMT>(P, a, b, span0, xsm);
         if (!active) return;
     } else {
         pdl_wait();
     }
+#pragma unroll
+    for (int i = 1; i < kRingDepth; ++i) feed_issue<FMT>(P, f, ring + i * kStage, lane);
 
     const int S = ring_kstride(M);
     const int xlane = min(g, M - 1) * 16 + 4 * t * S;    // code columns: block 4t of each 64-column quarter
