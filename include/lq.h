@@ -145,10 +145,10 @@ typedef struct lq_problem {
     int format;                /* lq_format */
     int M, N, K;
     const uint8_t* codes;
-    const void* scales;        /* binary16 S_g (2-bit) or fp32 absmax (NF4) */
-    const void* offsets;       /* binary16 Z_g (2-bit), int32 perm[K] (INT4), or NULL (NF4) */
-    const int32_t* anchor_idx; /* 2-bit only, may be NULL when A == 0 */
-    const uint16_t* anchor_w;  /* 2-bit only, may be NULL when A == 0 */
+    const void* scales;        /* binary16 S_g (2-bit, INT4), fp32 absmax (NF4) or E4M3 maxima (NF4-DQ) */
+    const void* offsets;       /* binary16 Z_g (2-bit), int32 perm[K] (INT4), NULL (NF4) or fp32 second level (NF4-DQ) */
+    const int32_t* anchor_idx; /* 2-bit and INT4, may be NULL when A == 0 */
+    const uint16_t* anchor_w;  /* 2-bit and INT4, may be NULL when A == 0 */
     int A;
     int ld_anchor;
     const void* x;
@@ -194,10 +194,11 @@ LQ_API lq_status lq_dequant(lq_handle h, int format,
                             void* w_out, int out_dtype, int N, int K, void* stream);
 
 /*
- * lq_gemv — decode-sized product y = x * W_eff^T for 1 <= M <= 32 tokens, with
- * split-K over thread blocks and the anchor columns folded into the same fp32
- * accumulator.  x: [M][K] binary16 or bf16; y: [M][N] in y_dtype.
- * LQ_ERR_UNSUPPORTED for M outside 1..32.
+ * lq_gemv — decode-sized product y = x * W_eff^T for 1 <= M <= 32 tokens, the
+ * weights streamed once and dequantized in registers, the anchor columns folded
+ * into the same fp32 accumulator.  x: [M][K] binary16 or bf16; y: [M][N] in
+ * y_dtype.  LQ_ERR_UNSUPPORTED for M outside 1..32, and for INT4 or NF4-DQ when
+ * K % 256 != 0.
  */
 LQ_API lq_status lq_gemv(lq_handle h, int format,
                          const uint8_t* codes, const void* scales, const void* offsets,
@@ -219,7 +220,10 @@ LQ_API lq_status lq_gemv_grouped(lq_handle h, const lq_problem* problems, int co
  * the CTA into tensor memory, the fp32 accumulator lives in tensor memory, and
  * the anchor columns are appended as extra K-blocks of the same accumulator.
  * x: [M][K] bf16 or binary16 (the multiply runs in that dtype); y: [M][N] in
- * y_dtype.  2-bit: K % 64 == 0; NF4: K % 64 == 0.
+ * y_dtype.  K % 64 == 0, every format.  INT4 first writes x in the permuted
+ * column order into the handle's workspace (M * K values per problem), and NF4-DQ
+ * its decoded block maxima (N * K / 64 floats per problem); LQ_ERR_WORKSPACE when
+ * they do not fit.
  */
 LQ_API lq_status lq_gemm(lq_handle h, int format,
                          const uint8_t* codes, const void* scales, const void* offsets,
@@ -370,7 +374,8 @@ LQ_API lq_status lq_quantize_nf4(lq_handle h, const float* W, int N, int K, uint
  * object serves one pass at a time; its handle's workspace rules apply.
  * Errors: LQ_ERR_INVALID_ARG (shapes, offsets outside the layer),
  * LQ_ERR_ALIGNMENT, LQ_ERR_WORKSPACE (layer_bytes > slot_bytes), LQ_ERR_UNSUPPORTED
- * (count > 16), then those of lq_gemv_grouped; LQ_ERR_CUDA from the runtime.
+ * (count > 16, or an INT4 or NF4-DQ layer: the stream carries 2-bit and NF4 layers),
+ * then those of lq_gemv_grouped; LQ_ERR_CUDA from the runtime.
  */
 typedef struct lq_layer_stream_s* lq_layer_stream;
 
