@@ -1,22 +1,31 @@
 // lq_gemm: prefill-sized y = x * W_eff^T on tcgen05 tensor cores.
 //
-// A dense contraction at M = 2048 tokens, so the weights are dequantized into
-// shared memory and multiplied on the 5th-generation tensor cores:
+// A dense contraction at M = 2048 tokens, so the weights are dequantized in
+// registers and multiplied on the 5th-generation tensor cores by CTA pairs:
 //
-//  * Persistent CTAs, one per SM, walk output tiles of 128 weight rows x 256
-//    tokens.  The fp32 accumulator (128 lanes x 256 columns) lives in tensor
-//    memory.
-//  * Warp 0 streams x tiles (256 tokens x 64 columns, 16-bit, 128-byte swizzle)
-//    by TMA into a 4-stage ring.
-//  * Warps 2-9 dequantize: each thread turns 32 columns of one weight row into
-//    16-bit values (2-bit: fmaf(S, C[q], Z) per group, otf-llm README sections
-//    2-3; NF4: T[q] * absmax, AirQuant README NF4) and writes them in the
-//    canonical K-major 128-byte-swizzled layout.  Anchor columns (section 4) are
-//    zeroed in the weight tile, and the anchors join as extra K-blocks: binary16
-//    anchor weights against x gathered at the anchor columns.
-//  * Warp 1 (one thread) issues tcgen05.mma (M=128, N=256, K=16) from the two
-//    shared-memory descriptors and commits each stage back to the producers.
-//  * The same eight warps read the accumulator back with tcgen05.ld and write y.
+//  * Clusters of two CTAs (one per SM) walk output tiles of 256 weight rows x
+//    256 tokens.  The pair's MMA (tcgen05.mma.cta_group::2, M = 256, N = 256,
+//    K = 16) is issued by one thread of the even CTA; each CTA holds 128 rows of
+//    the fp32 accumulator in its own tensor memory.
+//  * Each CTA dequantizes its own 128 weight rows (2-bit: fmaf(S, C[q], Z) per
+//    group, otf-llm README sections 2-3; NF4: T[q] * absmax, AirQuant README NF4;
+//    INT4: S * q): a thread turns the 64 columns of one row in a K-block into
+//    16-bit values and stores them straight into its tensor-memory lane
+//    (tcgen05.st), which the MMA reads as its A operand.  Anchor columns
+//    (section 4) are zeroed in the weight tile, and the anchors join as extra
+//    K-blocks: binary16 anchor weights against x gathered at the anchor columns.
+//  * Each CTA loads its own half of every x tile (128 tokens x 64 columns,
+//    16-bit, 128-byte swizzle) by TMA; the pair MMA reads both halves.  Per SM,
+//    shared memory carries only that half: a quarter of what one CTA with a
+//    256-token tile and a shared-memory weight operand moves per K-block.
+//  * One ring of K-block stages (weights in tensor memory, x in shared memory)
+//    with one "stage full" barrier per stage in the even CTA and one pair commit
+//    per K-block back to both CTAs: the MMA thread waits once and commits once
+//    per K-block (extra barrier work in that thread shows up as tensor-pipe idle
+//    time; measured).  The odd CTA's x arrival is relayed to the even CTA's
+//    barrier by its otherwise idle MMA warp.
+//  * A metadata warp streams codes, scales and anchor weights by TMA; the last
+//    warps read the accumulator back with tcgen05.ld and write y.
 // The multiply runs in the dtype of x (bf16 or binary16) with fp32 accumulation.
 // Every mbarrier wait is bounded in time.
 
@@ -37,28 +46,45 @@
 namespace lq {
 namespace {
 
-constexpr int kBM = 128;                 // weight rows per tile (MMA M)
+constexpr int kSmemLimit = 227 * 1024;   // dynamic shared memory per CTA (opt-in maximum)
+constexpr int kBM = 128;                 // weight rows per CTA; a CTA pair's MMA covers 2 x 128
+constexpr int kPairM = 2 * kBM;          // weight rows per tile
 constexpr int kBN = 256;                 // tokens per tile (MMA N)
+constexpr int kHalfN = kBN / 2;          // x rows each CTA of the pair holds
 constexpr int kBK = 64;                  // columns per K-block (one 128-byte swizzle row of 16-bit values)
-constexpr int kStagesB = 4;              // x ring depth
-constexpr int kATile = kBM * kBK * 2;    // 16 KiB
-constexpr int kBTile = kBN * kBK * 2;    // 32 KiB
+constexpr int kATile = kBM * kBK * 2;    // 16 KiB: one anchor weight tile in a metadata slot
+constexpr int kBTile = kHalfN * kBK * 2; // 16 KiB: this CTA's half of one x tile
 constexpr int kChunk = 4;                // K-blocks of codes and scales per metadata load
-constexpr int kDqWarps = 8;
-constexpr int kEpiWarps = 4;
-constexpr int kDqWarp0 = 3;              // warps: 0 x TMA, 1 MMA, 2 metadata, 3..10 dequant, 11..14 epilogue
-constexpr int kEpiWarp0 = kDqWarp0 + kDqWarps;
-constexpr int kGemmThreads = (kEpiWarp0 + kEpiWarps) * 32;
-constexpr int kTmemCols = 2 * kBN;       // two accumulators: the epilogue drains one while the MMA fills the other
+constexpr int kMetaSlots = 3;            // metadata chunks in flight
+constexpr int kDqWarp0 = 3;              // warps: 0 x TMA, 1 MMA (relay in the odd CTA), 2 metadata, dequant, epilogue
+// tensor memory of each CTA: the accumulator (128 lanes x kBN columns), then the weight stages
+// (32 columns each: one K-block of 64 16-bit values per lane)
+constexpr int kTmemCols = 512;
+constexpr int kACol0 = kBN;
+// One ring of K-block stages: stage s holds the weights in tensor memory columns kACol0 + 32 s
+// and this CTA's half of the x tile in shared memory.
+constexpr int kStages = (kTmemCols - kACol0) / 32;
+static_assert(kStages >= 4 && kACol0 + 32 * kStages <= kTmemCols, "tensor memory columns");
+static_assert(kTmemCols >= 32 && kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0,
+              "tcgen05.alloc takes a power of two from 32 to 512 columns");
+static_assert(kBN % 16 == 0 && kBN <= 256 && kBN % 64 == 0, "MMA N");
 
-// Per-format layout of the shared memory.  The weight (A) ring is one stage shorter
-// for NF4, whose metadata chunks are larger.
+// Per-format layout of the shared memory: the x ring (this CTA's half of each x tile), two
+// metadata slots, the barriers.
 template <int FMT>
 struct GemmLayout {
     static constexpr bool kNF4Fmt = FMT == LQ_FMT_NF4_B64;
     static constexpr bool kInt4Fmt = FMT == LQ_FMT_INT4_G32;
     static constexpr bool kNib = kNF4Fmt || kInt4Fmt;   // 4-bit codes, 32 bytes per row and K-block
-    static constexpr int kStagesA = kNib ? 3 : 4;
+    // Warp roles (measured per format on the 14B prefill layer): groups of four dequant warps
+    // take the K-blocks in turn (three for the 4-bit codes, whose expansion costs more; two for
+    // 2-bit), then the epilogue warps (one or two per tensor-memory lane quarter).
+    static constexpr int kDqGroups = kNib ? 3 : 2;
+    static constexpr int kDqWarps = 4 * kDqGroups;
+    static constexpr int kEpiWarps = kNib ? 4 : 8;
+    static constexpr int kEpiWarp0 = kDqWarp0 + kDqWarps;
+    static constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;
+    static_assert(kBN * 4 % (32 * kEpiWarps) == 0, "epilogue split");
     // one metadata chunk (kChunk K-blocks of 128 rows):
     //   2-bit: codes [128][64 B] (64-byte swizzle) | scales [128][8 x f16] | offsets [128][8 x f16] |
     //          anchor bits [4][u64] | keep masks [4][32 x u32] (word w clears the halves of anchor columns 2w, 2w+1)
@@ -72,12 +98,12 @@ struct GemmLayout {
     // a 2-bit or INT4 slot also carries one anchor weight tile [128][64 x f16] (128-byte swizzle)
     static constexpr int kMetaBytes = ((kNib ? kBitsOff : kMaskOff + kChunk * 128) + 1023) / 1024 * 1024;
     static constexpr int kChunkBytes = kNF4Fmt ? kMetaBytes : (kMetaBytes > kATile ? kMetaBytes : kATile);
-    static constexpr int kAOff = 0;
-    static constexpr int kBOff = kAOff + kStagesA * kATile;
-    static constexpr int kMetaOff = kBOff + kStagesB * kBTile;
-    static constexpr int kBarOff = kMetaOff + 2 * kChunkBytes;
-    static constexpr int kNumBars = 2 * kStagesA + 2 * kStagesB + 2 + 2 + 2 + 2;
+    static constexpr int kBOff = 0;
+    static constexpr int kMetaOff = kBOff + kStages * kBTile;
+    static constexpr int kBarOff = kMetaOff + kMetaSlots * kChunkBytes;
+    static constexpr int kNumBars = 3 * kStages + 2 * kMetaSlots + 2;
     static constexpr int kSmemBytes = 1024 + kBarOff + kNumBars * 8;
+    static_assert(kSmemBytes <= kSmemLimit, "shared memory");
 };
 
 // One problem of a (grouped) launch: tensor maps, pointers and shape.
@@ -93,24 +119,24 @@ struct GemmProb {
     const uint32_t* anchor_bits;   // [K/32 + 8] anchor columns of each 32-column half block
     void* y;
     int M, N, K, A, a_pad, y_dtype, meta_tma;
-    int tiles_m, tile_begin;   // token tiles per row tile; first tile of this problem in the launch
+    int tiles_m, tile_begin;   // token tiles per row tile (of kPairM rows); first tile of this problem in the launch
 };
 
 struct GemmParams {
     GemmProb d[kMaxGemmGroup];
     int count, bf16, total_tiles;
-    const int* sched_off;      // tile list of CTA b: sched_tiles[sched_off[b] .. sched_off[b+1]) (null: round robin)
+    const int* sched_off;      // tile list of CTA pair c: sched_tiles[sched_off[c] .. sched_off[c+1]) (null: round robin)
     const int* sched_tiles;
     int* status;
 };
 
-// Tiles of this CTA, the i-th of them, and the problem a tile belongs to.
-__device__ __forceinline__ int cta_tiles(const GemmParams& P) {
-    if (P.sched_off) return P.sched_off[blockIdx.x + 1] - P.sched_off[blockIdx.x];
-    return (int)blockIdx.x < P.total_tiles ? (P.total_tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+// Tiles of CTA pair c (of npair), the i-th of them, and the problem a tile belongs to.
+__device__ __forceinline__ int pair_tiles(const GemmParams& P, int c, int npair) {
+    if (P.sched_off) return P.sched_off[c + 1] - P.sched_off[c];
+    return c < P.total_tiles ? (P.total_tiles - 1 - c) / npair + 1 : 0;
 }
-__device__ __forceinline__ int tile_id(const GemmParams& P, int i) {
-    return P.sched_off ? __ldg(P.sched_tiles + P.sched_off[blockIdx.x] + i) : (int)blockIdx.x + i * (int)gridDim.x;
+__device__ __forceinline__ int tile_id(const GemmParams& P, int i, int c, int npair) {
+    return P.sched_off ? __ldg(P.sched_tiles + P.sched_off[c] + i) : c + i * npair;
 }
 __device__ __forceinline__ int tile_prob(const GemmParams& P, int gt) {
     int p = 0;
@@ -125,10 +151,6 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, int bf16) {
     else
         asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
     return d;
-}
-
-__device__ __forceinline__ void sts128(uint8_t* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-    *reinterpret_cast<uint4*>(p) = make_uint4(a, b, c, d);
 }
 
 // 16 natural-order weights of one code word -> two 16-byte chunks (8 values each).
@@ -161,105 +183,127 @@ struct Ring {
 };
 
 template <int FMT>
-__global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_constant__ GemmParams P) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmLayout<FMT>::kThreads, 1)
+    gemm_kernel(const __grid_constant__ GemmParams P) {
     using L = GemmLayout<FMT>;
-    constexpr int SA = L::kStagesA;
+    constexpr int kDqGroups = L::kDqGroups, kDqWarps = L::kDqWarps, kEpiWarps = L::kEpiWarps, kEpiWarp0 = L::kEpiWarp0;
+    constexpr int S = kStages;
     extern __shared__ uint8_t smem_raw[];
+    // (the same offsets in both CTAs of a pair: the pair's MMA reads x at one shared-memory
+    // offset in each, and commits arrive at one barrier offset in each)
     uint8_t* base = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-    uint8_t* atile = base + L::kAOff;       // [SA][128 rows][128 B], 128-byte swizzle
-    uint8_t* btile = base + L::kBOff;       // [SB][256 rows][128 B], 128-byte swizzle
-    uint8_t* meta = base + L::kMetaOff;     // [2][chunk]
+    uint8_t* btile = base + L::kBOff;       // [S][128 rows][128 B], 128-byte swizzle
+    uint8_t* meta = base + L::kMetaOff;     // [kMetaSlots][chunk]
     uint64_t* bars = reinterpret_cast<uint64_t*>(base + L::kBarOff);
     __shared__ uint32_t s_tmem;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const uint32_t a_full0 = smem_u32(bars), a_empty0 = a_full0 + 8 * SA;
-    const uint32_t b_full0 = a_empty0 + 8 * SA, b_empty0 = b_full0 + 8 * kStagesB;
-    const uint32_t m_full0 = b_empty0 + 8 * kStagesB, m_empty0 = m_full0 + 16;
-    const uint32_t acc_full0 = m_empty0 + 16, acc_empty0 = acc_full0 + 16;
+    const uint32_t rank = cluster_rank();   // 0: issues the pair's MMAs; 1: its partner
+    const int pair = (int)(blockIdx.x >> 1), npair = (int)(gridDim.x >> 1);
+    const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * S, xloc0 = empty0 + 8 * S;
+    const uint32_t m_full0 = xloc0 + 8 * S, m_empty0 = m_full0 + 8 * kMetaSlots;
+    const uint32_t acc_full0 = m_empty0 + 8 * kMetaSlots, acc_empty0 = acc_full0 + 8;
 
+    // Barriers.  full[s] (used in rank 0) completes when the stage is whole in both CTAs: the
+    // owning dequant group's four warps in each CTA, rank 0's x TMA (arrival and bytes) and the
+    // relay of rank 1's x TMA.  empty[s] (both CTAs) receives the pair commit of the MMAs that
+    // read the stage.  xloc[s] (rank 1) completes on rank 1's x TMA.  acc_full (both) receives
+    // the pair commit of a tile; acc_empty (rank 0) the epilogue warps of both CTAs.  The
+    // metadata ring is local.  The MMA thread waits on one barrier and commits to one per
+    // K-block: every extra wait or commit there shows up as tensor-pipe idle time.
     if (tid == 0) {
-        for (int s = 0; s < SA; ++s) {
-            mbar_init(a_full0 + 8 * s, kDqWarps / 2);   // the group of four warps that owns the K-block
-            mbar_init(a_empty0 + 8 * s, 1);
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full0 + 8 * s, 4 + 4 + 1 + 1);
+            mbar_init(empty0 + 8 * s, 1);
+            mbar_init(xloc0 + 8 * s, 1);
         }
-        for (int s = 0; s < kStagesB; ++s) {
-            mbar_init(b_full0 + 8 * s, 1);
-            mbar_init(b_empty0 + 8 * s, 1);
-        }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kMetaSlots; ++i) {
             mbar_init(m_full0 + 8 * i, 32);
             mbar_init(m_empty0 + 8 * i, kDqWarps);
-            mbar_init(acc_full0 + 8 * i, 1);
-            mbar_init(acc_empty0 + 8 * i, kEpiWarps);
         }
+        mbar_init(acc_full0, 1);
+        mbar_init(acc_empty0, 2 * kEpiWarps);
         fence_mbar_init();
     }
-    if (warp == 1) tmem_alloc(smem_u32(&s_tmem), kTmemCols);
+    if (warp == 1) tmem_alloc_pair(smem_u32(&s_tmem), kTmemCols);
     tc_fence_before();
-    __syncthreads();
+    __syncwarp();
+    cluster_sync_all();   // both CTAs' barriers initialised before any remote arrival or pair commit
     tc_fence_after();
     const uint32_t tmem = s_tmem;
 
-    const int ntiles = cta_tiles(P);
+    const int ntiles = pair_tiles(P, pair, npair);
     int own_abort = 0;
     volatile int* abort = &own_abort;
 
     if (warp == 0) {
-        // ---------------------------------------------------------------- TMA: x tiles
+        // ---------------------------------------------------------------- TMA: this CTA's half of the x tiles
         if (lane == 0) {
             for (int p = 0; p < P.count; ++p) {
                 prefetch_tensormap(&P.d[p].xmap);
                 if (P.d[p].a_pad) prefetch_tensormap(&P.d[p].xamap);
             }
-            Ring rb;
-            for (int i = 0; i < ntiles; ++i) {
-                const int gt = tile_id(P, i);
+            const uint32_t done0 = rank == 0 ? full0 : xloc0;   // where this CTA's x bytes complete
+            Ring rs;
+            bool ok = true;
+            for (int i = 0; ok && i < ntiles; ++i) {
+                const int gt = tile_id(P, i, pair, npair);
                 const GemmProb& D = P.d[tile_prob(P, gt)];
-                const int lt = gt - D.tile_begin, m0 = (lt % D.tiles_m) * kBN;
+                const int lt = gt - D.tile_begin, mh = (lt % D.tiles_m) * kBN + (int)rank * kHalfN;
                 const int KB = D.K / kBK, NKB = KB + D.a_pad / kBK;
-                bool ok = true;
                 for (int kb = 0; kb < NKB; ++kb) {
-                    if (!(ok = mbar_wait_bounded(b_empty0 + 8 * rb.s, rb.ph ^ 1, abort, P.status))) break;
-                    const uint32_t fb = b_full0 + 8 * rb.s;
+                    if (!(ok = mbar_wait_bounded<true>(empty0 + 8 * rs.s, rs.ph ^ 1, abort, P.status))) break;
+                    const uint32_t fb = done0 + 8 * rs.s, dst = smem_u32(btile + rs.s * kBTile);
                     mbar_arrive_expect_tx(fb, kBTile);
-                    if (kb < KB) tma_load_2d(smem_u32(btile + rb.s * kBTile), &D.xmap, kb * kBK, m0, fb);
-                    else tma_load_2d(smem_u32(btile + rb.s * kBTile), &D.xamap, (kb - KB) * kBK, m0, fb);   // x at the anchors
-                    rb.next(kStagesB);
+                    if (kb < KB) tma_load_2d(dst, &D.xmap, kb * kBK, mh, fb);
+                    else tma_load_2d(dst, &D.xamap, (kb - KB) * kBK, mh, fb);   // x at the anchors
+                    rs.next(S);
                 }
-                if (!ok) break;
+            }
+            // every stage's last release has arrived before this CTA may exit
+            for (int s = 0; ok && s < S; ++s) {
+                ok = mbar_wait_bounded<true>(empty0 + 8 * rs.s, rs.ph ^ 1, abort, P.status);
+                rs.next(S);
             }
         }
     } else if (warp == 1) {
-        // ---------------------------------------------------------------- MMA issue
-        if (lane == 0) {
-            const uint32_t idesc = idesc_f16(P.bf16 != 0, kBM, kBN);
-            Ring ra, rb;
+        if (rank == 0 && lane == 0) {
+            // ------------------------------------------------------------ pair MMA issue (M = 256, N = 256, K = 16)
+            const uint32_t idesc = idesc_f16(P.bf16 != 0, kPairM, kBN);
+            const uint32_t a_t0 = tmem + kACol0, b_t0 = smem_u32(btile);
+            Ring rs;
             bool ok = true;
             for (int i = 0; ok && i < ntiles; ++i) {
-                const GemmProb& D = P.d[tile_prob(P, tile_id(P, i))];
+                const GemmProb& D = P.d[tile_prob(P, tile_id(P, i, pair, npair))];
                 const int NKB = D.K / kBK + D.a_pad / kBK;
-                const int acc = i & 1;
-                // the epilogue has drained this accumulator (two tiles ago)
-                if (!(ok = mbar_wait_bounded(acc_empty0 + 8 * acc, ((i >> 1) & 1) ^ 1, abort, P.status))) break;
+                // both CTAs' epilogues have drained the accumulator (the tile before)
+                if (!(ok = mbar_wait_bounded<true>(acc_empty0, (i & 1) ^ 1, abort, P.status))) break;
                 tc_fence_after();
-                const uint32_t d = tmem + acc * kBN;
                 for (int kb = 0; kb < NKB; ++kb) {
-                    if (!(ok = mbar_wait_bounded(a_full0 + 8 * ra.s, ra.ph, abort, P.status))) break;
-                    if (!(ok = mbar_wait_bounded(b_full0 + 8 * rb.s, rb.ph, abort, P.status))) break;
+                    if (!(ok = mbar_wait_bounded<true>(full0 + 8 * rs.s, rs.ph, abort, P.status))) break;
                     tc_fence_after();
-                    const uint32_t a_addr = smem_u32(atile + ra.s * kATile), b_addr = smem_u32(btile + rb.s * kBTile);
+                    const uint32_t a_t = a_t0 + 32 * rs.s, b_addr = b_t0 + rs.s * kBTile;
 #pragma unroll
-                    for (int k = 0; k < kBK / 16; ++k)
-                        tc_mma_f16(d, smem_desc_sw128(a_addr + 32 * k), smem_desc_sw128(b_addr + 32 * k), idesc,
-                                   (kb | k) != 0);
-                    // both stages are free once these MMAs have read them
-                    tc_commit(a_empty0 + 8 * ra.s);
-                    tc_commit(b_empty0 + 8 * rb.s);
-                    ra.next(SA);
-                    rb.next(kStagesB);
+                    for (int k = 0; k < kBK / 16; ++k)   // K = 16: 8 columns of A, 32 bytes of each B row
+                        tc_mma_f16_ts_pair(tmem, a_t + 8 * k, smem_desc_sw128(b_addr + 32 * k), idesc, (kb | k) != 0);
+                    tc_commit_pair(empty0 + 8 * rs.s);   // both CTAs' stage is free once these MMAs have read it
+                    rs.next(S);
                 }
-                if (ok) tc_commit(acc_full0 + 8 * acc);
+                if (ok) tc_commit_pair(acc_full0);
+            }
+        } else if (rank == 1 && lane == 0) {
+            // ------------------------------------------------------------ relay: this CTA's x stages to rank 0
+            const uint32_t full_r0 = mapa_shared(full0, 0);
+            Ring rs;
+            bool ok = true;
+            for (int i = 0; ok && i < ntiles; ++i) {
+                const GemmProb& D = P.d[tile_prob(P, tile_id(P, i, pair, npair))];
+                const int NKB = D.K / kBK + D.a_pad / kBK;
+                for (int kb = 0; kb < NKB; ++kb) {
+                    if (!(ok = mbar_wait_bounded(xloc0 + 8 * rs.s, rs.ph, abort, P.status))) break;
+                    mbar_arrive_remote(full_r0 + 8 * rs.s);
+                    rs.next(S);
+                }
             }
         }
     } else if (warp == 2) {
@@ -276,9 +320,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         }
         Ring rm;
         for (int i = 0; i < ntiles; ++i) {
-            const int gt = tile_id(P, i);
+            const int gt = tile_id(P, i, pair, npair);
             const GemmProb& D = P.d[tile_prob(P, gt)];
-            const int lt = gt - D.tile_begin, n0 = (lt / D.tiles_m) * kBM;
+            const int lt = gt - D.tile_begin, n0 = (lt / D.tiles_m) * kPairM + (int)rank * kBM;   // this CTA's rows
             const int KB = D.K / kBK, NCH = (KB + kChunk - 1) / kChunk;
             for (int c = 0; c < NCH; ++c) {
                 if (!__all_sync(0xffffffffu, mbar_wait_bounded(m_empty0 + 8 * rm.s, rm.ph ^ 1, abort, P.status)))
@@ -339,7 +383,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                 } else {
                     mbar_arrive(fb);
                 }
-                rm.next(2);
+                rm.next(kMetaSlots);
             }
             // anchor weight tiles of this tile, one per slot
             for (int a = 0; a < D.a_pad / kBK; ++a) {
@@ -352,24 +396,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                 } else {
                     mbar_arrive(fb);
                 }
-                rm.next(2);
+                rm.next(kMetaSlots);
             }
         }
     meta_done:;
     } else if (warp < kEpiWarp0) {
         // ---------------------------------------------------------------- dequant into the A stages
-        // Two groups of four warps take alternate K-blocks (by K-block parity), so two
-        // K-blocks are in flight; each thread turns one row's 64 columns into 16-bit values.
-        const int g = (warp - kDqWarp0) >> 2, r = 32 * ((warp - kDqWarp0) & 3) + lane;
+        // kDqGroups groups of four warps take the K-blocks in turn, so that many K-blocks
+        // are in flight; each thread turns one row's 64 columns into 16-bit values
+        // and stores them to its tensor-memory lane (a warp reaches lanes 32 * (warp % 4) on).
+        const int g = (warp - kDqWarp0) >> 2, r = 32 * (warp & 3) + lane;
+        const uint32_t a_lane = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + kACol0;
+        const uint32_t full_r0 = mapa_shared(full0, 0);   // rank 0's stage barriers
         const int sw = r & 7;
         const float C0 = -1.52f, C1 = -0.45f, C2 = 0.45f, C3 = 1.52f;
         Ring ra, rm;
         for (int i = 0; i < ntiles; ++i) {
-          const GemmProb& D = P.d[tile_prob(P, tile_id(P, i))];
+          const GemmProb& D = P.d[tile_prob(P, tile_id(P, i, pair, npair))];
           const int KB = D.K / kBK, NKB = KB + D.a_pad / kBK;
           for (int kb = 0; kb < NKB; ++kb) {
-            const bool mine = (kb & 1) == g;
-            uint8_t* arow = atile + ra.s * kATile + r * 128;
+            const bool mine = kb % kDqGroups == g;
             if (kb < KB) {
                 const int j = kb % kChunk;
                 // every warp waits for each metadata chunk and releases it at its end, so a
@@ -377,8 +423,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                 if (j == 0 && !__all_sync(0xffffffffu, mbar_wait_bounded(m_full0 + 8 * rm.s, rm.ph, abort, P.status)))
                     goto dq_done;
                 if (mine) {
-                    if (!__all_sync(0xffffffffu, mbar_wait_bounded(a_empty0 + 8 * ra.s, ra.ph ^ 1, abort, P.status)))
+                    if (!__all_sync(0xffffffffu, mbar_wait_bounded<true>(empty0 + 8 * ra.s, ra.ph ^ 1, abort, P.status)))
                         goto dq_done;
+                    tc_fence_after();   // the MMAs that read this stage have completed
                     const uint8_t* ch = meta + rm.s * L::kChunkBytes;
                     uint32_t c[32];   // c[4q + k]: columns 8q + 2k, 8q + 2k + 1
                     if (FMT == LQ_FMT_2BIT_LM_G32) {
@@ -468,24 +515,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                             expand_nf4_fast(ws[wi], 1, BL, BH, c[4 * wi + 2], c[4 * wi + 3]);
                         }
                     }
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) sts128(arow + ((q ^ sw) << 4), c[4 * q], c[4 * q + 1], c[4 * q + 2], c[4 * q + 3]);
-                    fence_proxy_async_smem();   // generic-proxy stores -> visible to the tensor core
+                    tmem_st32(a_lane + 32 * ra.s, c);
+                    tc_fence_before();   // the stores are complete: order them before the arrival
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(a_full0 + 8 * ra.s);
+                    if (lane == 0) mbar_arrive_remote(full_r0 + 8 * ra.s);
                 }
                 if (j == kChunk - 1 || kb == KB - 1) {
                     if (lane == 0) mbar_arrive(m_empty0 + 8 * rm.s);
-                    rm.next(2);
+                    rm.next(kMetaSlots);
                 }
             } else {
                 // anchor block: the metadata slot holds 64 binary16 anchor weights per row; the
                 // owning group copies them into the stage, zero past A, in bf16 when x is bf16
                 if (!__all_sync(0xffffffffu, mbar_wait_bounded(m_full0 + 8 * rm.s, rm.ph, abort, P.status))) goto dq_done;
                 if (mine) {
-                    if (!__all_sync(0xffffffffu, mbar_wait_bounded(a_empty0 + 8 * ra.s, ra.ph ^ 1, abort, P.status)))
+                    if (!__all_sync(0xffffffffu, mbar_wait_bounded<true>(empty0 + 8 * ra.s, ra.ph ^ 1, abort, P.status)))
                         goto dq_done;
+                    tc_fence_after();
                     const uint8_t* srow = meta + rm.s * L::kChunkBytes + r * 128;
+                    uint32_t c[32];
                     const int a0 = (kb - KB) * kBK;
                     const bool fix = P.bf16 || a0 + kBK > D.A;
 #pragma unroll
@@ -504,38 +552,52 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                                 v[i] = w;
                             }
                         }
-                        sts128(arow + off, v[0], v[1], v[2], v[3]);
+                        c[4 * q] = v[0];
+                        c[4 * q + 1] = v[1];
+                        c[4 * q + 2] = v[2];
+                        c[4 * q + 3] = v[3];
                     }
-                    fence_proxy_async_smem();
+                    tmem_st32(a_lane + 32 * ra.s, c);
+                    tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(a_full0 + 8 * ra.s);
+                    if (lane == 0) mbar_arrive_remote(full_r0 + 8 * ra.s);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(m_empty0 + 8 * rm.s);
-                rm.next(2);
+                rm.next(kMetaSlots);
             }
-            ra.next(SA);
+            ra.next(S);
           }
         }
+        // every stage's last release has arrived before this CTA may exit
+        if (warp == kDqWarp0)
+            for (int s = 0; s < S; ++s) {
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded<true>(empty0 + 8 * ra.s, ra.ph ^ 1, abort, P.status)))
+                    break;
+                ra.next(S);
+            }
     dq_done:;
     } else {
         // ---------------------------------------------------------------- epilogue: TMEM -> y
+        // Each CTA holds its 128 rows of the pair's 256 x 256 accumulator.
         const int quarter = warp & 3;   // the TMEM lane quarter this warp may read
+        constexpr int kCols = kBN * 4 / kEpiWarps;   // accumulator columns this warp drains
+        const int c0 = kCols * ((warp - kEpiWarp0) >> 2);
+        const uint32_t acc_empty_r0 = mapa_shared(acc_empty0, 0);
         for (int i = 0; i < ntiles; ++i) {
-            const int gt = tile_id(P, i);
+            const int gt = tile_id(P, i, pair, npair);
             const GemmProb& D = P.d[tile_prob(P, gt)];
-            const int acc = i & 1;
-            if (!__all_sync(0xffffffffu, mbar_wait_bounded(acc_full0 + 8 * acc, (i >> 1) & 1, abort, P.status))) break;
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded<true>(acc_full0, i & 1, abort, P.status))) break;
             tc_fence_after();
             const int lt = gt - D.tile_begin;
-            const int n0 = (lt / D.tiles_m) * kBM, m0 = (lt % D.tiles_m) * kBN;
+            const int n0 = (lt / D.tiles_m) * kPairM + (int)rank * kBM, m0 = (lt % D.tiles_m) * kBN;
             const int n = n0 + 32 * quarter + lane;
 #pragma unroll 1
-            for (int cc = 0; cc < kBN / 32; ++cc) {
+            for (int cc = c0; cc < c0 + kCols && m0 + cc < D.M; cc += 32) {
                 uint32_t v[32];
-                tmem_ld32(tmem + ((uint32_t)(32 * quarter) << 16) + acc * kBN + 32 * cc, v);
+                tmem_ld32(tmem + ((uint32_t)(32 * quarter) << 16) + cc, v);
                 if (n < D.N) {
-                    const int mb = m0 + 32 * cc, mcount = min(32, D.M - mb);
+                    const int mb = m0 + cc, mcount = min(32, D.M - mb);
                     const size_t o = (size_t)mb * D.N + n;
                     if (D.y_dtype == LQ_BF16) {
                         __nv_bfloat16* yp = static_cast<__nv_bfloat16*>(D.y) + o;
@@ -557,13 +619,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(acc_empty0 + 8 * acc);
+            if (lane == 0) mbar_arrive_remote(acc_empty_r0);
         }
     }
     tc_fence_before();
-    __syncthreads();
+    __syncwarp();
+    cluster_sync_all();   // no arrival or tensor-memory access of either CTA is still to come
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+    if (warp == 1) tmem_dealloc_pair(tmem, kTmemCols);
 }
 
 // x gathered at the anchor columns ([M][a_pad], zero past A) and the anchor bitmap of
@@ -647,19 +710,40 @@ bool map_16bit(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, u
     return map_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, base, cols, rows, ld, kBK, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// CTA pairs of gemm_kernel<FMT> that fit on the device at once (0 on error); the first call
+// sets the kernel's shared-memory attribute.  Cached per format and device.
 template <int FMT>
-lq_status launch_fmt(const GemmParams& P, int grid, cudaStream_t stream) {
+int pair_capacity(int device) {
+    static std::mutex mu;
+    static std::vector<int> cache;
+    std::lock_guard<std::mutex> lock(mu);
+    if ((int)cache.size() <= device) cache.resize(device + 1, -1);
+    if (cache[device] >= 0) return cache[device];
     constexpr int smem = GemmLayout<FMT>::kSmemBytes;
-    if (cudaFuncSetAttribute(gemm_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-        return LQ_ERR_CUDA;
-    gemm_kernel<FMT><<<grid, kGemmThreads, smem, stream>>>(P);
+    int n = 0;
+    if (cudaFuncSetAttribute(gemm_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2, 1, 1);
+        cfg.blockDim = dim3(GemmLayout<FMT>::kThreads, 1, 1);
+        cfg.dynamicSmemBytes = smem;
+        if (cudaOccupancyMaxActiveClusters(&n, gemm_kernel<FMT>, &cfg) != cudaSuccess) n = 0;
+    }
+    cudaGetLastError();
+    cache[device] = n;
+    return n;
+}
+
+template <int FMT>
+lq_status launch_fmt(const GemmParams& P, int npair, cudaStream_t stream) {
+    constexpr int smem = GemmLayout<FMT>::kSmemBytes;
+    gemm_kernel<FMT><<<2 * npair, GemmLayout<FMT>::kThreads, smem, stream>>>(P);   // (compile-time clusters of two)
     return cudaPeekAtLastError() == cudaSuccess ? LQ_OK : LQ_ERR_CUDA;
 }
 
 }  // namespace
 
-// Longest-processing-time assignment of the launch's tiles to `grid` CTAs (each tile
-// costs its K-blocks), as per-CTA lists; kept on the device between calls with the same shapes.
+// Longest-processing-time assignment of the launch's tiles to `grid` CTA pairs (each tile
+// costs its K-blocks), as per-pair lists; kept on the device between calls with the same shapes.
 static lq_status upload_schedule(lq_handle h, const GemmParams& P, int grid, cudaStream_t stream) {
     std::vector<int64_t> key = {grid, P.count};
     for (int p = 0; p < P.count; ++p) {
@@ -793,7 +877,7 @@ lq_status launch_gemm_grouped_limited(lq_handle h, const lq_problem* probs, int 
         D.meta_tma = p.K % 256 == 0;   // scale rows 16-byte aligned: TMA boxes; else 4-byte loads
         D.tiles_m = (p.M + kBN - 1) / kBN;
         D.tile_begin = tiles;
-        const int64_t t = (int64_t)D.tiles_m * ((p.N + kBM - 1) / kBM);
+        const int64_t t = (int64_t)D.tiles_m * ((p.N + kPairM - 1) / kPairM);
         if (tiles + t > 0x7fffffffLL) return LQ_ERR_UNSUPPORTED;
         tiles += (int)t;
         unsigned long long* bits = reinterpret_cast<unsigned long long*>(ws + bits_off[i]);
@@ -808,7 +892,7 @@ lq_status launch_gemm_grouped_limited(lq_handle h, const lq_problem* probs, int 
                                          p.K};
             xsrc = xp;
         }
-        if (!map_16bit(&D.xmap, xsrc, (uint64_t)p.K, (uint64_t)p.M, (uint64_t)p.K, kBN)) return LQ_ERR_CUDA;
+        if (!map_16bit(&D.xmap, xsrc, (uint64_t)p.K, (uint64_t)p.M, (uint64_t)p.K, kHalfN)) return LQ_ERR_CUDA;
         const uint64_t cbytes = (uint64_t)p.K / (nib ? 2 : 4);
         if (!map_2d(&D.cmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.codes, cbytes, (uint64_t)p.N, cbytes,
                     kChunk * (nib ? 32 : 16), kBM, nib ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B))
@@ -828,7 +912,7 @@ lq_status launch_gemm_grouped_limited(lq_handle h, const lq_problem* probs, int 
             }
         }
         if (A > 0) {
-            if (!map_16bit(&D.xamap, xa, (uint64_t)a_pad, (uint64_t)p.M, (uint64_t)a_pad, kBN)) return LQ_ERR_CUDA;
+            if (!map_16bit(&D.xamap, xa, (uint64_t)a_pad, (uint64_t)p.M, (uint64_t)a_pad, kHalfN)) return LQ_ERR_CUDA;
             if (!map_16bit(&D.awmap, p.anchor_w, (uint64_t)p.ld_anchor, (uint64_t)p.N, (uint64_t)p.ld_anchor, kBM))
                 return LQ_ERR_CUDA;
             PrepProb& e = Q.d[prep_count++];
@@ -863,17 +947,21 @@ lq_status launch_gemm_grouped_limited(lq_handle h, const lq_problem* probs, int 
                      : int4 ? GemmLayout<LQ_FMT_INT4_G32>::kSmemBytes
                             : GemmLayout<LQ_FMT_2BIT_LM_G32>::kSmemBytes;
     if (smem > h->max_smem_optin) return LQ_ERR_UNSUPPORTED;
-    const int grid = std::min(tiles, h->num_sms);
+    const int cap = nf4 ? pair_capacity<LQ_FMT_NF4_B64>(h->device)
+                    : int4 ? pair_capacity<LQ_FMT_INT4_G32>(h->device)
+                           : pair_capacity<LQ_FMT_2BIT_LM_G32>(h->device);
+    if (cap < 1) return LQ_ERR_UNSUPPORTED;
+    const int npair = std::min(tiles, cap);
     if (count > 1) {
-        // problems of different lengths: balance the CTAs' K-blocks
-        const lq_status s = upload_schedule(h, P, grid, stream);
+        // problems of different lengths: balance the pairs' K-blocks
+        const lq_status s = upload_schedule(h, P, npair, stream);
         if (s != LQ_OK) return s;
         P.sched_off = h->sched;
-        P.sched_tiles = h->sched + grid + 1;
+        P.sched_tiles = h->sched + npair + 1;
     }
-    if (nf4) return launch_fmt<LQ_FMT_NF4_B64>(P, grid, stream);
-    if (int4) return launch_fmt<LQ_FMT_INT4_G32>(P, grid, stream);
-    return launch_fmt<LQ_FMT_2BIT_LM_G32>(P, grid, stream);
+    if (nf4) return launch_fmt<LQ_FMT_NF4_B64>(P, npair, stream);
+    if (int4) return launch_fmt<LQ_FMT_INT4_G32>(P, npair, stream);
+    return launch_fmt<LQ_FMT_2BIT_LM_G32>(P, npair, stream);
 }
 
 lq_status launch_gemm(lq_handle h, const lq_problem& p, cudaStream_t stream) { return launch_gemm_grouped(h, &p, 1, stream); }
