@@ -216,9 +216,12 @@ LQ_API lq_status lq_gemv_grouped(lq_handle h, const lq_problem* problems, int co
 
 /*
  * lq_gemm — prefill-sized product for M >= 1 (tuned for M >= 256) on the
- * tcgen05 tensor cores: x tiles arrive by TMA, weight tiles are dequantized by
- * the CTA into tensor memory, the fp32 accumulator lives in tensor memory, and
- * the anchor columns are appended as extra K-blocks of the same accumulator.
+ * tcgen05 tensor cores, run by clusters of two CTAs (one per SM) that share each
+ * 256-row x 256-token tile through one cta_group::2 MMA: each CTA TMA-loads its
+ * half of the x tile and dequantizes its 128 weight rows into its tensor memory,
+ * the fp32 accumulator lives in tensor memory, and the anchor columns are
+ * appended as extra K-blocks of the same accumulator.  LQ_ERR_UNSUPPORTED when
+ * the device cannot hold one such pair.
  * x: [M][K] bf16 or binary16 (the multiply runs in that dtype); y: [M][N] in
  * y_dtype.  K % 64 == 0, every format.  INT4 first writes x in the permuted
  * column order into the handle's workspace (M * K values per problem), and NF4-DQ
@@ -236,7 +239,7 @@ LQ_API lq_status lq_gemm(lq_handle h, int format,
  * decoder layer at prefill) in ONE persistent launch.  `problems` is a host
  * array of `count` (1..8) entries, read before the call returns; batch must be
  * 1 (strides ignored).  All problems share format and x_dtype; M, N, K, anchors
- * and y_dtype may differ.  The CTAs' tile lists balance the problems' K-blocks
+ * and y_dtype may differ.  The CTA pairs' tile lists balance the problems' K-blocks
  * (longest first); the lists are built on the host and kept in the handle's
  * workspace, so the first call with new shapes waits for their upload (the
  * stream is synchronized once) and later calls with the same shapes do not.
