@@ -17,7 +17,7 @@ F32, F16, BF16 = 0, 1, 2
 #: every entry point include/lq.h declares
 EXPORTED = ("lq_create", "lq_destroy", "lq_status_string", "lq_sync", "lq_dequant", "lq_gemv",
             "lq_anchor_count",
-            "lq_gemv_grouped", "lq_gemm", "lq_gemm_grouped", "lq_gemv_noalloc",
+            "lq_gemv_grouped", "lq_gemv_layers", "lq_gemm", "lq_gemm_grouped", "lq_gemv_noalloc",
             "lq_select_anchors", "lq_quantize_2bit", "lq_quantize_nf4",
             "lq_stream_create", "lq_stream_run", "lq_stream_destroy", "lq_stream_run_direct",
             "lq_selftest_wait")
@@ -82,6 +82,8 @@ def load_library(build_if_missing: bool = True):
     L.lq_gemv_noalloc.restype = I
     L.lq_gemv_grouped.argtypes = [P, ctypes.POINTER(lq_problem), I, P]
     L.lq_gemv_grouped.restype = I
+    L.lq_gemv_layers.argtypes = [P, ctypes.POINTER(lq_problem), ctypes.POINTER(I), I, P]
+    L.lq_gemv_layers.restype = I
     L.lq_gemm_grouped.argtypes = [P, ctypes.POINTER(lq_problem), I, P]
     L.lq_gemm_grouped.restype = I
     L.lq_anchor_count.argtypes = [I]
@@ -257,6 +259,16 @@ class Handle:
         st = self._lib.lq_gemv_grouped(self._h, arr, len(problems), _stream(stream))
         if st != LQ_OK:
             raise LQError(st, "lq_gemv_grouped")
+
+    def gemv_layers(self, layers, stream=None):
+        """Consecutive layers (each a list of problems) in one call; a layer may read what the
+        layers before it wrote."""
+        flat = [p for layer in layers for p in layer]
+        arr = (lq_problem * len(flat))(*flat)
+        counts = (ctypes.c_int * len(layers))(*[len(layer) for layer in layers])
+        st = self._lib.lq_gemv_layers(self._h, arr, counts, len(layers), _stream(stream))
+        if st != LQ_OK:
+            raise LQError(st, "lq_gemv_layers")
 
     def selftest_wait(self, limit_us: int, stream=None):
         """Run the bounded-wait self-test: a wait that nothing completes gives up after

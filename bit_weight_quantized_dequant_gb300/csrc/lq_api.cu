@@ -270,6 +270,35 @@ LQ_API lq_status lq_gemv_grouped(lq_handle h, const lq_problem* problems, int co
     return lq::launch_gemv(h, problems, count, st);
 }
 
+LQ_API lq_status lq_gemv_layers(lq_handle h, const lq_problem* problems, const int* counts, int layers, void* stream) {
+    if (!h || !problems || !counts || layers < 1) return LQ_ERR_INVALID_ARG;
+    int total = 0;
+    for (int l = 0; l < layers; ++l) {
+        if (counts[l] < 1) return LQ_ERR_INVALID_ARG;
+        if (counts[l] > lq::kMaxGroup) return LQ_ERR_UNSUPPORTED;
+        const lq_problem* g = problems + total;
+        for (int i = 0; i < counts[l]; ++i) {
+            lq_status s = check_problem(g[i]);
+            if (s != LQ_OK) return s;
+            if (g[i].M < 1 || g[i].M > 32) return LQ_ERR_UNSUPPORTED;
+            if (g[i].format != g[0].format || g[i].M != g[0].M || g[i].x_dtype != g[0].x_dtype ||
+                g[i].y_dtype != g[0].y_dtype)
+                return LQ_ERR_UNSUPPORTED;
+        }
+        total += counts[l];
+    }
+    DeviceGuard guard(h->device);
+    if (!guard.ok) return LQ_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    for (int i = 0; i < total; ++i) {
+        if (problems[i].batch == 1 || problems[i].stride_anchor_idx == 0) {
+            lq_status s = check_anchor_order(problems[i].anchor_idx, problems[i].A, problems[i].K, st);
+            if (s != LQ_OK) return s;
+        }
+    }
+    return lq::launch_gemv_layers(h, problems, counts, layers, st);
+}
+
 LQ_API lq_status lq_gemv(lq_handle h, int format, const uint8_t* codes, const void* scales, const void* offsets,
                          const int32_t* anchor_idx, const uint16_t* anchor_w, int A, int ld_anchor, const void* x,
                          int x_dtype, void* y, int y_dtype, int M, int N, int K, void* stream) {

@@ -514,6 +514,17 @@ lq_status launch_gemv(lq_handle h, const lq_problem* probs, int count, cudaStrea
     return launch_gemv_ws(ws, probs, count, stream);
 }
 
+lq_status launch_gemv_layers(lq_handle h, const lq_problem* probs, const int* counts, int layers, cudaStream_t stream) {
+    // One grouped launch per layer, in stream order: each ring-kernel launch lets the next one
+    // start its CTAs' first weight copies while its own last CTAs finish (programmatic
+    // dependent launch), and the next launch waits for it before reading its x.
+    for (int l = 0, off = 0; l < layers; off += counts[l], ++l) {
+        const lq_status st = launch_gemv(h, probs + off, counts[l], stream);
+        if (st != LQ_OK) return st;
+    }
+    return LQ_OK;
+}
+
 // The streaming kernel takes every launch whose K are multiples of 256; the
 // split-K kernel below covers the rest (any K % 32 == 0).
 // LQ_GEMV_KERNEL=regs forces the register-fed kernel (for comparisons and tests).

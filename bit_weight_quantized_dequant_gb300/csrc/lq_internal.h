@@ -90,6 +90,10 @@ lq_status launch_gemv_ws(const GemvWorkspace& ws, const lq_problem* problems, in
 bool gemv_stream_eligible(const lq_problem* problems, int count);
 lq_status launch_gemv_regs(const GemvWorkspace& ws, const lq_problem* problems, int count, cudaStream_t stream);
 lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* problems, int count, cudaStream_t stream);
+// Consecutive layers of grouped calls (counts[l] problems each), one launch per layer in
+// stream order; layer l may read what layer l - 1 wrote.
+lq_status launch_gemv_layers(lq_handle h, const lq_problem* problems, const int* counts, int layers,
+                             cudaStream_t stream);
 // bf16 x: each (member, token) row's max |x| (fp32 bit pattern) into words[], rows in problem order.
 lq_status launch_xmax_rows(const lq_problem* problems, int count, uint32_t* words, cudaStream_t stream);
 

@@ -215,6 +215,22 @@ LQ_API lq_status lq_gemv(lq_handle h, int format,
 LQ_API lq_status lq_gemv_grouped(lq_handle h, const lq_problem* problems, int count, void* stream);
 
 /*
+ * lq_gemv_layers — consecutive decode layers in one call: layer l is a grouped
+ * call of counts[l] problems (lq_gemv_grouped's rules), taken in order from
+ * `problems` (host array of sum(counts) entries, read before the call returns).
+ * Layer l's problems may read, as x, what any earlier layer of the call wrote as
+ * y (an LLM decode step: the next layer's input is the previous layer's output);
+ * results are those of one lq_gemv_grouped call per layer, in order, and that is
+ * how it runs: one launch per layer on `stream`, each overlapping its start with
+ * the end of the launch before (programmatic dependent launch).  Errors as
+ * lq_gemv_grouped; LQ_ERR_INVALID_ARG for layers < 1 or a count < 1.  (The
+ * decode loop this serves is the memory-bound one of the otf-llm README, "The
+ * Memory-Bound Bottleneck in Autoregressive LLM Decoding": one pass over every
+ * layer's weights per generated token.)
+ */
+LQ_API lq_status lq_gemv_layers(lq_handle h, const lq_problem* problems, const int* counts, int layers, void* stream);
+
+/*
  * lq_gemm — prefill-sized product for M >= 1 (tuned for M >= 256) on the
  * tcgen05 tensor cores, run by clusters of two CTAs (one per SM) that share each
  * 256-row x 256-token tile through one cta_group::2 MMA: each CTA TMA-loads its

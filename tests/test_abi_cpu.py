@@ -115,6 +115,31 @@ def test_grouped_validation(lib):
     assert L.lq_gemv_grouped(h, (_lq.lq_problem * 1)(r), 1, None) == _lq.LQ_ERR_ALIGNMENT
 
 
+def test_layers_validation(lib):
+    """lq_gemv_layers rejects bad layer lists on the host, before the handle or a device is touched."""
+    L, _ = lib
+    h = _fake_handle()
+    A16 = 0x10000
+    p = _lq.lq_problem()
+    p.format, p.M, p.N, p.K = 1, 1, 64, 256
+    p.codes = p.scales = p.offsets = p.x = p.y = A16
+    p.x_dtype, p.y_dtype, p.batch = 1, 0, 1
+    q = _lq.lq_problem.from_buffer_copy(p)
+    q.M = 2
+    arr = (_lq.lq_problem * 3)(p, p, q)
+    counts = (ctypes.c_int * 2)(1, 2)                # the second layer mixes M
+    assert L.lq_gemv_layers(h, arr, counts, 2, None) == _lq.LQ_ERR_UNSUPPORTED
+    assert L.lq_gemv_layers(h, arr, counts, 0, None) == _lq.LQ_ERR_INVALID_ARG
+    assert L.lq_gemv_layers(h, arr, None, 1, None) == _lq.LQ_ERR_INVALID_ARG
+    zero = (ctypes.c_int * 2)(1, 0)
+    assert L.lq_gemv_layers(h, arr, zero, 2, None) == _lq.LQ_ERR_INVALID_ARG
+    big = (_lq.lq_problem * 17)(*([p] * 17))
+    assert L.lq_gemv_layers(h, big, (ctypes.c_int * 1)(17), 1, None) == _lq.LQ_ERR_UNSUPPORTED
+    r = _lq.lq_problem.from_buffer_copy(p)
+    r.batch, r.stride_codes = 2, 8                  # stride not a multiple of 16 bytes
+    assert L.lq_gemv_layers(h, (_lq.lq_problem * 2)(p, r), (ctypes.c_int * 2)(1, 1), 2, None) == _lq.LQ_ERR_ALIGNMENT
+
+
 def test_create_without_device_reports_error(lib):
     """No GPU in this container: lq_create must fail cleanly, not crash."""
     import torch
