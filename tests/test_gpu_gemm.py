@@ -142,3 +142,48 @@ def test_gemm_grouped_mixed_shapes(lqm, handle, fmt):
             assert_within(y.cpu().numpy(), yref, E, TOL["bf16"], f"grouped {fmt}")
             y1 = handle.gemm(w, x)
             assert torch.equal(y1, y)
+
+
+# ---------------------------------------------------------------- 16-bit outputs
+
+TDT = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
+
+
+def gpu_bits(t):
+    return t.cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("ydt", ["bf16", "f16"])
+@pytest.mark.parametrize("shape", [(300, 200, 1088), (256, 128, 256), (1, 130, 512), (513, 384, 640), (2048, 264, 512)])
+def test_gemm_2bit_16bit_output(lqm, handle, ydt, shape):
+    """16-bit y is the RNE rounding of the fp32 result, bit for bit, over ragged token tiles, row
+    counts that are not a multiple of 8, and row tiles whose second CTA holds no rows."""
+    M, N, K = shape
+    p, outl = quantized_2bit(N, K, seed=M + N + K + 3)
+    xb = x_for(M, K, "bf16", outl, seed=M + 3)
+    w = lqm.QuantWeights.from_host(p, lqm.FMT_2BIT)
+    x = dev_x(xb, "bf16")
+    y16 = handle.gemm(w, x, y_dtype=TDT[ydt])
+    y32 = handle.gemm(w, x)
+    torch.cuda.synchronize()
+    assert np.array_equal(gpu_bits(y16), O.round_to(y32.cpu().numpy(), ydt))
+
+
+def test_gemm_grouped_mixed_output_dtypes(lqm, handle):
+    """One grouped launch over problems with different output dtypes: each output equals its own
+    single call bit for bit."""
+    cases = [((300, 200, 1088), "bf16"), ((300, 130, 512), "bf16"), ((300, 384, 640), "f32"), ((300, 128, 256), "f16")]
+    mats, probs = [], []
+    for i, ((M, N, K), ydt) in enumerate(cases):
+        p, outl = quantized_2bit(N, K, seed=50 + i)
+        w = lqm.QuantWeights.from_host(p, lqm.FMT_2BIT)
+        x = dev_x(x_for(M, K, "bf16", outl, seed=50 + i), "bf16")
+        y = torch.empty((M, N), dtype=TDT[ydt], device="cuda")
+        mats.append((w, x, y, ydt))
+        probs.append(handle.problem(w, x, y))
+    for _ in range(2):
+        handle.gemm_grouped(probs)
+        torch.cuda.synchronize()
+        for (w, x, y, ydt) in mats:
+            y1 = handle.gemm(w, x, y_dtype=TDT[ydt])
+            assert torch.equal(y1, y)
