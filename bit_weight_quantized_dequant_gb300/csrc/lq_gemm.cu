@@ -470,28 +470,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmLayout<FMT>::kTh
                         const uint4 cw0 = *reinterpret_cast<const uint4*>(crow + (((2 * j) ^ sw) << 4));
                         const uint4 cw1 = *reinterpret_cast<const uint4*>(crow + (((2 * j + 1) ^ sw) << 4));
                         const uint32_t s2 = *reinterpret_cast<const uint32_t*>(ch + L::kScaleOff + r * 16 + 4 * j);
+                        // both groups' products q * (S0, S1) per packed fp32 FMA (q * S + (-0) is the exact
+                        // product, sign of zero included, as one multiply would give)
+                        const float2 sg2 = make_float2(half_bits_to_float((uint16_t)(s2 & 0xFFFFu)),
+                                                       half_bits_to_float((uint16_t)(s2 >> 16)));
+                        uint32_t BL[2][4], BH[2][4];
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            float2 v[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int nib = 4 * q4 + e;
+                                v[e] = fma_f32x2(sg2, (float)(nib < 8 ? nib : nib - 16), make_float2(-0.f, -0.f));
+                            }
+#pragma unroll
+                            for (int hh = 0; hh < 2; ++hh) {
+                                const uint32_t p01 = pack2(hh ? v[0].y : v[0].x, hh ? v[1].y : v[1].x, P.bf16);
+                                const uint32_t p23 = pack2(hh ? v[2].y : v[2].x, hh ? v[3].y : v[3].x, P.bf16);
+                                BL[hh][q4] = prmt(p01, p23, 0x6420);
+                                BH[hh][q4] = prmt(p01, p23, 0x7531);
+                            }
+                        }
 #pragma unroll
                         for (int hh = 0; hh < 2; ++hh) {
-                            const float sg = half_bits_to_float((uint16_t)(hh ? s2 >> 16 : s2 & 0xFFFFu));
-                            uint32_t BL[4], BH[4];
-#pragma unroll
-                            for (int q4 = 0; q4 < 4; ++q4) {
-                                float v[4];
-#pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    const int nib = 4 * q4 + e;
-                                    v[e] = __fmul_rn((float)(nib < 8 ? nib : nib - 16), sg);
-                                }
-                                const uint32_t p01 = pack2(v[0], v[1], P.bf16), p23 = pack2(v[2], v[3], P.bf16);
-                                BL[q4] = prmt(p01, p23, 0x6420);
-                                BH[q4] = prmt(p01, p23, 0x7531);
-                            }
                             const uint4& cw = hh ? cw1 : cw0;
                             const uint32_t ws[4] = {cw.x, cw.y, cw.z, cw.w};
 #pragma unroll
                             for (int wi = 0; wi < 4; ++wi) {
-                                expand_nf4_fast(ws[wi], 0, BL, BH, c[16 * hh + 4 * wi + 0], c[16 * hh + 4 * wi + 1]);
-                                expand_nf4_fast(ws[wi], 1, BL, BH, c[16 * hh + 4 * wi + 2], c[16 * hh + 4 * wi + 3]);
+                                expand_nf4_fast(ws[wi], 0, BL[hh], BH[hh], c[16 * hh + 4 * wi + 0], c[16 * hh + 4 * wi + 1]);
+                                expand_nf4_fast(ws[wi], 1, BL[hh], BH[hh], c[16 * hh + 4 * wi + 2], c[16 * hh + 4 * wi + 3]);
                             }
                         }
                     } else {
