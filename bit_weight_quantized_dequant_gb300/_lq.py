@@ -254,9 +254,15 @@ class Handle:
             setattr(p, "stride_" + k, int(v))
         return p
 
+    @staticmethod
+    def prepare(problems):
+        """The C array of a list of problems, built once: a decode loop passes it to gemv_grouped
+        every token instead of the list (no per-call marshalling)."""
+        return (lq_problem * len(problems))(*problems)
+
     def gemv_grouped(self, problems, stream=None):
-        arr = (lq_problem * len(problems))(*problems)
-        st = self._lib.lq_gemv_grouped(self._h, arr, len(problems), _stream(stream))
+        arr = problems if isinstance(problems, ctypes.Array) else (lq_problem * len(problems))(*problems)
+        st = self._lib.lq_gemv_grouped(self._h, arr, len(arr), _stream(stream))
         if st != LQ_OK:
             raise LQError(st, "lq_gemv_grouped")
 

@@ -29,6 +29,8 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <string>
+#include <vector>
 
 #include "lq_common.cuh"
 #include "lq_dq.cuh"
@@ -1491,17 +1493,29 @@ __global__ void __launch_bounds__(32 * ring_warps(NT), 16 / ring_warps(NT)) gemv
     if (peak >= kHalfOverflow && P.status) atomicOr(P.status, 2);
 }
 
-// Resident CTAs per SM of a kernel at a given dynamic shared-memory size.  The first call
-// for a size sets the kernel's shared-memory attribute; the answer is cached per kernel
-// (the lock keeps host threads that launch different sizes from racing on the cache).
+// Resident CTAs per SM of a kernel at a given dynamic shared-memory size; the answer is cached
+// per kernel (the lock keeps host threads that launch different sizes from racing on the cache).
+// The kernel's shared-memory attribute only ever rises, to the largest size asked for, so that a
+// launch planned earlier for a larger size (and kept in the plan cache) stays valid.
 std::mutex g_occ_mutex;
 
 template <typename Kern>
 int resident_ctas_of(Kern kern, size_t smem, size_t& set_smem, int& per_sm, int threads = kThreadsS) {
     std::lock_guard<std::mutex> lock(g_occ_mutex);
     if (set_smem != smem) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-            return -1;
+        static std::vector<std::pair<const void*, size_t>> attr;   // (kernel, attribute set)
+        size_t* cur = nullptr;
+        for (auto& e : attr)
+            if (e.first == reinterpret_cast<const void*>(kern)) cur = &e.second;
+        if (!cur) {
+            attr.push_back({reinterpret_cast<const void*>(kern), 0});
+            cur = &attr.back().second;
+        }
+        if (smem > *cur) {
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+                return -1;
+            *cur = smem;
+        }
         int n = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, smem) != cudaSuccess) return -1;
         per_sm = n;
@@ -1686,9 +1700,19 @@ bool gemv_stream_eligible(const lq_problem* probs, int count) {
     return true;
 }
 
-lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* probs, int count, cudaStream_t stream) {
+// The launch description of one grouped call: descriptors, grid, kernel variant, shared memory
+// and the workspace regions.  units == 0: nothing to launch.
+struct GemvPlan {
     FParams P;
     PrepParams Q;
+    bool use_ring = false, ring_xs = false, staged = false;
+    int64_t grid = 0, jobs = 0, rows = 0, units = 0, blocks = 0;
+    size_t smem = 0;   // dynamic shared memory of the kernel variant that runs
+};
+
+lq_status plan_gemv(const GemvWorkspace& ws, const lq_problem* probs, int count, GemvPlan& G, cudaStream_t stream) {
+    FParams& P = G.P;
+    PrepParams& Q = G.Q;
     memset(&P, 0, sizeof(P));
     memset(&Q, 0, sizeof(Q));
     const int M = probs[0].M;
@@ -1772,6 +1796,8 @@ lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* probs, i
         rows += (int64_t)q.batch * M;
         max_k = std::max(max_k, q.K);
     }
+    G.units = units;
+    G.blocks = blocks;
     if (units == 0) return LQ_OK;
     // arrival counts live in the counter area, which every kernel leaves at zero
     if ((size_t)blocks > ws.num_counters) return LQ_ERR_UNSUPPORTED;
@@ -1861,15 +1887,30 @@ lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* probs, i
         d.cnt = cnt;
         cnt += (int64_t)q.batch * d.rblocks;
     }
-    if (ws.clear_counters && cudaMemsetAsync(ws.counters, 0, sizeof(unsigned) * (size_t)blocks, stream) != cudaSuccess)
-        return LQ_ERR_CUDA;
     Q.total_jobs = jobs;
     Q.total_rows = rows;
     Q.ring = use_ring ? 1 : 0;
     P.status = ws.status;
+    G.use_ring = use_ring;
+    G.ring_xs = use_ring && ring_xs;
+    G.staged = staged;
+    G.grid = grid;
+    G.jobs = jobs;
+    G.rows = rows;
+    G.smem = staged ? smem : (use_ring ? (ring_xs ? ring_xs_smem : ring_smem) : 0);
+    return LQ_OK;
+}
+
+// Launch a planned call: the kernel, after the x pre-pass when the x copy is in global memory.
+lq_status run_plan(const GemvPlan& G, cudaStream_t stream) {
+    const FParams& P = G.P;
+    const PrepParams& Q = G.Q;
+    const int fmt = P.format;
+    const int64_t grid = G.grid, jobs = G.jobs, rows = G.rows;
+    const bool use_ring = G.use_ring, ring_xs = G.ring_xs;
     int unused = 0;
-    if (staged) return dispatch(fmt, 1, true, P, grid, smem, &unused, stream);
-    if (use_ring && ring_xs) return dispatch_ring(1, true, P, grid, ring_xs_smem, &unused, stream);
+    if (G.staged) return dispatch(fmt, 1, true, P, grid, G.smem, &unused, stream);
+    if (use_ring && ring_xs) return dispatch_ring(1, true, P, grid, G.smem, &unused, stream);
 
     // x pre-pass (bf16 x: after each token's max |x|), then the main kernel, chained by
     // programmatic dependent launch
@@ -1881,8 +1922,71 @@ lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* probs, i
     }
     xprep_kernel<<<(unsigned)prep_ctas, 32 * kPrepWarps, 0, stream>>>(Q);
     if (cudaPeekAtLastError() != cudaSuccess) return LQ_ERR_CUDA;
-    if (use_ring) return dispatch_ring(1, ring_xs, P, grid, ring_xs ? ring_xs_smem : ring_smem, &unused, stream);
+    if (use_ring) return dispatch_ring(1, false, P, grid, G.smem, &unused, stream);
     return dispatch(fmt, 1, false, P, grid, 0, &unused, stream);
+}
+
+// Plans of recent calls.  A decode loop makes the same calls (the same layers, buffers and
+// workspace) every token; such a call launches its kept plan instead of planning again, which
+// takes the per-CTA span walk and the occupancy queries off the host's path.  The key is every
+// byte the plan depends on: the problems, the workspace, and the kernel-choice settings.
+constexpr int kPlanCache = 16;
+struct PlanEntry {
+    std::vector<unsigned char> key;
+    GemvPlan plan;
+    uint64_t used = 0;
+};
+std::mutex g_plan_mutex;
+std::vector<PlanEntry> g_plans;
+uint64_t g_plan_clock = 0;
+
+void plan_key(const GemvWorkspace& ws, const lq_problem* probs, int count, std::vector<unsigned char>& key) {
+    auto put = [&](const void* p, size_t n) {
+        const unsigned char* b = static_cast<const unsigned char*>(p);
+        key.insert(key.end(), b, b + n);
+    };
+    key.clear();
+    put(&count, sizeof(count));
+    put(probs, sizeof(lq_problem) * (size_t)count);
+    const void* wsp[4] = {ws.partials, ws.counters, ws.status, nullptr};
+    put(wsp, sizeof(wsp));
+    const size_t wsn[4] = {ws.partial_floats, ws.num_counters, (size_t)ws.num_sms, (size_t)ws.max_smem_optin};
+    put(wsn, sizeof(wsn));
+    for (const char* name : {"LQ_GEMV_KERNEL", "LQ_GEMV_STAGE", "LQ_GEMV_XS"}) {
+        const char* v = getenv(name);
+        const std::string sv = v ? std::string("=") + v : std::string("-");
+        put(sv.data(), sv.size() + 1);
+    }
+}
+
+lq_status launch_gemv_stream(const GemvWorkspace& ws, const lq_problem* probs, int count, cudaStream_t stream) {
+    thread_local std::vector<unsigned char> key;
+    plan_key(ws, probs, count, key);
+    std::lock_guard<std::mutex> lock(g_plan_mutex);
+    PlanEntry* hit = nullptr;
+    for (auto& e : g_plans)
+        if (e.key == key) hit = &e;
+    if (!hit) {
+        PlanEntry fresh;
+        const lq_status st = plan_gemv(ws, probs, count, fresh.plan, stream);
+        if (st != LQ_OK) return st;
+        fresh.key = key;
+        if ((int)g_plans.size() < kPlanCache) {
+            g_plans.push_back(std::move(fresh));
+            hit = &g_plans.back();
+        } else {
+            hit = &g_plans[0];
+            for (auto& e : g_plans)
+                if (e.used < hit->used) hit = &e;
+            *hit = std::move(fresh);
+        }
+    }
+    hit->used = ++g_plan_clock;
+    const GemvPlan& G = hit->plan;
+    if (G.units == 0) return LQ_OK;
+    if (ws.clear_counters && cudaMemsetAsync(ws.counters, 0, sizeof(unsigned) * (size_t)G.blocks, stream) != cudaSuccess)
+        return LQ_ERR_CUDA;
+    return run_plan(G, stream);
 }
 
 }  // namespace lq
