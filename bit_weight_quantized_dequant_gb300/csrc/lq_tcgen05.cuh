@@ -7,20 +7,9 @@
 
 namespace lq {
 
-// Allocate `ncols` (power of two >= 32) tensor-memory columns for this CTA; the
-// base address is written to shared memory at `dst`.  Executed by one full warp.
-__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-
-// The same for a CTA pair (cta_group::2): one warp of each of the two CTAs executes it,
-// and both receive the same column range.
+// Allocate `ncols` (power of two >= 32) tensor-memory columns for a CTA pair (cta_group::2):
+// one full warp of each of the two CTAs executes it, both receive the same column range, and
+// the base address is written to shared memory at `dst` in each CTA.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
                  : "memory");
@@ -56,30 +45,11 @@ __host__ __device__ constexpr uint32_t idesc_f16(bool bf16, int M, int N) {
            | ((uint32_t)(M >> 4) << 24);                    // M / 16
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
-__device__ __forceinline__ void tc_mma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                           uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem]^T, issued by one thread.  A (M = 128) sits in tensor
-// memory with row r in lane r and 16-bit elements 2c, 2c + 1 of the row in column c.
-__device__ __forceinline__ void tc_mma_f16_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t idesc,
-                                              uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
-        "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
 // CTA-pair MMA (M = 256): issued by one thread of the pair's even CTA.  Each CTA holds its
-// 128 rows of A in its own tensor memory at address tmem_a and its half of the N rows of B
-// at the same shared-memory offset; D rows land in each CTA's tensor memory at tmem_d.
+// 128 rows of A in its own tensor memory at address tmem_a (row r in lane r, 16-bit elements
+// 2c and 2c + 1 of the row in column c) and its half of the N rows of B at the same
+// shared-memory offset; D rows land in each CTA's tensor memory at tmem_d, the even CTA's B
+// rows in columns 0 .. N/2 - 1.
 __device__ __forceinline__ void tc_mma_f16_ts_pair(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t idesc,
                                                    uint32_t accumulate) {
     asm volatile(
@@ -97,12 +67,6 @@ __device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
         "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
         "h"(both)
         : "memory");
-}
-
-// Arrive on `bar` once every MMA issued so far by this thread has completed.
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
 }
 
 // 32 consecutive fp32 columns of this warp's 32 tensor-memory lanes (one lane per thread).
